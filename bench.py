@@ -1,0 +1,431 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused conv + norm forward on GB300.
+
+Default workload: Conv3d(3->16, k=4) on (512, 3, 16, 32, 32) -> HardSwish ->
+GroupNorm(4) -> mean over D,H,W (the conv tensor is never materialised).
+A step is one conv_norm_forward over the whole batch, inputs resident in
+HBM; L2 is flushed (256 MB write) before every timed step because the input
+(100 MB) fits in L2.  The metric is GFLOP/s of algorithmic conv FLOPs
+(2 per multiply-add over the outputs the method must compute) with the
+time per step; the roofline is max(FLOPs / FP32 peak, compulsory bytes /
+HBM bandwidth).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl reference] [--no-extras]
+
+Under torchrun each rank runs its own full batch (weak scaling, no
+collective on the data path); the value is the sum of FLOPs over ranks
+divided by the slowest rank's time.  --impl reference times the fp64 CPU
+oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from convolution_normalization_gb300 import workloads as wl  # noqa: E402
+
+DEFAULT_WORKLOAD = "conv3d_hswish_gn4_mean_n512"
+SMS = 152
+FP32_LANES_PER_SM = 128
+METRIC = "fused conv+norm forward ms & GFLOP/s, % of roofline (FP32 peak vs HBM)"
+
+
+# ---- workload arithmetic (for reporting only) ---------------------------------
+
+def conv_out_dims(s):
+    k = s["k"]
+    if s["conv"] == "conv3d":
+        return [s["D"] - k + 1, s["H"] - k + 1, s["W"] - k + 1]
+    if s["conv"] == "conv2d":
+        return [s["H"] - k + 1, s["W"] - k + 1]
+    return [s["H"] + k - 1, s["W"] + k - 1]
+
+
+def algorithmic_flops(s):
+    """2 x multiply-adds over the conv outputs the method must compute (for
+    the double max-pool only the kept 4*floor(L/4) region)."""
+    dims = conv_out_dims(s)
+    if s["red"] == "maxpool2_x2":
+        dims = [4 * (L // 4) for L in dims]
+    taps = (s["C_in"] // s["groups"]) * s["k"] ** (3 if s["conv"] == "conv3d" else 2)
+    return 2.0 * s["N"] * s["C_out"] * math.prod(dims) * taps
+
+
+def out_shape(s):
+    dims = conv_out_dims(s)
+    if s["red"] == "mean_spatial":
+        return (s["N"], s["C_out"])
+    if s["red"] == "maxpool2_x2":
+        return (s["N"], s["C_out"], *[(L // 2) // 2 for L in dims])
+    return (s["N"], s["C_out"], *dims)
+
+
+def compulsory_bytes(s):
+    shp = wl.input_shapes(s)
+    n = sum(math.prod(v) for v in shp.values() if v)
+    return 4.0 * (n + math.prod(out_shape(s)))
+
+
+def peaks():
+    p = {}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+    hbm = p.get("hbm_gbs")
+    sm_mhz = p.get("sm_max_mhz") or 2070.0
+    src = "measured" if hbm else "fallback"
+    if not hbm:
+        hbm = 6800.0
+    fp32 = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
+    return dict(hbm_gbs=hbm, fp32_tflops=fp32, sm_max_mhz=sm_mhz, source=src)
+
+
+def roofline_ms(s, pk):
+    t_c = algorithmic_flops(s) / (pk["fp32_tflops"] * 1e12)
+    t_m = compulsory_bytes(s) / (pk["hbm_gbs"] * 1e9)
+    return 1e3 * max(t_c, t_m), ("alu" if t_c >= t_m else "hbm")
+
+
+# ---- ncu traffic figure (only while the kernel source is unchanged) ------------
+
+KERNEL_SOURCES = {
+    "mean3d": "convolution_normalization_gb300/csrc/k_conv3d_mean.cu",
+    "pool3d": "convolution_normalization_gb300/csrc/k_conv3d_softmax_pool.cu",
+    "full2d": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
+}
+VARIANT_KEY = {0: "mean3d", 1: "pool3d", 2: "full2d"}
+
+
+def source_hash(key):
+    h = hashlib.sha256()
+    for p in (KERNEL_SOURCES[key], "convolution_normalization_gb300/csrc/cn_common.cuh"):
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, key):
+    """dram bytes per launch from profiles/<workload>.txt if it was captured
+    from the current kernel source (its 'source_hash' line matches)."""
+    path = os.path.join(ROOT, "profiles", f"{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"^source_hash:\s*(\S+)", txt, re.M)
+    t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
+    if not m or not t or m.group(1) != source_hash(key):
+        return None
+    return float(t.group(1))
+
+
+# ---- clocks ----------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                pw.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        busy = [s for s, p in zip(sm, pw) if p > 0.3 * max(pw)] if pw else []
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---- distributed plumbing ----------------------------------------------------------
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- oracle (CPU baseline and the reference arm) --------------------------------------
+
+def oracle_rate(spec, inp, target_s, max_samples=None):
+    """Times the fp64 oracle on a bounded number of samples; returns
+    (GFLOP/s, samples, seconds, threads)."""
+    import oracle
+    probe = min(spec["N"], 2)
+    t0 = time.perf_counter()
+    oracle.forward(spec, inp, samples=list(range(probe)))
+    per = max((time.perf_counter() - t0) / probe, 1e-6)
+    n = int(max(1, min(spec["N"], max_samples or spec["N"], target_s / per)))
+    t0 = time.perf_counter()
+    oracle.forward(spec, inp, samples=list(range(n)))
+    dt = time.perf_counter() - t0
+    flops = algorithmic_flops(wl.with_overrides(spec, N=n))
+    return flops / dt / 1e9, n, dt, oracle.num_threads()
+
+
+def run_reference(args, spec):
+    world, rank, _ = dist_setup(args.gpus)
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    inp = wl.make_inputs(spec)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    _, n, _, threads = oracle_rate(spec, inp, target_s=min(budget, 2.0))
+    sub = list(range(n))
+    for _ in range(args.warmup):
+        oracle.forward(spec, inp, samples=sub)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(spec, inp, samples=sub)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    flops = algorithmic_flops(wl.with_overrides(spec, N=n))
+    val = flops / (ms / 1e3) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "GFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": spec["name"], "samples_per_step": n, "N": spec["N"]},
+        "cpu_baseline": {"value": val, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {spec['N']} samples per step"},
+        "e2e": {"value": val, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- the CUDA path ------------------------------------------------------------------------
+
+def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf):
+    def fwd():
+        plan.forward(dev["x"], dev["w"], dev["b"], dev["gamma"], dev["beta"], out, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush_buf.zero_()
+            fwd()
+    stream.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        # Hold the stream for a moment so the host queues every step before
+        # the device starts them: the per-step events then time the kernels,
+        # not host enqueue latency.
+        torch.cuda._sleep(int(min(2e9, 2e5 * steps + 2e7)))
+        for i in range(steps):
+            flush_buf.zero_()
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
+    stream.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def run_cuda(args, spec):
+    import torch
+    world, rank, local = dist_setup(args.gpus)
+    from convolution_normalization_gb300 import build as cn_build
+    if rank == 0:
+        cn_build.build()
+    barrier(world)
+    from convolution_normalization_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    pk = peaks()
+    inp = wl.make_inputs(spec)
+    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
+    plan = B.Plan(spec)
+    info = plan.info()
+    out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    times = time_forward(B, torch, plan, dev, out, stream, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    assert plan.check_device(stream) == B.CN_OK
+
+    ms_rank = statistics.mean(times)
+    ms = max_over_ranks(world, ms_rank)
+    flops = algorithmic_flops(spec)
+    value = world * flops / (ms / 1e3) / 1e9
+    rl_ms, bound = roofline_ms(spec, pk)
+    key = VARIANT_KEY[info["variant"]]
+
+    # dominant kernel: for single-launch variants the step is that kernel
+    achieved = flops / (ms_rank / 1e3) / 1e12
+    roofline = {"bound": bound if bound == "hbm" else "alu",
+                "achieved": achieved if bound != "hbm" else compulsory_bytes(spec) / (ms_rank / 1e3) / 1e9,
+                "peak": pk["fp32_tflops"] if bound != "hbm" else pk["hbm_gbs"],
+                "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
+                "traffic": profiled_traffic(spec["name"], key),
+                "kernel": info["kernel_names"].split(",")[0],
+                "roofline_ms": rl_ms,
+                "frac_of_step_roofline": rl_ms / ms_rank,
+                "peak_source": f"FP32: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                               f"{pk['sm_max_mhz']:.0f} MHz; HBM: {pk['source']} {pk['hbm_gbs']} GB/s"}
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+
+    # end to end through the host-buffer entry point
+    hp = {k: (torch.from_numpy(v).pin_memory() if v is not None else None) for k, v in inp.items()}
+    hout = torch.empty(plan.out_shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 30))
+    for _ in range(2):
+        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
+    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
+    h2d = sum(v.numel() * 4 for v in hp.values() if v is not None)
+    e2e = {"value": world * flops / e2e_s / 1e9, "unit": "GFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 4,
+           "ms_per_step": e2e_s * 1e3}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded PCG64: x~N(0,1), w,b~U(+-1/sqrt(fan_in)), gamma=1+0.1N, beta=0.1N)",
+        "config": {"workload": spec["name"], "N": spec["N"], "C_in": spec["C_in"],
+                   "C_out": spec["C_out"], "D": spec["D"], "H": spec["H"], "W": spec["W"],
+                   "k": spec["k"], "per_rank_batch": spec["N"],
+                   "l2": "flushed before every timed step (256 MB write)"},
+        "roofline": roofline,
+        "gpu_launches": args.steps * info["launches_per_forward"],
+        "kernels": info["kernel_names"],
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+
+    if rank == 0 and not args.no_extras:
+        extras = []
+        for s2 in wl.WORKLOADS:
+            if s2["name"] == spec["name"]:
+                continue
+            extras.append(measure_extra(B, torch, s2, pk, stream, flush))
+        line["workloads"] = extras
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, n, dt, thr = oracle_rate(spec, inp, target_s=12.0)
+        line["cpu_baseline"] = {"value": rate, "unit": "GFLOP/s", "cores": thr, "kind": "oracle",
+                                "sample": f"{n} of {spec['N']} samples, {dt:.1f} s"}
+    plan.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_extra(B, torch, s, pk, stream, flush):
+    inp = wl.make_inputs(s)
+    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
+    plan = B.Plan(s)
+    out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+    big = compulsory_bytes(s) > 200e6
+    times = time_forward(B, torch, plan, dev, out, stream, 30, 5, flush)
+    ms = statistics.median(times)
+    rl_ms, bound = roofline_ms(s, pk)
+    info = plan.info()
+    plan.close()
+    del dev, out
+    return {"workload": s["name"], "ms": ms, "gflops": algorithmic_flops(s) / ms / 1e6,
+            "roofline_ms": rl_ms, "bound": bound, "frac": rl_ms / ms,
+            "launches": info["launches_per_forward"], "kernels": info["kernel_names"],
+            "l2": "flushed" if not big else "flushed (inputs larger than L2)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    spec = wl.WORKLOAD_BY_NAME[args.workload]
+    if args.impl == "reference":
+        run_reference(args, spec)
+    else:
+        run_cuda(args, spec)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,441 @@
+// C-ABI layer: descriptor validation, plans, dispatch to the kernel variants.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "cn_internal.h"
+
+using namespace cn;
+
+namespace {
+
+enum Variant { V_MEAN3D = 0, V_POOL3D = 1, V_FULL2D = 2 };
+
+struct HostStage {
+    float *x = nullptr, *w = nullptr, *b = nullptr, *gamma = nullptr, *beta = nullptr,
+          *out = nullptr;
+};
+
+}  // namespace
+
+struct conv_norm_plan_s {
+    conv_norm_desc d;
+    int variant;
+    int device;
+    int64_t out_numel;
+    int64_t x_numel, w_numel;
+    void *ws = nullptr;  // [error flag | variant workspace]
+    size_t ws_bytes = 0;
+    int *err_flag = nullptr;
+    Mean3dArgs mean_args;
+    Mean3dConfig mean_cfg;
+    Pool3dArgs pool_args;
+    Pool3dConfig pool_cfg;
+    Full2dArgs full_args;
+    Full2dConfig full_cfg;
+    HostStage stage;
+};
+
+namespace {
+
+bool is_finite(float v) { return std::isfinite(v); }
+
+// Malformed problems -> CN_ERR_INVALID_ARG.
+int check_wellformed(const conv_norm_desc &d) {
+    if (d.conv < CN_CONV3D || d.conv > CN_CONVT2D) return CN_ERR_INVALID_ARG;
+    if (d.N < 0 || d.C_in < 1 || d.C_out < 1 || d.H < 1 || d.W < 1 || d.D < 1 || d.k < 1 ||
+        d.groups < 1)
+        return CN_ERR_INVALID_ARG;
+    if (d.C_in % d.groups || d.C_out % d.groups) return CN_ERR_INVALID_ARG;
+    if (d.conv != CN_CONV3D && d.D != 1) return CN_ERR_INVALID_ARG;
+    if (d.conv != CN_CONVT2D) {
+        if (d.H < d.k || d.W < d.k) return CN_ERR_INVALID_ARG;
+        if (d.conv == CN_CONV3D && d.D < d.k) return CN_ERR_INVALID_ARG;
+    }
+    if (d.has_bias != 0 && d.has_bias != 1) return CN_ERR_INVALID_ARG;
+    if (d.act < CN_ACT_NONE || d.act > CN_ACT_SOFTMAX_C) return CN_ERR_INVALID_ARG;
+    if (d.norm < CN_NORM_NONE || d.norm > CN_NORM_INSTANCE) return CN_ERR_INVALID_ARG;
+    if (d.red < CN_RED_NONE || d.red > CN_RED_MAXPOOL2_X2) return CN_ERR_INVALID_ARG;
+    if (d.affine != 0 && d.affine != 1) return CN_ERR_INVALID_ARG;
+    if (d.norm == CN_NORM_GROUP && (d.num_groups < 1 || d.C_out % d.num_groups))
+        return CN_ERR_INVALID_ARG;
+    if (!is_finite(d.eps) || !is_finite(d.post_scale)) return CN_ERR_INVALID_ARG;
+    if (d.norm != CN_NORM_NONE && !(d.eps > 0.0f)) return CN_ERR_INVALID_ARG;
+    if (d.red == CN_RED_MAXPOOL2_X2 && d.conv != CN_CONV3D) return CN_ERR_INVALID_ARG;
+    // 32-bit index limits of the kernels
+    const double big = (double)d.N * d.C_out * d.D * (double)(d.H + d.k) * (d.W + d.k);
+    const double bigx = (double)d.N * d.C_in * d.D * (double)d.H * d.W;
+    if (big > 4.0e18 || bigx > 4.0e18) return CN_ERR_INVALID_ARG;
+    return CN_OK;
+}
+
+void conv_dims(const conv_norm_desc &d, int &Do, int &Ho, int &Wo) {
+    if (d.conv == CN_CONVT2D) {
+        Do = 1;
+        Ho = d.H + d.k - 1;
+        Wo = d.W + d.k - 1;
+    } else {
+        Do = d.conv == CN_CONV3D ? d.D - d.k + 1 : 1;
+        Ho = d.H - d.k + 1;
+        Wo = d.W - d.k + 1;
+    }
+}
+
+int pick_variant(const conv_norm_desc &d, int &variant) {
+    if (d.red == CN_RED_MEAN_SPATIAL) {
+        if (d.conv != CN_CONV3D || d.act == CN_ACT_SOFTMAX_C) return CN_ERR_UNSUPPORTED;
+        variant = V_MEAN3D;
+        return CN_OK;
+    }
+    if (d.red == CN_RED_MAXPOOL2_X2) {
+        if (d.act != CN_ACT_SOFTMAX_C || d.norm != CN_NORM_NONE) return CN_ERR_UNSUPPORTED;
+        variant = V_POOL3D;
+        return CN_OK;
+    }
+    if (d.conv == CN_CONV3D || d.act == CN_ACT_SOFTMAX_C) return CN_ERR_UNSUPPORTED;
+    variant = V_FULL2D;
+    return CN_OK;
+}
+
+int plan_variant(conv_norm_plan_s &p) {
+    switch (p.variant) {
+        case V_MEAN3D:
+            return mean3d_plan(p.d, p.mean_args, p.mean_cfg);
+        case V_POOL3D:
+            return pool3d_plan(p.d, p.pool_args, p.pool_cfg);
+        default:
+            return full2d_plan(p.d, p.full_args, p.full_cfg);
+    }
+}
+
+int64_t numel_out(const conv_norm_desc &d) {
+    int64_t dims[5];
+    int nd = 0;
+    conv_norm_output_shape(&d, dims, &nd);
+    int64_t n = 1;
+    for (int i = 0; i < nd; ++i) n *= dims[i];
+    return n;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char *conv_norm_status_string(int s) {
+    switch (s) {
+        case CN_OK: return "ok";
+        case CN_ERR_INVALID_ARG: return "invalid argument";
+        case CN_ERR_UNSUPPORTED: return "unsupported problem";
+        case CN_ERR_CUDA: return "CUDA error";
+        case CN_ERR_TIMEOUT: return "device wait timed out";
+        case CN_ERR_DEVICE_CHECK: return "device bounds check failed";
+        case CN_ERR_ALLOC: return "allocation failed";
+        default: return "unknown status";
+    }
+}
+
+int conv_norm_output_shape(const conv_norm_desc *d, int64_t dims[5], int *ndim) {
+    if (!d || !dims || !ndim) return CN_ERR_INVALID_ARG;
+    int st = check_wellformed(*d);
+    if (st != CN_OK) return st;
+    int Do, Ho, Wo;
+    conv_dims(*d, Do, Ho, Wo);
+    dims[0] = d->N;
+    dims[1] = d->C_out;
+    if (d->red == CN_RED_MEAN_SPATIAL) {
+        *ndim = 2;
+    } else if (d->red == CN_RED_MAXPOOL2_X2) {
+        dims[2] = Do / 4;
+        dims[3] = Ho / 4;
+        dims[4] = Wo / 4;
+        *ndim = 5;
+    } else if (d->conv == CN_CONV3D) {
+        dims[2] = Do;
+        dims[3] = Ho;
+        dims[4] = Wo;
+        *ndim = 5;
+    } else {
+        dims[2] = Ho;
+        dims[3] = Wo;
+        *ndim = 4;
+    }
+    return CN_OK;
+}
+
+int conv_norm_desc_validate(const conv_norm_desc *d) {
+    if (!d) return CN_ERR_INVALID_ARG;
+    int st = check_wellformed(*d);
+    if (st != CN_OK) return st;
+    conv_norm_plan_s *p = new (std::nothrow) conv_norm_plan_s();
+    if (!p) return CN_ERR_ALLOC;
+    p->d = *d;
+    st = pick_variant(*d, p->variant);
+    if (st == CN_OK) st = plan_variant(*p);
+    delete p;
+    return st;
+}
+
+int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
+    if (!d || !out) return CN_ERR_INVALID_ARG;
+    *out = nullptr;
+    int st = check_wellformed(*d);
+    if (st != CN_OK) return st;
+    conv_norm_plan_s *p = new (std::nothrow) conv_norm_plan_s();
+    if (!p) return CN_ERR_ALLOC;
+    p->d = *d;
+    st = pick_variant(*d, p->variant);
+    if (st == CN_OK) st = plan_variant(*p);
+    if (st != CN_OK) {
+        delete p;
+        return st;
+    }
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return CN_ERR_CUDA;
+    }
+    p->out_numel = numel_out(*d);
+    p->x_numel = (int64_t)d->N * d->C_in * d->D * d->H * d->W;
+    const int kd = d->conv == CN_CONV3D ? d->k : 1;
+    p->w_numel = (int64_t)d->C_out * (d->C_in / d->groups) * kd * d->k * d->k;
+    size_t vws = 0;
+    switch (p->variant) {
+        case V_MEAN3D:
+            st = mean3d_prepare(p->mean_cfg);
+            vws = mean3d_workspace(p->mean_args);
+            break;
+        case V_POOL3D:
+            st = pool3d_prepare(p->pool_cfg);
+            vws = 0;
+            break;
+        default:
+            st = full2d_prepare(p->full_cfg);
+            vws = full2d_workspace(p->full_args);
+            break;
+    }
+    if (st != CN_OK) {
+        cudaGetLastError();
+        delete p;
+        return st;
+    }
+    p->ws_bytes = 256 + vws;
+    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return CN_ERR_ALLOC;
+    }
+    if (cudaMemset(p->ws, 0, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p->ws);
+        delete p;
+        return CN_ERR_CUDA;
+    }
+    p->err_flag = static_cast<int *>(p->ws);
+    char *vbase = static_cast<char *>(p->ws) + 256;
+    switch (p->variant) {
+        case V_MEAN3D: {
+            Mean3dArgs &a = p->mean_args;
+            const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
+            a.partial = reinterpret_cast<double *>(vbase);
+            a.tickets = reinterpret_cast<int *>(vbase + ((part + 255) & ~(size_t)255));
+            break;
+        }
+        case V_POOL3D:
+            break;
+        default:
+            full2d_bind_workspace(p->full_args, vbase, p->err_flag);
+            break;
+    }
+    *out = p;
+    return CN_OK;
+}
+
+void conv_norm_plan_destroy(conv_norm_plan p) {
+    if (!p) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    cudaFree(p->ws);
+    cudaFree(p->stage.x);
+    cudaFree(p->stage.w);
+    cudaFree(p->stage.b);
+    cudaFree(p->stage.gamma);
+    cudaFree(p->stage.beta);
+    cudaFree(p->stage.out);
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    cudaGetLastError();
+    delete p;
+}
+
+size_t conv_norm_workspace_bytes(conv_norm_plan p) { return p ? p->ws_bytes : 0; }
+
+int conv_norm_plan_info(conv_norm_plan p, conv_norm_info *info) {
+    if (!p || !info) return CN_ERR_INVALID_ARG;
+    memset(info, 0, sizeof(*info));
+    info->variant = p->variant;
+    info->out_numel = p->out_numel;
+    info->workspace_bytes = p->ws_bytes;
+    switch (p->variant) {
+        case V_MEAN3D:
+            info->launches_per_forward = p->d.N > 0 ? 1 : 0;
+            info->kernel_names = p->mean_cfg.name;
+            info->grid_ctas = p->mean_cfg.grid;
+            info->threads_per_cta = p->mean_cfg.threads;
+            info->smem_bytes_per_cta = p->mean_cfg.smem;
+            break;
+        case V_POOL3D:
+            info->launches_per_forward = p->pool_cfg.grid > 0 ? 1 : 0;
+            info->kernel_names = p->pool_cfg.name;
+            info->grid_ctas = p->pool_cfg.grid;
+            info->threads_per_cta = p->pool_cfg.threads;
+            info->smem_bytes_per_cta = p->pool_cfg.smem;
+            break;
+        default:
+            info->launches_per_forward = full2d_launches(p->full_cfg, p->full_args);
+            info->kernel_names = p->full_cfg.names;
+            info->grid_ctas = p->full_cfg.grid;
+            info->threads_per_cta = p->full_cfg.threads;
+            info->smem_bytes_per_cta = p->full_cfg.smem;
+            break;
+    }
+    return CN_OK;
+}
+
+static int forward_impl(conv_norm_plan p, const float *x, const float *w, const float *b,
+                        const float *gamma, const float *beta, float *out, cudaStream_t s) {
+    const conv_norm_desc &d = p->d;
+    const bool need_aff = d.affine && d.norm != CN_NORM_NONE;
+    // An empty problem launches nothing; its (zero-size) tensors may have null pointers.
+    if (d.N == 0 || p->out_numel == 0) return CN_OK;
+    if (!x || !w || !out) return CN_ERR_INVALID_ARG;
+    if ((b != nullptr) != (d.has_bias == 1)) return CN_ERR_INVALID_ARG;
+    if (need_aff && (!gamma || !beta)) return CN_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16) || !aligned(w, 4)) return CN_ERR_INVALID_ARG;
+    if (!need_aff) gamma = beta = nullptr;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    if (cur != p->device && cudaSetDevice(p->device) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    int st;
+    switch (p->variant) {
+        case V_MEAN3D: {
+            Mean3dArgs a = p->mean_args;
+            a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
+            st = mean3d_launch(p->mean_cfg, a, s);
+            break;
+        }
+        case V_POOL3D: {
+            Pool3dArgs a = p->pool_args;
+            a.x = x; a.w = w; a.b = b; a.out = out;
+            st = pool3d_launch(p->pool_cfg, a, s);
+            break;
+        }
+        default: {
+            Full2dArgs a = p->full_args;
+            a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
+            st = full2d_launch(p->full_cfg, a, s);
+            break;
+        }
+    }
+    if (st != CN_OK) cudaGetLastError();
+    if (cur != p->device) cudaSetDevice(cur);
+    return st;
+}
+
+int conv_norm_forward(conv_norm_plan p, const float *x, const float *w, const float *b,
+                      const float *gamma, const float *beta, float *out, void *stream) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    return forward_impl(p, x, w, b, gamma, beta, out, static_cast<cudaStream_t>(stream));
+}
+
+static int stage_alloc(float **dst, int64_t n) {
+    if (*dst || n <= 0) return CN_OK;
+    if (cudaMalloc(reinterpret_cast<void **>(dst), (size_t)n * sizeof(float)) != cudaSuccess) {
+        cudaGetLastError();
+        *dst = nullptr;
+        return CN_ERR_ALLOC;
+    }
+    return CN_OK;
+}
+
+int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, const float *b,
+                           const float *gamma, const float *beta, float *out, void *stream) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    const conv_norm_desc &d = p->d;
+    const bool need_aff = d.affine && d.norm != CN_NORM_NONE;
+    if (d.N == 0 || p->out_numel == 0) return CN_OK;
+    if (!x || !w || !out) return CN_ERR_INVALID_ARG;
+    if ((b != nullptr) != (d.has_bias == 1)) return CN_ERR_INVALID_ARG;
+    if (need_aff && (!gamma || !beta)) return CN_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    if (cur != p->device) cudaSetDevice(p->device);
+    int st = CN_OK;
+    HostStage &hs = p->stage;
+    if (st == CN_OK) st = stage_alloc(&hs.x, p->x_numel);
+    if (st == CN_OK) st = stage_alloc(&hs.w, p->w_numel);
+    if (st == CN_OK && b) st = stage_alloc(&hs.b, d.C_out);
+    if (st == CN_OK && need_aff) st = stage_alloc(&hs.gamma, d.C_out);
+    if (st == CN_OK && need_aff) st = stage_alloc(&hs.beta, d.C_out);
+    if (st == CN_OK) st = stage_alloc(&hs.out, p->out_numel);
+    bool ok = st == CN_OK;
+    ok = ok && cudaMemcpyAsync(hs.x, x, p->x_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(hs.w, w, p->w_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    if (b) ok = ok && cudaMemcpyAsync(hs.b, b, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    if (need_aff) {
+        ok = ok && cudaMemcpyAsync(hs.gamma, gamma, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(hs.beta, beta, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    }
+    if (ok) {
+        st = forward_impl(p, hs.x, hs.w, b ? hs.b : nullptr, need_aff ? hs.gamma : nullptr,
+                          need_aff ? hs.beta : nullptr, hs.out, s);
+        ok = st == CN_OK;
+    } else if (st == CN_OK) {
+        st = CN_ERR_CUDA;
+    }
+    if (ok) {
+        ok = cudaMemcpyAsync(out, hs.out, p->out_numel * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
+             cudaStreamSynchronize(s) == cudaSuccess;
+        if (!ok) st = CN_ERR_CUDA;
+    }
+    if (!ok) cudaGetLastError();
+    if (cur != p->device) cudaSetDevice(cur);
+    return st;
+}
+
+int conv_norm_plan_check_device(conv_norm_plan p, void *stream) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != p->device) cudaSetDevice(p->device);
+    int flag = 0;
+    int st = CN_OK;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+        cudaMemcpy(&flag, p->err_flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        st = CN_ERR_CUDA;
+    } else if (flag != 0) {
+        const int zero = 0;
+        cudaMemcpy(p->err_flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        st = flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
+    }
+    if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
+    return st;
+}
+
+}  // extern "C"

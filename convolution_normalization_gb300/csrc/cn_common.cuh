@@ -1,0 +1,92 @@
+// Device helpers shared by the conv_norm kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define CN_DEV __device__ __forceinline__
+#define CN_PRAGMA(x) _Pragma(#x)
+#define CN_UNROLL(n) CN_PRAGMA(unroll n)
+// Unroll depth of the kernel-tap loops outside the innermost (kw, output)
+// block.  1 keeps each loop body a few KB of code so it stays resident in
+// the instruction cache; full unrolling repeats the FFMA block K^2 (or K^3)
+// times.
+#ifndef CN_TAP_UNROLL
+#define CN_TAP_UNROLL 1
+#endif
+
+namespace cn {
+
+// ---- activations -----------------------------------------------------------
+enum { ACT_NONE = 0, ACT_HARDSWISH = 1, ACT_GELU = 2, ACT_SOFTMAX = 3 };
+
+// HardSwish: v * clamp(v + 3, 0, 6) / 6  (l2_p27, HardSwish definition).
+CN_DEV float hardswish(float v) {
+    return v * fminf(fmaxf(v + 3.0f, 0.0f), 6.0f) * (1.0f / 6.0f);
+}
+// Exact GELU: 0.5 v (1 + erf(v / sqrt 2))  (l2_p19, nn.GELU default form).
+CN_DEV float gelu_erf(float v) {
+    return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+}
+CN_DEV float apply_act(int act, float v) {
+    if (act == ACT_HARDSWISH) return hardswish(v);
+    if (act == ACT_GELU) return gelu_erf(v);
+    return v;
+}
+
+// ---- running statistics ------------------------------------------------------
+// (count, mean, M2) triples merged with the pairwise update of Chan et al.:
+//   n = na + nb, d = mb - ma, mean = ma + d nb / n, M2 = M2a + M2b + d^2 na nb / n.
+// Merging in a fixed order makes every reduction deterministic.
+template <typename T>
+struct Moments {
+    T n, mean, m2;
+};
+template <typename T>
+CN_DEV Moments<T> merge(Moments<T> a, Moments<T> b) {
+    T n = a.n + b.n;
+    if (n == T(0)) return a;
+    T d = b.mean - a.mean;
+    T fb = b.n / n;
+    Moments<T> r;
+    r.n = n;
+    r.mean = a.mean + d * fb;
+    r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
+    return r;
+}
+// Butterfly merge over the 32 lanes of a warp; every lane ends with the result.
+CN_DEV Moments<float> warp_merge(Moments<float> m) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        Moments<float> o;
+        o.n = __shfl_xor_sync(0xffffffffu, m.n, off);
+        o.mean = __shfl_xor_sync(0xffffffffu, m.mean, off);
+        o.m2 = __shfl_xor_sync(0xffffffffu, m.m2, off);
+        // Lower lane is always the left operand so both lanes compute the
+        // same value bit for bit.
+        m = ((threadIdx.x & off) == 0) ? merge(m, o) : merge(o, m);
+    }
+    return m;
+}
+
+// ---- cp.async (LDGSTS) staging with zero fill --------------------------------
+CN_DEV uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Copies 16 bytes global -> shared; when !pred the destination is zero-filled
+// and the source is not read.
+CN_DEV void cp_async16(void *smem, const void *gmem, bool pred) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)),
+                 "l"(gmem), "r"(pred ? 16 : 0));
+}
+CN_DEV void cp_async4(void *smem, const void *gmem, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(smem)),
+                 "l"(gmem), "r"(pred ? 4 : 0));
+}
+CN_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+CN_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+CN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::); }
+
+CN_DEV double ldcg_f64(const double *p) { return __ldcg(p); }
+
+}  // namespace cn

@@ -1,0 +1,114 @@
+// Internal interfaces between the C-ABI layer (cn_api.cu) and the kernel
+// translation units.  Not installed; not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/conv_norm.h"
+
+namespace cn {
+
+// ---------------------------------------------------------------------------
+// Variant 0: 3-D conv -> activation -> (GroupNorm | InstanceNorm | none)
+// -> spatial mean.  One launch; the conv tensor is never written.
+struct Mean3dArgs {
+    const float *x, *w, *b, *gamma, *beta;
+    float *out;
+    int N, Ci, Co, D, H, W, Do, Ho, Wo;
+    int nseg;         // W-segments of RW outputs per output row
+    int rows;         // Do * Ho * nseg thread-rows per sample
+    int rows_per_cta; // 32 * wrows
+    int nchunks;      // ceil(rows / rows_per_cta)
+    int ncob;         // co blocks per sample
+    int wco;          // warps (co-slices of 4 channels) per co block
+    int wrows;        // row groups per CTA
+    int planes_max;   // input depth planes staged per CTA
+    int pitch;        // shared-memory row pitch in floats
+    int vec16;        // 1: 16-byte cp.async staging is legal
+    int act, norm, G, affine;
+    float eps, post_scale;
+    double *partial;  // [N][nchunks][Co][3]  (count, mean, M2)
+    int *tickets;     // [N], zero between launches
+};
+typedef void (*Mean3dKernel)(Mean3dArgs);
+struct Mean3dConfig {
+    Mean3dKernel kern;
+    const char *name;
+    int K, RW;
+    int threads, smem;
+    int grid;
+};
+// Chooses tiling + instantiation; fills the geometry fields of args.
+// Returns CN_OK or CN_ERR_UNSUPPORTED.
+int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+size_t mean3d_workspace(const Mean3dArgs &a);
+int mean3d_prepare(const Mean3dConfig &cfg);  // sets smem attribute (needs a device)
+int mean3d_launch(const Mean3dConfig &cfg, const Mean3dArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Variant 1: 3-D conv -> channel softmax -> MaxPool3d(2,2) twice (= one
+// 4x4x4 stride-4 max pool).  One launch, only the pooled output is written.
+struct Pool3dArgs {
+    const float *x, *w, *b;
+    float *out;
+    int N, Ci, D, H, W, Do, Ho, Wo;
+    int Pd, Ph, Pw;      // pooled extents: floor(Do/4), floor(Ho/4), floor(Wo/4)
+    long long nvox;      // N * Pd * Ph * Pw
+    int vox_per_cta;     // pooled voxels per CTA (16 threads each)
+    int pw_pitch;        // shared-memory patch row pitch (floats)
+    int vox_stride;      // floats per staged voxel patch
+};
+typedef void (*Pool3dKernel)(Pool3dArgs);
+struct Pool3dConfig {
+    Pool3dKernel kern;
+    const char *name;
+    int threads, smem, grid;
+};
+int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &args, Pool3dConfig &cfg);
+int pool3d_prepare(const Pool3dConfig &cfg);
+int pool3d_launch(const Pool3dConfig &cfg, const Pool3dArgs &a, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Variant 2: 2-D conv or transposed conv (groups) -> activation ->
+// GroupNorm/InstanceNorm/none -> post scale, full output.
+// Kernel A computes conv + activation for a tile, writes the pre-norm value
+// to out and per-(n, c, tile) moments; the last CTA of each sample merges
+// the moments into per-channel coefficients.  Kernel B rewrites out in place
+// as (y - mu) * a + bb.
+struct Full2dArgs {
+    const float *x, *w, *b, *gamma, *beta;
+    float *out;
+    int N, Ci, Co, H, W, Ho, Wo;
+    int Cig, Cog;         // conv channels per group (in / out)
+    int TR, NT;           // CTA tile: TR output rows x NT row segments
+    int row_tiles, col_tiles, ncob, ntiles;
+    int wco, wsp;         // warps: channel slices x spatial groups
+    int cib, nchunk;      // input channels per pipeline stage, stages
+    int rows_in, cols_in, pitch;
+    int stage_floats;     // floats per pipeline stage (input + filter)
+    int act, norm, NG, affine;
+    float eps, post_scale;
+    int apply_needed, vec4;
+    long long S;          // Ho * Wo
+    double *partial;      // [N][Co][ntiles][3]
+    float4 *coef;         // [N][Co]: (mu, a, bb, 0)
+    int *tickets;         // [N]
+    int *err;
+};
+typedef void (*Full2dKernel)(Full2dArgs);
+struct Full2dConfig {
+    Full2dKernel kern;
+    const char *names;
+    int K, RW, transposed;
+    int threads, smem, grid;
+    int apply_threads, apply_grid_x, apply_grid_y;
+};
+int full2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
+size_t full2d_workspace(const Full2dArgs &a);
+void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag);
+int full2d_prepare(const Full2dConfig &cfg);
+int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a);
+int full2d_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s);
+
+}  // namespace cn

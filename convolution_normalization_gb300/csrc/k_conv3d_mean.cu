@@ -1,0 +1,374 @@
+// Variant 0: Conv3d -> activation -> GroupNorm/InstanceNorm -> mean over D,H,W
+// in ONE launch, without writing the conv tensor.
+//
+// Method (l2_p27, Conv3d -> HardSwish -> GroupNorm -> mean): the mean over
+// space of a GroupNorm output only needs, per channel c of sample n, the
+// spatial mean m_c and the spread of the activated conv values:
+//   out[n,c] = gamma_c * (m_c - mu_g) / sqrt(var_g + eps) + beta_c,
+// with mu_g, var_g the (population) mean and variance over the group's
+// channels and all positions.  So the kernel computes the conv + activation
+// in registers, reduces each channel to (count, mean, M2) moments, and the
+// last CTA of each sample merges the moments (fixed order, fp64) and writes
+// the (N, C_out) result.
+//
+// Mapping: each thread owns COT=4 output channels x RW consecutive outputs of
+// one output row (d, h, w-segment); lanes of a warp own 32 consecutive rows
+// of the sample's flattened (d, h, segment) row list; warps of a CTA split
+// the channel block.  The CTA stages every input depth plane its rows need,
+// for all input channels, plus the filter of its channel block, in shared
+// memory once (cp.async, zero-filled pad columns).  The inner loop per
+// (ci, kd, kh) loads one input row segment into registers and issues
+// 4*K*RW FFMAs per thread against float4-broadcast weights.
+#include "cn_common.cuh"
+#include "cn_internal.h"
+
+#include <algorithm>
+#include <cstdlib>
+
+namespace cn {
+
+namespace {
+constexpr int COT = 4;
+
+template <int K, int RW>
+__global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    constexpr int KKK = K * K * K;
+    constexpr int LOADW = (RW + K - 1 + 3) & ~3;
+    const int COB = COT * a.wco;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cs = warp % a.wco;
+    const int rg = warp / a.wco;
+    int bid = blockIdx.x;
+    const int chunk = bid % a.nchunks;
+    bid /= a.nchunks;
+    const int cob = bid % a.ncob;
+    const int n = bid / a.ncob;
+    const int co0 = cob * COB;
+
+    const int HP = a.H * a.pitch;
+    float *sx = smem;
+    float *sw = sx + (size_t)a.Ci * a.planes_max * HP;
+    double *sred = reinterpret_cast<double *>(sw + (size_t)a.Ci * KKK * COB);
+
+    const int r_begin = chunk * a.rows_per_cta;
+    const int r_end = min(a.rows, r_begin + a.rows_per_cta);
+    const int d_lo = (r_begin / a.nseg) / a.Ho;
+    const int d_hi = ((r_end - 1) / a.nseg) / a.Ho;
+    const int np = d_hi - d_lo + K;
+
+    // ---- stage input planes [d_lo, d_lo + np) of every input channel ----
+    {
+        const float *xn = a.x + (size_t)n * a.Ci * a.D * a.H * a.W;
+        if (a.vec16) {
+            const int cpr = a.W >> 2;
+            const int total = a.Ci * np * a.H * cpr;
+            for (int i = tid; i < total; i += blockDim.x) {
+                const int c4 = i % cpr;
+                int t = i / cpr;
+                const int h = t % a.H;
+                t /= a.H;
+                const int p = t % np, ci = t / np;
+                const float *src = xn + (((size_t)ci * a.D + d_lo + p) * a.H + h) * a.W + c4 * 4;
+                float *dst = sx + ((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + c4 * 4;
+                cp_async16(dst, src, true);
+            }
+        } else {
+            const int total = a.Ci * np * a.H * a.W;
+            for (int i = tid; i < total; i += blockDim.x) {
+                const int c = i % a.W;
+                int t = i / a.W;
+                const int h = t % a.H;
+                t /= a.H;
+                const int p = t % np, ci = t / np;
+                const float *src = xn + (((size_t)ci * a.D + d_lo + p) * a.H + h) * a.W + c;
+                float *dst = sx + ((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + c;
+                cp_async4(dst, src, true);
+            }
+        }
+        cp_async_commit();
+        const int padw = a.pitch - a.W;
+        const int totalz = a.Ci * np * a.H * padw;
+        for (int i = tid; i < totalz; i += blockDim.x) {
+            const int c = i % padw;
+            int t = i / padw;
+            const int h = t % a.H;
+            t /= a.H;
+            const int p = t % np, ci = t / np;
+            sx[((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + a.W + c] = 0.0f;
+        }
+        // filter of this channel block, transposed to [ci][tap][co]
+        const int totalw = a.Ci * KKK * COB;
+        for (int i = tid; i < totalw; i += blockDim.x) {
+            const int col = i % COB, t = i / COB;
+            sw[i] = __ldg(a.w + (size_t)(co0 + col) * a.Ci * KKK + t);
+        }
+        cp_async_wait_all();
+        __syncthreads();
+    }
+
+    // ---- mainloop ----
+    int r = r_begin + rg * 32 + lane;
+    const bool rvalid = r < r_end;
+    if (!rvalid) r = r_end - 1;
+    const int seg = r % a.nseg;
+    const int t0 = r / a.nseg;
+    const int h = t0 % a.Ho, d = t0 / a.Ho;
+
+    float acc[COT][RW];
+#pragma unroll
+    for (int c = 0; c < COT; ++c)
+#pragma unroll
+        for (int i = 0; i < RW; ++i) acc[c][i] = 0.0f;
+
+    const float *xbase = sx + ((size_t)(d - d_lo) * a.H + h) * a.pitch + seg * RW;
+    const float4 *wbase = reinterpret_cast<const float4 *>(sw) + cs;
+    const int ws4 = a.wco;  // float4 stride between taps
+    for (int ci = 0; ci < a.Ci; ++ci) {
+        const float *xc = xbase + (size_t)ci * a.planes_max * HP;
+        const float4 *wc = wbase + (size_t)ci * KKK * ws4;
+        CN_UNROLL(CN_TAP_UNROLL)
+        for (int kd = 0; kd < K; ++kd) {
+            CN_UNROLL(CN_TAP_UNROLL)
+            for (int kh = 0; kh < K; ++kh) {
+                const float *xp = xc + kd * HP + kh * a.pitch;
+                float xr[LOADW];
+#pragma unroll
+                for (int j = 0; j < LOADW / 4; ++j) {
+                    const float4 v = *reinterpret_cast<const float4 *>(xp + 4 * j);
+                    xr[4 * j + 0] = v.x;
+                    xr[4 * j + 1] = v.y;
+                    xr[4 * j + 2] = v.z;
+                    xr[4 * j + 3] = v.w;
+                }
+#pragma unroll
+                for (int kw = 0; kw < K; ++kw) {
+                    const float4 wv = wc[((kd * K + kh) * K + kw) * ws4];
+#pragma unroll
+                    for (int i = 0; i < RW; ++i) {
+                        const float xv = xr[i + kw];
+                        acc[0][i] = fmaf(xv, wv.x, acc[0][i]);
+                        acc[1][i] = fmaf(xv, wv.y, acc[1][i]);
+                        acc[2][i] = fmaf(xv, wv.z, acc[2][i]);
+                        acc[3][i] = fmaf(xv, wv.w, acc[3][i]);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- epilogue: bias + activation, per-channel moments ----
+    const int wbase_col = seg * RW;
+#pragma unroll
+    for (int c = 0; c < COT; ++c) {
+        const int co = co0 + cs * COT + c;
+        const float bias = a.b ? __ldg(a.b + co) : 0.0f;
+        float s = 0.0f, cnt = 0.0f;
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            const float v = apply_act(a.act, acc[c][i] + bias);
+            acc[c][i] = v;
+            if (rvalid && wbase_col + i < a.Wo) {
+                s += v;
+                cnt += 1.0f;
+            }
+        }
+        const float mean = cnt > 0.0f ? s / cnt : 0.0f;
+        float m2 = 0.0f;
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            if (rvalid && wbase_col + i < a.Wo) {
+                const float dv = acc[c][i] - mean;
+                m2 = fmaf(dv, dv, m2);
+            }
+        }
+        Moments<float> m{cnt, mean, m2};
+        m = warp_merge(m);
+        if (lane == 0) {
+            double *o = sred + ((size_t)rg * COB + cs * COT + c) * 3;
+            o[0] = m.n;
+            o[1] = m.mean;
+            o[2] = m.m2;
+        }
+    }
+    __syncthreads();
+    for (int c = tid; c < COB; c += blockDim.x) {
+        Moments<double> m{0.0, 0.0, 0.0};
+        for (int g = 0; g < a.wrows; ++g) {
+            const double *o = sred + ((size_t)g * COB + c) * 3;
+            m = merge(m, Moments<double>{o[0], o[1], o[2]});
+        }
+        double *p = a.partial + (((size_t)n * a.nchunks + chunk) * a.Co + co0 + c) * 3;
+        p[0] = m.n;
+        p[1] = m.mean;
+        p[2] = m.m2;
+    }
+
+    // ---- the last CTA of sample n merges all partial moments ----
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const int prev = atomicAdd(a.tickets + n, 1);
+        s_last = (prev == a.nchunks * a.ncob - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    double *sch = reinterpret_cast<double *>(smem);  // staging no longer needed
+    for (int c = tid; c < a.Co; c += blockDim.x) {
+        Moments<double> m{0.0, 0.0, 0.0};
+        for (int ch = 0; ch < a.nchunks; ++ch) {
+            const double *p = a.partial + (((size_t)n * a.nchunks + ch) * a.Co + c) * 3;
+            m = merge(m, Moments<double>{ldcg_f64(p), ldcg_f64(p + 1), ldcg_f64(p + 2)});
+        }
+        sch[c * 3 + 0] = m.n;
+        sch[c * 3 + 1] = m.mean;
+        sch[c * 3 + 2] = m.m2;
+    }
+    __syncthreads();
+    for (int c = tid; c < a.Co; c += blockDim.x) {
+        const double mc = sch[c * 3 + 1];
+        double val;
+        if (a.norm == CN_NORM_NONE) {
+            val = mc;
+        } else {
+            const int cpg = a.Co / a.G, g = c / cpg;
+            Moments<double> mg{0.0, 0.0, 0.0};
+            for (int j = 0; j < cpg; ++j) {
+                const int cc = g * cpg + j;
+                mg = merge(mg, Moments<double>{sch[cc * 3], sch[cc * 3 + 1], sch[cc * 3 + 2]});
+            }
+            const double var = mg.m2 / mg.n;
+            const double rstd = 1.0 / sqrt(var + (double)a.eps);
+            const double ga = a.affine ? (double)a.gamma[c] : 1.0;
+            const double be = a.affine ? (double)a.beta[c] : 0.0;
+            val = ga * (mc - mg.mean) * rstd + be;
+        }
+        a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
+    }
+    if (tid == 0) a.tickets[n] = 0;
+}
+
+struct Inst {
+    int K, RW;
+    Mean3dKernel fn;
+    const char *name;
+};
+#define CN_MEAN_INST(K, RW) {K, RW, k_conv3d_act_mean<K, RW>, "k_conv3d_act_mean<" #K "," #RW ">"}
+const Inst kInst[] = {
+    CN_MEAN_INST(1, 8),  CN_MEAN_INST(1, 16), CN_MEAN_INST(2, 8),  CN_MEAN_INST(2, 16),
+    CN_MEAN_INST(3, 8),  CN_MEAN_INST(3, 16), CN_MEAN_INST(3, 14), CN_MEAN_INST(3, 29),
+    CN_MEAN_INST(4, 8),  CN_MEAN_INST(4, 16), CN_MEAN_INST(4, 14), CN_MEAN_INST(4, 29),
+};
+#undef CN_MEAN_INST
+
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return v ? atoi(v) : dflt;
+}
+}  // namespace
+
+int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
+    const int K = d.k;
+    const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
+    if (d.groups != 1 || d.C_out % COT != 0) return CN_ERR_UNSUPPORTED;
+    // pick the row width: an exact instantiation if there is one, else the
+    // segmented width with the least padding.
+    const Inst *best = nullptr;
+    double best_cost = 1e30;
+    for (const Inst &in : kInst) {
+        if (in.K != K) continue;
+        const int nseg = (Wo + in.RW - 1) / in.RW;
+        if (nseg > 1 && (in.RW % 4) != 0) continue;  // float4 row loads need aligned segments
+        const double waste = (double)nseg * in.RW / Wo;
+        const double load = 1.0 + (double)(((in.RW + K - 1 + 3) / 4) + K) / (4.0 * K * in.RW);
+        const double cost = waste * load;
+        if (cost < best_cost - 1e-12) {
+            best_cost = cost;
+            best = &in;
+        }
+    }
+    if (!best) return CN_ERR_UNSUPPORTED;
+    const int RW = best->RW;
+    const int LOADW = (RW + K - 1 + 3) & ~3;
+    a.N = d.N;
+    a.Ci = d.C_in;
+    a.Co = d.C_out;
+    a.D = d.D;
+    a.H = d.H;
+    a.W = d.W;
+    a.Do = Do;
+    a.Ho = Ho;
+    a.Wo = Wo;
+    a.nseg = (Wo + RW - 1) / RW;
+    a.rows = Do * Ho * a.nseg;
+    int wco = 1;
+    for (int c = 8; c >= 1; --c)
+        if ((d.C_out / COT) % c == 0) {
+            wco = c;
+            break;
+        }
+    a.wco = wco;
+    a.ncob = d.C_out / (COT * wco);
+    int wrows = env_int("CN_MEAN3D_WROWS", std::max(1, 8 / wco));
+    wrows = std::max(1, std::min(wrows, 8 / wco > 0 ? 8 / wco : 1));
+    a.wrows = wrows;
+    a.rows_per_cta = 32 * wrows;
+    a.nchunks = (a.rows + a.rows_per_cta - 1) / a.rows_per_cta;
+    int pm = 0;
+    for (int ch = 0; ch < a.nchunks; ++ch) {
+        const int rb = ch * a.rows_per_cta;
+        const int re = std::min(a.rows, rb + a.rows_per_cta);
+        const int dl = (rb / a.nseg) / Ho, dh = ((re - 1) / a.nseg) / Ho;
+        pm = std::max(pm, dh - dl + K);
+    }
+    a.planes_max = pm;
+    int need = std::max((a.nseg - 1) * RW + LOADW, d.W);
+    int pitch = (need + 3) & ~3;
+    if (((pitch / 4) & 1) == 0) pitch += 4;  // pitch = 4 (mod 8): conflict-free row loads
+    a.pitch = pitch;
+    a.vec16 = (d.W % 4 == 0);
+    a.act = d.act;
+    a.norm = d.norm;
+    a.G = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
+    a.affine = d.affine && d.norm != CN_NORM_NONE;
+    a.eps = d.eps;
+    a.post_scale = d.post_scale;
+    const int COB = COT * wco;
+    size_t smem = (size_t)d.C_in * pm * d.H * pitch * 4 + (size_t)d.C_in * K * K * K * COB * 4 +
+                  (size_t)wrows * COB * 3 * 8;
+    smem = std::max(smem, (size_t)d.C_out * 3 * 8);
+    if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
+    cfg.kern = best->fn;
+    cfg.name = best->name;
+    cfg.K = K;
+    cfg.RW = RW;
+    cfg.threads = 32 * wco * wrows;
+    cfg.smem = (int)smem;
+    const long long grid = (long long)d.N * a.ncob * a.nchunks;
+    if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.grid = (int)grid;
+    return CN_OK;
+}
+
+size_t mean3d_workspace(const Mean3dArgs &a) {
+    const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
+    return ((part + 255) & ~(size_t)255) + (size_t)a.N * sizeof(int);
+}
+
+int mean3d_prepare(const Mean3dConfig &cfg) {
+    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+        cudaSuccess)
+        return CN_ERR_CUDA;
+    return CN_OK;
+}
+
+int mean3d_launch(const Mean3dConfig &cfg, const Mean3dArgs &a, cudaStream_t s) {
+    if (cfg.grid == 0) return CN_OK;
+    cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
+}
+
+}  // namespace cn

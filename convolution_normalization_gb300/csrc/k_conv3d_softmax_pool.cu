@@ -1,0 +1,213 @@
+// Variant 1: Conv3d -> Softmax over channels -> MaxPool3d(2,2) -> MaxPool3d(2,2)
+// in one launch; only the pooled tensor is written.
+//
+// Method (l2_p6, Conv3d -> Softmax -> MaxPool3d x2):
+//  * two stacked 2x2x2 stride-2 floor-mode pools equal one 4x4x4 stride-4
+//    pool, since floor(floor(L/2)/2) = floor(L/4) and max is associative;
+//  * only the conv outputs inside the kept 4*floor(L/4) region are needed,
+//    so the dropped tail is never computed;
+//  * softmax is taken per voxel over the channels BEFORE the max (the two do
+//    not commute).
+// Mapping: 16 threads per pooled voxel, one per (dz, dy) row of the 4x4x4
+// window; each thread computes all CO channels x the 4 w positions of its
+// row (4*CO accumulators), applies bias + softmax per position in registers,
+// takes the max over its 4 positions, then a 4-step xor-shuffle max over the
+// voxel's 16 lanes.  Each CTA stages the (4+K-1)^3 input patch of each of its
+// voxels (all input channels) and the whole filter in shared memory.
+#include "cn_common.cuh"
+#include "cn_internal.h"
+
+#include <algorithm>
+
+namespace cn {
+namespace {
+
+template <int K, int CO>
+__global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(Pool3dArgs a) {
+    extern __shared__ __align__(16) float smem[];
+    constexpr int P = 4 + K - 1;  // patch extent per axis
+    constexpr int KKK = K * K * K;
+    const int tid = threadIdx.x;
+    const int v = tid >> 4, l16 = tid & 15;
+    const int dz = l16 >> 2, dy = l16 & 3;
+    float *sx = smem;
+    float *sw = smem + (size_t)a.vox_per_cta * a.vox_stride;
+
+    // ---- stage the filter, transposed to [ci][tap][co] ----
+    const int totalw = a.Ci * KKK * CO;
+    for (int i = tid; i < totalw; i += blockDim.x) {
+        const int co = i % CO, t = i / CO;
+        sw[i] = __ldg(a.w + (size_t)co * a.Ci * KKK + t);
+    }
+    // ---- stage each voxel's input patch ----
+    const long long vbase = (long long)blockIdx.x * a.vox_per_cta;
+    const int rows = a.vox_per_cta * a.Ci * P * P;
+    for (int rI = tid; rI < rows; rI += blockDim.x) {
+        int t = rI;
+        const int yy = t % P;
+        t /= P;
+        const int zz = t % P;
+        t /= P;
+        const int ci = t % a.Ci;
+        const int vv = t / a.Ci;
+        long long gv = vbase + vv;
+        if (gv >= a.nvox) continue;
+        const int pw = (int)(gv % a.Pw);
+        gv /= a.Pw;
+        const int ph = (int)(gv % a.Ph);
+        gv /= a.Ph;
+        const int pd = (int)(gv % a.Pd);
+        const int n = (int)(gv / a.Pd);
+        const float *src = a.x + ((((size_t)n * a.Ci + ci) * a.D + 4 * pd + zz) * a.H + 4 * ph + yy) *
+                                     (size_t)a.W + 4 * pw;
+        float *dst = sx + (size_t)vv * a.vox_stride + ((ci * P + zz) * P + yy) * a.pw_pitch;
+#pragma unroll
+        for (int c = 0; c < P; ++c) cp_async4(dst + c, src + c, true);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+
+    const long long gvox = vbase + v;
+    const bool valid = gvox < a.nvox;
+
+    float acc[CO][4];
+#pragma unroll
+    for (int c = 0; c < CO; ++c)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[c][i] = 0.0f;
+
+    const float *xv = sx + (size_t)v * a.vox_stride;
+    for (int ci = 0; ci < a.Ci; ++ci) {
+        CN_UNROLL(CN_TAP_UNROLL)
+        for (int kd = 0; kd < K; ++kd) {
+            CN_UNROLL(CN_TAP_UNROLL)
+            for (int kh = 0; kh < K; ++kh) {
+                const float *row = xv + ((ci * P + dz + kd) * P + dy + kh) * a.pw_pitch;
+                float xr[P];
+#pragma unroll
+                for (int j = 0; j < P; ++j) xr[j] = row[j];
+#pragma unroll
+                for (int kw = 0; kw < K; ++kw) {
+                    const float4 *wp =
+                        reinterpret_cast<const float4 *>(sw + ((size_t)ci * KKK + (kd * K + kh) * K + kw) * CO);
+#pragma unroll
+                    for (int c4 = 0; c4 < CO / 4; ++c4) {
+                        const float4 wv = wp[c4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            acc[4 * c4 + 0][i] = fmaf(xr[i + kw], wv.x, acc[4 * c4 + 0][i]);
+                            acc[4 * c4 + 1][i] = fmaf(xr[i + kw], wv.y, acc[4 * c4 + 1][i]);
+                            acc[4 * c4 + 2][i] = fmaf(xr[i + kw], wv.z, acc[4 * c4 + 2][i]);
+                            acc[4 * c4 + 3][i] = fmaf(xr[i + kw], wv.w, acc[4 * c4 + 3][i]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- bias + softmax over channels per position, then max ----
+    float best[CO];
+#pragma unroll
+    for (int c = 0; c < CO; ++c) best[c] = 0.0f;  // softmax values are > 0
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < CO; ++c) {
+            acc[c][i] += a.b ? __ldg(a.b + c) : 0.0f;
+            m = fmaxf(m, acc[c][i]);
+        }
+        float s = 0.0f;
+#pragma unroll
+        for (int c = 0; c < CO; ++c) {
+            acc[c][i] = __expf(acc[c][i] - m);
+            s += acc[c][i];
+        }
+        const float inv = 1.0f / s;
+#pragma unroll
+        for (int c = 0; c < CO; ++c) best[c] = fmaxf(best[c], acc[c][i] * inv);
+    }
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+#pragma unroll
+        for (int c = 0; c < CO; ++c) best[c] = fmaxf(best[c], __shfl_xor_sync(0xffffffffu, best[c], off));
+
+    if (valid) {
+        long long g = gvox;
+        const int pw = (int)(g % a.Pw);
+        g /= a.Pw;
+        const int ph = (int)(g % a.Ph);
+        g /= a.Ph;
+        const int pd = (int)(g % a.Pd);
+        const int n = (int)(g / a.Pd);
+#pragma unroll
+        for (int c = 0; c < CO; ++c) {
+            if ((c % 16) == l16) {
+                a.out[((((size_t)n * CO + c) * a.Pd + pd) * a.Ph + ph) * a.Pw + pw] = best[c];
+            }
+        }
+    }
+}
+
+struct Inst {
+    int K, CO;
+    Pool3dKernel fn;
+    const char *name;
+};
+#define CN_POOL_INST(K, CO) {K, CO, k_conv3d_softmax_pool4<K, CO>, "k_conv3d_softmax_pool4<" #K "," #CO ">"}
+const Inst kInst[] = {CN_POOL_INST(1, 16), CN_POOL_INST(2, 16), CN_POOL_INST(3, 16),
+                      CN_POOL_INST(4, 16)};
+#undef CN_POOL_INST
+}  // namespace
+
+int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
+    const Inst *in = nullptr;
+    for (const Inst &i : kInst)
+        if (i.K == d.k && i.CO == d.C_out) in = &i;
+    if (!in || d.groups != 1) return CN_ERR_UNSUPPORTED;
+    const int K = d.k, P = 4 + K - 1;
+    a.N = d.N;
+    a.Ci = d.C_in;
+    a.D = d.D;
+    a.H = d.H;
+    a.W = d.W;
+    a.Do = d.D - K + 1;
+    a.Ho = d.H - K + 1;
+    a.Wo = d.W - K + 1;
+    a.Pd = a.Do / 4;
+    a.Ph = a.Ho / 4;
+    a.Pw = a.Wo / 4;
+    a.nvox = (long long)d.N * a.Pd * a.Ph * a.Pw;
+    a.vox_per_cta = 16;
+    a.pw_pitch = P;
+    int vs = d.C_in * P * P * P;
+    vs += (16 - vs % 32 + 32) % 32;  // voxel stride = 16 (mod 32): the two voxels of a warp use other banks
+    a.vox_stride = vs;
+    const size_t smem = ((size_t)a.vox_per_cta * vs + (size_t)d.C_in * K * K * K * in->CO) * 4;
+    if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
+    const long long grid = (a.nvox + a.vox_per_cta - 1) / a.vox_per_cta;
+    if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.kern = in->fn;
+    cfg.name = in->name;
+    cfg.threads = 16 * a.vox_per_cta;
+    cfg.smem = (int)smem;
+    cfg.grid = (int)grid;
+    return CN_OK;
+}
+
+int pool3d_prepare(const Pool3dConfig &cfg) {
+    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+        cudaSuccess)
+        return CN_ERR_CUDA;
+    return CN_OK;
+}
+
+int pool3d_launch(const Pool3dConfig &cfg, const Pool3dArgs &a, cudaStream_t s) {
+    if (cfg.grid == 0) return CN_OK;
+    cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
+}
+
+}  // namespace cn

@@ -1,0 +1,185 @@
+/*
+ * conv_norm — fused convolution + normalization forward for GB300 (sm_103a).
+ *
+ * One call computes, on one GPU and on the caller's stream,
+ *
+ *   conv  ->  activation  ->  normalization  ->  post scale  ->  reduction
+ *
+ * for fp32 tensors in PyTorch's contiguous NCDHW / NCHW layout, stride 1,
+ * padding 0.  The computation is the one four problem transcripts build
+ * fused kernels for (their pages are named by problem id):
+ *
+ *   l2_p27  Conv3d(3->16, k) -> HardSwish -> GroupNorm(4) -> mean over D,H,W
+ *   l2_p17  Conv2d(64->128, k=3) -> InstanceNorm2d -> divide by 2
+ *   l2_p6   Conv3d(3->16, k=3) -> Softmax(dim=1) -> MaxPool3d(2) -> MaxPool3d(2)
+ *   l2_p19  ConvTranspose2d(64->64, k=3, s=1, groups) -> GELU -> GroupNorm(8)
+ *
+ * Status codes: every function that returns int returns CN_OK (0) on
+ * success and a negative CN_ERR_* value on failure; no function aborts the
+ * process.  All tensors are caller-owned.  The library is not thread-safe
+ * per plan: calls that use one plan must be ordered (one stream, or
+ * explicit synchronization), because the plan's workspace is shared by its
+ * launches.
+ */
+#ifndef CONV_NORM_H
+#define CONV_NORM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define CN_OK 0
+#define CN_ERR_INVALID_ARG (-1)  /* bad descriptor, null/misaligned pointer  */
+#define CN_ERR_UNSUPPORTED (-2)  /* valid problem, no kernel for this shape  */
+#define CN_ERR_CUDA (-3)         /* a CUDA runtime call or launch failed     */
+#define CN_ERR_TIMEOUT (-4)      /* a bounded device-side wait ran out       */
+#define CN_ERR_DEVICE_CHECK (-5) /* a kernel's own bounds check tripped      */
+#define CN_ERR_ALLOC (-6)        /* device or host allocation failed         */
+
+/* ---- problem descriptor -------------------------------------------------- */
+typedef enum { CN_CONV3D = 0, CN_CONV2D = 1, CN_CONVT2D = 2 } cn_conv_kind;
+typedef enum {
+    CN_ACT_NONE = 0,
+    CN_ACT_HARDSWISH = 1, /* v * clamp(v + 3, 0, 6) / 6            (l2_p27) */
+    CN_ACT_GELU_ERF = 2,  /* 0.5 v (1 + erf(v / sqrt 2)), exact     (l2_p19) */
+    CN_ACT_SOFTMAX_C = 3  /* softmax over the channel axis          (l2_p6)  */
+} cn_act;
+typedef enum {
+    CN_NORM_NONE = 0,
+    CN_NORM_GROUP = 1,    /* per (n, group) over C/G channels x space (l2_p27, l2_p19) */
+    CN_NORM_INSTANCE = 2  /* per (n, c) over space                    (l2_p17) */
+} cn_norm;
+typedef enum {
+    CN_RED_NONE = 0,         /* full normalized tensor is the output            */
+    CN_RED_MEAN_SPATIAL = 1, /* mean over all spatial axes -> (N, C_out) (l2_p27) */
+    CN_RED_MAXPOOL2_X2 = 2   /* MaxPool3d(2,2) applied twice, floor mode (l2_p6) */
+} cn_red;
+
+/*
+ * All fields are plain ints/floats so the struct has the same layout from C,
+ * C++ and Python ctypes.
+ *   conv        cn_conv_kind.  CN_CONV3D: x (N,C_in,D,H,W), weight
+ *               (C_out, C_in/groups, k, k, k).  CN_CONV2D: x (N,C_in,H,W),
+ *               weight (C_out, C_in/groups, k, k), D must be 1.
+ *               CN_CONVT2D: transposed conv, stride 1, padding 0, x
+ *               (N,C_in,H,W), weight (C_in, C_out/groups, k, k) (PyTorch's
+ *               ConvTranspose2d layout), D must be 1.
+ *   N           batch size; N = 0 is an empty problem (forward does nothing).
+ *   k, groups   cubic/square kernel extent; channel groups of the conv.
+ *   has_bias    0/1: whether a conv bias of length C_out is added.
+ *   act         cn_act.   norm: cn_norm.  red: cn_red.
+ *   num_groups  GroupNorm groups (C_out % num_groups == 0); ignored otherwise.
+ *   affine      0/1: per-channel gamma/beta after normalization.
+ *   eps         added to the variance inside the square root (> 0).
+ *   post_scale  multiplies the normalized value (0.5 for "divide by 2").
+ * Conv output extent per spatial axis: L - k + 1 (conv), L + k - 1 (convT).
+ */
+typedef struct {
+    int conv;
+    int N, C_in, C_out, D, H, W, k, groups;
+    int has_bias;
+    int act;
+    int norm;
+    int num_groups;
+    int affine;
+    float eps;
+    float post_scale;
+    int red;
+} conv_norm_desc;
+
+typedef struct conv_norm_plan_s *conv_norm_plan;
+
+/* Facts about a created plan, for reporting (kernel names are static
+ * strings owned by the library). */
+typedef struct {
+    int variant;               /* 0 mean-3d, 1 softmax-pool-3d, 2 full-2d */
+    int launches_per_forward;  /* kernels one conv_norm_forward launches   */
+    const char *kernel_names;  /* comma-separated, in launch order         */
+    int64_t out_numel;         /* number of fp32 values written to out     */
+    size_t workspace_bytes;    /* device workspace owned by the plan        */
+    int grid_ctas;             /* CTAs of the main (conv) kernel            */
+    int threads_per_cta;
+    int smem_bytes_per_cta;
+} conv_norm_info;
+
+/* ---- host-only queries (need no GPU) ------------------------------------- */
+
+/* Checks a descriptor.  Returns CN_OK, CN_ERR_INVALID_ARG for a malformed
+ * problem (e.g. C_in % groups != 0, kernel larger than the input) or
+ * CN_ERR_UNSUPPORTED for a valid problem this library has no kernel for. */
+int conv_norm_desc_validate(const conv_norm_desc *desc);
+
+/* Writes the output shape implied by desc into dims[0..*ndim-1] (ndim <= 5):
+ * (N, C_out) for CN_RED_MEAN_SPATIAL; (N, C_out, Do/4, Ho/4, Wo/4) with
+ * floor division for CN_RED_MAXPOOL2_X2; the conv output shape otherwise. */
+int conv_norm_output_shape(const conv_norm_desc *desc, int64_t dims[5], int *ndim);
+
+/* Human-readable name of a status code (static string). */
+const char *conv_norm_status_string(int status);
+
+/* ---- plans ---------------------------------------------------------------- */
+
+/* Validates desc, picks the kernel variant and its tiling for the CURRENT
+ * CUDA device, and allocates the plan's device workspace there (partial
+ * statistics, tickets, an error flag).  On success *out_plan owns that
+ * memory until conv_norm_plan_destroy. */
+int conv_norm_plan_create(const conv_norm_desc *desc, conv_norm_plan *out_plan);
+
+/* Frees the plan and its workspace.  NULL is ignored.  The caller must make
+ * sure no forward that uses the plan is still running. */
+void conv_norm_plan_destroy(conv_norm_plan plan);
+
+/* Bytes of device workspace the plan owns (0 when none is needed). */
+size_t conv_norm_workspace_bytes(conv_norm_plan plan);
+
+/* Fills *info; returns CN_ERR_INVALID_ARG for NULL arguments. */
+int conv_norm_plan_info(conv_norm_plan plan, conv_norm_info *info);
+
+/* ---- forward -------------------------------------------------------------- */
+
+/*
+ * Runs the fused forward asynchronously on cuda_stream (a cudaStream_t; NULL
+ * is the legacy default stream).  All pointers are DEVICE pointers on the
+ * plan's device, fp32, contiguous, 16-byte aligned:
+ *   x      input, layout given by desc->conv                     (read)
+ *   w      conv weight (layout in conv_norm_desc)                (read)
+ *   b      bias (C_out), NULL iff has_bias == 0                  (read)
+ *   gamma  (C_out), beta (C_out): NULL iff affine == 0 or norm == NONE
+ *   out    output, shape from conv_norm_output_shape            (written)
+ * out must not overlap the inputs.  No host synchronization happens and no
+ * memory is allocated.  Errors: CN_ERR_INVALID_ARG (null/misaligned pointer,
+ * NULL plan), CN_ERR_CUDA (launch failure; cudaGetLastError is cleared).
+ * Device-side problems (a bounded wait that ran out) are reported later by
+ * conv_norm_plan_check_device.
+ */
+int conv_norm_forward(conv_norm_plan plan, const float *x, const float *w,
+                      const float *b, const float *gamma, const float *beta,
+                      float *out, void *cuda_stream);
+
+/*
+ * Same computation with HOST buffers: copies x, w, b, gamma, beta to device
+ * buffers owned by the plan (allocated on the first call), runs the
+ * forward on cuda_stream, copies the result back into the host buffer out
+ * and synchronizes the stream before returning.  Pinned (page-locked) host
+ * memory gives asynchronous full-bandwidth copies; pageable memory works
+ * too.  Errors as conv_norm_forward, plus CN_ERR_ALLOC.
+ */
+int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
+                           const float *b, const float *gamma, const float *beta,
+                           float *out, void *cuda_stream);
+
+/*
+ * Synchronizes cuda_stream, then reads and clears the plan's device error
+ * flag.  Returns CN_OK, CN_ERR_TIMEOUT (a bounded device wait gave up; the
+ * output of that forward is undefined), CN_ERR_DEVICE_CHECK or CN_ERR_CUDA.
+ */
+int conv_norm_plan_check_device(conv_norm_plan plan, void *cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CONV_NORM_H */
