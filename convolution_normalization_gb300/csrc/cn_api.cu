@@ -244,9 +244,11 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
             const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
             a.partial = reinterpret_cast<double *>(vbase);
             a.tickets = reinterpret_cast<int *>(vbase + ((part + 255) & ~(size_t)255));
+            a.err = p->err_flag;
             break;
         }
         case V_POOL3D:
+            p->pool_args.err = p->err_flag;
             break;
         default:
             full2d_bind_workspace(p->full_args, vbase, p->err_flag);
@@ -330,13 +332,13 @@ static int forward_impl(conv_norm_plan p, const float *x, const float *w, const 
     int st;
     switch (p->variant) {
         case V_MEAN3D: {
-            Mean3dArgs a = p->mean_args;
+            Mean3dArgs &a = p->mean_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
             st = mean3d_launch(p->mean_cfg, a, s);
             break;
         }
         case V_POOL3D: {
-            Pool3dArgs a = p->pool_args;
+            Pool3dArgs &a = p->pool_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.out = out;
             st = pool3d_launch(p->pool_cfg, a, s);
             break;

@@ -5,14 +5,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "../../include/conv_norm.h"
 
 namespace cn {
+
+// Tensor-map encoding (cn_tma_host.cu).
+bool tma_available();
+int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], const uint32_t box[4]);
+
+// Upper bound on any device-side wait (ns of GPU wall time) before a kernel
+// gives up, records CN_ERR_TIMEOUT in the plan's flag and carries on.
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 // ---------------------------------------------------------------------------
 // Variant 0: 3-D conv -> activation -> (GroupNorm | InstanceNorm | none)
 // -> spatial mean.  One launch; the conv tensor is never written.
 struct Mean3dArgs {
+    CUtensorMap tmap;           // x viewed as (W, H, D, N*C_in), box (pitch, H, planes_max, C_in)
+    const float *tmap_base;     // x pointer the map was encoded for
+    int use_tma;                // 1: stage with one TMA tensor copy per CTA
+    int *err;                   // device error flag
     const float *x, *w, *b, *gamma, *beta;
     float *out;
     int N, Ci, Co, D, H, W, Do, Ho, Wo;
@@ -35,7 +50,7 @@ typedef void (*Mean3dKernel)(Mean3dArgs);
 struct Mean3dConfig {
     Mean3dKernel kern;
     const char *name;
-    int K, RW;
+    int K, RW, COT;
     int threads, smem;
     int grid;
 };
@@ -44,19 +59,23 @@ struct Mean3dConfig {
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(const Mean3dConfig &cfg);  // sets smem attribute (needs a device)
-int mean3d_launch(const Mean3dConfig &cfg, const Mean3dArgs &a, cudaStream_t s);
+int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Variant 1: 3-D conv -> channel softmax -> MaxPool3d(2,2) twice (= one
 // 4x4x4 stride-4 max pool).  One launch, only the pooled output is written.
 struct Pool3dArgs {
+    CUtensorMap tmap;     // x viewed as (W, H, D, N*C_in), box (pxb, P, P, C_in)
+    const float *tmap_base;
+    int use_tma;
+    int *err;
     const float *x, *w, *b;
     float *out;
     int N, Ci, D, H, W, Do, Ho, Wo;
     int Pd, Ph, Pw;      // pooled extents: floor(Do/4), floor(Ho/4), floor(Wo/4)
     long long nvox;      // N * Pd * Ph * Pw
     int vox_per_cta;     // pooled voxels per CTA (16 threads each)
-    int pw_pitch;        // shared-memory patch row pitch (floats)
+    int pw_pitch;        // shared-memory patch row pitch (floats), P rounded up to 4
     int vox_stride;      // floats per staged voxel patch
 };
 typedef void (*Pool3dKernel)(Pool3dArgs);
@@ -67,7 +86,7 @@ struct Pool3dConfig {
 };
 int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &args, Pool3dConfig &cfg);
 int pool3d_prepare(const Pool3dConfig &cfg);
-int pool3d_launch(const Pool3dConfig &cfg, const Pool3dArgs &a, cudaStream_t s);
+int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Variant 2: 2-D conv or transposed conv (groups) -> activation ->
@@ -77,6 +96,7 @@ int pool3d_launch(const Pool3dConfig &cfg, const Pool3dArgs &a, cudaStream_t s);
 // the moments into per-channel coefficients.  Kernel B rewrites out in place
 // as (y - mu) * a + bb.
 struct Full2dArgs {
+    int use_bulk;         // 1: rows staged with bulk async copies (W % 4 == 0)
     const float *x, *w, *b, *gamma, *beta;
     float *out;
     int N, Ci, Co, H, W, Ho, Wo;
@@ -100,7 +120,7 @@ typedef void (*Full2dKernel)(Full2dArgs);
 struct Full2dConfig {
     Full2dKernel kern;
     const char *names;
-    int K, RW, transposed;
+    int K, RW, COT, VECW, transposed;
     int threads, smem, grid;
     int apply_threads, apply_grid_x, apply_grid_y;
 };

@@ -19,27 +19,55 @@
 // the filter taps are reversed while staging, so both kinds share one
 // mainloop.
 //
-// Mapping of kernel A: a thread owns COT=8 output channels x RW consecutive
+// Mapping of kernel A: a thread owns COT output channels x RW consecutive
 // outputs of one output row; the lanes of a warp own (row, segment) items of
-// the CTA tile, rows fastest (conflict-free shared loads with a row pitch
-// of 4 mod 8 floats); warps split into channel slices x spatial groups.
-// Input channels stream through a two-stage cp.async pipeline holding the
-// haloed input tile and the tile's filter slice.
+// the CTA tile, rows fastest (conflict-free shared loads with a row pitch of
+// 4 mod 8 floats); warps split into channel slices x spatial groups.  Input
+// channels stream through a two-stage pipeline: each in-image input row of a
+// stage arrives with one bulk async copy (TMA engine, completion on an
+// mbarrier), out-of-image halo cells are zeroed once per kernel; the tile's
+// filter slice is transposed into shared memory by the threads.
 #include "cn_common.cuh"
 #include "cn_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace cn {
 namespace {
-constexpr int COT = 8;
 
-template <int K, int RW, bool TRANSPOSED>
-__global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
-    extern __shared__ __align__(16) float smem[];
+// Bias + activation of RW values in place, then the moments of the first
+// nvalid of them.
+template <int RW, int ACT>
+CN_DEV Moments<float> act_moments(float (&v)[RW], float bias, int nvalid) {
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        float t = v[i] + bias;
+        if (ACT == ACT_HARDSWISH) t = hardswish(t);
+        if (ACT == ACT_GELU) t = gelu_erf(t);
+        v[i] = t;
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) s += (i < nvalid) ? v[i] : 0.0f;
+    const float mean = nvalid > 0 ? s / (float)nvalid : 0.0f;
+    float m2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        const float d = (i < nvalid) ? v[i] - mean : 0.0f;
+        m2 = fmaf(d, d, m2);
+    }
+    return Moments<float>{(float)nvalid, mean, m2};
+}
+
+template <int K, int RW, int COT, int VECW, bool TRANSPOSED>
+__global__ void __launch_bounds__(256) k_conv2d_act_stats(const __grid_constant__ Full2dArgs a) {
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int s_last;
+    static_assert(COT == 4 || COT == 8, "channel slice of 4 or 8");
     constexpr int XW = RW + K - 1;
-    constexpr bool VEC = (RW % 4) == 0;
-    constexpr int LOADW = VEC ? ((XW + 3) & ~3) : XW;
+    constexpr int LOADW = (XW + VECW - 1) / VECW * VECW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     const int cs = warp % a.wco;
@@ -59,6 +87,13 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
     const int c0 = ct * a.NT * RW;
     const int ir0 = TRANSPOSED ? r0 - (K - 1) : r0;
     const int ic0 = TRANSPOSED ? c0 - (K - 1) : c0;
+    // Shared row buffers start at global column xs (a multiple of 4 when
+    // rows arrive by bulk copy); the tile's first column sits at offset off.
+    const int xs = a.use_bulk ? (ic0 & ~3) : ic0;
+    const int off = ic0 - xs;
+    const int gc_lo = max(ic0, 0) & ~3;
+    const int gc_hi = min((ic0 + a.cols_in + 3) & ~3, a.W);
+    const int gr_lo = max(ir0, 0), gr_hi = min(ir0 + a.rows_in, a.H);
 
     const int item = sg * 32 + lane;
     const int il = item % a.TR;
@@ -70,9 +105,27 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
 
     const int xstage = a.cib * a.rows_in * a.pitch;
 
-    auto load_stage = [&](int chunk, int buf) {
+    // in-image rows of one stage by bulk async copies (issued by warp 0)
+    auto issue_bulk = [&](int chunk, int buf) {
+        const int cbase = chunk * a.cib;
+        const int ncl = min(a.cib, a.Cig - cbase);
+        const int nr = gr_hi - gr_lo;
+        const uint32_t row_bytes = (uint32_t)(gc_hi - gc_lo) * 4u;
         float *sxb = smem + (size_t)buf * a.stage_floats;
-        float *swb = sxb + xstage;
+        fence_proxy_async();
+        if (lane == 0) mbar_arrive_expect_tx(&bars[buf], (uint32_t)(ncl * nr) * row_bytes);
+        __syncwarp();
+        for (int q = lane; q < ncl * nr; q += 32) {
+            const int cl = q / nr, gr = gr_lo + q % nr;
+            const float *src =
+                a.x + (((size_t)n * a.Ci + ci0 + cbase + cl) * a.H + gr) * a.W + gc_lo;
+            float *dst = sxb + (size_t)(cl * a.rows_in + gr - ir0) * a.pitch + (gc_lo - xs);
+            bulk_load(dst, src, row_bytes, &bars[buf]);
+        }
+    };
+    // fallback for rows that are not 16-byte multiples: cp.async with zero fill
+    auto issue_cpasync = [&](int chunk, int buf) {
+        float *sxb = smem + (size_t)buf * a.stage_floats;
         const int cbase = chunk * a.cib;
         const int nrows = a.cib * a.rows_in;
         for (int rI = warp; rI < nrows; rI += nwarps) {
@@ -88,24 +141,28 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
                 cp_async4(dst + cc, ok ? (const void *)(src + gc) : (const void *)a.x, ok);
             }
         }
-        const int totw = a.cib * K * K * COB;
-        for (int i = tid; i < totw; i += blockDim.x) {
-            const int col = i % COB;
-            const int t = i / COB;
-            const int tap = t % (K * K), cl = t / (K * K);
+    };
+    // filter slice of one stage, taps reversed for the transposed conv
+    auto stage_weights = [&](int chunk, int buf) {
+        float *swb = smem + (size_t)buf * a.stage_floats + xstage;
+        const int cbase = chunk * a.cib;
+        for (int t = warp; t < a.cib * K * K; t += nwarps) {
+            const int cl = t / (K * K), tap = t - cl * (K * K);
             const int kh = tap / K, kw = tap - kh * K;
             const int cil = cbase + cl;
-            float v = 0.0f;
-            if (cil < a.Cig) {
-                if (TRANSPOSED) {
-                    const int col_g = co0 - g * a.Cog + col;
-                    v = __ldg(a.w + (((size_t)(ci0 + cil) * a.Cog + col_g) * K + (K - 1 - kh)) * K +
-                              (K - 1 - kw));
-                } else {
-                    v = __ldg(a.w + (((size_t)(co0 + col) * a.Cig + cil) * K + kh) * K + kw);
+            for (int col = lane; col < COB; col += 32) {
+                float v = 0.0f;
+                if (cil < a.Cig) {
+                    if (TRANSPOSED) {
+                        const int col_g = co0 - g * a.Cog + col;
+                        v = __ldg(a.w + (((size_t)(ci0 + cil) * a.Cog + col_g) * K + (K - 1 - kh)) * K +
+                                  (K - 1 - kw));
+                    } else {
+                        v = __ldg(a.w + (((size_t)(co0 + col) * a.Cig + cil) * K + kh) * K + kw);
+                    }
                 }
+                swb[t * COB + col] = v;
             }
-            swb[i] = v;
         }
     };
 
@@ -115,22 +172,64 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
 #pragma unroll
         for (int i = 0; i < RW; ++i) acc[c][i] = 0.0f;
 
-    load_stage(0, 0);
-    cp_async_commit();
-    for (int chunk = 0; chunk < a.nchunk; ++chunk) {
-        if (chunk + 1 < a.nchunk) load_stage(chunk + 1, (chunk + 1) & 1);
-        cp_async_commit();
-        cp_async_wait<1>();
+    bool ok = true;
+    if (a.use_bulk) {
+        // Out-of-image rows and columns of both buffers stay zero for the
+        // whole kernel: bulk copies only ever write the in-image part of a row.
+        const int rows2 = 2 * a.cib * a.rows_in;
+        for (int rI = warp; rI < rows2; rI += nwarps) {
+            const int buf = rI / (a.cib * a.rows_in), rem = rI - buf * (a.cib * a.rows_in);
+            const int gr = ir0 + rem % a.rows_in;
+            float *row = smem + (size_t)buf * a.stage_floats + (size_t)rem * a.pitch;
+            const bool rin = gr >= 0 && gr < a.H;
+            const int z0 = rin ? gc_lo - xs : a.pitch;
+            const int z1 = rin ? gc_hi - xs : a.pitch;
+            for (int c = lane; c < a.pitch; c += 32)
+                if (c < z0 || c >= z1) row[c] = 0.0f;
+        }
+        if (tid == 0) {
+            mbar_init(&bars[0], 1);
+            mbar_init(&bars[1], 1);
+            fence_barrier_init();
+        }
+        fence_proxy_async();
         __syncthreads();
-        const float *sxb = smem + (size_t)(chunk & 1) * a.stage_floats;
+        if (warp == 0) issue_bulk(0, 0);
+    } else {
+        issue_cpasync(0, 0);
+        cp_async_commit();
+    }
+    stage_weights(0, 0);
+
+    for (int chunk = 0; chunk < a.nchunk; ++chunk) {
+        const int buf = chunk & 1;
+        if (chunk + 1 < a.nchunk) {
+            if (a.use_bulk) {
+                if (warp == 0) issue_bulk(chunk + 1, buf ^ 1);
+            } else {
+                issue_cpasync(chunk + 1, buf ^ 1);
+            }
+            stage_weights(chunk + 1, buf ^ 1);
+        }
+        if (a.use_bulk) {
+            if (ok && !mbar_wait_bounded(&bars[buf], (chunk >> 1) & 1, kWaitLimitNs)) {
+                ok = false;
+                flag_error(a.err, ERR_TIMEOUT);
+            }
+        } else {
+            cp_async_commit();
+            cp_async_wait<1>();
+        }
+        __syncthreads();
+        const float *sxb = smem + (size_t)buf * a.stage_floats;
         const float *swb = sxb + xstage;
-        const int ncl = min(a.cib, a.Cig - chunk * a.cib);
+        const int ncl = ok ? min(a.cib, a.Cig - chunk * a.cib) : 0;
         for (int cl = 0; cl < ncl; ++cl) {
             CN_UNROLL(CN_TAP_UNROLL)
             for (int kh = 0; kh < K; ++kh) {
-                const float *xp = sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + sl * RW;
+                const float *xp = sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + off + sl * RW;
                 float xr[LOADW];
-                if constexpr (VEC) {
+                if constexpr (VECW == 4) {
 #pragma unroll
                     for (int j = 0; j < LOADW / 4; ++j) {
                         const float4 v = *reinterpret_cast<const float4 *>(xp + 4 * j);
@@ -138,6 +237,13 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
                         xr[4 * j + 1] = v.y;
                         xr[4 * j + 2] = v.z;
                         xr[4 * j + 3] = v.w;
+                    }
+                } else if constexpr (VECW == 2) {
+#pragma unroll
+                    for (int j = 0; j < LOADW / 2; ++j) {
+                        const float2 v = *reinterpret_cast<const float2 *>(xp + 2 * j);
+                        xr[2 * j + 0] = v.x;
+                        xr[2 * j + 1] = v.y;
                     }
                 } else {
 #pragma unroll
@@ -147,54 +253,57 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
                 for (int kw = 0; kw < K; ++kw) {
                     const float4 *wp = reinterpret_cast<const float4 *>(
                         swb + (size_t)((cl * K + kh) * K + kw) * COB + cs * COT);
-                    const float4 w0 = wp[0], w1 = wp[1];
+                    float wv[COT];
+#pragma unroll
+                    for (int q = 0; q < COT / 4; ++q) {
+                        const float4 t = wp[q];
+                        wv[4 * q + 0] = t.x;
+                        wv[4 * q + 1] = t.y;
+                        wv[4 * q + 2] = t.z;
+                        wv[4 * q + 3] = t.w;
+                    }
 #pragma unroll
                     for (int i = 0; i < RW; ++i) {
                         const float xv = xr[i + kw];
-                        acc[0][i] = fmaf(xv, w0.x, acc[0][i]);
-                        acc[1][i] = fmaf(xv, w0.y, acc[1][i]);
-                        acc[2][i] = fmaf(xv, w0.z, acc[2][i]);
-                        acc[3][i] = fmaf(xv, w0.w, acc[3][i]);
-                        acc[4][i] = fmaf(xv, w1.x, acc[4][i]);
-                        acc[5][i] = fmaf(xv, w1.y, acc[5][i]);
-                        acc[6][i] = fmaf(xv, w1.z, acc[6][i]);
-                        acc[7][i] = fmaf(xv, w1.w, acc[7][i]);
+#pragma unroll
+                        for (int c = 0; c < COT; ++c) acc[c][i] = fmaf(xv, wv[c], acc[c][i]);
                     }
                 }
             }
         }
         __syncthreads();
     }
+    if (!ok && a.use_bulk) {
+        // let any copy still in flight land before this CTA's memory is reused
+        mbar_wait_bounded(&bars[0], 0, kWaitLimitNs);
+        mbar_wait_bounded(&bars[1], 0, kWaitLimitNs);
+    }
 
     // ---- epilogue: bias + activation, store the pre-norm value, moments ----
     double *sred = reinterpret_cast<double *>(smem + 2 * (size_t)a.stage_floats);
     const bool row_ok = item_ok && orow < a.Ho;
+    const int nvalid = row_ok ? max(0, min(RW, a.Wo - ocol0)) : 0;
 #pragma unroll
     for (int c = 0; c < COT; ++c) {
         const int co = co0 + cs * COT + c;
         const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-        float s = 0.0f, cnt = 0.0f;
-#pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            const float v = apply_act(a.act, acc[c][i] + bias);
-            acc[c][i] = v;
-            if (row_ok && ocol0 + i < a.Wo) {
-                s += v;
-                cnt += 1.0f;
-            }
-        }
-        const float mean = cnt > 0.0f ? s / cnt : 0.0f;
-        float m2 = 0.0f;
+        Moments<float> m;
+        if (a.act == ACT_HARDSWISH)
+            m = act_moments<RW, ACT_HARDSWISH>(acc[c], bias, nvalid);
+        else if (a.act == ACT_GELU)
+            m = act_moments<RW, ACT_GELU>(acc[c], bias, nvalid);
+        else
+            m = act_moments<RW, ACT_NONE>(acc[c], bias, nvalid);
         float *op = a.out + (((size_t)n * a.Co + co) * a.Ho + (row_ok ? orow : 0)) * a.Wo + ocol0;
+        if (nvalid == RW && (RW % 2) == 0 && (reinterpret_cast<uintptr_t>(op) & 7) == 0) {
 #pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            if (row_ok && ocol0 + i < a.Wo) {
-                const float dv = acc[c][i] - mean;
-                m2 = fmaf(dv, dv, m2);
-                op[i] = acc[c][i];
-            }
+            for (int i = 0; i < RW; i += 2)
+                *reinterpret_cast<float2 *>(op + i) = make_float2(acc[c][i], acc[c][i + 1]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < RW; ++i)
+                if (i < nvalid) op[i] = acc[c][i];
         }
-        Moments<float> m{cnt, mean, m2};
         m = warp_merge(m);
         if (lane == 0) {
             double *o = sred + ((size_t)sg * COB + cs * COT + c) * 3;
@@ -218,7 +327,6 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(Full2dArgs a) {
     }
 
     // ---- the last CTA of sample n turns the moments into coefficients ----
-    __shared__ int s_last;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -287,48 +395,31 @@ __global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *co
 }
 
 struct Inst {
-    int K, RW, T;
+    int K, RW, COT, VECW, T;
     Full2dKernel fn;
     const char *name;
 };
-#define CN_FULL_INST(K, RW, T)                                       \
-    {K, RW, T, k_conv2d_act_stats<K, RW, (T != 0)>,                  \
-     "k_conv2d_act_stats<" #K "," #RW "," #T ">,k_norm_apply"}
+#define CN_FULL_INST(K, RW, C, V, T)                            \
+    {K, RW, C, V, T, k_conv2d_act_stats<K, RW, C, V, (T != 0)>, \
+     "k_conv2d_act_stats<" #K "," #RW "," #C "," #V "," #T ">,k_norm_apply"}
 const Inst kInst[] = {
-    CN_FULL_INST(1, 16, 0), CN_FULL_INST(2, 16, 0), CN_FULL_INST(3, 16, 0), CN_FULL_INST(3, 13, 0),
-    CN_FULL_INST(4, 16, 0), CN_FULL_INST(1, 16, 1), CN_FULL_INST(2, 16, 1), CN_FULL_INST(3, 16, 1),
-    CN_FULL_INST(3, 13, 1), CN_FULL_INST(4, 16, 1),
+    CN_FULL_INST(3, 16, 8, 4, 0), CN_FULL_INST(3, 16, 4, 4, 0), CN_FULL_INST(1, 16, 8, 4, 0),
+    CN_FULL_INST(2, 16, 8, 4, 0), CN_FULL_INST(4, 16, 8, 4, 0), CN_FULL_INST(3, 13, 8, 1, 1),
+    CN_FULL_INST(3, 13, 4, 1, 1), CN_FULL_INST(3, 16, 8, 2, 1), CN_FULL_INST(3, 16, 4, 2, 1),
+    CN_FULL_INST(1, 16, 8, 4, 1), CN_FULL_INST(2, 16, 8, 1, 1), CN_FULL_INST(4, 16, 8, 1, 1),
 };
 #undef CN_FULL_INST
 
-struct Tiling {
-    int wsp, TR, NT;
-    double cost;
-};
-
-Tiling choose_tiling(int Ho, int Wo, int RW, int max_wsp) {
-    Tiling best{1, 1, 1, 1e30};
-    const int nseg = (Wo + RW - 1) / RW;
-    for (int wsp = 1; wsp <= max_wsp; ++wsp) {
-        const int lanes = 32 * wsp;
-        int NT, TR;
-        if (nseg <= lanes) {
-            NT = nseg;
-            TR = lanes / nseg;
-        } else {
-            NT = lanes;
-            TR = 1;
-        }
-        TR = std::min(TR, std::max(1, Ho));
-        const int rtiles = (Ho + TR - 1) / TR, ctiles = (nseg + NT - 1) / NT;
-        const double row_w = (double)rtiles * TR / Ho;
-        const double col_w = (double)ctiles * NT * RW / Wo;
-        const double lane_w = (double)lanes / (TR * NT);
-        const double cost = row_w * col_w * lane_w * (1.0 + 0.02 * (1.0 / wsp));
-        if (cost < best.cost - 1e-9) best = Tiling{wsp, TR, NT, cost};
-    }
-    return best;
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return v ? atoi(v) : dflt;
 }
+
+struct Choice {
+    const Inst *in = nullptr;
+    int wco = 1, wsp = 1, TR = 1, NT = 1;
+    double cost = 1e30;
+};
 
 int pick_wco(int units) {
     for (int c = 8; c >= 1; --c)
@@ -343,29 +434,59 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     const int Ho = T ? d.H + K - 1 : d.H - K + 1;
     const int Wo = T ? d.W + K - 1 : d.W - K + 1;
     const int Cig = d.C_in / d.groups, Cog = d.C_out / d.groups;
-    if (Cog % COT != 0) return CN_ERR_UNSUPPORTED;
-    const int wco = pick_wco(Cog / COT);
-    const int max_wsp = std::max(1, 8 / wco);
-    const Inst *best = nullptr;
-    Tiling bt{};
-    double best_cost = 1e30;
+    const bool bulk = (d.W % 4 == 0) && env_int("CN_NO_TMA", 0) == 0;
+    const int f_cot = env_int("CN_FULL2D_COT", 0), f_rw = env_int("CN_FULL2D_RW", 0),
+              f_wsp = env_int("CN_FULL2D_WSP", 0);
+    const int off = bulk ? (((-(K - 1) * T) % 4) + 4) % 4 : 0;
+    Choice best;
     for (const Inst &in : kInst) {
-        if (in.K != K || in.T != T) continue;
-        const Tiling t = choose_tiling(Ho, Wo, in.RW, max_wsp);
+        if (in.K != K || in.T != T || Cog % in.COT != 0) continue;
+        if ((f_cot && in.COT != f_cot) || (f_rw && in.RW != f_rw)) continue;
+        if (off % in.VECW != 0) continue;
+        const int wco = pick_wco(Cog / in.COT);
+        const int nseg = (Wo + in.RW - 1) / in.RW;
         const int XW = in.RW + K - 1;
-        const double loads = (in.RW % 4 == 0) ? (XW + 3) / 4 : XW;
-        const double ratio = 1.0 + (loads + 2.0 * K) / (8.0 * K * in.RW);
-        const double cost = t.cost * ratio;
-        if (cost < best_cost - 1e-9) {
-            best_cost = cost;
-            best = &in;
-            bt = t;
+        const int loadw = (XW + in.VECW - 1) / in.VECW * in.VECW;
+        const int regs = std::min(255, in.COT * in.RW + loadw + in.COT + 40);
+        for (int wsp = 1; wco * wsp <= 8; ++wsp) {
+            if (f_wsp && wsp != f_wsp) continue;
+            const int lanes = 32 * wsp;
+            const int NT = std::min(nseg, lanes);
+            const int TR = std::max(1, std::min(lanes / NT, Ho));
+            // segments of every column tile must keep the load alignment
+            const int ctiles = (nseg + NT - 1) / NT;
+            if (ctiles > 1 && ((NT * in.RW) % 4 != 0)) continue;
+            if (NT > 1 && (in.RW % in.VECW) != 0) continue;
+            const int rtiles = (Ho + TR - 1) / TR;
+            const double waste = ((double)rtiles * TR / Ho) * ((double)ctiles * NT * in.RW / Wo) *
+                                 ((double)lanes / (TR * NT));
+            const double loads = (double)loadw / in.VECW + 3.0 * in.COT / 4.0;
+            const double ratio = 1.0 + loads / ((double)in.COT * K * in.RW);
+            const int threads = 32 * wco * wsp;
+            const int ctas = std::max(1, std::min(65536 / (threads * ((regs + 7) & ~7)), 2));
+            const int warps_sm = ctas * wco * wsp;
+            // scheduler balance (warps spread over 4 SM sub-partitions) and
+            // latency hiding (fewer than 16 warps measured slower)
+            const double balance =
+                (warps_sm % 4 == 0) ? 1.0 : (double)((warps_sm + 3) / 4 * 4) / warps_sm;
+            const double occ = warps_sm >= 16 ? 1.0 : 1.0 + 0.025 * (16 - warps_sm);
+            const double cost = waste * ratio * balance * occ;
+            if (cost < best.cost - 1e-9) {
+                best.in = &in;
+                best.wco = wco;
+                best.wsp = wsp;
+                best.TR = TR;
+                best.NT = NT;
+                best.cost = cost;
+            }
         }
     }
-    if (!best) return CN_ERR_UNSUPPORTED;
-    const int RW = best->RW;
+    if (!best.in) return CN_ERR_UNSUPPORTED;
+    const Inst &in = *best.in;
+    const int RW = in.RW, COT = in.COT;
     const int XW = RW + K - 1;
-    const int LOADW = (RW % 4 == 0) ? ((XW + 3) & ~3) : XW;
+    const int LOADW = (XW + in.VECW - 1) / in.VECW * in.VECW;
+    a.use_bulk = bulk ? 1 : 0;
     a.N = d.N;
     a.Ci = d.C_in;
     a.Co = d.C_out;
@@ -375,28 +496,30 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.Wo = Wo;
     a.Cig = Cig;
     a.Cog = Cog;
-    a.wco = wco;
-    a.wsp = bt.wsp;
-    a.TR = bt.TR;
-    a.NT = bt.NT;
+    a.wco = best.wco;
+    a.wsp = best.wsp;
+    a.TR = best.TR;
+    a.NT = best.NT;
     const int nseg = (Wo + RW - 1) / RW;
     a.row_tiles = (Ho + a.TR - 1) / a.TR;
     a.col_tiles = (nseg + a.NT - 1) / a.NT;
-    a.ncob = d.C_out / (COT * wco);
+    a.ncob = d.C_out / (COT * a.wco);
     a.ntiles = a.row_tiles * a.col_tiles;
     a.rows_in = a.TR + K - 1;
     a.cols_in = a.NT * RW + K - 1;
-    int pitch = std::max((a.NT - 1) * RW + LOADW, a.cols_in);
+    // row buffer: the tile's reads reach off + (NT-1)*RW + LOADW; bulk copies
+    // of whole 16-byte groups reach at most off + cols_in + 3.
+    int pitch = std::max(off + (a.NT - 1) * RW + LOADW, off + a.cols_in + 3);
     pitch = (pitch + 3) & ~3;
-    if (((pitch / 4) & 1) == 0) pitch += 4;
+    if (((pitch / 4) & 1) == 0) pitch += 4;  // 4 (mod 8) floats: conflict-free row loads
     a.pitch = pitch;
-    const int COB = COT * wco;
+    const int COB = COT * a.wco;
     const int per_ci = a.rows_in * pitch + K * K * COB;
     int cib = std::min(Cig, 8);
     while (cib > 1 && 2 * (size_t)cib * per_ci * 4 > 100 * 1024) --cib;
     a.cib = cib;
     a.nchunk = (Cig + cib - 1) / cib;
-    a.stage_floats = ((cib * per_ci) + 3) & ~3;
+    a.stage_floats = ((cib * per_ci) + 31) & ~31;  // 128-byte aligned stages
     a.act = d.act;
     a.norm = d.norm;
     a.NG = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
@@ -406,16 +529,18 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.S = (long long)Ho * Wo;
     a.apply_needed = !(d.norm == CN_NORM_NONE && d.post_scale == 1.0f);
     a.vec4 = (a.S % 4) == 0;
-    const int threads = 32 * wco * a.wsp;
+    const int threads = 32 * a.wco * a.wsp;
     size_t smem = (size_t)2 * a.stage_floats * 4 + (size_t)a.wsp * COB * 3 * 8;
     smem = std::max(smem, (size_t)d.C_out * 3 * 8);
     if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
     const long long grid = (long long)d.N * a.ncob * a.ntiles;
     if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
-    cfg.kern = best->fn;
-    cfg.names = best->name;
+    cfg.kern = in.fn;
+    cfg.names = in.name;
     cfg.K = K;
     cfg.RW = RW;
+    cfg.COT = COT;
+    cfg.VECW = in.VECW;
     cfg.transposed = T;
     cfg.threads = threads;
     cfg.smem = (int)smem;

@@ -11,14 +11,15 @@
 // last CTA of each sample merges the moments (fixed order, fp64) and writes
 // the (N, C_out) result.
 //
-// Mapping: each thread owns COT=4 output channels x RW consecutive outputs of
-// one output row (d, h, w-segment); lanes of a warp own 32 consecutive rows
-// of the sample's flattened (d, h, segment) row list; warps of a CTA split
-// the channel block.  The CTA stages every input depth plane its rows need,
-// for all input channels, plus the filter of its channel block, in shared
-// memory once (cp.async, zero-filled pad columns).  The inner loop per
-// (ci, kd, kh) loads one input row segment into registers and issues
-// 4*K*RW FFMAs per thread against float4-broadcast weights.
+// Mapping: each thread owns COT output channels x RW consecutive outputs of
+// one output row (d, h, w-segment); the lanes of a warp own 32 consecutive
+// rows of the sample's flattened (d, h, segment) row list; warps of a CTA
+// split the channel block.  The CTA stages every input depth plane its rows
+// need, for all input channels, in shared memory with ONE TMA tensor copy
+// (box = pitch x H x planes x C_in; columns past W arrive zero-filled), and
+// the filter of its channel block transposed to [ci][tap][co].  The inner
+// loop per (ci, kd, kh) loads one input row segment into registers and
+// issues COT*K*RW FFMAs per thread against broadcast weights.
 #include "cn_common.cuh"
 #include "cn_internal.h"
 
@@ -28,15 +29,67 @@
 namespace cn {
 
 namespace {
-constexpr int COT = 4;
 
-template <int K, int RW>
-__global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
-    extern __shared__ __align__(16) float smem[];
+template <int COT>
+struct WVec;
+template <>
+struct WVec<4> {
+    typedef float4 T;
+    static CN_DEV float get(const float4 &v, int c) {
+        return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+    }
+};
+template <>
+struct WVec<2> {
+    typedef float2 T;
+    static CN_DEV float get(const float2 &v, int c) { return c == 0 ? v.x : v.y; }
+};
+
+// Bias + activation of RW values in place, then their moments (the first
+// nvalid values are valid; all are when nvalid == RW).
+template <int RW, int ACT>
+CN_DEV Moments<float> row_moments(float (&v)[RW], float bias, int nvalid) {
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        float t = v[i] + bias;
+        if (ACT == ACT_HARDSWISH) t = hardswish(t);
+        if (ACT == ACT_GELU) t = gelu_erf(t);
+        v[i] = t;
+    }
+    float s = 0.0f, m2 = 0.0f;
+    if (nvalid == RW) {
+#pragma unroll
+        for (int i = 0; i < RW; ++i) s += v[i];
+        const float mean = s * (1.0f / RW);
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            const float d = v[i] - mean;
+            m2 = fmaf(d, d, m2);
+        }
+        return Moments<float>{(float)RW, mean, m2};
+    }
+#pragma unroll
+    for (int i = 0; i < RW; ++i) s += (i < nvalid) ? v[i] : 0.0f;
+    const float mean = nvalid > 0 ? s / (float)nvalid : 0.0f;
+#pragma unroll
+    for (int i = 0; i < RW; ++i) {
+        const float d = (i < nvalid) ? v[i] - mean : 0.0f;
+        m2 = fmaf(d, d, m2);
+    }
+    return Moments<float>{(float)nvalid, mean, m2};
+}
+
+template <int K, int RW, int COT>
+__global__ void __launch_bounds__(256) k_conv3d_act_mean(const __grid_constant__ Mean3dArgs a) {
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int s_last;
+    typedef typename WVec<COT>::T wvec;
     constexpr int KKK = K * K * K;
     constexpr int LOADW = (RW + K - 1 + 3) & ~3;
     const int COB = COT * a.wco;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
     const int cs = warp % a.wco;
     const int rg = warp / a.wco;
     int bid = blockIdx.x;
@@ -58,54 +111,44 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
     const int np = d_hi - d_lo + K;
 
     // ---- stage input planes [d_lo, d_lo + np) of every input channel ----
-    {
+    if (a.use_tma) {
+        if (tid == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&bar, (uint32_t)(a.Ci * a.planes_max * HP * 4));
+            tma_load_4d(sx, &a.tmap, 0, 0, d_lo, n * a.Ci, &bar);
+        }
+    } else {
         const float *xn = a.x + (size_t)n * a.Ci * a.D * a.H * a.W;
-        if (a.vec16) {
-            const int cpr = a.W >> 2;
-            const int total = a.Ci * np * a.H * cpr;
-            for (int i = tid; i < total; i += blockDim.x) {
-                const int c4 = i % cpr;
-                int t = i / cpr;
-                const int h = t % a.H;
-                t /= a.H;
-                const int p = t % np, ci = t / np;
-                const float *src = xn + (((size_t)ci * a.D + d_lo + p) * a.H + h) * a.W + c4 * 4;
-                float *dst = sx + ((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + c4 * 4;
-                cp_async16(dst, src, true);
-            }
-        } else {
-            const int total = a.Ci * np * a.H * a.W;
-            for (int i = tid; i < total; i += blockDim.x) {
-                const int c = i % a.W;
-                int t = i / a.W;
-                const int h = t % a.H;
-                t /= a.H;
-                const int p = t % np, ci = t / np;
-                const float *src = xn + (((size_t)ci * a.D + d_lo + p) * a.H + h) * a.W + c;
-                float *dst = sx + ((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + c;
-                cp_async4(dst, src, true);
-            }
+        const int nrows = a.Ci * np * a.H;
+        for (int row = warp; row < nrows; row += nwarps) {
+            const int h = row % a.H, t = row / a.H;
+            const int p = t % np, ci = t / np;
+            const float *src = xn + (((size_t)ci * a.D + d_lo + p) * a.H + h) * a.W;
+            float *dst = sx + ((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch;
+            for (int c = lane; c < a.W; c += 32) cp_async4(dst + c, src + c, true);
+            for (int c = a.W + lane; c < a.pitch; c += 32) dst[c] = 0.0f;
         }
         cp_async_commit();
-        const int padw = a.pitch - a.W;
-        const int totalz = a.Ci * np * a.H * padw;
-        for (int i = tid; i < totalz; i += blockDim.x) {
-            const int c = i % padw;
-            int t = i / padw;
-            const int h = t % a.H;
-            t /= a.H;
-            const int p = t % np, ci = t / np;
-            sx[((size_t)(ci * a.planes_max + p) * a.H + h) * a.pitch + a.W + c] = 0.0f;
-        }
-        // filter of this channel block, transposed to [ci][tap][co]
-        const int totalw = a.Ci * KKK * COB;
-        for (int i = tid; i < totalw; i += blockDim.x) {
-            const int col = i % COB, t = i / COB;
-            sw[i] = __ldg(a.w + (size_t)(co0 + col) * a.Ci * KKK + t);
-        }
-        cp_async_wait_all();
-        __syncthreads();
     }
+    // filter of this channel block, transposed to [ci][tap][co]
+    for (int t = warp; t < a.Ci * KKK; t += nwarps)
+        for (int col = lane; col < COB; col += 32)
+            sw[t * COB + col] = __ldg(a.w + (size_t)(co0 + col) * a.Ci * KKK + t);
+    bool staged = true;
+    if (a.use_tma) {
+        __syncthreads();  // barrier initialised before anyone polls it
+        staged = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        if (!staged) {
+            flag_error(a.err, ERR_TIMEOUT);
+            // let a late copy land before this CTA's shared memory is reused
+            mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        }
+    } else {
+        cp_async_wait_all();
+    }
+    __syncthreads();
 
     // ---- mainloop ----
     int r = r_begin + rg * 32 + lane;
@@ -122,11 +165,12 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
         for (int i = 0; i < RW; ++i) acc[c][i] = 0.0f;
 
     const float *xbase = sx + ((size_t)(d - d_lo) * a.H + h) * a.pitch + seg * RW;
-    const float4 *wbase = reinterpret_cast<const float4 *>(sw) + cs;
-    const int ws4 = a.wco;  // float4 stride between taps
-    for (int ci = 0; ci < a.Ci; ++ci) {
+    const wvec *wbase = reinterpret_cast<const wvec *>(sw) + cs;
+    const int wstride = a.wco;  // wvec stride between taps
+    const int nci = staged ? a.Ci : 0;
+    for (int ci = 0; ci < nci; ++ci) {
         const float *xc = xbase + (size_t)ci * a.planes_max * HP;
-        const float4 *wc = wbase + (size_t)ci * KKK * ws4;
+        const wvec *wc = wbase + (size_t)ci * KKK * wstride;
         CN_UNROLL(CN_TAP_UNROLL)
         for (int kd = 0; kd < K; ++kd) {
             CN_UNROLL(CN_TAP_UNROLL)
@@ -141,16 +185,16 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
                     xr[4 * j + 2] = v.z;
                     xr[4 * j + 3] = v.w;
                 }
+                const wvec *wt = wc + (kd * K + kh) * K * wstride;
 #pragma unroll
                 for (int kw = 0; kw < K; ++kw) {
-                    const float4 wv = wc[((kd * K + kh) * K + kw) * ws4];
+                    const wvec wv = wt[kw * wstride];
 #pragma unroll
                     for (int i = 0; i < RW; ++i) {
                         const float xv = xr[i + kw];
-                        acc[0][i] = fmaf(xv, wv.x, acc[0][i]);
-                        acc[1][i] = fmaf(xv, wv.y, acc[1][i]);
-                        acc[2][i] = fmaf(xv, wv.z, acc[2][i]);
-                        acc[3][i] = fmaf(xv, wv.w, acc[3][i]);
+#pragma unroll
+                        for (int c = 0; c < COT; ++c)
+                            acc[c][i] = fmaf(xv, WVec<COT>::get(wv, c), acc[c][i]);
                     }
                 }
             }
@@ -158,31 +202,18 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
     }
 
     // ---- epilogue: bias + activation, per-channel moments ----
-    const int wbase_col = seg * RW;
+    const int nvalid = rvalid ? max(0, min(RW, a.Wo - seg * RW)) : 0;
 #pragma unroll
     for (int c = 0; c < COT; ++c) {
         const int co = co0 + cs * COT + c;
         const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-        float s = 0.0f, cnt = 0.0f;
-#pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            const float v = apply_act(a.act, acc[c][i] + bias);
-            acc[c][i] = v;
-            if (rvalid && wbase_col + i < a.Wo) {
-                s += v;
-                cnt += 1.0f;
-            }
-        }
-        const float mean = cnt > 0.0f ? s / cnt : 0.0f;
-        float m2 = 0.0f;
-#pragma unroll
-        for (int i = 0; i < RW; ++i) {
-            if (rvalid && wbase_col + i < a.Wo) {
-                const float dv = acc[c][i] - mean;
-                m2 = fmaf(dv, dv, m2);
-            }
-        }
-        Moments<float> m{cnt, mean, m2};
+        Moments<float> m;
+        if (a.act == ACT_HARDSWISH)
+            m = row_moments<RW, ACT_HARDSWISH>(acc[c], bias, nvalid);
+        else if (a.act == ACT_GELU)
+            m = row_moments<RW, ACT_GELU>(acc[c], bias, nvalid);
+        else
+            m = row_moments<RW, ACT_NONE>(acc[c], bias, nvalid);
         m = warp_merge(m);
         if (lane == 0) {
             double *o = sred + ((size_t)rg * COB + cs * COT + c) * 3;
@@ -205,7 +236,6 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
     }
 
     // ---- the last CTA of sample n merges all partial moments ----
-    __shared__ int s_last;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
@@ -252,15 +282,17 @@ __global__ void __launch_bounds__(256) k_conv3d_act_mean(Mean3dArgs a) {
 }
 
 struct Inst {
-    int K, RW;
+    int K, RW, COT;
     Mean3dKernel fn;
     const char *name;
 };
-#define CN_MEAN_INST(K, RW) {K, RW, k_conv3d_act_mean<K, RW>, "k_conv3d_act_mean<" #K "," #RW ">"}
+#define CN_MEAN_INST(K, RW, C) \
+    {K, RW, C, k_conv3d_act_mean<K, RW, C>, "k_conv3d_act_mean<" #K "," #RW "," #C ">"}
 const Inst kInst[] = {
-    CN_MEAN_INST(1, 8),  CN_MEAN_INST(1, 16), CN_MEAN_INST(2, 8),  CN_MEAN_INST(2, 16),
-    CN_MEAN_INST(3, 8),  CN_MEAN_INST(3, 16), CN_MEAN_INST(3, 14), CN_MEAN_INST(3, 29),
-    CN_MEAN_INST(4, 8),  CN_MEAN_INST(4, 16), CN_MEAN_INST(4, 14), CN_MEAN_INST(4, 29),
+    CN_MEAN_INST(1, 8, 4),  CN_MEAN_INST(1, 16, 4), CN_MEAN_INST(2, 8, 4),  CN_MEAN_INST(2, 16, 4),
+    CN_MEAN_INST(3, 8, 4),  CN_MEAN_INST(3, 16, 4), CN_MEAN_INST(3, 14, 4), CN_MEAN_INST(3, 29, 4),
+    CN_MEAN_INST(4, 8, 4),  CN_MEAN_INST(4, 16, 4), CN_MEAN_INST(4, 14, 4), CN_MEAN_INST(4, 29, 4),
+    CN_MEAN_INST(4, 29, 2), CN_MEAN_INST(3, 29, 2), CN_MEAN_INST(3, 14, 2),
 };
 #undef CN_MEAN_INST
 
@@ -273,7 +305,11 @@ int env_int(const char *name, int dflt) {
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     const int K = d.k;
     const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
-    if (d.groups != 1 || d.C_out % COT != 0) return CN_ERR_UNSUPPORTED;
+    if (d.groups != 1 || d.C_out % 4 != 0) return CN_ERR_UNSUPPORTED;
+    // Channel slice per thread: 2 lets two 256-thread CTAs share an SM
+    // (about 110 registers); 4 halves shared-memory traffic per FFMA but
+    // needs about 190.  Measured on the k=4 workload: 0.80 ms vs 0.93 ms.
+    const int want_cot = env_int("CN_MEAN3D_COT", 2);
     // pick the row width: an exact instantiation if there is one, else the
     // segmented width with the least padding.
     const Inst *best = nullptr;
@@ -284,14 +320,14 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
         if (nseg > 1 && (in.RW % 4) != 0) continue;  // float4 row loads need aligned segments
         const double waste = (double)nseg * in.RW / Wo;
         const double load = 1.0 + (double)(((in.RW + K - 1 + 3) / 4) + K) / (4.0 * K * in.RW);
-        const double cost = waste * load;
+        const double cost = waste * load * (in.COT == want_cot ? 1.0 : 1.001);
         if (cost < best_cost - 1e-12) {
             best_cost = cost;
             best = &in;
         }
     }
     if (!best) return CN_ERR_UNSUPPORTED;
-    const int RW = best->RW;
+    const int RW = best->RW, COT = best->COT;
     const int LOADW = (RW + K - 1 + 3) & ~3;
     a.N = d.N;
     a.Ci = d.C_in;
@@ -312,8 +348,9 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
         }
     a.wco = wco;
     a.ncob = d.C_out / (COT * wco);
-    int wrows = env_int("CN_MEAN3D_WROWS", std::max(1, 8 / wco));
-    wrows = std::max(1, std::min(wrows, 8 / wco > 0 ? 8 / wco : 1));
+    const int max_wrows = std::max(1, 8 / wco);
+    int wrows = env_int("CN_MEAN3D_WROWS", COT == 2 ? 1 : max_wrows);
+    wrows = std::max(1, std::min(wrows, max_wrows));
     a.wrows = wrows;
     a.rows_per_cta = 32 * wrows;
     a.nchunks = (a.rows + a.rows_per_cta - 1) / a.rows_per_cta;
@@ -330,6 +367,11 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     if (((pitch / 4) & 1) == 0) pitch += 4;  // pitch = 4 (mod 8): conflict-free row loads
     a.pitch = pitch;
     a.vec16 = (d.W % 4 == 0);
+    // One TMA box covers the CTA's planes: every box extent must be <= 256
+    // and the row stride a multiple of 16 bytes.
+    a.use_tma = (d.W % 4 == 0) && pitch <= 256 && d.H <= 256 && pm <= 256 && d.C_in <= 256 &&
+                env_int("CN_NO_TMA", 0) == 0;
+    a.tmap_base = nullptr;
     a.act = d.act;
     a.norm = d.norm;
     a.G = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
@@ -345,6 +387,7 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     cfg.name = best->name;
     cfg.K = K;
     cfg.RW = RW;
+    cfg.COT = COT;
     cfg.threads = 32 * wco * wrows;
     cfg.smem = (int)smem;
     const long long grid = (long long)d.N * a.ncob * a.nchunks;
@@ -365,8 +408,19 @@ int mean3d_prepare(const Mean3dConfig &cfg) {
     return CN_OK;
 }
 
-int mean3d_launch(const Mean3dConfig &cfg, const Mean3dArgs &a, cudaStream_t s) {
+int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s) {
     if (cfg.grid == 0) return CN_OK;
+    if (a.use_tma && a.tmap_base != a.x) {
+        const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D,
+                                  (uint64_t)a.N * a.Ci};
+        const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                     (uint64_t)a.D * a.H * a.W * 4};
+        const uint32_t box[4] = {(uint32_t)a.pitch, (uint32_t)a.H, (uint32_t)a.planes_max,
+                                 (uint32_t)a.Ci};
+        const int st = encode_tmap_f32_4d(&a.tmap, a.x, dims, strides, box);
+        if (st != CN_OK) return st;
+        a.tmap_base = a.x;
+    }
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }

@@ -12,64 +12,95 @@
 // window; each thread computes all CO channels x the 4 w positions of its
 // row (4*CO accumulators), applies bias + softmax per position in registers,
 // takes the max over its 4 positions, then a 4-step xor-shuffle max over the
-// voxel's 16 lanes.  Each CTA stages the (4+K-1)^3 input patch of each of its
-// voxels (all input channels) and the whole filter in shared memory.
+// voxel's 16 lanes.  Each CTA stages the (4+K-1)^3 x C_in input patch of each
+// of its 16 voxels with one TMA tensor copy per voxel, and the whole filter.
 #include "cn_common.cuh"
 #include "cn_internal.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace cn {
 namespace {
 
 template <int K, int CO>
-__global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(Pool3dArgs a) {
-    extern __shared__ __align__(16) float smem[];
-    constexpr int P = 4 + K - 1;  // patch extent per axis
+__global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_constant__ Pool3dArgs a) {
+    extern __shared__ __align__(128) float smem[];
+    __shared__ __align__(8) uint64_t bar;
+    constexpr int P = 4 + K - 1;      // patch extent per axis
+    constexpr int PX = (P + 3) & ~3;  // patch row pitch
     constexpr int KKK = K * K * K;
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int v = tid >> 4, l16 = tid & 15;
     const int dz = l16 >> 2, dy = l16 & 3;
     float *sx = smem;
     float *sw = smem + (size_t)a.vox_per_cta * a.vox_stride;
-
-    // ---- stage the filter, transposed to [ci][tap][co] ----
-    const int totalw = a.Ci * KKK * CO;
-    for (int i = tid; i < totalw; i += blockDim.x) {
-        const int co = i % CO, t = i / CO;
-        sw[i] = __ldg(a.w + (size_t)co * a.Ci * KKK + t);
-    }
-    // ---- stage each voxel's input patch ----
     const long long vbase = (long long)blockIdx.x * a.vox_per_cta;
-    const int rows = a.vox_per_cta * a.Ci * P * P;
-    for (int rI = tid; rI < rows; rI += blockDim.x) {
-        int t = rI;
-        const int yy = t % P;
-        t /= P;
-        const int zz = t % P;
-        t /= P;
-        const int ci = t % a.Ci;
-        const int vv = t / a.Ci;
-        long long gv = vbase + vv;
-        if (gv >= a.nvox) continue;
-        const int pw = (int)(gv % a.Pw);
-        gv /= a.Pw;
-        const int ph = (int)(gv % a.Ph);
-        gv /= a.Ph;
-        const int pd = (int)(gv % a.Pd);
-        const int n = (int)(gv / a.Pd);
-        const float *src = a.x + ((((size_t)n * a.Ci + ci) * a.D + 4 * pd + zz) * a.H + 4 * ph + yy) *
-                                     (size_t)a.W + 4 * pw;
-        float *dst = sx + (size_t)vv * a.vox_stride + ((ci * P + zz) * P + yy) * a.pw_pitch;
+    const int nv = (int)min((long long)a.vox_per_cta, a.nvox - vbase);
+
+    // ---- stage each voxel's (P x P x P) x C_in input patch ----
+    if (a.use_tma) {
+        if (tid == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+            fence_proxy_async();
+            mbar_arrive_expect_tx(&bar, (uint32_t)(nv * a.Ci * P * P * PX * 4));
+        }
+        __syncthreads();
+        if (tid < nv) {
+            long long gv = vbase + tid;
+            const int pw = (int)(gv % a.Pw);
+            gv /= a.Pw;
+            const int ph = (int)(gv % a.Ph);
+            gv /= a.Ph;
+            const int pd = (int)(gv % a.Pd);
+            const int n = (int)(gv / a.Pd);
+            tma_load_4d(sx + (size_t)tid * a.vox_stride, &a.tmap, 4 * pw, 4 * ph, 4 * pd, n * a.Ci,
+                        &bar);
+        }
+    } else {
+        const int rows = nv * a.Ci * P * P;
+        for (int rI = tid; rI < rows; rI += blockDim.x) {
+            int t = rI;
+            const int yy = t % P;
+            t /= P;
+            const int zz = t % P;
+            t /= P;
+            const int ci = t % a.Ci;
+            const int vv = t / a.Ci;
+            long long gv = vbase + vv;
+            const int pw = (int)(gv % a.Pw);
+            gv /= a.Pw;
+            const int ph = (int)(gv % a.Ph);
+            gv /= a.Ph;
+            const int pd = (int)(gv % a.Pd);
+            const int n = (int)(gv / a.Pd);
+            const float *src = a.x + ((((size_t)n * a.Ci + ci) * a.D + 4 * pd + zz) * a.H + 4 * ph + yy) *
+                                         (size_t)a.W + 4 * pw;
+            float *dst = sx + (size_t)vv * a.vox_stride + ((ci * P + zz) * P + yy) * PX;
 #pragma unroll
-        for (int c = 0; c < P; ++c) cp_async4(dst + c, src + c, true);
+            for (int c = 0; c < P; ++c) cp_async4(dst + c, src + c, true);
+        }
+        cp_async_commit();
     }
-    cp_async_commit();
-    cp_async_wait_all();
+    // ---- the filter, transposed to [ci][tap][co] ----
+    for (int t = warp; t < a.Ci * KKK; t += nwarps)
+        for (int co = lane; co < CO; co += 32) sw[t * CO + co] = __ldg(a.w + (size_t)co * a.Ci * KKK + t);
+    bool staged = true;
+    if (a.use_tma) {
+        staged = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        if (!staged) {
+            flag_error(a.err, ERR_TIMEOUT);
+            mbar_wait_bounded(&bar, 0, kWaitLimitNs);
+        }
+    } else {
+        cp_async_wait_all();
+    }
     __syncthreads();
 
     const long long gvox = vbase + v;
-    const bool valid = gvox < a.nvox;
+    const bool valid = v < nv;
 
     float acc[CO][4];
 #pragma unroll
@@ -77,16 +108,23 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(Pool3dArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[c][i] = 0.0f;
 
-    const float *xv = sx + (size_t)v * a.vox_stride;
-    for (int ci = 0; ci < a.Ci; ++ci) {
+    const float *xv = sx + (size_t)(valid ? v : 0) * a.vox_stride;
+    const int nci = staged ? a.Ci : 0;
+    for (int ci = 0; ci < nci; ++ci) {
         CN_UNROLL(CN_TAP_UNROLL)
         for (int kd = 0; kd < K; ++kd) {
             CN_UNROLL(CN_TAP_UNROLL)
             for (int kh = 0; kh < K; ++kh) {
-                const float *row = xv + ((ci * P + dz + kd) * P + dy + kh) * a.pw_pitch;
-                float xr[P];
+                const float *row = xv + ((ci * P + dz + kd) * P + dy + kh) * PX;
+                float xr[PX];
 #pragma unroll
-                for (int j = 0; j < P; ++j) xr[j] = row[j];
+                for (int j = 0; j < PX / 4; ++j) {
+                    const float4 t = *reinterpret_cast<const float4 *>(row + 4 * j);
+                    xr[4 * j + 0] = t.x;
+                    xr[4 * j + 1] = t.y;
+                    xr[4 * j + 2] = t.z;
+                    xr[4 * j + 3] = t.w;
+                }
 #pragma unroll
                 for (int kw = 0; kw < K; ++kw) {
                     const float4 *wp =
@@ -160,6 +198,11 @@ struct Inst {
 const Inst kInst[] = {CN_POOL_INST(1, 16), CN_POOL_INST(2, 16), CN_POOL_INST(3, 16),
                       CN_POOL_INST(4, 16)};
 #undef CN_POOL_INST
+
+int env_int(const char *name, int dflt) {
+    const char *v = getenv(name);
+    return v ? atoi(v) : dflt;
+}
 }  // namespace
 
 int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
@@ -167,7 +210,7 @@ int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
     for (const Inst &i : kInst)
         if (i.K == d.k && i.CO == d.C_out) in = &i;
     if (!in || d.groups != 1) return CN_ERR_UNSUPPORTED;
-    const int K = d.k, P = 4 + K - 1;
+    const int K = d.k, P = 4 + K - 1, PX = (P + 3) & ~3;
     a.N = d.N;
     a.Ci = d.C_in;
     a.D = d.D;
@@ -181,11 +224,12 @@ int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
     a.Pw = a.Wo / 4;
     a.nvox = (long long)d.N * a.Pd * a.Ph * a.Pw;
     a.vox_per_cta = 16;
-    a.pw_pitch = P;
-    int vs = d.C_in * P * P * P;
-    vs += (16 - vs % 32 + 32) % 32;  // voxel stride = 16 (mod 32): the two voxels of a warp use other banks
-    a.vox_stride = vs;
-    const size_t smem = ((size_t)a.vox_per_cta * vs + (size_t)d.C_in * K * K * K * in->CO) * 4;
+    a.pw_pitch = PX;
+    // each voxel patch starts 128-byte aligned (TMA destination)
+    a.vox_stride = (d.C_in * P * P * PX + 31) & ~31;
+    a.use_tma = (d.W % 4 == 0) && d.C_in <= 256 && env_int("CN_NO_TMA", 0) == 0;
+    a.tmap_base = nullptr;
+    const size_t smem = ((size_t)a.vox_per_cta * a.vox_stride + (size_t)d.C_in * K * K * K * in->CO) * 4;
     if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
     const long long grid = (a.nvox + a.vox_per_cta - 1) / a.vox_per_cta;
     if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
@@ -204,8 +248,18 @@ int pool3d_prepare(const Pool3dConfig &cfg) {
     return CN_OK;
 }
 
-int pool3d_launch(const Pool3dConfig &cfg, const Pool3dArgs &a, cudaStream_t s) {
+int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s) {
     if (cfg.grid == 0) return CN_OK;
+    if (a.use_tma && a.tmap_base != a.x) {
+        const int K = a.D - a.Do + 1, P = 4 + K - 1, PX = (P + 3) & ~3;
+        const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D, (uint64_t)a.N * a.Ci};
+        const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                     (uint64_t)a.D * a.H * a.W * 4};
+        const uint32_t box[4] = {(uint32_t)PX, (uint32_t)P, (uint32_t)P, (uint32_t)a.Ci};
+        const int st = encode_tmap_f32_4d(&a.tmap, a.x, dims, strides, box);
+        if (st != CN_OK) return st;
+        a.tmap_base = a.x;
+    }
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
     return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }

@@ -75,7 +75,7 @@ def _base(**kw):
     (dict(N=-1), -1),
     (dict(k=0), -1),
     (dict(act="softmax_c"), -2),              # no full-output softmax kernel
-    (dict(C_out=12), -2),                     # channel blocks of 8
+    (dict(C_out=10), -2),                     # channel slices of 4 or 8
     (dict(conv="conv3d", D=6, red="mean_spatial", groups=2, C_in=8), -2),
     (dict(N=0), 0),                           # empty batch is valid
 ])
