@@ -58,7 +58,7 @@ class conv_norm_info(ctypes.Structure):
 EXPORTED = ("conv_norm_desc_validate", "conv_norm_output_shape", "conv_norm_status_string",
             "conv_norm_plan_create", "conv_norm_plan_destroy", "conv_norm_workspace_bytes",
             "conv_norm_plan_info", "conv_norm_forward", "conv_norm_forward_host",
-            "conv_norm_plan_check_device")
+            "conv_norm_plan_check_device", "conv_norm_forward_noalloc")
 
 
 def _load():
@@ -89,6 +89,8 @@ def _load():
     lib.conv_norm_forward_host.restype = i
     lib.conv_norm_plan_check_device.argtypes = [vp, vp]
     lib.conv_norm_plan_check_device.restype = i
+    lib.conv_norm_forward_noalloc.argtypes = [pd] + fwd[1:]
+    lib.conv_norm_forward_noalloc.restype = i
     return lib
 
 
@@ -199,6 +201,14 @@ def conv_norm_forward_host(plan, x, w, b, gamma, beta, out, stream=None) -> int:
     return _check(lib.conv_norm_forward_host(plan, _ptr(x), _ptr(w), _ptr(b), _ptr(gamma),
                                              _ptr(beta), _ptr(out), _stream(stream)),
                   "conv_norm_forward_host")
+
+
+def conv_norm_forward_noalloc(desc, x, w, b, gamma, beta, out, stream=None) -> int:
+    """Forward without a plan or any allocation (spatial-mean problems only):
+    for callers that cannot call cudaMalloc; see include/conv_norm.h."""
+    return _check(lib.conv_norm_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(w), _ptr(b),
+                                                _ptr(gamma), _ptr(beta), _ptr(out),
+                                                _stream(stream)), "conv_norm_forward_noalloc")
 
 
 def conv_norm_plan_check_device(plan, stream=None) -> int:

@@ -179,6 +179,44 @@ int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
  */
 int conv_norm_plan_check_device(conv_norm_plan plan, void *cuda_stream);
 
+/* ---- forward without any allocation ------------------------------------------ */
+
+/*
+ * No counterpart in the transcripts: this exists for callers that cannot
+ * allocate device memory.  conv_norm_plan_create gets its workspace from
+ * cudaMalloc; an engine plugin or a real-time loop whose device memory is
+ * reserved up front by another allocator (a framework's caching allocator,
+ * a memory pool) may see that call fail or synchronize the device, and some
+ * programs must keep a fixed device-memory footprint after start-up.
+ *
+ * conv_norm_forward_noalloc runs the same computation as conv_norm_forward
+ * for the spatial-mean problems (desc->conv == CN_CONV3D, desc->red ==
+ * CN_RED_MEAN_SPATIAL; l2_p27's Conv3d -> HardSwish -> GroupNorm -> mean)
+ * without a plan and without any allocation: the kernel's scratch (partial
+ * moments and per-sample tickets) lives in one fixed array of 4 MiB in the
+ * library's device globals, which every GPU that loads the library holds
+ * until the process exits.  Arguments, layouts and alignment are those of
+ * conv_norm_forward; x, w, b, gamma, beta and out are caller-owned device
+ * pointers.  The call is asynchronous on cuda_stream.
+ *
+ * Limits and errors:
+ *  - a problem needing more than 4 MiB of scratch returns CN_ERR_UNSUPPORTED;
+ *    it needs about N * ceil(rows/32) * C_out * 24 bytes + 4 N bytes, where
+ *    rows = D_out * H_out (for example 2.4 MB for N=512, 16x32x32, k=4);
+ *  - other problem kinds return CN_ERR_UNSUPPORTED; malformed descriptors or
+ *    null/misaligned pointers CN_ERR_INVALID_ARG; a failed launch CN_ERR_CUDA;
+ *  - device-side wait timeouts are not recorded (there is no plan flag).
+ * All calls share the one array: calls whose work overlaps on the GPU (two
+ * streams, or two host threads) race and give wrong results; order them.
+ * Each call clears the tickets it needs before its kernel runs.
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (device current at the time of the call); make that
+ * first call before any stream capture on that device.
+ */
+int conv_norm_forward_noalloc(const conv_norm_desc *desc, const float *x, const float *w,
+                              const float *b, const float *gamma, const float *beta,
+                              float *out, void *cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
