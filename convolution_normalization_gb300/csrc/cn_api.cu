@@ -207,7 +207,7 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
     size_t vws = 0;
     switch (p->variant) {
         case V_MEAN3D:
-            st = mean3d_prepare(p->mean_cfg);
+            st = mean3d_prepare(p->mean_cfg, p->mean_args);
             vws = mean3d_workspace(p->mean_args);
             break;
         case V_POOL3D:

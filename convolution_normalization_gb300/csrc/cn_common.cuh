@@ -14,6 +14,12 @@
 #ifndef CN_TAP_UNROLL
 #define CN_TAP_UNROLL 1
 #endif
+// Unroll depth of the kh loop (the loop directly around one input-row load)
+// of the 3-D mean kernel: 4 measured fastest (0.756 / 0.729 / 0.710 ms for
+// 1 / 2 / 4 on the n512 workload).
+#ifndef CN_KH_UNROLL
+#define CN_KH_UNROLL 4
+#endif
 
 namespace cn {
 

@@ -38,13 +38,16 @@ struct Mean3dArgs {
     int ncob;         // co blocks per sample
     int wco;          // warps (co-slices of 4 channels) per co block
     int wrows;        // row groups per CTA
-    int planes_max;   // input depth planes staged per CTA
+    int planes_max;   // input depth planes staged per chunk
     int pitch;        // shared-memory row pitch in floats
+    int nbuf;         // staging buffers (2: next chunk prefetched during compute)
+    int buf_stride;   // floats per staging buffer (multiple of 32)
+    int items;        // N * ncob * nchunks work items, ordered (cob, n, chunk)
     int vec16;        // 1: 16-byte cp.async staging is legal
     int act, norm, G, affine;
     float eps, post_scale;
     double *partial;  // [N][nchunks][Co][3]  (count, mean, M2)
-    int *tickets;     // [N], zero between launches
+    int *tickets;     // [N] per-sample tickets, then [2] work/exit counters; zero between launches
 };
 typedef void (*Mean3dKernel)(Mean3dArgs);
 struct Mean3dConfig {
@@ -52,13 +55,13 @@ struct Mean3dConfig {
     const char *name;
     int K, RW, COT;
     int threads, smem;
-    int grid;
+    int grid;         // persistent CTAs (set by mean3d_prepare from the device)
 };
 // Chooses tiling + instantiation; fills the geometry fields of args.
 // Returns CN_OK or CN_ERR_UNSUPPORTED.
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
 size_t mean3d_workspace(const Mean3dArgs &a);
-int mean3d_prepare(const Mean3dConfig &cfg);  // sets smem attribute (needs a device)
+int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s);
 
 // ---------------------------------------------------------------------------

@@ -72,7 +72,8 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     // the scratch this problem needs: moments, then tickets (256-byte aligned)
     const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
     const size_t part_al = (part + 255) & ~(size_t)255;
-    if (part_al + (size_t)a.N * sizeof(int) > CN_NOALLOC_SCRATCH_BYTES) return CN_ERR_UNSUPPORTED;
+    if (part_al + (size_t)(a.N + 2) * sizeof(int) > CN_NOALLOC_SCRATCH_BYTES)
+        return CN_ERR_UNSUPPORTED;
     const bool need_aff = d->affine && d->norm != CN_NORM_NONE;
     if (!x || !w || !out) return CN_ERR_INVALID_ARG;
     if ((b != nullptr) != (d->has_bias == 1)) return CN_ERR_INVALID_ARG;
@@ -91,13 +92,14 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     a.partial = static_cast<double *>(base);
     a.tickets = reinterpret_cast<int *>(static_cast<char *>(base) + part_al);
     a.err = nullptr;  // no plan, so device-side timeouts are not recorded
-    // The array keeps the previous call's contents: the tickets must start at
-    // zero (every partial-moment slot is overwritten before it is read).
-    if (cudaMemsetAsync(a.tickets, 0, (size_t)a.N * sizeof(int), s) != cudaSuccess) {
+    // The array keeps the previous call's contents: the tickets and work
+    // counters must start at zero (every partial-moment slot is overwritten
+    // before it is read).
+    if (cudaMemsetAsync(a.tickets, 0, (size_t)(a.N + 2) * sizeof(int), s) != cudaSuccess) {
         cudaGetLastError();
         return CN_ERR_CUDA;
     }
-    st = cn::mean3d_prepare(cfg);
+    st = cn::mean3d_prepare(cfg, a);
     if (st != CN_OK) {
         cudaGetLastError();
         return st;

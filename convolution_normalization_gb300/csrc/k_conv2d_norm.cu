@@ -223,7 +223,8 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(const __grid_constant_
         __syncthreads();
         const float *sxb = smem + (size_t)buf * a.stage_floats;
         const float *swb = sxb + xstage;
-        const int ncl = ok ? min(a.cib, a.Cig - chunk * a.cib) : 0;
+        // uniform bound; after a timeout the flagged forward computes on stale data
+        const int ncl = min(a.cib, a.Cig - chunk * a.cib);
         for (int cl = 0; cl < ncl; ++cl) {
             CN_UNROLL(CN_TAP_UNROLL)
             for (int kh = 0; kh < K; ++kh) {

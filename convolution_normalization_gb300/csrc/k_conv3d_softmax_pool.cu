@@ -109,8 +109,10 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
         for (int i = 0; i < 4; ++i) acc[c][i] = 0.0f;
 
     const float *xv = sx + (size_t)(valid ? v : 0) * a.vox_stride;
-    const int nci = staged ? a.Ci : 0;
-    for (int ci = 0; ci < nci; ++ci) {
+    // Loop bounds depend only on kernel parameters (warp-uniform); after a
+    // staging timeout the flagged forward computes on stale shared memory.
+    (void)staged;
+    for (int ci = 0; ci < a.Ci; ++ci) {
         CN_UNROLL(CN_TAP_UNROLL)
         for (int kd = 0; kd < K; ++kd) {
             CN_UNROLL(CN_TAP_UNROLL)
