@@ -215,7 +215,7 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
             vws = 0;
             break;
         default:
-            st = full2d_prepare(p->full_cfg);
+            st = full2d_prepare(p->full_cfg, p->full_args);
             vws = full2d_workspace(p->full_args);
             break;
     }

@@ -107,16 +107,21 @@ struct Full2dArgs {
     int TR, NT;           // CTA tile: TR output rows x NT row segments
     int row_tiles, col_tiles, ncob, ntiles;
     int wco, wsp;         // warps: channel slices x spatial groups
-    int cib, nchunk;      // input channels per pipeline stage, stages
+    int cib, nchunk;      // input channels per pipeline stage, stages per tile
+    int nstage;           // stage buffers in shared memory (2..4)
     int rows_in, cols_in, pitch;
     int stage_floats;     // floats per pipeline stage (input + filter)
+    int xstage;           // floats of the input part of a stage
+    int wstage;           // floats of the filter part of a stage (cib * K*K * COB)
+    int items;            // tiles: N * ncob * ntiles, claimed through the work counter
+    float *wprep;         // filter regrouped per (channel block, chunk) stage layout
     int act, norm, NG, affine;
     float eps, post_scale;
     int apply_needed, vec4;
     long long S;          // Ho * Wo
-    double *partial;      // [N][Co][ntiles][3]
+    double *partial;      // [N][Co][ntiles * wsp][3]: one (count, mean, M2) per warp and tile
     float4 *coef;         // [N][Co]: (mu, a, bb, 0)
-    int *tickets;         // [N]
+    int *tickets;         // [N] (unused), then [2] work/exit counters
     int *err;
 };
 typedef void (*Full2dKernel)(Full2dArgs);
@@ -126,11 +131,13 @@ struct Full2dConfig {
     int K, RW, COT, VECW, transposed;
     int threads, smem, grid;
     int apply_threads, apply_grid_x, apply_grid_y;
+    int prep_grid;
+    int fin_threads;
 };
 int full2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
 size_t full2d_workspace(const Full2dArgs &a);
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag);
-int full2d_prepare(const Full2dConfig &cfg);
+int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a);  // needs a device: smem attribute, grid
 int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a);
 int full2d_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s);
 

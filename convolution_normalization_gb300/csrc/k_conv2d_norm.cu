@@ -37,7 +37,7 @@ namespace cn {
 namespace {
 
 // Bias + activation of RW values in place, then the moments of the first
-// nvalid of them.
+// nvalid of them (all of them on the common unmasked path).
 template <int RW, int ACT>
 CN_DEV Moments<float> act_moments(float (&v)[RW], float bias, int nvalid) {
 #pragma unroll
@@ -47,11 +47,21 @@ CN_DEV Moments<float> act_moments(float (&v)[RW], float bias, int nvalid) {
         if (ACT == ACT_GELU) t = gelu_erf(t);
         v[i] = t;
     }
-    float s = 0.0f;
+    float s = 0.0f, m2 = 0.0f;
+    if (nvalid == RW) {
+#pragma unroll
+        for (int i = 0; i < RW; ++i) s += v[i];
+        const float mean = s * (1.0f / RW);
+#pragma unroll
+        for (int i = 0; i < RW; ++i) {
+            const float d = v[i] - mean;
+            m2 = fmaf(d, d, m2);
+        }
+        return Moments<float>{(float)RW, mean, m2};
+    }
 #pragma unroll
     for (int i = 0; i < RW; ++i) s += (i < nvalid) ? v[i] : 0.0f;
     const float mean = nvalid > 0 ? s / (float)nvalid : 0.0f;
-    float m2 = 0.0f;
 #pragma unroll
     for (int i = 0; i < RW; ++i) {
         const float d = (i < nvalid) ? v[i] - mean : 0.0f;
@@ -60,11 +70,54 @@ CN_DEV Moments<float> act_moments(float (&v)[RW], float bias, int nvalid) {
     return Moments<float>{(float)nvalid, mean, m2};
 }
 
-template <int K, int RW, int COT, int VECW, bool TRANSPOSED>
-__global__ void __launch_bounds__(256) k_conv2d_act_stats(const __grid_constant__ Full2dArgs a) {
+// Filter pre-pass: writes, for every (channel block, input-channel chunk)
+// stage, the block's filter slice exactly as the conv kernel reads it from
+// shared memory: [cl][kh][kw][col], taps reversed for the transposed conv,
+// zero past the group's input channels.  One contiguous bulk copy per stage.
+__global__ void __launch_bounds__(256) k_prep_weights(const float *__restrict__ w, float *wprep,
+                                                      int K, int transposed, int Cig, int Cog,
+                                                      int COB, int cib, int nchunk, int total) {
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        int t = e;
+        const int col = t % COB;
+        t /= COB;
+        const int tap = t % (K * K);
+        t /= K * K;
+        const int cl = t % cib;
+        t /= cib;
+        const int chunk = t % nchunk;
+        const int cob = t / nchunk;
+        const int kh = tap / K, kw = tap - kh * K;
+        const int cil = chunk * cib + cl;
+        const int co = cob * COB + col;
+        float v = 0.0f;
+        if (cil < Cig) {
+            if (transposed) {
+                const int g = co / Cog, col_g = co - g * Cog;
+                v = w[(((size_t)(g * Cig + cil) * Cog + col_g) * K + (K - 1 - kh)) * K + (K - 1 - kw)];
+            } else {
+                v = w[(((size_t)co * Cig + cil) * K + kh) * K + kw];
+            }
+        }
+        wprep[e] = v;
+    }
+}
+
+// CTAs per SM an instantiation is compiled for: two with the small
+// 4-channel x 16-output thread tile (at most 128 registers), else one.
+constexpr int full_min_ctas(int COT, int RW) { return COT * RW <= 64 ? 2 : 1; }
+constexpr int kMaxStages = 4;  // deepest input pipeline the kernel supports
+
+// ACTT >= 0 compiles the epilogue for that one activation; -1 switches at
+// run time (three copies of the unrolled epilogue, more instruction cache).
+template <int K, int RW, int COT, int VECW, bool TRANSPOSED, int ACTT>
+__global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
+    k_conv2d_act_stats(const __grid_constant__ Full2dArgs a) {
     extern __shared__ __align__(128) float smem[];
-    __shared__ __align__(8) uint64_t bars[2];
-    __shared__ int s_last;
+    // full[b]: stage data in buffer b has landed; empty[b]: every warp is done
+    // reading buffer b
+    __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
+    __shared__ int s_tile[kMaxStages], s_chunk[kMaxStages];
     static_assert(COT == 4 || COT == 8, "channel slice of 4 or 8");
     constexpr int XW = RW + K - 1;
     constexpr int LOADW = (XW + VECW - 1) / VECW * VECW;
@@ -73,162 +126,224 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(const __grid_constant_
     const int cs = warp % a.wco;
     const int sg = warp / a.wco;
     const int COB = COT * a.wco;
-    int bid = blockIdx.x;
-    const int ct = bid % a.col_tiles;
-    bid /= a.col_tiles;
-    const int rt = bid % a.row_tiles;
-    bid /= a.row_tiles;
-    const int cob = bid % a.ncob;
-    const int n = bid / a.ncob;
-    const int co0 = cob * COB;
-    const int g = co0 / a.Cog;
-    const int ci0 = g * a.Cig;
-    const int r0 = rt * a.TR;
-    const int c0 = ct * a.NT * RW;
-    const int ir0 = TRANSPOSED ? r0 - (K - 1) : r0;
-    const int ic0 = TRANSPOSED ? c0 - (K - 1) : c0;
-    // Shared row buffers start at global column xs (a multiple of 4 when
-    // rows arrive by bulk copy); the tile's first column sits at offset off.
-    const int xs = a.use_bulk ? (ic0 & ~3) : ic0;
-    const int off = ic0 - xs;
-    const int gc_lo = max(ic0, 0) & ~3;
-    const int gc_hi = min((ic0 + a.cols_in + 3) & ~3, a.W);
-    const int gr_lo = max(ir0, 0), gr_hi = min(ir0 + a.rows_in, a.H);
 
-    const int item = sg * 32 + lane;
-    const int il = item % a.TR;
-    const int sl_raw = item / a.TR;
-    const bool item_ok = sl_raw < a.NT;
-    const int sl = item_ok ? sl_raw : 0;
-    const int orow = r0 + il;
-    const int ocol0 = c0 + sl * RW;
+    // tile t -> geometry; tiles are ordered (n, channel block, row tile, col tile)
+    struct Geo {
+        int n, cob, rt, ct, co0, ci0, r0, c0, ir0, ic0, xs, off, gc_lo, gc_hi;
+    };
+    auto geo = [&](int t) {
+        Geo G;
+        G.ct = t % a.col_tiles;
+        t /= a.col_tiles;
+        G.rt = t % a.row_tiles;
+        t /= a.row_tiles;
+        G.cob = t % a.ncob;
+        G.n = t / a.ncob;
+        G.co0 = G.cob * COB;
+        G.ci0 = (G.co0 / a.Cog) * a.Cig;
+        G.r0 = G.rt * a.TR;
+        G.c0 = G.ct * a.NT * RW;
+        G.ir0 = TRANSPOSED ? G.r0 - (K - 1) : G.r0;
+        G.ic0 = TRANSPOSED ? G.c0 - (K - 1) : G.c0;
+        // Shared row buffers start at global column xs (a multiple of 4 when
+        // rows arrive by bulk copy); the tile's first column sits at offset off.
+        G.xs = a.use_bulk ? (G.ic0 & ~3) : G.ic0;
+        G.off = G.ic0 - G.xs;
+        G.gc_lo = max(G.ic0, 0) & ~3;
+        G.gc_hi = min((G.ic0 + a.cols_in + 3) & ~3, a.W);
+        return G;
+    };
 
-    const int xstage = a.cib * a.rows_in * a.pitch;
-
-    // in-image rows of one stage by bulk async copies (issued by warp 0)
-    auto issue_bulk = [&](int chunk, int buf) {
+    // ---- producer (warp 0): one stage = (tile, chunk of cib input channels) ----
+    // Zeroes the stage's out-of-image rows (and, with several column tiles,
+    // its out-of-image columns), then brings the in-image part of each input
+    // row with one bulk copy and the prepared filter slice with another.  A
+    // tile of -1 marks the end of this CTA's work.
+    Geo PG{};          // producer's decoded current tile
+    int pg_tile = -1;
+    auto produce = [&](int tile, int chunk, int buf) {
+        float *sxb = smem + (size_t)buf * a.stage_floats;
+        if (tile < 0) {
+            if (lane == 0) {
+                s_tile[buf] = -1;
+                s_chunk[buf] = 0;
+                mbar_arrive_expect_tx(&full[buf], 0);
+            }
+            __syncwarp();
+            return;
+        }
+        if (tile != pg_tile) {
+            PG = geo(tile);
+            pg_tile = tile;
+        }
+        const Geo &G = PG;
         const int cbase = chunk * a.cib;
         const int ncl = min(a.cib, a.Cig - cbase);
+        const int gr_lo = max(G.ir0, 0), gr_hi = min(G.ir0 + a.rows_in, a.H);
+        const int top = gr_lo - G.ir0, bot = gr_hi - G.ir0;  // in-image rows are [top, bot)
+        for (int cl = 0; cl < ncl; ++cl) {
+            float *rows = sxb + (size_t)cl * a.rows_in * a.pitch;
+            for (int i = lane; i < top * a.pitch; i += 32) rows[i] = 0.0f;
+            for (int i = bot * a.pitch + lane; i < a.rows_in * a.pitch; i += 32) rows[i] = 0.0f;
+            if (a.col_tiles > 1) {
+                for (int rr = top; rr < bot; ++rr) {
+                    float *row = rows + (size_t)rr * a.pitch;
+                    for (int c = lane; c < G.gc_lo - G.xs; c += 32) row[c] = 0.0f;
+                    for (int c = G.gc_hi - G.xs + lane; c < a.pitch; c += 32) row[c] = 0.0f;
+                }
+            }
+        }
         const int nr = gr_hi - gr_lo;
-        const uint32_t row_bytes = (uint32_t)(gc_hi - gc_lo) * 4u;
-        float *sxb = smem + (size_t)buf * a.stage_floats;
+        const uint32_t row_bytes = (uint32_t)(G.gc_hi - G.gc_lo) * 4u;
         fence_proxy_async();
-        if (lane == 0) mbar_arrive_expect_tx(&bars[buf], (uint32_t)(ncl * nr) * row_bytes);
+        if (lane == 0) {
+            s_tile[buf] = tile;
+            s_chunk[buf] = chunk;
+            mbar_arrive_expect_tx(&full[buf],
+                                  (uint32_t)(ncl * nr) * row_bytes + (uint32_t)a.wstage * 4u);
+            bulk_load(sxb + a.xstage, a.wprep + ((size_t)G.cob * a.nchunk + chunk) * a.wstage,
+                      (uint32_t)a.wstage * 4u, &full[buf]);
+        }
         __syncwarp();
         for (int q = lane; q < ncl * nr; q += 32) {
             const int cl = q / nr, gr = gr_lo + q % nr;
             const float *src =
-                a.x + (((size_t)n * a.Ci + ci0 + cbase + cl) * a.H + gr) * a.W + gc_lo;
-            float *dst = sxb + (size_t)(cl * a.rows_in + gr - ir0) * a.pitch + (gc_lo - xs);
-            bulk_load(dst, src, row_bytes, &bars[buf]);
+                a.x + (((size_t)G.n * a.Ci + G.ci0 + cbase + cl) * a.H + gr) * a.W + G.gc_lo;
+            float *dst = sxb + (size_t)(cl * a.rows_in + gr - G.ir0) * a.pitch + (G.gc_lo - G.xs);
+            bulk_load(dst, src, row_bytes, &full[buf]);
         }
     };
-    // fallback for rows that are not 16-byte multiples: cp.async with zero fill
-    auto issue_cpasync = [&](int chunk, int buf) {
-        float *sxb = smem + (size_t)buf * a.stage_floats;
-        const int cbase = chunk * a.cib;
-        const int nrows = a.cib * a.rows_in;
-        for (int rI = warp; rI < nrows; rI += nwarps) {
-            const int cl = rI / a.rows_in, rr = rI - cl * a.rows_in;
-            const int gr = ir0 + rr;
-            const bool rok = (cbase + cl < a.Cig) && gr >= 0 && gr < a.H;
-            const float *src =
-                a.x + (((size_t)n * a.Ci + ci0 + (rok ? cbase + cl : 0)) * a.H + (rok ? gr : 0)) * a.W;
-            float *dst = sxb + (size_t)rI * a.pitch;
-            for (int cc = lane; cc < a.cols_in; cc += 32) {
-                const int gc = ic0 + cc;
-                const bool ok = rok && gc >= 0 && gc < a.W;
-                cp_async4(dst + cc, ok ? (const void *)(src + gc) : (const void *)a.x, ok);
+    // Work claims (warp 0): the first tile is blockIdx.x; later tiles come
+    // from the work counter, one claim kept in flight so its latency hides
+    // behind a whole tile of work.  A claimed tile is always processed.
+    int pending = 0;
+    auto claim = [&]() {
+        int t = __shfl_sync(0xffffffffu, pending, 0);
+        if (lane == 0 && t < a.items) pending = (int)gridDim.x + atomicAdd(a.tickets + a.N, 1);
+        return t < a.items ? t : -1;
+    };
+
+    // Both buffers start all zero: cells outside the image stay zero unless a
+    // stage of another column tile writes them (then the producer re-zeroes).
+    for (int i = tid; i < a.nstage * a.stage_floats; i += blockDim.x) smem[i] = 0.0f;
+    if (tid == 0) {
+        for (int b = 0; b < a.nstage; ++b) {
+            mbar_init(&full[b], 1);
+            mbar_init(&empty[b], nwarps);
+        }
+        fence_barrier_init();
+    }
+    fence_proxy_async();
+    __syncthreads();
+
+    // Producer state (warp 0): the last stage issued.  Stages run
+    // (tile, chunk 0 .. nchunk-1) per claimed tile; nstage-1 stages are kept
+    // in flight ahead of the consumers.
+    int p_tile = -1, p_chunk = 0;
+    bool p_done = false;
+    auto advance = [&]() {
+        if (p_chunk + 1 < a.nchunk) {
+            ++p_chunk;
+        } else {
+            p_tile = claim();
+            p_chunk = 0;
+        }
+    };
+    if (warp == 0) {
+        pending = (int)blockIdx.x;
+        p_tile = claim();
+        p_chunk = 0;
+        if (a.use_bulk) {
+            produce(p_tile, 0, 0);
+            p_done = p_tile < 0;
+            for (int b = 1; b < a.nstage - 1 && !p_done; ++b) {
+                advance();
+                produce(p_tile, p_chunk, b);
+                p_done = p_tile < 0;
             }
         }
-    };
-    // filter slice of one stage, taps reversed for the transposed conv
-    auto stage_weights = [&](int chunk, int buf) {
-        float *swb = smem + (size_t)buf * a.stage_floats + xstage;
-        const int cbase = chunk * a.cib;
-        for (int t = warp; t < a.cib * K * K; t += nwarps) {
-            const int cl = t / (K * K), tap = t - cl * (K * K);
-            const int kh = tap / K, kw = tap - kh * K;
-            const int cil = cbase + cl;
-            for (int col = lane; col < COB; col += 32) {
-                float v = 0.0f;
-                if (cil < a.Cig) {
-                    if (TRANSPOSED) {
-                        const int col_g = co0 - g * a.Cog + col;
-                        v = __ldg(a.w + (((size_t)(ci0 + cil) * a.Cog + col_g) * K + (K - 1 - kh)) * K +
-                                  (K - 1 - kw));
-                    } else {
-                        v = __ldg(a.w + (((size_t)(co0 + col) * a.Cig + cil) * K + kh) * K + kw);
-                    }
-                }
-                swb[t * COB + col] = v;
-            }
-        }
-    };
+    }
 
     float acc[COT][RW];
-#pragma unroll
-    for (int c = 0; c < COT; ++c)
-#pragma unroll
-        for (int i = 0; i < RW; ++i) acc[c][i] = 0.0f;
-
-    bool ok = true;
-    if (a.use_bulk) {
-        // Out-of-image rows and columns of both buffers stay zero for the
-        // whole kernel: bulk copies only ever write the in-image part of a row.
-        const int rows2 = 2 * a.cib * a.rows_in;
-        for (int rI = warp; rI < rows2; rI += nwarps) {
-            const int buf = rI / (a.cib * a.rows_in), rem = rI - buf * (a.cib * a.rows_in);
-            const int gr = ir0 + rem % a.rows_in;
-            float *row = smem + (size_t)buf * a.stage_floats + (size_t)rem * a.pitch;
-            const bool rin = gr >= 0 && gr < a.H;
-            const int z0 = rin ? gc_lo - xs : a.pitch;
-            const int z1 = rin ? gc_hi - xs : a.pitch;
-            for (int c = lane; c < a.pitch; c += 32)
-                if (c < z0 || c >= z1) row[c] = 0.0f;
-        }
-        if (tid == 0) {
-            mbar_init(&bars[0], 1);
-            mbar_init(&bars[1], 1);
-            fence_barrier_init();
-        }
-        fence_proxy_async();
-        __syncthreads();
-        if (warp == 0) issue_bulk(0, 0);
-    } else {
-        issue_cpasync(0, 0);
-        cp_async_commit();
-    }
-    stage_weights(0, 0);
-
-    for (int chunk = 0; chunk < a.nchunk; ++chunk) {
-        const int buf = chunk & 1;
-        if (chunk + 1 < a.nchunk) {
-            if (a.use_bulk) {
-                if (warp == 0) issue_bulk(chunk + 1, buf ^ 1);
-            } else {
-                issue_cpasync(chunk + 1, buf ^ 1);
-            }
-            stage_weights(chunk + 1, buf ^ 1);
-        }
+    Geo G{};
+    int il = 0, sl = 0;
+    bool item_ok = false;
+    for (int s = 0;; ++s) {
+        int buf = 0;
         if (a.use_bulk) {
-            if (ok && !mbar_wait_bounded(&bars[buf], (chunk >> 1) & 1, kWaitLimitNs)) {
-                ok = false;
+            buf = s % a.nstage;
+            // issue stage s+nstage-1 into the buffer stage s-1 used, once
+            // every warp has finished reading it
+            if (warp == 0 && !p_done) {
+                const int tb = (s + a.nstage - 1) % a.nstage;
+                advance();
+                if (s >= 1 && !mbar_wait_bounded(&empty[tb], ((s - 1) / a.nstage) & 1, kWaitLimitNs))
+                    flag_error(a.err, ERR_TIMEOUT);
+                produce(p_tile, p_chunk, tb);
+                p_done = p_tile < 0;
+            }
+            const uint32_t par = (uint32_t)(s / a.nstage) & 1u;
+            if (!mbar_wait_bounded(&full[buf], par, kWaitLimitNs)) {
                 flag_error(a.err, ERR_TIMEOUT);
+                mbar_wait_bounded(&full[buf], par, kWaitLimitNs);
             }
         } else {
-            cp_async_commit();
-            cp_async_wait<1>();
+            // synchronous staging with cp.async (rows not 16-byte multiples)
+            __syncthreads();  // everyone is done with the buffer and s_tile
+            if (warp == 0) {
+                if (s > 0) advance();
+                if (lane == 0) {
+                    s_tile[0] = p_tile;
+                    s_chunk[0] = p_chunk;
+                }
+            }
+            __syncthreads();
+            const int t = s_tile[0], ch = s_chunk[0];
+            if (t >= 0) {
+                const Geo H = geo(t);
+                float *sxb = smem;
+                const int cbase = ch * a.cib;
+                for (int rI = warp; rI < a.cib * a.rows_in; rI += nwarps) {
+                    const int cl = rI / a.rows_in, rr = rI - cl * a.rows_in;
+                    const int gr = H.ir0 + rr;
+                    const bool rok = (cbase + cl < a.Cig) && gr >= 0 && gr < a.H;
+                    const float *src = a.x + (((size_t)H.n * a.Ci + H.ci0 + (rok ? cbase + cl : 0)) * a.H +
+                                              (rok ? gr : 0)) * a.W;
+                    float *dst = sxb + (size_t)rI * a.pitch;
+                    for (int cc = lane; cc < a.cols_in; cc += 32) {
+                        const int gc = H.ic0 + cc;
+                        const bool okc = rok && gc >= 0 && gc < a.W;
+                        cp_async4(dst + cc, okc ? (const void *)(src + gc) : (const void *)a.x, okc);
+                    }
+                }
+                cp_async_commit();
+                const float *wsrc = a.wprep + ((size_t)H.cob * a.nchunk + ch) * a.wstage;
+                for (int i = tid; i < a.wstage; i += blockDim.x) sxb[a.xstage + i] = __ldg(wsrc + i);
+                cp_async_wait_all();
+            }
+            __syncthreads();
         }
-        __syncthreads();
+        const int tile = s_tile[buf], chunk = s_chunk[buf];
+        if (tile < 0) break;
+        if (chunk == 0) {
+            G = geo(tile);
+            const int it = sg * 32 + lane;
+            il = it % a.TR;
+            const int sl_raw = it / a.TR;
+            item_ok = sl_raw < a.NT;
+            sl = item_ok ? sl_raw : 0;
+#pragma unroll
+            for (int c = 0; c < COT; ++c)
+#pragma unroll
+                for (int i = 0; i < RW; ++i) acc[c][i] = 0.0f;
+        }
         const float *sxb = smem + (size_t)buf * a.stage_floats;
-        const float *swb = sxb + xstage;
-        // uniform bound; after a timeout the flagged forward computes on stale data
+        const float *swb = sxb + a.xstage;
         const int ncl = min(a.cib, a.Cig - chunk * a.cib);
         for (int cl = 0; cl < ncl; ++cl) {
             CN_UNROLL(CN_TAP_UNROLL)
             for (int kh = 0; kh < K; ++kh) {
-                const float *xp = sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + off + sl * RW;
+                const float *xp = sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + G.off + sl * RW;
                 float xr[LOADW];
                 if constexpr (VECW == 4) {
 #pragma unroll
@@ -272,103 +387,113 @@ __global__ void __launch_bounds__(256) k_conv2d_act_stats(const __grid_constant_
                 }
             }
         }
+        // this warp is done reading the buffer
+        if (a.use_bulk) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[buf]);
+        }
+
+        if (chunk == a.nchunk - 1) {
+            // ---- epilogue: bias + activation, pre-norm store, per-warp moments ----
+            const int orow = G.r0 + il;
+            const int ocol0 = G.c0 + sl * RW;
+            const bool row_ok = item_ok && orow < a.Ho;
+            const int nvalid = row_ok ? max(0, min(RW, a.Wo - ocol0)) : 0;
+            const int tin = G.rt * a.col_tiles + G.ct;
+#pragma unroll
+            for (int c = 0; c < COT; ++c) {
+                const int co = G.co0 + cs * COT + c;
+                const float bias = a.b ? __ldg(a.b + co) : 0.0f;
+                Moments<float> m;
+                if constexpr (ACTT >= 0) {
+                    m = act_moments<RW, ACTT>(acc[c], bias, nvalid);
+                } else {
+                    if (a.act == ACT_HARDSWISH)
+                        m = act_moments<RW, ACT_HARDSWISH>(acc[c], bias, nvalid);
+                    else if (a.act == ACT_GELU)
+                        m = act_moments<RW, ACT_GELU>(acc[c], bias, nvalid);
+                    else
+                        m = act_moments<RW, ACT_NONE>(acc[c], bias, nvalid);
+                }
+                float *op = a.out + (((size_t)G.n * a.Co + co) * a.Ho + (row_ok ? orow : 0)) * a.Wo + ocol0;
+                if (nvalid == RW) {
+                    if ((RW % 2) == 0 && (reinterpret_cast<uintptr_t>(op) & 7) == 0) {
+#pragma unroll
+                        for (int i = 0; i < RW - 1; i += 2)
+                            *reinterpret_cast<float2 *>(op + i) = make_float2(acc[c][i], acc[c][i + 1]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < RW; ++i) op[i] = acc[c][i];
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < RW; ++i)
+                        if (i < nvalid) op[i] = acc[c][i];
+                }
+                m = warp_merge(m);
+                if (lane == 0) {
+                    double *p = a.partial +
+                                ((((size_t)G.n * a.Co + co) * a.ntiles + tin) * a.wsp + sg) * 3;
+                    p[0] = m.n;
+                    p[1] = m.mean;
+                    p[2] = m.m2;
+                }
+            }
+        }
+    }
+    // the last CTA to leave resets the work counters for the next launch
+    __syncthreads();
+    if (tid == 0 && atomicAdd(a.tickets + a.N + 1, 1) == (int)gridDim.x - 1) {
+        a.tickets[a.N] = 0;
+        a.tickets[a.N + 1] = 0;
+    }
+}
+
+// Statistics of one normalization group: merges its channels' per-warp,
+// per-tile moments in a fixed order (fp64) and writes each channel's
+// coefficients (mu, a = gamma * rstd * scale, bb = beta * scale).
+__global__ void __launch_bounds__(256) k_group_stats(const __grid_constant__ Full2dArgs a) {
+    __shared__ double sm[256 * 3];
+    const int tid = threadIdx.x;
+    const int ng = blockIdx.x;  // (n, group)
+    const int n = ng / a.NG, g = ng % a.NG;
+    const int cpg = a.Co / a.NG;
+    const int per_c = a.ntiles * a.wsp;
+    const int total = cpg * per_c;
+    const double *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c * 3;
+    Moments<double> m{0.0, 0.0, 0.0};
+    for (int i = tid; i < total; i += blockDim.x)
+        m = merge(m, Moments<double>{p0[3 * i], p0[3 * i + 1], p0[3 * i + 2]});
+    sm[tid * 3] = m.n;
+    sm[tid * 3 + 1] = m.mean;
+    sm[tid * 3 + 2] = m.m2;
+    __syncthreads();
+    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+        if (tid < w) {
+            Moments<double> l{sm[tid * 3], sm[tid * 3 + 1], sm[tid * 3 + 2]};
+            const Moments<double> r{sm[(tid + w) * 3], sm[(tid + w) * 3 + 1], sm[(tid + w) * 3 + 2]};
+            l = merge(l, r);
+            sm[tid * 3] = l.n;
+            sm[tid * 3 + 1] = l.mean;
+            sm[tid * 3 + 2] = l.m2;
+        }
         __syncthreads();
     }
-    if (!ok && a.use_bulk) {
-        // let any copy still in flight land before this CTA's memory is reused
-        mbar_wait_bounded(&bars[0], 0, kWaitLimitNs);
-        mbar_wait_bounded(&bars[1], 0, kWaitLimitNs);
+    const double mean = sm[1], var = sm[2] / sm[0];
+    const double rstd = 1.0 / sqrt(var + (double)a.eps);
+    for (int cl = tid; cl < cpg; cl += blockDim.x) {
+        const int c = g * cpg + cl;
+        const double ga = a.affine ? (double)a.gamma[c] : 1.0;
+        const double be = a.affine ? (double)a.beta[c] : 0.0;
+        a.coef[(size_t)n * a.Co + c] = make_float4((float)mean, (float)(rstd * ga * a.post_scale),
+                                                   (float)(be * a.post_scale), 0.0f);
     }
+}
 
-    // ---- epilogue: bias + activation, store the pre-norm value, moments ----
-    double *sred = reinterpret_cast<double *>(smem + 2 * (size_t)a.stage_floats);
-    const bool row_ok = item_ok && orow < a.Ho;
-    const int nvalid = row_ok ? max(0, min(RW, a.Wo - ocol0)) : 0;
-#pragma unroll
-    for (int c = 0; c < COT; ++c) {
-        const int co = co0 + cs * COT + c;
-        const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-        Moments<float> m;
-        if (a.act == ACT_HARDSWISH)
-            m = act_moments<RW, ACT_HARDSWISH>(acc[c], bias, nvalid);
-        else if (a.act == ACT_GELU)
-            m = act_moments<RW, ACT_GELU>(acc[c], bias, nvalid);
-        else
-            m = act_moments<RW, ACT_NONE>(acc[c], bias, nvalid);
-        float *op = a.out + (((size_t)n * a.Co + co) * a.Ho + (row_ok ? orow : 0)) * a.Wo + ocol0;
-        if (nvalid == RW && (RW % 2) == 0 && (reinterpret_cast<uintptr_t>(op) & 7) == 0) {
-#pragma unroll
-            for (int i = 0; i < RW; i += 2)
-                *reinterpret_cast<float2 *>(op + i) = make_float2(acc[c][i], acc[c][i + 1]);
-        } else {
-#pragma unroll
-            for (int i = 0; i < RW; ++i)
-                if (i < nvalid) op[i] = acc[c][i];
-        }
-        m = warp_merge(m);
-        if (lane == 0) {
-            double *o = sred + ((size_t)sg * COB + cs * COT + c) * 3;
-            o[0] = m.n;
-            o[1] = m.mean;
-            o[2] = m.m2;
-        }
-    }
-    __syncthreads();
-    const int tile = rt * a.col_tiles + ct;
-    for (int c = tid; c < COB; c += blockDim.x) {
-        Moments<double> m{0.0, 0.0, 0.0};
-        for (int q = 0; q < a.wsp; ++q) {
-            const double *o = sred + ((size_t)q * COB + c) * 3;
-            m = merge(m, Moments<double>{o[0], o[1], o[2]});
-        }
-        double *p = a.partial + (((size_t)n * a.Co + co0 + c) * a.ntiles + tile) * 3;
-        p[0] = m.n;
-        p[1] = m.mean;
-        p[2] = m.m2;
-    }
-
-    // ---- the last CTA of sample n turns the moments into coefficients ----
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int prev = atomicAdd(a.tickets + n, 1);
-        s_last = (prev == a.ncob * a.ntiles - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    double *sch = reinterpret_cast<double *>(smem);
-    for (int c = tid; c < a.Co; c += blockDim.x) {
-        Moments<double> m{0.0, 0.0, 0.0};
-        const double *p = a.partial + ((size_t)n * a.Co + c) * a.ntiles * 3;
-        for (int t = 0; t < a.ntiles; ++t)
-            m = merge(m, Moments<double>{ldcg_f64(p + 3 * t), ldcg_f64(p + 3 * t + 1),
-                                         ldcg_f64(p + 3 * t + 2)});
-        sch[c * 3 + 0] = m.n;
-        sch[c * 3 + 1] = m.mean;
-        sch[c * 3 + 2] = m.m2;
-    }
-    __syncthreads();
-    for (int c = tid; c < a.Co; c += blockDim.x) {
-        float4 cf;
-        if (a.norm == CN_NORM_NONE) {
-            cf = make_float4(0.0f, a.post_scale, 0.0f, 0.0f);
-        } else {
-            const int cpg = a.Co / a.NG, gg = c / cpg;
-            Moments<double> mg{0.0, 0.0, 0.0};
-            for (int j = 0; j < cpg; ++j) {
-                const int cc = gg * cpg + j;
-                mg = merge(mg, Moments<double>{sch[cc * 3], sch[cc * 3 + 1], sch[cc * 3 + 2]});
-            }
-            const double rstd = 1.0 / sqrt(mg.m2 / mg.n + (double)a.eps);
-            const double ga = a.affine ? (double)a.gamma[c] : 1.0;
-            const double be = a.affine ? (double)a.beta[c] : 0.0;
-            cf = make_float4((float)mg.mean, (float)(rstd * ga * a.post_scale),
-                             (float)(be * a.post_scale), 0.0f);
-        }
-        a.coef[(size_t)n * a.Co + c] = cf;
-    }
-    if (tid == 0) a.tickets[n] = 0;
+// Coefficients of a pure post scale (no normalization): (0, scale, 0).
+__global__ void k_fill_scale(float4 *coef, int n, float scale) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) coef[i] = make_float4(0.0f, scale, 0.0f, 0.0f);
 }
 
 // Normalize pass: out = (y - mu) * a + bb per (n, c) plane, in place.
@@ -396,18 +521,21 @@ __global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *co
 }
 
 struct Inst {
-    int K, RW, COT, VECW, T;
+    int K, RW, COT, VECW, T, ACT;  // ACT -1: activation chosen at run time
     Full2dKernel fn;
     const char *name;
 };
-#define CN_FULL_INST(K, RW, C, V, T)                            \
-    {K, RW, C, V, T, k_conv2d_act_stats<K, RW, C, V, (T != 0)>, \
-     "k_conv2d_act_stats<" #K "," #RW "," #C "," #V "," #T ">,k_norm_apply"}
+#define CN_FULL_INST(K, RW, C, V, T, A)                            \
+    {K, RW, C, V, T, A, k_conv2d_act_stats<K, RW, C, V, (T != 0), A>, \
+     "k_prep_weights,k_conv2d_act_stats<" #K "," #RW "," #C "," #V "," #T "," #A ">,k_group_stats,k_norm_apply"}
 const Inst kInst[] = {
-    CN_FULL_INST(3, 16, 8, 4, 0), CN_FULL_INST(3, 16, 4, 4, 0), CN_FULL_INST(1, 16, 8, 4, 0),
-    CN_FULL_INST(2, 16, 8, 4, 0), CN_FULL_INST(4, 16, 8, 4, 0), CN_FULL_INST(3, 13, 8, 1, 1),
-    CN_FULL_INST(3, 13, 4, 1, 1), CN_FULL_INST(3, 16, 8, 2, 1), CN_FULL_INST(3, 16, 4, 2, 1),
-    CN_FULL_INST(1, 16, 8, 4, 1), CN_FULL_INST(2, 16, 8, 1, 1), CN_FULL_INST(4, 16, 8, 1, 1),
+    // activation-specialised: the 64->128 conv (none), the grouped transposed conv (GELU)
+    CN_FULL_INST(3, 16, 4, 4, 0, 0), CN_FULL_INST(3, 16, 4, 2, 1, 2), CN_FULL_INST(3, 13, 4, 1, 1, 2),
+    // run-time activation
+    CN_FULL_INST(3, 16, 8, 4, 0, -1), CN_FULL_INST(3, 16, 4, 4, 0, -1), CN_FULL_INST(1, 16, 8, 4, 0, -1),
+    CN_FULL_INST(2, 16, 8, 4, 0, -1), CN_FULL_INST(4, 16, 8, 4, 0, -1), CN_FULL_INST(3, 13, 4, 1, 1, -1),
+    CN_FULL_INST(3, 16, 4, 2, 1, -1), CN_FULL_INST(1, 16, 8, 4, 1, -1), CN_FULL_INST(2, 16, 8, 1, 1, -1),
+    CN_FULL_INST(4, 16, 8, 1, 1, -1),
 };
 #undef CN_FULL_INST
 
@@ -442,6 +570,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     Choice best;
     for (const Inst &in : kInst) {
         if (in.K != K || in.T != T || Cog % in.COT != 0) continue;
+        if (in.ACT >= 0 && in.ACT != d.act) continue;
         if ((f_cot && in.COT != f_cot) || (f_rw && in.RW != f_rw)) continue;
         if (off % in.VECW != 0) continue;
         const int wco = pick_wco(Cog / in.COT);
@@ -471,7 +600,9 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
             const double balance =
                 (warps_sm % 4 == 0) ? 1.0 : (double)((warps_sm + 3) / 4 * 4) / warps_sm;
             const double occ = warps_sm >= 16 ? 1.0 : 1.0 + 0.025 * (16 - warps_sm);
-            const double cost = waste * ratio * balance * occ;
+            // a specialised epilogue is smaller and cheaper than the run-time switch
+            const double spec = in.ACT >= 0 ? 0.97 : 1.0;
+            const double cost = waste * ratio * balance * occ * spec;
             if (cost < best.cost - 1e-9) {
                 best.in = &in;
                 best.wco = wco;
@@ -516,11 +647,23 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.pitch = pitch;
     const int COB = COT * a.wco;
     const int per_ci = a.rows_in * pitch + K * K * COB;
-    int cib = std::min(Cig, 8);
-    while (cib > 1 && 2 * (size_t)cib * per_ci * 4 > 100 * 1024) --cib;
+    // Pipeline: 3 stages (measured best of 2..4 on both 2-D workloads) when
+    // they fit the shared-memory budget with chunks of at least 2 input
+    // channels, fewer otherwise.
+    const size_t budget = (in.COT * in.RW <= 64 ? 108 : 216) * 1024;
+    int nstage = std::max(2, std::min(kMaxStages, env_int("CN_FULL2D_NSTAGE", 3)));
+    int cib = 1;
+    for (;; --nstage) {
+        cib = std::min(Cig, std::max(1, env_int("CN_FULL2D_CIB", 8)));
+        while (cib > 1 && (size_t)nstage * cib * per_ci * 4 > budget) --cib;
+        if (cib >= std::min(Cig, 2) || nstage == 2) break;
+    }
+    a.nstage = nstage;
     a.cib = cib;
     a.nchunk = (Cig + cib - 1) / cib;
-    a.stage_floats = ((cib * per_ci) + 31) & ~31;  // 128-byte aligned stages
+    a.xstage = cib * a.rows_in * pitch;
+    a.wstage = cib * K * K * COB;
+    a.stage_floats = ((a.xstage + a.wstage) + 31) & ~31;  // 128-byte aligned stages
     a.act = d.act;
     a.norm = d.norm;
     a.NG = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
@@ -531,11 +674,12 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.apply_needed = !(d.norm == CN_NORM_NONE && d.post_scale == 1.0f);
     a.vec4 = (a.S % 4) == 0;
     const int threads = 32 * a.wco * a.wsp;
-    size_t smem = (size_t)2 * a.stage_floats * 4 + (size_t)a.wsp * COB * 3 * 8;
-    smem = std::max(smem, (size_t)d.C_out * 3 * 8);
+    const size_t smem = (size_t)a.nstage * a.stage_floats * 4;
     if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
-    const long long grid = (long long)d.N * a.ncob * a.ntiles;
-    if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    const long long items = (long long)d.N * a.ncob * a.ntiles;
+    if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    a.items = (int)items;
+    a.wprep = nullptr;
     cfg.kern = in.fn;
     cfg.names = in.name;
     cfg.K = K;
@@ -545,7 +689,9 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     cfg.transposed = T;
     cfg.threads = threads;
     cfg.smem = (int)smem;
-    cfg.grid = (int)grid;
+    cfg.grid = (int)std::min<long long>(items, 148);  // refined from the device in full2d_prepare
+    const long long wtotal = (long long)a.ncob * a.nchunk * a.wstage;
+    cfg.prep_grid = (int)std::max(1LL, std::min((wtotal + 255) / 256, 1024LL));
     cfg.apply_threads = 256;
     const long long units = a.vec4 ? a.S / 4 : a.S;
     long long gy = (units + 256 * 4 - 1) / (256 * 4);
@@ -557,38 +703,62 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
 }
 
 size_t full2d_workspace(const Full2dArgs &a) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * 3 * sizeof(double);
+    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * 3 * sizeof(double);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
-    return ((part + 255) & ~(size_t)255) + ((coef + 255) & ~(size_t)255) + (size_t)a.N * sizeof(int);
+    const size_t tick = (size_t)(a.N + 2) * sizeof(int);
+    const size_t wprep = (size_t)a.ncob * a.nchunk * a.wstage * sizeof(float);
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    return al(part) + al(coef) + al(tick) + al(wprep);
 }
 
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * 3 * sizeof(double);
+    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * 3 * sizeof(double);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
+    const size_t tick = (size_t)(a.N + 2) * sizeof(int);
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
     a.partial = reinterpret_cast<double *>(base);
-    a.coef = reinterpret_cast<float4 *>(base + ((part + 255) & ~(size_t)255));
-    a.tickets = reinterpret_cast<int *>(base + ((part + 255) & ~(size_t)255) +
-                                        ((coef + 255) & ~(size_t)255));
+    a.coef = reinterpret_cast<float4 *>(base + al(part));
+    a.tickets = reinterpret_cast<int *>(base + al(part) + al(coef));
+    a.wprep = reinterpret_cast<float *>(base + al(part) + al(coef) + al(tick));
     a.err = err_flag;
 }
 
-int full2d_prepare(const Full2dConfig &cfg) {
+int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a) {
     if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
+    // persistent grid: every CTA slot of the device, capped by the tiles
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kern, cfg.threads, cfg.smem) !=
+            cudaSuccess)
+        return CN_ERR_CUDA;
+    if (per_sm < 1) return CN_ERR_UNSUPPORTED;
+    cfg.grid = (int)std::min<long long>((long long)sms * per_sm, (long long)a.items);
     return CN_OK;
 }
 
 int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a) {
-    if (cfg.grid == 0) return 0;
-    return 1 + (a.apply_needed ? 1 : 0);
+    if (cfg.grid == 0 || a.items == 0) return 0;
+    return 2 + (a.apply_needed ? 2 : 0);
 }
 
 int full2d_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s) {
-    if (cfg.grid == 0) return CN_OK;
+    if (cfg.grid == 0 || a.items == 0) return CN_OK;
+    const int wtotal = a.ncob * a.nchunk * a.wstage;
+    k_prep_weights<<<cfg.prep_grid, 256, 0, s>>>(a.w, a.wprep, cfg.K, cfg.transposed, a.Cig, a.Cog,
+                                                  cfg.COT * a.wco, a.cib, a.nchunk, wtotal);
+    if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
     if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     if (a.apply_needed) {
+        if (a.norm == CN_NORM_NONE) {
+            k_fill_scale<<<(a.N * a.Co + 255) / 256, 256, 0, s>>>(a.coef, a.N * a.Co, a.post_scale);
+        } else {
+            k_group_stats<<<a.N * a.NG, 256, 0, s>>>(a);
+        }
+        if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
         dim3 grid(cfg.apply_grid_x, cfg.apply_grid_y);
         k_norm_apply<<<grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4);
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
