@@ -84,6 +84,24 @@ CN_DEV Moments<T> merge(Moments<T> a, Moments<T> b) {
     r.m2 = a.m2 + b.m2 + d * d * a.n * fb;
     return r;
 }
+// Shifted power sums (count, S1 = sum(v - K), S2 = sum((v - K)^2)) with a
+// shift K close to the data: summed with plain additions (a butterfly of
+// commutative adds gives every lane the identical result), converted to
+// (count, mean, M2) once, in fp64, as mean = K + S1/n, M2 = S2 - S1^2/n.
+CN_DEV float3 warp_sum3(float3 v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
+        v.z += __shfl_xor_sync(0xffffffffu, v.z, off);
+    }
+    return v;
+}
+CN_DEV Moments<double> moments_from_sums(double n, double K, double s1, double s2) {
+    if (n <= 0.0) return Moments<double>{0.0, 0.0, 0.0};
+    const double m2 = s2 - s1 * s1 / n;
+    return Moments<double>{n, K + s1 / n, m2 > 0.0 ? m2 : 0.0};
+}
 // Butterfly merge over the 32 lanes of a warp; every lane ends with the result.
 CN_DEV Moments<float> warp_merge(Moments<float> m) {
 #pragma unroll

@@ -119,7 +119,8 @@ struct Full2dArgs {
     float eps, post_scale;
     int apply_needed, vec4;
     long long S;          // Ho * Wo
-    double *partial;      // [N][Co][ntiles * wsp][3]: one (count, mean, M2) per warp and tile
+    float4 *partial;      // [N][Co][ntiles * wsp]: per warp and tile (count, K, S1, S2),
+                          // shifted sums S1 = sum(v - K), S2 = sum((v - K)^2)
     float4 *coef;         // [N][Co]: (mu, a, bb, 0)
     int *tickets;         // [N] (unused), then [2] work/exit counters
     int *err;

@@ -7,12 +7,13 @@
 // group span a whole (C/G) x H x W block of one sample, so nothing can be
 // normalized before the whole block is computed.  The transcripts' answer is
 // a pass that computes the conv, a statistics step and a normalize pass; here
-// that is two launches:
+// that is three launches (after a tiny filter pre-pass):
 //   A. conv + bias + activation for a tile, the pre-norm value written to
-//      out, and per-(n, c, tile) moments (count, mean, M2); the last CTA of
-//      each sample merges the moments in a fixed order (fp64) into
-//      per-channel coefficients (mu_g, a = gamma*rstd*scale, bb = beta*scale);
-//   B. a single read-modify-write of out: (y - mu) * a + bb.
+//      out, and per-(n, c, tile, warp) shifted power sums;
+//   B. a small pass merging each normalization group's sums in a fixed order
+//      (fp64) into per-channel coefficients (mu_g, a = gamma*rstd*scale,
+//      bb = beta*scale);
+//   C. a single read-modify-write of out: (y - mu) * a + bb.
 // The transposed conv is handled as the adjoint of the stride-1 conv
 // (l2_p19 derivation): output (i, j) gathers x[i - p][j - q] * w[ci][co][p][q]
 // with out-of-range x read as zero; the tile origin is shifted by K-1 and
@@ -36,38 +37,36 @@
 namespace cn {
 namespace {
 
-// Bias + activation of RW values in place, then the moments of the first
-// nvalid of them (all of them on the common unmasked path).
+template <int ACT>
+CN_DEV float act_value(float t) {
+    if (ACT == ACT_HARDSWISH) return hardswish(t);
+    if (ACT == ACT_GELU) return gelu_erf(t);
+    return t;
+}
+
+// Bias + activation of RW values in place, then the shifted sums
+// (count, S1, S2) of the first nvalid of them (all on the common path).
 template <int RW, int ACT>
-CN_DEV Moments<float> act_moments(float (&v)[RW], float bias, int nvalid) {
+CN_DEV float3 act_sums(float (&v)[RW], float bias, float K, int nvalid) {
 #pragma unroll
-    for (int i = 0; i < RW; ++i) {
-        float t = v[i] + bias;
-        if (ACT == ACT_HARDSWISH) t = hardswish(t);
-        if (ACT == ACT_GELU) t = gelu_erf(t);
-        v[i] = t;
-    }
-    float s = 0.0f, m2 = 0.0f;
+    for (int i = 0; i < RW; ++i) v[i] = act_value<ACT>(v[i] + bias);
+    float s1 = 0.0f, s2 = 0.0f;
     if (nvalid == RW) {
 #pragma unroll
-        for (int i = 0; i < RW; ++i) s += v[i];
-        const float mean = s * (1.0f / RW);
+        for (int i = 0; i < RW; ++i) {
+            const float d = v[i] - K;
+            s1 += d;
+            s2 = fmaf(d, d, s2);
+        }
+    } else {
 #pragma unroll
         for (int i = 0; i < RW; ++i) {
-            const float d = v[i] - mean;
-            m2 = fmaf(d, d, m2);
+            const float d = (i < nvalid) ? v[i] - K : 0.0f;
+            s1 += d;
+            s2 = fmaf(d, d, s2);
         }
-        return Moments<float>{(float)RW, mean, m2};
     }
-#pragma unroll
-    for (int i = 0; i < RW; ++i) s += (i < nvalid) ? v[i] : 0.0f;
-    const float mean = nvalid > 0 ? s / (float)nvalid : 0.0f;
-#pragma unroll
-    for (int i = 0; i < RW; ++i) {
-        const float d = (i < nvalid) ? v[i] - mean : 0.0f;
-        m2 = fmaf(d, d, m2);
-    }
-    return Moments<float>{(float)nvalid, mean, m2};
+    return make_float3((float)nvalid, s1, s2);
 }
 
 // Filter pre-pass: writes, for every (channel block, input-channel chunk)
@@ -404,16 +403,23 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
             for (int c = 0; c < COT; ++c) {
                 const int co = G.co0 + cs * COT + c;
                 const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-                Moments<float> m;
+                // shift: the activated bias, a typical value of this channel
+                float3 m;
+                float K;
                 if constexpr (ACTT >= 0) {
-                    m = act_moments<RW, ACTT>(acc[c], bias, nvalid);
+                    K = act_value<ACTT>(bias);
+                    m = act_sums<RW, ACTT>(acc[c], bias, K, nvalid);
                 } else {
-                    if (a.act == ACT_HARDSWISH)
-                        m = act_moments<RW, ACT_HARDSWISH>(acc[c], bias, nvalid);
-                    else if (a.act == ACT_GELU)
-                        m = act_moments<RW, ACT_GELU>(acc[c], bias, nvalid);
-                    else
-                        m = act_moments<RW, ACT_NONE>(acc[c], bias, nvalid);
+                    if (a.act == ACT_HARDSWISH) {
+                        K = act_value<ACT_HARDSWISH>(bias);
+                        m = act_sums<RW, ACT_HARDSWISH>(acc[c], bias, K, nvalid);
+                    } else if (a.act == ACT_GELU) {
+                        K = act_value<ACT_GELU>(bias);
+                        m = act_sums<RW, ACT_GELU>(acc[c], bias, K, nvalid);
+                    } else {
+                        K = bias;
+                        m = act_sums<RW, ACT_NONE>(acc[c], bias, K, nvalid);
+                    }
                 }
                 float *op = a.out + (((size_t)G.n * a.Co + co) * a.Ho + (row_ok ? orow : 0)) * a.Wo + ocol0;
                 if (nvalid == RW) {
@@ -430,14 +436,10 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                     for (int i = 0; i < RW; ++i)
                         if (i < nvalid) op[i] = acc[c][i];
                 }
-                m = warp_merge(m);
-                if (lane == 0) {
-                    double *p = a.partial +
-                                ((((size_t)G.n * a.Co + co) * a.ntiles + tin) * a.wsp + sg) * 3;
-                    p[0] = m.n;
-                    p[1] = m.mean;
-                    p[2] = m.m2;
-                }
+                m = warp_sum3(m);
+                if (lane == 0)
+                    a.partial[(((size_t)G.n * a.Co + co) * a.ntiles + tin) * a.wsp + sg] =
+                        make_float4(m.x, K, m.y, m.z);
             }
         }
     }
@@ -460,10 +462,12 @@ __global__ void __launch_bounds__(256) k_group_stats(const __grid_constant__ Ful
     const int cpg = a.Co / a.NG;
     const int per_c = a.ntiles * a.wsp;
     const int total = cpg * per_c;
-    const double *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c * 3;
+    const float4 *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c;
     Moments<double> m{0.0, 0.0, 0.0};
-    for (int i = tid; i < total; i += blockDim.x)
-        m = merge(m, Moments<double>{p0[3 * i], p0[3 * i + 1], p0[3 * i + 2]});
+    for (int i = tid; i < total; i += blockDim.x) {
+        const float4 q = p0[i];
+        m = merge(m, moments_from_sums(q.x, q.y, q.z, q.w));
+    }
     sm[tid * 3] = m.n;
     sm[tid * 3 + 1] = m.mean;
     sm[tid * 3 + 2] = m.m2;
@@ -590,7 +594,9 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
             const int rtiles = (Ho + TR - 1) / TR;
             const double waste = ((double)rtiles * TR / Ho) * ((double)ctiles * NT * in.RW / Wo) *
                                  ((double)lanes / (TR * NT));
-            const double loads = (double)loadw / in.VECW + 3.0 * in.COT / 4.0;
+            // scalar row loads count double: more instructions in flight and
+            // bank conflicts (measured: 16-wide float2 rows beat 13-wide scalar)
+            const double loads = (double)loadw / in.VECW * (in.VECW == 1 ? 2.0 : 1.0) + 3.0 * in.COT / 4.0;
             const double ratio = 1.0 + loads / ((double)in.COT * K * in.RW);
             const int threads = 32 * wco * wsp;
             const int ctas = std::max(1, std::min(65536 / (threads * ((regs + 7) & ~7)), 2));
@@ -703,7 +709,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
 }
 
 size_t full2d_workspace(const Full2dArgs &a) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * 3 * sizeof(double);
+    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
     const size_t tick = (size_t)(a.N + 2) * sizeof(int);
     const size_t wprep = (size_t)a.ncob * a.nchunk * a.wstage * sizeof(float);
@@ -712,11 +718,11 @@ size_t full2d_workspace(const Full2dArgs &a) {
 }
 
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * 3 * sizeof(double);
+    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
     const size_t tick = (size_t)(a.N + 2) * sizeof(int);
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
-    a.partial = reinterpret_cast<double *>(base);
+    a.partial = reinterpret_cast<float4 *>(base);
     a.coef = reinterpret_cast<float4 *>(base + al(part));
     a.tickets = reinterpret_cast<int *>(base + al(part) + al(coef));
     a.wprep = reinterpret_cast<float *>(base + al(part) + al(coef) + al(tick));
