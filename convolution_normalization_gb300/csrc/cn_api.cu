@@ -1,6 +1,7 @@
 // C-ABI layer: descriptor validation, plans, dispatch to the kernel variants.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -15,9 +16,20 @@ namespace {
 
 enum Variant { V_MEAN3D = 0, V_POOL3D = 1, V_FULL2D = 2 };
 
+constexpr int kMaxHostChunks = 8;
+
+// Device staging for conv_norm_forward_host, created on its first call:
+// buffers, per-chunk plans, and the upload / download streams and events
+// that overlap chunk i+1's upload (and chunk i-1's download) with chunk i's
+// kernels.
 struct HostStage {
     float *x = nullptr, *w = nullptr, *b = nullptr, *gamma = nullptr, *beta = nullptr,
           *out = nullptr;
+    bool ready = false;
+    int nchunk = 1, chunk_n = 0;
+    conv_norm_plan_s *sub[kMaxHostChunks] = {};  // one plan per chunk (keeps its tensor map)
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t ev_up[kMaxHostChunks] = {}, ev_done[kMaxHostChunks] = {};
 };
 
 }  // namespace
@@ -270,6 +282,13 @@ void conv_norm_plan_destroy(conv_norm_plan p) {
     cudaFree(p->stage.gamma);
     cudaFree(p->stage.beta);
     cudaFree(p->stage.out);
+    for (int i = 0; i < kMaxHostChunks; ++i) conv_norm_plan_destroy(p->stage.sub[i]);
+    if (p->stage.up) cudaStreamDestroy(p->stage.up);
+    if (p->stage.down) cudaStreamDestroy(p->stage.down);
+    for (int i = 0; i < kMaxHostChunks; ++i) {
+        if (p->stage.ev_up[i]) cudaEventDestroy(p->stage.ev_up[i]);
+        if (p->stage.ev_done[i]) cudaEventDestroy(p->stage.ev_done[i]);
+    }
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     cudaGetLastError();
     delete p;
@@ -371,6 +390,53 @@ static int stage_alloc(float **dst, int64_t n) {
     return CN_OK;
 }
 
+// Sets up the staging of conv_norm_forward_host: the batch is cut into up
+// to kMaxHostChunks chunks of whole samples (every step of the computation
+// is per sample) so uploads, kernels and downloads of different chunks
+// overlap.  One chunk when the batch is small or a sample's tensors are not
+// 16-byte multiples.
+static int host_stage_setup(conv_norm_plan p) {
+    HostStage &hs = p->stage;
+    const conv_norm_desc &d = p->d;
+    const bool need_aff = d.affine && d.norm != CN_NORM_NONE;
+    int st = CN_OK;
+    if (st == CN_OK) st = stage_alloc(&hs.x, p->x_numel);
+    if (st == CN_OK) st = stage_alloc(&hs.w, p->w_numel);
+    if (st == CN_OK && d.has_bias) st = stage_alloc(&hs.b, d.C_out);
+    if (st == CN_OK && need_aff) st = stage_alloc(&hs.gamma, d.C_out);
+    if (st == CN_OK && need_aff) st = stage_alloc(&hs.beta, d.C_out);
+    if (st == CN_OK) st = stage_alloc(&hs.out, p->out_numel);
+    if (st != CN_OK) return st;
+    const int64_t xs = p->x_numel / d.N, os = p->out_numel / d.N;
+    // Measured on GB300 (host copies ~200 GB/s each way): 2 chunks when the
+    // output is small next to the input (only the first chunk's upload stays
+    // exposed), 4 when a large output download can overlap the kernels;
+    // more chunks cost more in per-chunk overhead than they hide.
+    const double xbytes = (double)p->x_numel * 4, obytes = (double)p->out_numel * 4;
+    int nch = xbytes < 16.0 * 1024 * 1024 ? 1 : (obytes > 0.25 * xbytes ? 4 : 2);
+    if (const char *e = getenv("CN_HOST_CHUNKS")) nch = std::max(1, std::min(kMaxHostChunks, atoi(e)));
+    if (xs % 4 != 0 || os % 4 != 0) nch = 1;
+    nch = std::min(nch, d.N);
+    hs.chunk_n = (d.N + nch - 1) / nch;
+    hs.nchunk = (d.N + hs.chunk_n - 1) / hs.chunk_n;
+    if (hs.nchunk > 1) {
+        conv_norm_desc dc = d;
+        for (int i = 0; i < hs.nchunk; ++i) {
+            dc.N = std::min(hs.chunk_n, d.N - i * hs.chunk_n);
+            if ((st = conv_norm_plan_create(&dc, &hs.sub[i])) != CN_OK) return st;
+        }
+        if (cudaStreamCreateWithFlags(&hs.up, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking) != cudaSuccess)
+            return CN_ERR_CUDA;
+        for (int i = 0; i < hs.nchunk; ++i)
+            if (cudaEventCreateWithFlags(&hs.ev_up[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hs.ev_done[i], cudaEventDisableTiming) != cudaSuccess)
+                return CN_ERR_CUDA;
+    }
+    hs.ready = true;
+    return CN_OK;
+}
+
 int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, const float *b,
                            const float *gamma, const float *beta, float *out, void *stream) {
     if (!p) return CN_ERR_INVALID_ARG;
@@ -387,35 +453,54 @@ int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, con
         return CN_ERR_CUDA;
     }
     if (cur != p->device) cudaSetDevice(p->device);
-    int st = CN_OK;
     HostStage &hs = p->stage;
-    if (st == CN_OK) st = stage_alloc(&hs.x, p->x_numel);
-    if (st == CN_OK) st = stage_alloc(&hs.w, p->w_numel);
-    if (st == CN_OK && b) st = stage_alloc(&hs.b, d.C_out);
-    if (st == CN_OK && need_aff) st = stage_alloc(&hs.gamma, d.C_out);
-    if (st == CN_OK && need_aff) st = stage_alloc(&hs.beta, d.C_out);
-    if (st == CN_OK) st = stage_alloc(&hs.out, p->out_numel);
+    int st = hs.ready ? CN_OK : host_stage_setup(p);
     bool ok = st == CN_OK;
-    ok = ok && cudaMemcpyAsync(hs.x, x, p->x_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(hs.w, w, p->w_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
     if (b) ok = ok && cudaMemcpyAsync(hs.b, b, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
     if (need_aff) {
         ok = ok && cudaMemcpyAsync(hs.gamma, gamma, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
         ok = ok && cudaMemcpyAsync(hs.beta, beta, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
     }
-    if (ok) {
-        st = forward_impl(p, hs.x, hs.w, b ? hs.b : nullptr, need_aff ? hs.gamma : nullptr,
-                          need_aff ? hs.beta : nullptr, hs.out, s);
-        ok = st == CN_OK;
-    } else if (st == CN_OK) {
-        st = CN_ERR_CUDA;
+    const float *db = b ? hs.b : nullptr;
+    const float *dg = need_aff ? hs.gamma : nullptr, *dbe = need_aff ? hs.beta : nullptr;
+    if (ok && hs.nchunk == 1) {
+        ok = cudaMemcpyAsync(hs.x, x, p->x_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+        if (ok) {
+            st = forward_impl(p, hs.x, hs.w, db, dg, dbe, hs.out, s);
+            ok = st == CN_OK;
+        }
+        ok = ok && cudaMemcpyAsync(out, hs.out, p->out_numel * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
+    } else if (ok) {
+        const int64_t xs = p->x_numel / d.N, os = p->out_numel / d.N;
+        // uploads run ahead on their own stream
+        for (int i = 0; ok && i < hs.nchunk; ++i) {
+            const int64_t n0 = (int64_t)i * hs.chunk_n, nn = std::min<int64_t>(hs.chunk_n, d.N - n0);
+            ok = cudaMemcpyAsync(hs.x + n0 * xs, x + n0 * xs, nn * xs * 4, cudaMemcpyHostToDevice,
+                                 hs.up) == cudaSuccess &&
+                 cudaEventRecord(hs.ev_up[i], hs.up) == cudaSuccess;
+        }
+        // kernels on the caller's stream, each chunk's download on the third
+        for (int i = 0; ok && i < hs.nchunk; ++i) {
+            const int64_t n0 = (int64_t)i * hs.chunk_n, nn = std::min<int64_t>(hs.chunk_n, d.N - n0);
+            conv_norm_plan_s *sp = hs.sub[i];
+            ok = cudaStreamWaitEvent(s, hs.ev_up[i], 0) == cudaSuccess;
+            if (ok) {
+                st = forward_impl(sp, hs.x + n0 * xs, hs.w, db, dg, dbe, hs.out + n0 * os, s);
+                ok = st == CN_OK;
+            }
+            ok = ok && cudaEventRecord(hs.ev_done[i], s) == cudaSuccess &&
+                 cudaStreamWaitEvent(hs.down, hs.ev_done[i], 0) == cudaSuccess &&
+                 cudaMemcpyAsync(out + n0 * os, hs.out + n0 * os, nn * os * 4, cudaMemcpyDeviceToHost,
+                                 hs.down) == cudaSuccess;
+        }
+        ok = ok && cudaStreamSynchronize(hs.down) == cudaSuccess;
     }
-    if (ok) {
-        ok = cudaMemcpyAsync(out, hs.out, p->out_numel * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess &&
-             cudaStreamSynchronize(s) == cudaSuccess;
-        if (!ok) st = CN_ERR_CUDA;
+    ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
+    if (!ok) {
+        if (st == CN_OK) st = CN_ERR_CUDA;
+        cudaGetLastError();
     }
-    if (!ok) cudaGetLastError();
     if (cur != p->device) cudaSetDevice(cur);
     return st;
 }

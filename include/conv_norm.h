@@ -162,11 +162,16 @@ int conv_norm_forward(conv_norm_plan plan, const float *x, const float *w,
 
 /*
  * Same computation with HOST buffers: copies x, w, b, gamma, beta to device
- * buffers owned by the plan (allocated on the first call), runs the
- * forward on cuda_stream, copies the result back into the host buffer out
- * and synchronizes the stream before returning.  Pinned (page-locked) host
- * memory gives asynchronous full-bandwidth copies; pageable memory works
- * too.  Errors as conv_norm_forward, plus CN_ERR_ALLOC.
+ * buffers owned by the plan, runs the forward on cuda_stream, copies the
+ * result back into the host buffer out and synchronizes before returning.
+ * Batches of more than about 16 MB of input are cut into up to 8 chunks of
+ * whole samples (every step is per sample): chunk i+1 uploads on a
+ * plan-owned stream while chunk i computes on cuda_stream, and each chunk's
+ * result downloads on a second plan-owned stream as soon as it is done.
+ * The first call allocates the staging buffers, the per-chunk plans, the
+ * two streams and their events.  Pinned (page-locked) host memory gives
+ * asynchronous full-bandwidth copies; pageable memory works too.  Errors as
+ * conv_norm_forward, plus CN_ERR_ALLOC.
  */
 int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
                            const float *b, const float *gamma, const float *beta,
