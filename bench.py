@@ -91,7 +91,8 @@ def peaks():
     if not hbm:
         hbm = 6800.0
     fp32 = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
-    return dict(hbm_gbs=hbm, fp32_tflops=fp32, sm_max_mhz=sm_mhz, source=src)
+    bf16 = p.get("bf16_tflops") or 1900.0
+    return dict(hbm_gbs=hbm, fp32_tflops=fp32, sm_max_mhz=sm_mhz, source=src, bf16_tflops=bf16)
 
 
 def roofline_ms(s, pk):
@@ -103,11 +104,39 @@ def roofline_ms(s, pk):
 # ---- ncu traffic figure (only while the kernel source is unchanged) ------------
 
 KERNEL_SOURCES = {
-    "mean3d": "convolution_normalization_gb300/csrc/k_conv3d_mean.cu",
-    "pool3d": "convolution_normalization_gb300/csrc/k_conv3d_softmax_pool.cu",
-    "full2d": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
+    "k_conv3d_act_mean": "convolution_normalization_gb300/csrc/k_conv3d_mean.cu",
+    "k_conv3d_softmax_pool4": "convolution_normalization_gb300/csrc/k_conv3d_softmax_pool.cu",
+    "k_conv2d_act_stats": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
+    "k_conv2d_tc": "convolution_normalization_gb300/csrc/k_conv2d_tc.cu",
+    "k_norm_apply": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
 }
-VARIANT_KEY = {0: "mean3d", 1: "pool3d", 2: "full2d"}
+# tf32 tensor peak from the measured bf16 one and the nominal dense ratio
+# (1.1 / 2.25 PFLOP/s); split-TF32 runs 3 tf32 products per fp32 product
+TF32_PER_BF16 = 1.1 / 2.25
+SPLIT_TF32_PRODUCTS = 3
+
+
+def split_names(s):
+    """Kernel names of plan_info, split at the commas outside template < >."""
+    out, depth, cur = [], 0, ""
+    for ch in s:
+        if ch == "<":
+            depth += 1
+        elif ch == ">":
+            depth -= 1
+        if ch == "," and depth == 0:
+            out.append(cur)
+            cur = ""
+        else:
+            cur += ch
+    if cur:
+        out.append(cur)
+    return out
+
+
+def kernel_key(name):
+    base = name.split("<")[0]
+    return base if base in KERNEL_SOURCES else None
 
 
 def source_hash(key):
@@ -118,17 +147,43 @@ def source_hash(key):
 
 
 def profiled_traffic(workload, key):
-    """dram bytes per launch from profiles/<workload>.txt if it was captured
-    from the current kernel source (its 'source_hash' line matches)."""
+    """dram bytes per launch of the dominant kernel from
+    profiles/<workload>.txt if it was captured from the current kernel source
+    (its 'kernel' and 'source_hash' lines match)."""
     path = os.path.join(ROOT, "profiles", f"{workload}.txt")
-    if not os.path.exists(path):
+    if key is None or not os.path.exists(path):
         return None
     txt = open(path).read()
+    k = re.search(r"^kernel:\s*(\S+)", txt, re.M)
     m = re.search(r"^source_hash:\s*(\S+)", txt, re.M)
     t = re.search(r"^dram_bytes_per_launch:\s*([0-9.eE+]+)", txt, re.M)
-    if not m or not t or m.group(1) != source_hash(key):
+    if not k or not m or not t or kernel_key(k.group(1)) != key or m.group(1) != source_hash(key):
         return None
     return float(t.group(1))
+
+
+def kernel_roofline(spec, name, ms, pk):
+    """Roofline of one kernel launch of the forward: algorithmic work per
+    launch / its measured duration against the peak of the unit bounding it."""
+    flops = algorithmic_flops(spec)
+    base = name.split("<")[0]
+    if base == "k_conv2d_tc":
+        work = SPLIT_TF32_PRODUCTS * flops  # tf32 tensor-core flops the split method needs
+        peak = pk["bf16_tflops"] * TF32_PER_BF16
+        return {"bound": "tensor", "achieved": work / (ms / 1e3) / 1e12, "peak": peak,
+                "unit": "TFLOP/s",
+                "work": f"{SPLIT_TF32_PRODUCTS} tf32 products x 2 x MACs = {work:.4g} flop",
+                "peak_source": f"measured bf16 {pk['bf16_tflops']} TFLOP/s x nominal tf32/bf16 "
+                               f"{TF32_PER_BF16:.3f}"}
+    if base == "k_norm_apply":
+        nbytes = 2.0 * 4 * math.prod(out_shape(spec))
+        return {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "work": f"read + write of the output = {nbytes:.4g} B",
+                "peak_source": f"{pk['source']} HBM {pk['hbm_gbs']} GB/s"}
+    return {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12, "peak": pk["fp32_tflops"],
+            "unit": "TFLOP/s", "work": f"2 x MACs = {flops:.4g} flop",
+            "peak_source": f"FP32: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
+                           f"{pk['sm_max_mhz']:.0f} MHz"}
 
 
 # ---- clocks ----------------------------------------------------------------------
@@ -265,7 +320,11 @@ def run_reference(args, spec):
 
 # ---- the CUDA path ------------------------------------------------------------------------
 
-def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf):
+def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf, nlaunch):
+    """Times `steps` forwards (L2 flushed before each) with CUDA events on the
+    forward's stream; every step also records one event before each kernel
+    launch and one after the last.  Returns (step ms list, per-launch ms
+    lists)."""
     def fwd():
         plan.forward(dev["x"], dev["w"], dev["b"], dev["gamma"], dev["beta"], out, stream)
 
@@ -273,9 +332,15 @@ def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf):
         for _ in range(warmup):
             flush_buf.zero_()
             fwd()
-    stream.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    lev = [[torch.cuda.Event(enable_timing=True) for _ in range(nlaunch + 1)]
+           for _ in range(steps)]
+    with torch.cuda.stream(stream):
+        for row in lev:  # the CUDA events exist once recorded
+            for e in row:
+                e.record(stream)
+    stream.synchronize()
     with torch.cuda.stream(stream):
         # Hold the stream for a moment so the host queues every step before
         # the device starts them: the per-step events then time the kernels,
@@ -283,11 +348,16 @@ def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf):
         torch.cuda._sleep(int(min(2e9, 2e5 * steps + 2e7)))
         for i in range(steps):
             flush_buf.zero_()
+            plan.set_launch_events(lev[i] if nlaunch else None)
             starts[i].record(stream)
             fwd()
             ends[i].record(stream)
     stream.synchronize()
-    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    plan.set_launch_events(None)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    launch_ms = [[lev[i][j].elapsed_time(lev[i][j + 1]) for i in range(steps)]
+                 for j in range(nlaunch)]
+    return step_ms, launch_ms
 
 
 def run_cuda(args, spec):
@@ -313,7 +383,9 @@ def run_cuda(args, spec):
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
-    times = time_forward(B, torch, plan, dev, out, stream, args.steps, args.warmup, flush)
+    nlaunch = info["launches_per_forward"]
+    times, launch_ms = time_forward(B, torch, plan, dev, out, stream, args.steps, args.warmup,
+                                    flush, nlaunch)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -324,20 +396,20 @@ def run_cuda(args, spec):
     flops = algorithmic_flops(spec)
     value = world * flops / (ms / 1e3) / 1e9
     rl_ms, bound = roofline_ms(spec, pk)
-    key = VARIANT_KEY[info["variant"]]
 
-    # dominant kernel: for single-launch variants the step is that kernel
-    achieved = flops / (ms_rank / 1e3) / 1e12
-    roofline = {"bound": bound if bound == "hbm" else "alu",
-                "achieved": achieved if bound != "hbm" else compulsory_bytes(spec) / (ms_rank / 1e3) / 1e9,
-                "peak": pk["fp32_tflops"] if bound != "hbm" else pk["hbm_gbs"],
-                "unit": "TFLOP/s" if bound != "hbm" else "GB/s",
-                "traffic": profiled_traffic(spec["name"], key),
-                "kernel": info["kernel_names"].split(",")[0],
-                "roofline_ms": rl_ms,
-                "frac_of_step_roofline": rl_ms / ms_rank,
-                "peak_source": f"FP32: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                               f"{pk['sm_max_mhz']:.0f} MHz; HBM: {pk['source']} {pk['hbm_gbs']} GB/s"}
+    # dominant kernel: the launch with the largest mean device time
+    names = split_names(info["kernel_names"])[:nlaunch]
+    means = [statistics.mean(v) for v in launch_ms]
+    dom = max(range(nlaunch), key=lambda j: means[j])
+    roofline = kernel_roofline(spec, names[dom], means[dom], pk)
+    roofline.update({
+        "traffic": profiled_traffic(spec["name"], kernel_key(names[dom])),
+        "kernel": names[dom], "kernel_ms": means[dom],
+        "launch_ms": {n: m for n, m in zip(names, means)},
+        # the workload's metric: FP32-peak / HBM roofline time of the whole step
+        "step_roofline_ms": rl_ms, "step_roofline_bound": bound,
+        "frac_of_step_roofline": rl_ms / ms_rank,
+    })
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
 
     # end to end through the host-buffer entry point
@@ -395,17 +467,27 @@ def measure_extra(B, torch, s, pk, stream, flush):
     inp = wl.make_inputs(s)
     dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
     plan = B.Plan(s)
+    info = plan.info()
+    nl = info["launches_per_forward"]
     out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
     big = compulsory_bytes(s) > 200e6
-    times = time_forward(B, torch, plan, dev, out, stream, 30, 5, flush)
+    times, launch_ms = time_forward(B, torch, plan, dev, out, stream, 30, 5, flush, nl)
     ms = statistics.median(times)
     rl_ms, bound = roofline_ms(s, pk)
-    info = plan.info()
+    names = split_names(info["kernel_names"])[:nl]
+    means = [statistics.mean(v) for v in launch_ms]
+    dom = max(range(nl), key=lambda j: means[j])
+    kr = kernel_roofline(s, names[dom], means[dom], pk)
     plan.close()
     del dev, out
     return {"workload": s["name"], "ms": ms, "gflops": algorithmic_flops(s) / ms / 1e6,
             "roofline_ms": rl_ms, "bound": bound, "frac": rl_ms / ms,
-            "launches": info["launches_per_forward"], "kernels": info["kernel_names"],
+            "kernel": names[dom], "kernel_ms": means[dom],
+            "kernel_roofline": {"bound": kr["bound"], "achieved": kr["achieved"],
+                                "peak": kr["peak"], "unit": kr["unit"],
+                                "frac": kr["achieved"] / kr["peak"]},
+            "launch_ms": {n: m for n, m in zip(names, means)},
+            "launches": nl, "kernels": info["kernel_names"],
             "l2": "flushed" if not big else "flushed (inputs larger than L2)"}
 
 

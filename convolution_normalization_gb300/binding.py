@@ -58,7 +58,8 @@ class conv_norm_info(ctypes.Structure):
 EXPORTED = ("conv_norm_desc_validate", "conv_norm_output_shape", "conv_norm_status_string",
             "conv_norm_plan_create", "conv_norm_plan_destroy", "conv_norm_workspace_bytes",
             "conv_norm_plan_info", "conv_norm_forward", "conv_norm_forward_host",
-            "conv_norm_plan_check_device", "conv_norm_forward_noalloc")
+            "conv_norm_plan_check_device", "conv_norm_forward_noalloc",
+            "conv_norm_plan_set_launch_events")
 
 
 def _load():
@@ -91,6 +92,8 @@ def _load():
     lib.conv_norm_plan_check_device.restype = i
     lib.conv_norm_forward_noalloc.argtypes = [pd] + fwd[1:]
     lib.conv_norm_forward_noalloc.restype = i
+    lib.conv_norm_plan_set_launch_events.argtypes = [vp, ctypes.POINTER(vp), i]
+    lib.conv_norm_plan_set_launch_events.restype = i
     return lib
 
 
@@ -215,6 +218,17 @@ def conv_norm_plan_check_device(plan, stream=None) -> int:
     return lib.conv_norm_plan_check_device(plan, _stream(stream))
 
 
+def conv_norm_plan_set_launch_events(plan, events) -> int:
+    """events: launches_per_forward + 1 torch.cuda.Event objects (already
+    recorded once, so the CUDA events exist), or None/[] to stop."""
+    if not events:
+        return _check(lib.conv_norm_plan_set_launch_events(plan, None, 0),
+                      "conv_norm_plan_set_launch_events")
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return _check(lib.conv_norm_plan_set_launch_events(plan, arr, len(events)),
+                  "conv_norm_plan_set_launch_events")
+
+
 class Plan:
     """Owns one conv_norm plan; a convenience wrapper over the C calls."""
 
@@ -234,6 +248,9 @@ class Plan:
 
     def check_device(self, stream=None):
         return conv_norm_plan_check_device(self.handle, stream)
+
+    def set_launch_events(self, events):
+        return conv_norm_plan_set_launch_events(self.handle, events)
 
     def close(self):
         if self.handle:

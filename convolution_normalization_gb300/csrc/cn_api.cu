@@ -50,6 +50,7 @@ struct conv_norm_plan_s {
     Full2dArgs full_args;
     Full2dConfig full_cfg;
     HostStage stage;
+    LaunchEvents events{};  // per-launch timing, off unless set
 };
 
 namespace {
@@ -329,7 +330,8 @@ int conv_norm_plan_info(conv_norm_plan p, conv_norm_info *info) {
 }
 
 static int forward_impl(conv_norm_plan p, const float *x, const float *w, const float *b,
-                        const float *gamma, const float *beta, float *out, cudaStream_t s) {
+                        const float *gamma, const float *beta, float *out, cudaStream_t s,
+                        const LaunchEvents *ev = nullptr) {
     const conv_norm_desc &d = p->d;
     const bool need_aff = d.affine && d.norm != CN_NORM_NONE;
     // An empty problem launches nothing; its (zero-size) tensors may have null pointers.
@@ -353,19 +355,19 @@ static int forward_impl(conv_norm_plan p, const float *x, const float *w, const 
         case V_MEAN3D: {
             Mean3dArgs &a = p->mean_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
-            st = mean3d_launch(p->mean_cfg, a, s);
+            st = mean3d_launch(p->mean_cfg, a, s, ev);
             break;
         }
         case V_POOL3D: {
             Pool3dArgs &a = p->pool_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.out = out;
-            st = pool3d_launch(p->pool_cfg, a, s);
+            st = pool3d_launch(p->pool_cfg, a, s, ev);
             break;
         }
         default: {
-            Full2dArgs a = p->full_args;
+            Full2dArgs &a = p->full_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
-            st = full2d_launch(p->full_cfg, a, s);
+            st = full2d_launch(p->full_cfg, a, s, ev);
             break;
         }
     }
@@ -377,7 +379,34 @@ static int forward_impl(conv_norm_plan p, const float *x, const float *w, const 
 int conv_norm_forward(conv_norm_plan p, const float *x, const float *w, const float *b,
                       const float *gamma, const float *beta, float *out, void *stream) {
     if (!p) return CN_ERR_INVALID_ARG;
-    return forward_impl(p, x, w, b, gamma, beta, out, static_cast<cudaStream_t>(stream));
+    return forward_impl(p, x, w, b, gamma, beta, out, static_cast<cudaStream_t>(stream),
+                        p->events.n ? &p->events : nullptr);
+}
+
+int conv_norm_plan_set_launch_events(conv_norm_plan p, void *const *events, int n) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    if (n == 0) {
+        p->events.n = 0;
+        return CN_OK;
+    }
+    int L = 0;
+    switch (p->variant) {
+        case V_MEAN3D:
+            L = p->d.N > 0 ? 1 : 0;
+            break;
+        case V_POOL3D:
+            L = p->pool_cfg.grid > 0 ? 1 : 0;
+            break;
+        default:
+            L = full2d_launches(p->full_cfg, p->full_args);
+            break;
+    }
+    if (!events || n != L + 1 || n > kMaxLaunchEvents) return CN_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!events[i]) return CN_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) p->events.ev[i] = static_cast<cudaEvent_t>(events[i]);
+    p->events.n = n;
+    return CN_OK;
 }
 
 static int stage_alloc(float **dst, int64_t n) {

@@ -11,6 +11,17 @@
 
 namespace cn {
 
+// Per-launch timing events of a plan (conv_norm_plan_set_launch_events):
+// record(i) marks the start of launch i, record(L) the end of the last one.
+constexpr int kMaxLaunchEvents = 8;
+struct LaunchEvents {
+    cudaEvent_t ev[kMaxLaunchEvents];
+    int n;  // 0: off
+};
+inline void record_launch(const LaunchEvents *e, int i, cudaStream_t s) {
+    if (e && i < e->n) cudaEventRecord(e->ev[i], s);
+}
+
 // Tensor-map encoding (cn_tma_host.cu).
 bool tma_available();
 int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[4],
@@ -62,7 +73,8 @@ struct Mean3dConfig {
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
-int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s);
+int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s,
+                  const LaunchEvents *ev = nullptr);
 
 // ---------------------------------------------------------------------------
 // Variant 1: 3-D conv -> channel softmax -> MaxPool3d(2,2) twice (= one
@@ -89,7 +101,8 @@ struct Pool3dConfig {
 };
 int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &args, Pool3dConfig &cfg);
 int pool3d_prepare(const Pool3dConfig &cfg);
-int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s);
+int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s,
+                  const LaunchEvents *ev = nullptr);
 
 // ---------------------------------------------------------------------------
 // Variant 2: 2-D conv or transposed conv (groups) -> activation ->
@@ -99,6 +112,22 @@ int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s);
 // the moments into per-channel coefficients.  Kernel B rewrites out in place
 // as (y - mu) * a + bb.
 struct Full2dArgs {
+    // Tensor-core conv (k_conv2d_tc, tc = 1): dense Conv2d as a split-TF32
+    // implicit GEMM; the fields below tc_* describe its tiles and stages.
+    CUtensorMap tc_xmap;        // x as (W, H, C_in, N), box (W, tc_R + K - 1, 4, 1)
+    const float *tc_xmap_base;  // x pointer the map was encoded for
+    int tc;
+    int tc_K;                   // filter size
+    int tc_R;                   // output rows per tile
+    int tc_npos;                // MMA N: positions per tile (multiple of 32, <= 256)
+    int tc_ngrp;                // 4-channel input groups = pipeline stages per tile
+    int tc_xbuf_bytes;          // one interleaved input operand buffer (hi or lo)
+    int tc_wblk_bytes;          // one (channel block, group) filter block, lo | hi
+    int tc_stage_bytes;         // 2 * tc_xbuf_bytes + tc_wblk_bytes
+    int tc_land_bytes;          // raw input box of a stage
+    int tc_stages;              // operand stages in shared memory
+    int tc_acc_cols;            // TMEM columns per accumulator (two are allocated)
+
     int use_bulk;         // 1: rows staged with bulk async copies (W % 4 == 0)
     const float *x, *w, *b, *gamma, *beta;
     float *out;
@@ -136,10 +165,17 @@ struct Full2dConfig {
     int fin_threads;
 };
 int full2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
+// Tensor-core path (k_conv2d_tc.cu): plan (CN_ERR_UNSUPPORTED when the problem
+// does not fit it), filter-block bytes, x tensor map, filter pre-pass.
+int tc2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
+size_t tc2d_wprep_bytes(const Full2dArgs &a);
+int tc2d_bind_x(Full2dArgs &a);
+int tc2d_prep_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s);
 size_t full2d_workspace(const Full2dArgs &a);
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag);
 int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a);  // needs a device: smem attribute, grid
 int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a);
-int full2d_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s);
+int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s,
+                  const LaunchEvents *ev = nullptr);  // may cache a tensor map in a
 
 }  // namespace cn

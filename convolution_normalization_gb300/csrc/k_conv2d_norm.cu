@@ -451,41 +451,46 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
     }
 }
 
-// Statistics of one normalization group: merges its channels' per-warp,
-// per-tile moments in a fixed order (fp64) and writes each channel's
-// coefficients (mu, a = gamma * rstd * scale, bb = beta * scale).
-__global__ void __launch_bounds__(256) k_group_stats(const __grid_constant__ Full2dArgs a) {
-    __shared__ double sm[256 * 3];
-    const int tid = threadIdx.x;
-    const int ng = blockIdx.x;  // (n, group)
+// Statistics of the normalization groups, one warp per (n, group).  All
+// partials of one channel share that channel's shift K, so per channel the
+// lanes add the shifted sums (count, S1, S2) of every tile: fp32 within a
+// lane, then an fp64 butterfly of commutative adds (every lane gets the same
+// bits, and the order is fixed, so the result is deterministic).  The
+// channels of a group are then merged as (count, mean, M2) in fp64, in channel
+// order.  The warp writes each channel's coefficients (mu, a = gamma * rstd *
+// scale, bb = beta * scale).  fp64 work is a few dozen operations per group:
+// the FP64 pipe of this GPU is narrow.
+constexpr int kStatsWarps = 4;
+__global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int ng = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);  // (n, group)
+    if (ng >= a.N * a.NG) return;
     const int n = ng / a.NG, g = ng % a.NG;
     const int cpg = a.Co / a.NG;
     const int per_c = a.ntiles * a.wsp;
-    const int total = cpg * per_c;
-    const float4 *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c;
     Moments<double> m{0.0, 0.0, 0.0};
-    for (int i = tid; i < total; i += blockDim.x) {
-        const float4 q = p0[i];
-        m = merge(m, moments_from_sums(q.x, q.y, q.z, q.w));
-    }
-    sm[tid * 3] = m.n;
-    sm[tid * 3 + 1] = m.mean;
-    sm[tid * 3 + 2] = m.m2;
-    __syncthreads();
-    for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-        if (tid < w) {
-            Moments<double> l{sm[tid * 3], sm[tid * 3 + 1], sm[tid * 3 + 2]};
-            const Moments<double> r{sm[(tid + w) * 3], sm[(tid + w) * 3 + 1], sm[(tid + w) * 3 + 2]};
-            l = merge(l, r);
-            sm[tid * 3] = l.n;
-            sm[tid * 3 + 1] = l.mean;
-            sm[tid * 3 + 2] = l.m2;
+    for (int cl = 0; cl < cpg; ++cl) {
+        const float4 *p = a.partial + ((size_t)n * a.Co + (size_t)g * cpg + cl) * per_c;
+        int cnt = 0;
+        float s1 = 0.0f, s2 = 0.0f;
+        for (int i = lane; i < per_c; i += 32) {
+            const float4 q = p[i];
+            cnt += (int)q.x;
+            s1 += q.z;
+            s2 += q.w;
         }
-        __syncthreads();
+        double d1 = s1, d2 = s2;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, off);
+            d2 += __shfl_xor_sync(0xffffffffu, d2, off);
+        }
+        m = merge(m, moments_from_sums((double)cnt, (double)p[0].y, d1, d2));
     }
-    const double mean = sm[1], var = sm[2] / sm[0];
+    const double mean = m.mean, var = m.n > 0.0 ? m.m2 / m.n : 0.0;
     const double rstd = 1.0 / sqrt(var + (double)a.eps);
-    for (int cl = tid; cl < cpg; cl += blockDim.x) {
+    for (int cl = lane; cl < cpg; cl += 32) {
         const int c = g * cpg + cl;
         const double ga = a.affine ? (double)a.gamma[c] : 1.0;
         const double be = a.affine ? (double)a.beta[c] : 0.0;
@@ -562,6 +567,9 @@ int pick_wco(int units) {
 }  // namespace
 
 int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
+    // dense Conv2d shapes that fit it go to the tensor cores
+    if (tc2d_plan(d, a, cfg) == CN_OK) return CN_OK;
+    a.tc = 0;
     const int T = d.conv == CN_CONVT2D ? 1 : 0;
     const int K = d.k;
     const int Ho = T ? d.H + K - 1 : d.H - K + 1;
@@ -712,7 +720,8 @@ size_t full2d_workspace(const Full2dArgs &a) {
     const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
     const size_t tick = (size_t)(a.N + 2) * sizeof(int);
-    const size_t wprep = (size_t)a.ncob * a.nchunk * a.wstage * sizeof(float);
+    const size_t wprep =
+        a.tc ? tc2d_wprep_bytes(a) : (size_t)a.ncob * a.nchunk * a.wstage * sizeof(float);
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
     return al(part) + al(coef) + al(tick) + al(wprep);
 }
@@ -750,23 +759,37 @@ int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a) {
     return 2 + (a.apply_needed ? 2 : 0);
 }
 
-int full2d_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s) {
+int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0 || a.items == 0) return CN_OK;
-    const int wtotal = a.ncob * a.nchunk * a.wstage;
-    k_prep_weights<<<cfg.prep_grid, 256, 0, s>>>(a.w, a.wprep, cfg.K, cfg.transposed, a.Cig, a.Cog,
-                                                  cfg.COT * a.wco, a.cib, a.nchunk, wtotal);
-    if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
+    if (a.tc) {
+        const int st = tc2d_bind_x(a);
+        if (st != CN_OK) return st;
+    }
+    record_launch(ev, 0, s);
+    if (a.tc) {
+        const int st = tc2d_prep_launch(cfg, a, s);
+        if (st != CN_OK) return st;
+    } else {
+        const int wtotal = a.ncob * a.nchunk * a.wstage;
+        k_prep_weights<<<cfg.prep_grid, 256, 0, s>>>(a.w, a.wprep, cfg.K, cfg.transposed, a.Cig,
+                                                      a.Cog, cfg.COT * a.wco, a.cib, a.nchunk, wtotal);
+        if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
+    }
+    record_launch(ev, 1, s);
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    record_launch(ev, 2, s);
     if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     if (a.apply_needed) {
         if (a.norm == CN_NORM_NONE) {
             k_fill_scale<<<(a.N * a.Co + 255) / 256, 256, 0, s>>>(a.coef, a.N * a.Co, a.post_scale);
         } else {
-            k_group_stats<<<a.N * a.NG, 256, 0, s>>>(a);
+            k_group_stats<<<(a.N * a.NG + kStatsWarps - 1) / kStatsWarps, 32 * kStatsWarps, 0, s>>>(a);
         }
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
+        record_launch(ev, 3, s);
         dim3 grid(cfg.apply_grid_x, cfg.apply_grid_y);
         k_norm_apply<<<grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4);
+        record_launch(ev, 4, s);
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     }
     return CN_OK;

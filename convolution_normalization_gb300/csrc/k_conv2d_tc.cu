@@ -1,0 +1,580 @@
+// Variant 2, tensor-core conv: dense Conv2d (groups 1) as an implicit GEMM on
+// the 5th-generation tensor cores, for the l2_p17 problem shape (Conv2d
+// 64 -> 128, k = 3, then InstanceNorm and a division by 2).
+//
+// The convolution is a contraction over K = C_in * k * k, so it maps onto
+// tcgen05.mma: D[co][p] += sum_k W[co][k] * X[k][p], M = 128 output channels,
+// N = up to 256 output positions, D in tensor memory (TMEM).  fp32 inputs
+// with fp32 accuracy come from the split-TF32 scheme: the tensor cores read a
+// tf32 operand by dropping the low 13 mantissa bits of an fp32 word, so with
+// v = hi(v) + lo(v), hi = truncation, lo = the exact remainder,
+//   W * X ~= Wh*Xh + Wl*Xh + Wh*Xl        (Wl*Xl, about 2^-22 relative, dropped)
+// where the raw fp32 words serve as Wh and Xh.  That keeps every product to
+// about fp32 accuracy; the conv then matches an fp32 conv to ~1e-6 relative.
+//
+// Operands (K-major, no swizzle): a K step of 8 is two 4-channel "core
+// matrices" whose rows are 16 bytes apart.  The input part of a stage holds
+// one 4-channel group of R + k - 1 input rows, position-major:
+// [row * W + col][4 channels].  Output position p of the tile (row p / W,
+// column p % W of the R-row block) reads input position p + kh * W + kw for
+// tap (kh, kw), so every tap is the same buffer with its start address moved
+// by (kh * W + kw) rows: no im2col copy.  Positions whose column is >= the
+// output width read into the next row and are discarded.  The second core
+// matrix of a K step is any 16-byte-multiple offset away, which lets one MMA
+// take two taps (hi*hi products) or a hi/lo pair of one tap (the cross
+// terms): 14 MMAs of K = 8 per group for k = 3 (27 tap products, one padded
+// with a zero filter block).
+//
+// Warp roles (one CTA per SM, persistent, tiles claimed from a counter):
+//   warp 0      producer: TMA of the raw input rows of a 4-channel group into
+//               a landing buffer, bulk copy of the group's pre-split filter
+//               block (lo | hi) into the stage;
+//   warps 2-5   converters: landing [c][row][col] -> interleaved hi and lo
+//               operand buffers of the stage;
+//   warp 1      MMA issuer (one thread): 14 tcgen05.mma per stage into one of
+//               two TMEM accumulators (double buffered across tiles);
+//   warps 6-9   epilogue: tcgen05.ld of the accumulator (thread = channel),
+//               bias + activation, per-channel shifted sums (count, S1, S2)
+//               in registers, then a 32x32 transpose through shared memory so
+//               the pre-norm output is stored with coalesced rows.
+// The statistics and normalize passes that follow are the ones of the CUDA
+// core path (k_group_stats, k_norm_apply).
+#include "cn_common.cuh"
+#include "cn_internal.h"
+
+#include <algorithm>
+#include <cstdlib>
+
+namespace cn {
+namespace {
+
+constexpr int kTcThreads = 320;
+constexpr int kTcM = 128;                 // output channels per tile
+constexpr int kTapBytes = kTcM * 16;      // filter slice of one tap: 128 rows x 4 channels
+constexpr int kTcMaxStages = 3;
+constexpr int kTcLand = 2;
+constexpr int kScratchFloats = 4 * 32 * 33;  // epilogue transpose, 4 warps
+constexpr int kMaxMmas = 14;                   // MMAs per stage for k <= 3: k*k + ceil(k*k / 2)
+
+// ---- tcgen05 / UMMA helpers (inline PTX) --------------------------------------
+
+// Shared-memory matrix descriptor: start address, leading-dimension byte
+// offset (between the two K core matrices), stride byte offset (between
+// 8-row core-matrix groups), descriptor version 1, no swizzle.
+CN_DEV uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+// Instruction descriptor of kind::tf32: fp32 accumulator, tf32 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+CN_DEV uint32_t idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+CN_DEV void umma_tf32(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// Arrives on bar once every MMA this thread issued so far has completed.
+CN_DEV void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+CN_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+CN_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// 32 lanes x 32 consecutive columns of TMEM: thread i gets lane (base + i).
+CN_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+// The tf32 part the tensor cores read (low 13 mantissa bits dropped) and
+// the exact remainder.
+CN_DEV float tf32_trunc(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+CN_DEV float tf32_rest(float v) { return v - tf32_trunc(v); }
+
+// Filter pre-pass: per (channel block of 128, 4-channel group) one block of
+// [lo | hi] x [tap][128 rows][4 channels], the A operands of that group's
+// MMAs in core-matrix order.
+__global__ void __launch_bounds__(256) k_prep_weights_tc(const float *__restrict__ w,
+                                                         float *wprep, int Ci, int K, int ngrp,
+                                                         long long total) {
+    const int T = K * K;
+    for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total;
+         e += (long long)gridDim.x * blockDim.x) {
+        long long r = e;
+        const int j = (int)(r % 4);
+        r /= 4;
+        const int row = (int)(r % kTcM);
+        r /= kTcM;
+        const int t = (int)(r % T);
+        r /= T;
+        const int hi = (int)(r % 2);
+        r /= 2;
+        const int g = (int)(r % ngrp);
+        const int cob = (int)(r / ngrp);
+        const int co = cob * kTcM + row, c = 4 * g + j;
+        const float v = w[((size_t)co * Ci + c) * T + t];
+        wprep[e] = hi ? v : tf32_rest(v);
+    }
+}
+
+// Bounded wait with a CTA-local abort: after one wait gives up, every role
+// stops at its next wait instead of running into further timeouts.
+CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                flag_error(err, ERR_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_constant__ Full2dArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t land_full[kTcLand], land_empty[kTcLand];
+    __shared__ __align__(8) uint64_t w_full[kTcMaxStages], x_full[kTcMaxStages],
+        st_empty[kTcMaxStages];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
+    __shared__ int s_land_tile[kTcLand], s_st_tile[kTcMaxStages], s_acc_tile[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ uint64_t s_desc[kTcMaxStages][kMaxMmas][2];  // (A, B) descriptors per stage slot
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int NS = a.tc_stages;
+    const int T = a.tc_K * a.tc_K;
+    const int rows_in = a.tc_R + a.tc_K - 1;
+    unsigned char *smem = smem_raw;
+    auto stage = [&](int b) { return smem + (size_t)b * a.tc_stage_bytes; };
+    unsigned char *land0 = smem + (size_t)NS * a.tc_stage_bytes;
+    const int land_stride = (a.tc_land_bytes + 127) & ~127;
+    auto land = [&](int b) { return land0 + (size_t)b * land_stride; };
+    unsigned char *zero_blk = land0 + (size_t)kTcLand * land_stride;
+    float *scratch = reinterpret_cast<float *>(zero_blk + kTapBytes);
+    const int acc_cols = a.tc_acc_cols;
+
+    // ---- setup: zero the operand tails and the zero block, barriers, TMEM ----
+    {
+        const int tail0 = rows_in * a.W;  // first position never written by the converters
+        const int npos_buf = a.tc_xbuf_bytes / 16;
+        for (int b = 0; b < NS; ++b) {
+            float4 *xh = reinterpret_cast<float4 *>(stage(b));
+            float4 *xl = reinterpret_cast<float4 *>(stage(b) + a.tc_xbuf_bytes);
+            for (int i = tail0 + tid; i < npos_buf; i += blockDim.x) {
+                xh[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                xl[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float4 *z = reinterpret_cast<float4 *>(zero_blk);
+        for (int i = tid; i < kTapBytes / 16; i += blockDim.x) z[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < kTcLand; ++i) {
+            mbar_init(&land_full[i], 1);
+            mbar_init(&land_empty[i], 4);
+        }
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&x_full[i], 4);
+            mbar_init(&st_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 2);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(&fin_bar, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(2 * acc_cols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    int *abort_p = const_cast<int *>(&s_abort);
+    auto wait = [&](uint64_t *bar, uint32_t par) { return tc_wait(bar, par, abort_p, a.err); };
+
+    const int per_sample = a.row_tiles * a.ncob;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int kl = 0, kw = 0;  // landing / filter stages armed so far
+            int next = (int)blockIdx.x;
+            bool live = true;
+            while (live) {
+                const int tile = next < a.items ? next : -1;
+                if (tile >= 0) next = (int)gridDim.x + atomicAdd(a.tickets + a.N, 1);
+                int n = 0, rt = 0, cob = 0;
+                if (tile >= 0) {
+                    n = tile / per_sample;
+                    const int rem = tile - n * per_sample;
+                    cob = rem / a.row_tiles;
+                    rt = rem - cob * a.row_tiles;
+                }
+                const int ng = tile >= 0 ? a.tc_ngrp : 1;  // a stop marker is one stage
+                for (int g = 0; g < ng; ++g) {
+                    const int k = kl;
+                    const int lb = k % kTcLand, b = k % NS;
+                    if (k >= kTcLand && !wait(&land_empty[lb], ((k / kTcLand) - 1) & 1)) {
+                        live = false;
+                        break;
+                    }
+                    s_land_tile[lb] = tile;
+                    if (tile >= 0) {
+                        mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.tc_land_bytes);
+                        tma_load_4d(land(lb), &a.tc_xmap, 0, rt * a.tc_R, 4 * g, n, &land_full[lb]);
+                    } else {
+                        mbar_arrive(&land_full[lb]);
+                    }
+                    ++kl;
+                    if (k >= NS && !wait(&st_empty[b], ((k / NS) - 1) & 1)) {
+                        live = false;
+                        break;
+                    }
+                    s_st_tile[b] = tile;
+                    if (tile >= 0) {
+                        mbar_arrive_expect_tx(&w_full[b], (uint32_t)a.tc_wblk_bytes);
+                        bulk_load(stage(b) + 2 * (size_t)a.tc_xbuf_bytes,
+                                  reinterpret_cast<const unsigned char *>(a.wprep) +
+                                      ((size_t)cob * a.tc_ngrp + g) * a.tc_wblk_bytes,
+                                  (uint32_t)a.tc_wblk_bytes, &w_full[b]);
+                    } else {
+                        mbar_arrive(&w_full[b]);
+                    }
+                    ++kw;
+                }
+                if (tile < 0) live = false;
+            }
+            // copies still in flight (only after an abort) land before the CTA exits
+            for (int j = std::max(0, kl - kTcLand); j < kl; ++j)
+                mbar_wait_bounded(&land_full[j % kTcLand], (j / kTcLand) & 1, kWaitLimitNs);
+            for (int j = std::max(0, kw - NS); j < kw; ++j)
+                mbar_wait_bounded(&w_full[j % NS], (j / NS) & 1, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_tf32(kTcM, a.tc_npos);
+            // The operand descriptors of a stage depend only on its slot:
+            // built once here, so issuing a stage is loads and MMAs only.
+            const uint32_t zaddr = smem_u32(zero_blk);
+            int nm = 0;
+            for (int b = 0; b < NS; ++b) {
+                const uint32_t sb = smem_u32(stage(b));
+                const uint32_t xh = sb;
+                const uint32_t wl = sb + 2u * (uint32_t)a.tc_xbuf_bytes;
+                const uint32_t wh = wl + (uint32_t)(T * kTapBytes);
+                auto off = [&](int tp) { return (tp / a.tc_K) * a.W + tp % a.tc_K; };
+                nm = 0;
+                // cross terms: Wl(t) Xh(t) + Wh(t) Xl(t)
+                for (int tp = 0; tp < T; ++tp, ++nm) {
+                    s_desc[b][nm][0] = umma_desc(wl + tp * kTapBytes, (uint32_t)(T * kTapBytes), 128);
+                    s_desc[b][nm][1] = umma_desc(xh + off(tp) * 16, (uint32_t)a.tc_xbuf_bytes, 128);
+                }
+                // hi * hi, two taps per MMA
+                int tp = 0;
+                for (; tp + 1 < T; tp += 2, ++nm) {
+                    s_desc[b][nm][0] = umma_desc(wh + tp * kTapBytes, kTapBytes, 128);
+                    s_desc[b][nm][1] =
+                        umma_desc(xh + off(tp) * 16, (uint32_t)((off(tp + 1) - off(tp)) * 16), 128);
+                }
+                if (tp < T) {  // odd tap count: the last tap with the zero block
+                    const uint32_t wa = wh + tp * kTapBytes;
+                    s_desc[b][nm][0] = umma_desc(wa, zaddr - wa, 128);
+                    s_desc[b][nm][1] = umma_desc(xh + off(tp) * 16, 16, 128);
+                    ++nm;
+                }
+            }
+            int k = 0;
+            for (int t = 0;; ++t) {
+                const int as = t & 1;
+                bool stop = false, ok = true;
+                for (int g = 0; g < a.tc_ngrp; ++g, ++k) {
+                    const int b = k % NS;
+                    const uint32_t par = (uint32_t)(k / NS) & 1u;
+                    if (!wait(&w_full[b], par) || !wait(&x_full[b], par)) {
+                        ok = false;
+                        break;
+                    }
+                    const int tile = s_st_tile[b];
+                    if (tile < 0) {
+                        stop = true;
+                        break;
+                    }
+                    if (g == 0) {
+                        if (t >= 2 && !wait(&acc_empty[as], ((t >> 1) - 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        s_acc_tile[as] = tile;
+                        mbar_arrive(&acc_full[as]);  // publishes the tile id (1 of 2 arrivals)
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + (uint32_t)(as * acc_cols);
+                    for (int i = 0; i < nm; ++i)
+                        umma_tf32(d, s_desc[b][i][0], s_desc[b][i][1], idesc, (g | i) ? 1u : 0u);
+                    umma_commit(&st_empty[b]);
+                }
+                if (!ok) break;
+                if (stop) {
+                    if (t >= 2 && !wait(&acc_empty[as], ((t >> 1) - 1) & 1)) break;
+                    s_acc_tile[as] = -1;
+                    mbar_arrive(&acc_full[as]);
+                    mbar_arrive(&acc_full[as]);
+                    break;
+                }
+                umma_commit(&acc_full[as]);  // the tile's MMAs are done (2 of 2)
+            }
+            // every MMA issued by this thread completes before TMEM is freed
+            umma_commit(&fin_bar);
+            mbar_wait_bounded(&fin_bar, 0, kWaitLimitNs);
+        }
+    } else if (warp < 6) {
+        // ---------------- converters ----------------
+        const int ct = tid - 64;
+        const int npix = rows_in * a.W;
+        for (int k = 0;; ++k) {
+            const int lb = k % kTcLand, b = k % NS;
+            if (!wait(&land_full[lb], (k / kTcLand) & 1)) break;
+            const int tile = s_land_tile[lb];
+            if (k >= NS && !wait(&st_empty[b], ((k / NS) - 1) & 1)) break;
+            if (tile >= 0) {
+                const float *src = reinterpret_cast<const float *>(land(lb));
+                float4 *xh = reinterpret_cast<float4 *>(stage(b));
+                float4 *xl = reinterpret_cast<float4 *>(stage(b) + a.tc_xbuf_bytes);
+                for (int p = ct; p < npix; p += 128) {
+                    const float v0 = src[p], v1 = src[npix + p], v2 = src[2 * npix + p],
+                                v3 = src[3 * npix + p];
+                    xh[p] = make_float4(v0, v1, v2, v3);
+                    xl[p] = make_float4(tf32_rest(v0), tf32_rest(v1), tf32_rest(v2), tf32_rest(v3));
+                }
+                fence_proxy_async();
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&land_empty[lb]);
+                mbar_arrive(&x_full[b]);
+            }
+            if (tile < 0) break;
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;  // TMEM lane quadrant this warp may read
+        float *scr = scratch + (warp - 6) * 32 * 33;
+        const long long S = a.S;
+        for (int t = 0;; ++t) {
+            const int as = t & 1;
+            if (!wait(&acc_full[as], (t >> 1) & 1)) break;
+            const int tile = s_acc_tile[as];
+            if (tile < 0) break;
+            tc_fence_after();
+            const int n = tile / per_sample;
+            const int rem = tile - n * per_sample;
+            const int cob = rem / a.row_tiles;
+            const int rt = rem - cob * a.row_tiles;
+            const int r0 = rt * a.tc_R;
+            const int co = cob * kTcM + q * 32 + lane;
+            const float bias = a.b ? __ldg(a.b + co) : 0.0f;
+            const float Ksh = apply_act(a.act, bias);
+            const int rows_ok = min(a.tc_R, a.Ho - r0);
+            float s1 = 0.0f, s2 = 0.0f;
+            float *obase = a.out + ((size_t)n * a.Co + cob * kTcM + q * 32) * (size_t)S;
+            for (int i = 0; i < a.tc_npos / 32; ++i) {
+                uint32_t v[32];
+                tmem_ld32(tmem + (uint32_t)(as * acc_cols + 32 * i) + ((uint32_t)(q * 32) << 16), v);
+                // lane l owns position 32i + l for the stores; the warp's
+                // validity mask serves the per-channel sums over j
+                const int p = 32 * i + lane;
+                const int rr = p / a.W;
+                const int col = p - rr * a.W;
+                const bool vl = rr < rows_ok && col < a.Wo;
+                const unsigned vmask = __ballot_sync(0xffffffffu, vl);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float y = apply_act(a.act, __uint_as_float(v[j]) + bias);
+                    if ((vmask >> j) & 1u) {
+                        const float dlt = y - Ksh;
+                        s1 += dlt;
+                        s2 = fmaf(dlt, dlt, s2);
+                    }
+                    scr[lane * 33 + j] = y;
+                }
+                __syncwarp();
+                if (vl) {
+                    float *op = obase + (size_t)(r0 + rr) * a.Wo + col;
+#pragma unroll 8
+                    for (int c = 0; c < 32; ++c) op[(size_t)c * S] = scr[c * 33 + lane];
+                }
+                __syncwarp();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[as]);
+            const float cnt = (float)(rows_ok * a.Wo);
+            a.partial[((size_t)n * a.Co + co) * a.ntiles + rt] = make_float4(cnt, Ksh, s1, s2);
+        }
+    }
+
+    // ---- teardown ----
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                     "r"(2 * acc_cols)
+                     : "memory");
+    if (tid == 0 && atomicAdd(a.tickets + a.N + 1, 1) == (int)gridDim.x - 1) {
+        a.tickets[a.N] = 0;
+        a.tickets[a.N + 1] = 0;
+    }
+}
+
+}  // namespace
+
+// Plans the tensor-core path; CN_ERR_UNSUPPORTED when the problem does not
+// fit it (the CUDA-core kernels then take it).
+int tc2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
+    if (d.conv != CN_CONV2D || d.groups != 1) return CN_ERR_UNSUPPORTED;
+    if (d.C_in % 4 != 0 || d.C_out % kTcM != 0 || d.W % 4 != 0 || d.k > 3) return CN_ERR_UNSUPPORTED;
+    if (!tma_available()) return CN_ERR_UNSUPPORTED;
+    const char *e = getenv("CN_NO_TC");
+    if (e && atoi(e)) return CN_ERR_UNSUPPORTED;
+    const int K = d.k, W = d.W, H = d.H;
+    const int Ho = H - K + 1, Wo = W - K + 1;
+    if (W > 256 || Wo > 256) return CN_ERR_UNSUPPORTED;
+    int R = 1 + (256 - Wo) / W;
+    R = std::max(1, std::min(R, Ho));
+    // MMA N: the tile's positions, a multiple of 32 (the epilogue reads TMEM
+    // in 32-column pieces)
+    const int npos = (((R - 1) * W + Wo) + 31) / 32 * 32;
+    if (npos > 256) return CN_ERR_UNSUPPORTED;
+    const int rows_in = R + K - 1;
+    if (rows_in > 256) return CN_ERR_UNSUPPORTED;
+    // operand buffer: rows_in * W positions, plus a zeroed tail covering the
+    // farthest read (last tap, last position, +1 for the padded pair)
+    const int need = (K - 1) * W + (K - 1) + npos + 1;
+    const int pos_buf = std::max(rows_in * W, need) + 8;
+    const int xbuf = (pos_buf * 16 + 127) / 128 * 128;
+    const int T = K * K;
+    const int wblk = 2 * T * kTapBytes;
+    const int stage_bytes = 2 * xbuf + wblk;
+    const int land_bytes = 4 * rows_in * W * 4;  // buffers 128-byte aligned apart
+    const int fixed = kTcLand * ((land_bytes + 127) & ~127) + kTapBytes + kScratchFloats * 4;
+    int ns = kTcMaxStages;
+    while (ns > 2 && ns * stage_bytes + fixed > 225 * 1024) --ns;
+    if (ns * stage_bytes + fixed > 225 * 1024) return CN_ERR_UNSUPPORTED;
+    const int row_tiles = (Ho + R - 1) / R;
+    const long long items = (long long)d.N * row_tiles * (d.C_out / kTcM);
+    if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+
+    a.tc = 1;
+    a.tc_xmap_base = nullptr;
+    a.tc_K = K;
+    a.tc_R = R;
+    a.tc_npos = npos;
+    a.tc_ngrp = d.C_in / 4;
+    a.tc_xbuf_bytes = xbuf;
+    a.tc_wblk_bytes = wblk;
+    a.tc_stage_bytes = stage_bytes;
+    a.tc_land_bytes = land_bytes;
+    a.tc_stages = ns;
+    a.tc_acc_cols = npos <= 32 ? 32 : npos <= 64 ? 64 : npos <= 128 ? 128 : 256;
+    a.use_bulk = 1;
+    a.N = d.N;
+    a.Ci = d.C_in;
+    a.Co = d.C_out;
+    a.H = H;
+    a.W = W;
+    a.Ho = Ho;
+    a.Wo = Wo;
+    a.Cig = d.C_in;
+    a.Cog = d.C_out;
+    a.row_tiles = row_tiles;
+    a.col_tiles = 1;
+    a.ncob = d.C_out / kTcM;
+    a.ntiles = row_tiles;
+    a.wsp = 1;
+    a.items = (int)items;
+    a.wprep = nullptr;
+    a.act = d.act;
+    a.norm = d.norm;
+    a.NG = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
+    a.affine = d.affine && d.norm != CN_NORM_NONE;
+    a.eps = d.eps;
+    a.post_scale = d.post_scale;
+    a.S = (long long)Ho * Wo;
+    a.apply_needed = !(d.norm == CN_NORM_NONE && d.post_scale == 1.0f);
+    a.vec4 = (a.S % 4) == 0;
+
+    cfg.kern = k_conv2d_tc;
+    cfg.names = "k_prep_weights_tc,k_conv2d_tc,k_group_stats,k_norm_apply";
+    cfg.K = K;
+    cfg.RW = 0;
+    cfg.COT = kTcM;
+    cfg.VECW = 0;
+    cfg.transposed = 0;
+    cfg.threads = kTcThreads;
+    cfg.smem = ns * stage_bytes + fixed;
+    cfg.grid = (int)std::min<long long>(items, 148);
+    const long long wtotal = (long long)a.ncob * a.tc_ngrp * wblk / 4;
+    cfg.prep_grid = (int)std::max(1LL, std::min((wtotal + 255) / 256, 1024LL));
+    cfg.apply_threads = 256;
+    const long long units = a.vec4 ? a.S / 4 : a.S;
+    const long long gy = (units + 256 * 4 - 1) / (256 * 4);
+    cfg.apply_grid_y = (int)std::max(1LL, std::min(gy, 65535LL));
+    const long long gx = (long long)d.N * d.C_out;
+    if (gx > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.apply_grid_x = (int)gx;
+    return CN_OK;
+}
+
+size_t tc2d_wprep_bytes(const Full2dArgs &a) { return (size_t)a.ncob * a.tc_ngrp * a.tc_wblk_bytes; }
+
+// Encodes the input tensor map for this x (cached while x stays the same).
+int tc2d_bind_x(Full2dArgs &a) {
+    if (a.tc_xmap_base == a.x) return CN_OK;
+    const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Ci, (uint64_t)a.N};
+    const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                 (uint64_t)a.Ci * a.H * a.W * 4};
+    const uint32_t box[4] = {(uint32_t)a.W, (uint32_t)(a.tc_R + a.tc_K - 1), 4u, 1u};
+    const int st = encode_tmap_f32_4d(&a.tc_xmap, a.x, dims, strides, box);
+    if (st != CN_OK) return st;
+    a.tc_xmap_base = a.x;
+    return CN_OK;
+}
+
+int tc2d_prep_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s) {
+    const long long total = (long long)a.ncob * a.tc_ngrp * a.tc_wblk_bytes / 4;
+    k_prep_weights_tc<<<cfg.prep_grid, 256, 0, s>>>(a.w, a.wprep, a.Ci, a.tc_K, a.tc_ngrp, total);
+    return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
+}
+
+}  // namespace cn

@@ -512,7 +512,7 @@ int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
     return CN_OK;
 }
 
-int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s) {
+int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
     if (a.use_tma && a.tmap_base != a.x) {
         const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D,
@@ -525,7 +525,9 @@ int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s) {
         if (st != CN_OK) return st;
         a.tmap_base = a.x;
     }
+    record_launch(ev, 0, s);
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    record_launch(ev, 1, s);
     return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }
 

@@ -250,7 +250,7 @@ int pool3d_prepare(const Pool3dConfig &cfg) {
     return CN_OK;
 }
 
-int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s) {
+int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
     if (a.use_tma && a.tmap_base != a.x) {
         const int K = a.D - a.Do + 1, P = 4 + K - 1, PX = (P + 3) & ~3;
@@ -262,7 +262,9 @@ int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s) {
         if (st != CN_OK) return st;
         a.tmap_base = a.x;
     }
+    record_launch(ev, 0, s);
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    record_launch(ev, 1, s);
     return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }
 

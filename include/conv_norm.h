@@ -184,6 +184,22 @@ int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
  */
 int conv_norm_plan_check_device(conv_norm_plan plan, void *cuda_stream);
 
+/*
+ * Optional per-launch timing (a measurement aid; no counterpart in the
+ * transcripts).  After this call every conv_norm_forward on the plan records
+ * events[i] on its stream just before the plan's i-th kernel launch and
+ * events[L] after the last one, where L = conv_norm_info.launches_per_forward;
+ * cudaEventElapsedTime(events[i], events[i+1]) is then the device time of
+ * launch i (kernel names in order: conv_norm_info.kernel_names).
+ *   events  array of n cudaEvent_t handles, created and owned by the caller,
+ *           valid until the next call of this function (the handles are
+ *           copied, the array may be freed after the call)
+ *   n       L + 1, or 0 (events may be NULL) to stop recording
+ * Errors: CN_ERR_INVALID_ARG for a NULL plan, n not in {0, L + 1}, or a NULL
+ * handle.  conv_norm_forward_host does not record.
+ */
+int conv_norm_plan_set_launch_events(conv_norm_plan plan, void *const *events, int n);
+
 /* ---- forward without any allocation ------------------------------------------ */
 
 /*

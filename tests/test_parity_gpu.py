@@ -250,3 +250,25 @@ def test_plan_info_reports_kernels():
             assert info["launches_per_forward"] >= 1
             assert info["kernel_names"]
             assert info["grid_ctas"] > 0
+
+
+def test_launch_events_time_each_kernel():
+    s = wl.with_overrides(W["conv2d_in_half_n32"], N=2, H=24)
+    inp = wl.make_inputs(s)
+    dev = {k: to_dev(v) for k, v in inp.items()}
+    with B.Plan(s) as p:
+        L = p.info()["launches_per_forward"]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
+        for e in evs:
+            e.record()
+        torch.cuda.synchronize()
+        with pytest.raises(B.ConvNormError):
+            p.set_launch_events(evs[:-1])
+        p.set_launch_events(evs)
+        out = torch.empty(p.out_shape, dtype=torch.float32, device="cuda")
+        p.forward(dev["x"], dev["w"], dev["b"], dev["gamma"], dev["beta"], out, None)
+        torch.cuda.synchronize()
+        d = [evs[i].elapsed_time(evs[i + 1]) for i in range(L)]
+        assert all(v > 0 for v in d), d
+        p.set_launch_events(None)
+        assert_parity(out.cpu().numpy(), oracle.forward(s, inp), s["name"])
