@@ -34,29 +34,42 @@ CN_DEV float hardswish(float v) {
 // 7.1.26 (Hastings' rational approximation): for x >= 0,
 //   erf(x) = 1 - (a1 t + a2 t^2 + a3 t^3 + a4 t^4 + a5 t^5) exp(-x^2),
 //   t = 1 / (1 + p x),  |error| <= 1.5e-7;  erf(-x) = -erf(x).
-// About 13 instructions (one reciprocal, one exp2) instead of ~30; the
-// constants are checked against the stated bound by a CPU test.
+// The constants, and the GELU below built from them, are checked against
+// the stated bound by a CPU test.
 #define CN_AS_P 0.3275911f
 #define CN_AS_A1 0.254829592f
 #define CN_AS_A2 -0.284496736f
 #define CN_AS_A3 1.421413741f
 #define CN_AS_A4 -1.453152027f
 #define CN_AS_A5 1.061405429f
-CN_DEV float erf_as7126(float x) {
-    const float ax = fabsf(x);
-    const float t = __fdividef(1.0f, fmaf(CN_AS_P, ax, 1.0f));
-    float y = fmaf(t, CN_AS_A5, CN_AS_A4);
-    y = fmaf(t, y, CN_AS_A3);
-    y = fmaf(t, y, CN_AS_A2);
-    y = fmaf(t, y, CN_AS_A1);
-    y *= t;
-    const float r = fmaf(-y, __expf(-ax * ax), 1.0f);
-    return copysignf(r, x);
+// Hardware approximations (PTX rcp.approx / ex2.approx, ~1 ulp).
+CN_DEV float rcp_approx(float x) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+CN_DEV float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 // Exact (erf-form) GELU: 0.5 v (1 + erf(v / sqrt 2))  (l2_p19, nn.GELU's
-// default approximate='none'), with erf from erf_as7126.
+// default approximate='none'), with erf from 7.1.26 at x = |v| / sqrt 2.
+// There 0.5 (1 - erf(x)) = g = 0.5 y(t) exp(-v^2 / 2) >= 0, so
+//   GELU(v) = v - v g = max(v, 0) - |v| g   for v >= 0,
+//   GELU(v) = v g     = max(v, 0) - |v| g   for v < 0,
+// with 1/sqrt 2 folded into p, the 0.5 into the a_i and log2(e) / 2 into
+// the exponent: 11 operations, one reciprocal and one exp2.
 CN_DEV float gelu_erf(float v) {
-    return 0.5f * v * (1.0f + erf_as7126(v * 0.70710678118654752f));
+    const float av = fabsf(v);
+    const float t = rcp_approx(fmaf(CN_AS_P * 0.70710678118654752f, av, 1.0f));
+    float y = fmaf(t, 0.5f * CN_AS_A5, 0.5f * CN_AS_A4);
+    y = fmaf(t, y, 0.5f * CN_AS_A3);
+    y = fmaf(t, y, 0.5f * CN_AS_A2);
+    y = fmaf(t, y, 0.5f * CN_AS_A1);
+    y *= t;
+    const float e = ex2_approx(v * (v * (-0.5f * 1.4426950408889634f)));
+    return fmaf(-av, y * e, fmaxf(v, 0.0f));
 }
 CN_DEV float apply_act(int act, float v) {
     if (act == ACT_HARDSWISH) return hardswish(v);

@@ -128,6 +128,12 @@ struct Full2dArgs {
     int tc_stages;              // operand stages in shared memory
     int tc_acc_cols;            // TMEM columns per accumulator (two are allocated)
 
+    // CUDA-core kernel staging: use_tma = one tensor copy per stage (box
+    // (pitch, rows_in, cib, 1) of x viewed as (W, H, C_in, N), zero fill
+    // outside); else use_bulk = one bulk copy per row; else cp.async.
+    CUtensorMap xmap;
+    const float *xmap_base;     // x pointer xmap was encoded for
+    int use_tma;
     int use_bulk;         // 1: rows staged with bulk async copies (W % 4 == 0)
     const float *x, *w, *b, *gamma, *beta;
     float *out;

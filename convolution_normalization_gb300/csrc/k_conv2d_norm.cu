@@ -109,7 +109,11 @@ constexpr int kMaxStages = 4;  // deepest input pipeline the kernel supports
 
 // ACTT >= 0 compiles the epilogue for that one activation; -1 switches at
 // run time (three copies of the unrolled epilogue, more instruction cache).
-template <int K, int RW, int COT, int VECW, bool TRANSPOSED, int ACTT>
+// OFF (with VECW = 4): the tile's first input column sits OFF floats past a
+// 16-byte boundary of the row buffer (2 for the transposed k = 3 conv, whose
+// tile origin moves left by k - 1); rows are then read as aligned float4
+// windows starting OFF floats early, which keeps the loads conflict-free.
+template <int K, int RW, int COT, int VECW, bool TRANSPOSED, int ACTT, int OFF = 0>
 __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
     k_conv2d_act_stats(const __grid_constant__ Full2dArgs a) {
     extern __shared__ __align__(128) float smem[];
@@ -118,8 +122,9 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
     __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
     __shared__ int s_tile[kMaxStages], s_chunk[kMaxStages];
     static_assert(COT == 4 || COT == 8, "channel slice of 4 or 8");
+    static_assert(OFF == 0 || VECW == 4, "an input offset needs float4 row loads");
     constexpr int XW = RW + K - 1;
-    constexpr int LOADW = (XW + VECW - 1) / VECW * VECW;
+    constexpr int LOADW = (OFF + XW + VECW - 1) / VECW * VECW;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nwarps = blockDim.x >> 5;
     const int cs = warp % a.wco;
@@ -177,6 +182,21 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
         }
         const Geo &G = PG;
         const int cbase = chunk * a.cib;
+        if (a.use_tma) {
+            // one tensor copy of the stage's rows x columns x channels; the
+            // parts outside the image (and past the group's channels at the
+            // end of the tensor) arrive as zeros
+            if (lane == 0) {
+                s_tile[buf] = tile;
+                s_chunk[buf] = chunk;
+                mbar_arrive_expect_tx(&full[buf], (uint32_t)(a.xstage + a.wstage) * 4u);
+                tma_load_4d(sxb, &a.xmap, G.xs, G.ir0, G.ci0 + cbase, G.n, &full[buf]);
+                bulk_load(sxb + a.xstage, a.wprep + ((size_t)G.cob * a.nchunk + chunk) * a.wstage,
+                          (uint32_t)a.wstage * 4u, &full[buf]);
+            }
+            __syncwarp();
+            return;
+        }
         const int ncl = min(a.cib, a.Cig - cbase);
         const int gr_lo = max(G.ir0, 0), gr_hi = min(G.ir0 + a.rows_in, a.H);
         const int top = gr_lo - G.ir0, bot = gr_hi - G.ir0;  // in-image rows are [top, bot)
@@ -342,7 +362,8 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
         for (int cl = 0; cl < ncl; ++cl) {
             CN_UNROLL(CN_TAP_UNROLL)
             for (int kh = 0; kh < K; ++kh) {
-                const float *xp = sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + G.off + sl * RW;
+                const float *xp =
+                    sxb + (size_t)(cl * a.rows_in + il + kh) * a.pitch + (G.off - OFF) + sl * RW;
                 float xr[LOADW];
                 if constexpr (VECW == 4) {
 #pragma unroll
@@ -379,7 +400,7 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                     }
 #pragma unroll
                     for (int i = 0; i < RW; ++i) {
-                        const float xv = xr[i + kw];
+                        const float xv = xr[OFF + i + kw];
 #pragma unroll
                         for (int c = 0; c < COT; ++c) acc[c][i] = fmaf(xv, wv[c], acc[c][i]);
                     }
@@ -451,51 +472,70 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
     }
 }
 
-// Statistics of the normalization groups, one warp per (n, group).  All
-// partials of one channel share that channel's shift K, so per channel the
-// lanes add the shifted sums (count, S1, S2) of every tile: fp32 within a
-// lane, then an fp64 butterfly of commutative adds (every lane gets the same
-// bits, and the order is fixed, so the result is deterministic).  The
-// channels of a group are then merged as (count, mean, M2) in fp64, in channel
-// order.  The warp writes each channel's coefficients (mu, a = gamma * rstd *
-// scale, bb = beta * scale).  fp64 work is a few dozen operations per group:
-// the FP64 pipe of this GPU is narrow.
+// Statistics of the normalization groups.  A group of one channel
+// (InstanceNorm) gets one warp, four per block; a wider group gets the four
+// warps of a block, warp w taking channels w, w + 4, ... .  All partials of
+// one channel share that channel's shift K, so per channel the lanes add the
+// shifted sums (count, S1, S2) of every tile, then a butterfly of
+// commutative adds gives every lane the same bits.  Channel moments are
+// merged as (count, mean, M2): within a warp in channel order, then the
+// warps' results in warp order, so the result is deterministic.  The group's
+// coefficients (mu, a = gamma * rstd * scale, bb = beta * scale) go to
+// every channel.  Arithmetic is fp32: its ~1e-6 relative error in mean and
+// variance is far inside the 1e-4 output bound, and the FP64 pipe of this
+// GPU is narrow enough that a few fp64 divisions per group cost more than
+// the pass's memory traffic.
 constexpr int kStatsWarps = 4;
+CN_DEV Moments<float> channel_moments(const float4 *p, int per_c, int lane) {
+    long long cnt = 0;  // exact count
+    float3 v = make_float3(0.0f, 0.0f, 0.0f);  // (-, S1, S2)
+    for (int i = lane; i < per_c; i += 32) {
+        const float4 q = p[i];
+        cnt += (long long)q.x;
+        v.y += q.z;
+        v.z += q.w;
+    }
+    v = warp_sum3(v);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    if (cnt <= 0) return Moments<float>{0.0f, 0.0f, 0.0f};
+    const float fn = (float)cnt;
+    const float mu_s = v.y / fn;  // mean - K
+    return Moments<float>{fn, p[0].y + mu_s, fmaxf(v.z - v.y * mu_s, 0.0f)};
+}
+
 __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a) {
-    const int lane = threadIdx.x & 31;
-    const int ng = blockIdx.x * kStatsWarps + (threadIdx.x >> 5);  // (n, group)
-    if (ng >= a.N * a.NG) return;
-    const int n = ng / a.NG, g = ng % a.NG;
+    __shared__ float sm[kStatsWarps][3];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int cpg = a.Co / a.NG;
     const int per_c = a.ntiles * a.wsp;
-    Moments<double> m{0.0, 0.0, 0.0};
-    for (int cl = 0; cl < cpg; ++cl) {
-        const float4 *p = a.partial + ((size_t)n * a.Co + (size_t)g * cpg + cl) * per_c;
-        int cnt = 0;
-        float s1 = 0.0f, s2 = 0.0f;
-        for (int i = lane; i < per_c; i += 32) {
-            const float4 q = p[i];
-            cnt += (int)q.x;
-            s1 += q.z;
-            s2 += q.w;
+    const bool wide = cpg > 1;
+    const int ng = wide ? (int)blockIdx.x : (int)blockIdx.x * kStatsWarps + w;  // (n, group)
+    if (ng >= a.N * a.NG) return;  // uniform per block when wide
+    const int n = ng / a.NG, g = ng % a.NG;
+    const float4 *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c;
+    Moments<float> m{0.0f, 0.0f, 0.0f};
+    for (int cl = wide ? w : 0; cl < cpg; cl += wide ? kStatsWarps : 1)
+        m = merge(m, channel_moments(p0 + (size_t)cl * per_c, per_c, lane));
+    if (wide) {
+        if (lane == 0) {
+            sm[w][0] = m.n;
+            sm[w][1] = m.mean;
+            sm[w][2] = m.m2;
         }
-        double d1 = s1, d2 = s2;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-            d1 += __shfl_xor_sync(0xffffffffu, d1, off);
-            d2 += __shfl_xor_sync(0xffffffffu, d2, off);
-        }
-        m = merge(m, moments_from_sums((double)cnt, (double)p[0].y, d1, d2));
+        __syncthreads();
+        if (w != 0) return;
+        m = Moments<float>{sm[0][0], sm[0][1], sm[0][2]};
+        for (int j = 1; j < kStatsWarps; ++j) m = merge(m, Moments<float>{sm[j][0], sm[j][1], sm[j][2]});
     }
-    const double mean = m.mean, var = m.n > 0.0 ? m.m2 / m.n : 0.0;
-    const double rstd = 1.0 / sqrt(var + (double)a.eps);
+    const float var = m.n > 0.0f ? m.m2 / m.n : 0.0f;
+    const float rstd = 1.0f / sqrtf(var + a.eps);
     for (int cl = lane; cl < cpg; cl += 32) {
         const int c = g * cpg + cl;
-        const double ga = a.affine ? (double)a.gamma[c] : 1.0;
-        const double be = a.affine ? (double)a.beta[c] : 0.0;
-        a.coef[(size_t)n * a.Co + c] = make_float4((float)mean, (float)(rstd * ga * a.post_scale),
-                                                   (float)(be * a.post_scale), 0.0f);
+        const float ga = a.affine ? a.gamma[c] : 1.0f;
+        const float be = a.affine ? a.beta[c] : 0.0f;
+        a.coef[(size_t)n * a.Co + c] =
+            make_float4(m.mean, rstd * ga * a.post_scale, be * a.post_scale, 0.0f);
     }
 }
 
@@ -506,9 +546,11 @@ __global__ void k_fill_scale(float4 *coef, int n, float scale) {
 }
 
 // Normalize pass: out = (y - mu) * a + bb per (n, c) plane, in place.
+// Planes run last-written first: the conv pass wrote samples roughly in
+// order, so the newest planes are the ones still in L2.
 __global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *coef, long long S,
                                                     int vec4) {
-    const size_t plane = blockIdx.x;
+    const size_t plane = gridDim.x - 1 - blockIdx.x;
     const float4 cf = coef[plane];
     float *p = out + plane * (size_t)S;
     const long long step = (long long)gridDim.y * blockDim.x;
@@ -531,15 +573,21 @@ __global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *co
 
 struct Inst {
     int K, RW, COT, VECW, T, ACT;  // ACT -1: activation chosen at run time
+    int OFF;                       // fixed input-column offset (float4 windows), 0: none
     Full2dKernel fn;
     const char *name;
 };
-#define CN_FULL_INST(K, RW, C, V, T, A)                            \
-    {K, RW, C, V, T, A, k_conv2d_act_stats<K, RW, C, V, (T != 0), A>, \
+#define CN_FULL_INST(K, RW, C, V, T, A)                               \
+    {K, RW, C, V, T, A, 0, k_conv2d_act_stats<K, RW, C, V, (T != 0), A>, \
      "k_prep_weights,k_conv2d_act_stats<" #K "," #RW "," #C "," #V "," #T "," #A ">,k_group_stats,k_norm_apply"}
+#define CN_FULL_INST_OFF(K, RW, C, T, A, O)                                    \
+    {K, RW, C, 4, T, A, O, k_conv2d_act_stats<K, RW, C, 4, (T != 0), A, O>,      \
+     "k_prep_weights,k_conv2d_act_stats<" #K "," #RW "," #C ",4," #T "," #A "," #O \
+     ">,k_group_stats,k_norm_apply"}
 const Inst kInst[] = {
     // activation-specialised: the 64->128 conv (none), the grouped transposed conv (GELU)
     CN_FULL_INST(3, 16, 4, 4, 0, 0), CN_FULL_INST(3, 16, 4, 2, 1, 2), CN_FULL_INST(3, 13, 4, 1, 1, 2),
+    CN_FULL_INST_OFF(3, 12, 4, 1, 2, 2), CN_FULL_INST_OFF(3, 12, 4, 1, -1, 2),
     // run-time activation
     CN_FULL_INST(3, 16, 8, 4, 0, -1), CN_FULL_INST(3, 16, 4, 4, 0, -1), CN_FULL_INST(1, 16, 8, 4, 0, -1),
     CN_FULL_INST(2, 16, 8, 4, 0, -1), CN_FULL_INST(4, 16, 8, 4, 0, -1), CN_FULL_INST(3, 13, 4, 1, 1, -1),
@@ -547,6 +595,7 @@ const Inst kInst[] = {
     CN_FULL_INST(4, 16, 8, 1, 1, -1),
 };
 #undef CN_FULL_INST
+#undef CN_FULL_INST_OFF
 
 int env_int(const char *name, int dflt) {
     const char *v = getenv(name);
@@ -576,6 +625,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     const int Wo = T ? d.W + K - 1 : d.W - K + 1;
     const int Cig = d.C_in / d.groups, Cog = d.C_out / d.groups;
     const bool bulk = (d.W % 4 == 0) && env_int("CN_NO_TMA", 0) == 0;
+    const bool tma2d = bulk && tma_available() && env_int("CN_NO_TMA2D", 0) == 0;
     const int f_cot = env_int("CN_FULL2D_COT", 0), f_rw = env_int("CN_FULL2D_RW", 0),
               f_wsp = env_int("CN_FULL2D_WSP", 0);
     const int off = bulk ? (((-(K - 1) * T) % 4) + 4) % 4 : 0;
@@ -584,16 +634,21 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
         if (in.K != K || in.T != T || Cog % in.COT != 0) continue;
         if (in.ACT >= 0 && in.ACT != d.act) continue;
         if ((f_cot && in.COT != f_cot) || (f_rw && in.RW != f_rw)) continue;
-        if (off % in.VECW != 0) continue;
+        if (in.OFF ? in.OFF != off : off % in.VECW != 0) continue;
         const int wco = pick_wco(Cog / in.COT);
         const int nseg = (Wo + in.RW - 1) / in.RW;
         const int XW = in.RW + K - 1;
-        const int loadw = (XW + in.VECW - 1) / in.VECW * in.VECW;
+        const int loadw = (in.OFF + XW + in.VECW - 1) / in.VECW * in.VECW;
         const int regs = std::min(255, in.COT * in.RW + loadw + in.COT + 40);
-        for (int wsp = 1; wco * wsp <= 8; ++wsp) {
+        for (int cand = 0; cand < 8 * 3; ++cand) {
+            const int wsp = 1 + cand / 3, split = 1 + cand % 3;
+            if (wco * wsp > 8) break;
             if (f_wsp && wsp != f_wsp) continue;
             const int lanes = 32 * wsp;
-            const int NT = std::min(nseg, lanes);
+            // segments per column tile: all that fit the lanes, or the row
+            // split in two or three column tiles (narrower row buffers)
+            const int NT = std::min((nseg + split - 1) / split, lanes);
+            if (split > 1 && NT == std::min((nseg + split - 2) / (split - 1), lanes)) continue;
             const int TR = std::max(1, std::min(lanes / NT, Ho));
             // segments of every column tile must keep the load alignment
             const int ctiles = (nseg + NT - 1) / NT;
@@ -616,7 +671,16 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
             const double occ = warps_sm >= 16 ? 1.0 : 1.0 + 0.025 * (16 - warps_sm);
             // a specialised epilogue is smaller and cheaper than the run-time switch
             const double spec = in.ACT >= 0 ? 0.97 : 1.0;
-            const double cost = waste * ratio * balance * occ * spec;
+            // staging: one tensor copy per stage when the row buffer fits a TMA
+            // box; otherwise one bulk copy per row plus zeroing of the halo,
+            // measured at ~15% of the conv time on the 64-channel transposed conv
+            const int cols_in_c = NT * in.RW + K - 1;
+            int pitch_c = std::max(off - in.OFF + (NT - 1) * in.RW + loadw, off + cols_in_c + 3);
+            pitch_c = (pitch_c + 3) & ~3;
+            if (((pitch_c / 4) & 1) == 0) pitch_c += 4;
+            const bool tma_c = tma2d && pitch_c <= 256 && TR + K - 1 <= 256;
+            const double stage = tma_c ? 1.0 : 1.15;
+            const double cost = waste * ratio * balance * occ * spec * stage;
             if (cost < best.cost - 1e-9) {
                 best.in = &in;
                 best.wco = wco;
@@ -631,7 +695,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     const Inst &in = *best.in;
     const int RW = in.RW, COT = in.COT;
     const int XW = RW + K - 1;
-    const int LOADW = (XW + in.VECW - 1) / in.VECW * in.VECW;
+    const int LOADW = (in.OFF + XW + in.VECW - 1) / in.VECW * in.VECW;
     a.use_bulk = bulk ? 1 : 0;
     a.N = d.N;
     a.Ci = d.C_in;
@@ -653,12 +717,15 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.ntiles = a.row_tiles * a.col_tiles;
     a.rows_in = a.TR + K - 1;
     a.cols_in = a.NT * RW + K - 1;
-    // row buffer: the tile's reads reach off + (NT-1)*RW + LOADW; bulk copies
-    // of whole 16-byte groups reach at most off + cols_in + 3.
-    int pitch = std::max(off + (a.NT - 1) * RW + LOADW, off + a.cols_in + 3);
+    // row buffer: the tile's reads reach off - OFF + (NT-1)*RW + LOADW; bulk
+    // copies of whole 16-byte groups reach at most off + cols_in + 3.
+    int pitch = std::max(off - in.OFF + (a.NT - 1) * RW + LOADW, off + a.cols_in + 3);
     pitch = (pitch + 3) & ~3;
     if (((pitch / 4) & 1) == 0) pitch += 4;  // 4 (mod 8) floats: conflict-free row loads
     a.pitch = pitch;
+    // the whole stage as one tensor copy: box (pitch, rows_in, cib, 1)
+    a.use_tma = (tma2d && pitch <= 256 && a.rows_in <= 256) ? 1 : 0;
+    a.xmap_base = nullptr;
     const int COB = COT * a.wco;
     const int per_ci = a.rows_in * pitch + K * K * COB;
     // Pipeline: 3 stages (measured best of 2..4 on both 2-D workloads) when
@@ -764,6 +831,14 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
     if (a.tc) {
         const int st = tc2d_bind_x(a);
         if (st != CN_OK) return st;
+    } else if (a.use_tma && a.xmap_base != a.x) {
+        const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Ci, (uint64_t)a.N};
+        const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                     (uint64_t)a.Ci * a.H * a.W * 4};
+        const uint32_t box[4] = {(uint32_t)a.pitch, (uint32_t)a.rows_in, (uint32_t)a.cib, 1u};
+        const int st = encode_tmap_f32_4d(&a.xmap, a.x, dims, strides, box);
+        if (st != CN_OK) return st;
+        a.xmap_base = a.x;
     }
     record_launch(ev, 0, s);
     if (a.tc) {
@@ -783,7 +858,9 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
         if (a.norm == CN_NORM_NONE) {
             k_fill_scale<<<(a.N * a.Co + 255) / 256, 256, 0, s>>>(a.coef, a.N * a.Co, a.post_scale);
         } else {
-            k_group_stats<<<(a.N * a.NG + kStatsWarps - 1) / kStatsWarps, 32 * kStatsWarps, 0, s>>>(a);
+            const int cpg = a.Co / a.NG;
+            const int blocks = cpg > 1 ? a.N * a.NG : (a.N * a.NG + kStatsWarps - 1) / kStatsWarps;
+            k_group_stats<<<blocks, 32 * kStatsWarps, 0, s>>>(a);
         }
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
         record_launch(ev, 3, s);

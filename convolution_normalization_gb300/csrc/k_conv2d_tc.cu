@@ -75,8 +75,7 @@ CN_DEV void umma_tf32(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, 
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(accum)
-        : "memory");
+        "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
 }
 // Arrives on bar once every MMA this thread issued so far has completed.
 CN_DEV void umma_commit(uint64_t *bar) {
@@ -152,8 +151,9 @@ CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *er
 __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_constant__ Full2dArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t land_full[kTcLand], land_empty[kTcLand];
-    __shared__ __align__(8) uint64_t w_full[kTcMaxStages], x_full[kTcMaxStages],
-        st_empty[kTcMaxStages];
+    // full[b]: the stage's filter block landed (tx bytes) and the four
+    // converter warps wrote its input operands; st_empty[b]: its MMAs are done
+    __shared__ __align__(8) uint64_t full[kTcMaxStages], st_empty[kTcMaxStages];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
     __shared__ int s_land_tile[kTcLand], s_st_tile[kTcMaxStages], s_acc_tile[2];
     __shared__ uint32_t s_tmem;
@@ -194,8 +194,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
             mbar_init(&land_empty[i], 4);
         }
         for (int i = 0; i < NS; ++i) {
-            mbar_init(&w_full[i], 1);
-            mbar_init(&x_full[i], 4);
+            mbar_init(&full[i], 1 + 4);
             mbar_init(&st_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -224,8 +223,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
 
     if (warp == 0) {
         // ---------------- producer ----------------
+        // Stage k uses landing buffer k % kTcLand and stage slot k % NS;
+        // slot indices and phase parities advance incrementally.
         if (lane == 0) {
             int kl = 0, kw = 0;  // landing / filter stages armed so far
+            int lb = 0, b = 0;
+            uint32_t lph = 0, sph = 0;  // parity of the current pass over each ring
             int next = (int)blockIdx.x;
             bool live = true;
             while (live) {
@@ -240,9 +243,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                 }
                 const int ng = tile >= 0 ? a.tc_ngrp : 1;  // a stop marker is one stage
                 for (int g = 0; g < ng; ++g) {
-                    const int k = kl;
-                    const int lb = k % kTcLand, b = k % NS;
-                    if (k >= kTcLand && !wait(&land_empty[lb], ((k / kTcLand) - 1) & 1)) {
+                    // landing buffer lb was last used kTcLand stages ago
+                    if (kl >= kTcLand && !wait(&land_empty[lb], lph ^ 1u)) {
                         live = false;
                         break;
                     }
@@ -254,40 +256,52 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                         mbar_arrive(&land_full[lb]);
                     }
                     ++kl;
-                    if (k >= NS && !wait(&st_empty[b], ((k / NS) - 1) & 1)) {
+                    if (++lb == kTcLand) {
+                        lb = 0;
+                        lph ^= 1u;
+                    }
+                    if (kw >= NS && !wait(&st_empty[b], sph ^ 1u)) {
                         live = false;
                         break;
                     }
                     s_st_tile[b] = tile;
                     if (tile >= 0) {
-                        mbar_arrive_expect_tx(&w_full[b], (uint32_t)a.tc_wblk_bytes);
+                        mbar_arrive_expect_tx(&full[b], (uint32_t)a.tc_wblk_bytes);
                         bulk_load(stage(b) + 2 * (size_t)a.tc_xbuf_bytes,
                                   reinterpret_cast<const unsigned char *>(a.wprep) +
                                       ((size_t)cob * a.tc_ngrp + g) * a.tc_wblk_bytes,
-                                  (uint32_t)a.tc_wblk_bytes, &w_full[b]);
+                                  (uint32_t)a.tc_wblk_bytes, &full[b]);
                     } else {
-                        mbar_arrive(&w_full[b]);
+                        mbar_arrive(&full[b]);
                     }
                     ++kw;
+                    if (++b == NS) {
+                        b = 0;
+                        sph ^= 1u;
+                    }
                 }
                 if (tile < 0) live = false;
             }
-            // copies still in flight (only after an abort) land before the CTA exits
+            // copies still in flight (only after an abort) land before the CTA
+            // exits; in a normal run these phases are long complete
             for (int j = std::max(0, kl - kTcLand); j < kl; ++j)
                 mbar_wait_bounded(&land_full[j % kTcLand], (j / kTcLand) & 1, kWaitLimitNs);
             for (int j = std::max(0, kw - NS); j < kw; ++j)
-                mbar_wait_bounded(&w_full[j % NS], (j / NS) & 1, kWaitLimitNs);
+                mbar_wait_bounded(&full[j % NS], (j / NS) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
+        // Between two stages this thread only waits for one barrier and
+        // commits: the tensor pipe's queue holds a few MMAs (under ~1000
+        // cycles of work), so per-stage overhead shows up as idle time.
         if (lane == 0) {
             const uint32_t idesc = idesc_tf32(kTcM, a.tc_npos);
             // The operand descriptors of a stage depend only on its slot:
-            // built once here, so issuing a stage is loads and MMAs only.
+            // built once here.
             const uint32_t zaddr = smem_u32(zero_blk);
             int nm = 0;
-            for (int b = 0; b < NS; ++b) {
-                const uint32_t sb = smem_u32(stage(b));
+            for (int sb_i = 0; sb_i < NS; ++sb_i) {
+                const uint32_t sb = smem_u32(stage(sb_i));
                 const uint32_t xh = sb;
                 const uint32_t wl = sb + 2u * (uint32_t)a.tc_xbuf_bytes;
                 const uint32_t wh = wl + (uint32_t)(T * kTapBytes);
@@ -295,62 +309,64 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                 nm = 0;
                 // cross terms: Wl(t) Xh(t) + Wh(t) Xl(t)
                 for (int tp = 0; tp < T; ++tp, ++nm) {
-                    s_desc[b][nm][0] = umma_desc(wl + tp * kTapBytes, (uint32_t)(T * kTapBytes), 128);
-                    s_desc[b][nm][1] = umma_desc(xh + off(tp) * 16, (uint32_t)a.tc_xbuf_bytes, 128);
+                    s_desc[sb_i][nm][0] = umma_desc(wl + tp * kTapBytes, (uint32_t)(T * kTapBytes), 128);
+                    s_desc[sb_i][nm][1] = umma_desc(xh + off(tp) * 16, (uint32_t)a.tc_xbuf_bytes, 128);
                 }
                 // hi * hi, two taps per MMA
                 int tp = 0;
                 for (; tp + 1 < T; tp += 2, ++nm) {
-                    s_desc[b][nm][0] = umma_desc(wh + tp * kTapBytes, kTapBytes, 128);
-                    s_desc[b][nm][1] =
+                    s_desc[sb_i][nm][0] = umma_desc(wh + tp * kTapBytes, kTapBytes, 128);
+                    s_desc[sb_i][nm][1] =
                         umma_desc(xh + off(tp) * 16, (uint32_t)((off(tp + 1) - off(tp)) * 16), 128);
                 }
                 if (tp < T) {  // odd tap count: the last tap with the zero block
                     const uint32_t wa = wh + tp * kTapBytes;
-                    s_desc[b][nm][0] = umma_desc(wa, zaddr - wa, 128);
-                    s_desc[b][nm][1] = umma_desc(xh + off(tp) * 16, 16, 128);
+                    s_desc[sb_i][nm][0] = umma_desc(wa, zaddr - wa, 128);
+                    s_desc[sb_i][nm][1] = umma_desc(xh + off(tp) * 16, 16, 128);
                     ++nm;
                 }
             }
-            int k = 0;
-            for (int t = 0;; ++t) {
+            int b = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int t = 0; ok; ++t) {
                 const int as = t & 1;
-                bool stop = false, ok = true;
-                for (int g = 0; g < a.tc_ngrp; ++g, ++k) {
-                    const int b = k % NS;
-                    const uint32_t par = (uint32_t)(k / NS) & 1u;
-                    if (!wait(&w_full[b], par) || !wait(&x_full[b], par)) {
-                        ok = false;
-                        break;
-                    }
-                    const int tile = s_st_tile[b];
-                    if (tile < 0) {
-                        stop = true;
-                        break;
-                    }
-                    if (g == 0) {
-                        if (t >= 2 && !wait(&acc_empty[as], ((t >> 1) - 1) & 1)) {
-                            ok = false;
-                            break;
-                        }
-                        s_acc_tile[as] = tile;
-                        mbar_arrive(&acc_full[as]);  // publishes the tile id (1 of 2 arrivals)
-                    }
-                    tc_fence_after();
-                    const uint32_t d = tmem + (uint32_t)(as * acc_cols);
-                    for (int i = 0; i < nm; ++i)
-                        umma_tf32(d, s_desc[b][i][0], s_desc[b][i][1], idesc, (g | i) ? 1u : 0u);
-                    umma_commit(&st_empty[b]);
-                }
-                if (!ok) break;
-                if (stop) {
-                    if (t >= 2 && !wait(&acc_empty[as], ((t >> 1) - 1) & 1)) break;
-                    s_acc_tile[as] = -1;
-                    mbar_arrive(&acc_full[as]);
+                // first stage of a tile: its id (or the stop marker)
+                if (!wait(&full[b], ph)) break;
+                const int tile = s_st_tile[b];
+                if (t >= 2 && !wait(&acc_empty[as], ((t >> 1) - 1) & 1)) break;
+                tc_fence_after();  // the epilogue's reads of this accumulator are done
+                s_acc_tile[as] = tile;
+                mbar_arrive(&acc_full[as]);  // publishes the tile id (1 of 2 arrivals)
+                if (tile < 0) {
                     mbar_arrive(&acc_full[as]);
                     break;
                 }
-                umma_commit(&acc_full[as]);  // the tile's MMAs are done (2 of 2)
+                const uint32_t d = tmem + (uint32_t)(as * acc_cols);
+                for (int g = 0;;) {
+                    uint64_t da[kMaxMmas], db[kMaxMmas];
+#pragma unroll
+                    for (int i = 0; i < kMaxMmas; ++i) {
+                        if (i < nm) {
+                            da[i] = s_desc[b][i][0];
+                            db[i] = s_desc[b][i][1];
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < kMaxMmas; ++i)
+                        if (i < nm) umma_tf32(d, da[i], db[i], idesc, (g | i) ? 1u : 0u);
+                    umma_commit(&st_empty[b]);
+                    if (++b == NS) {
+                        b = 0;
+                        ph ^= 1u;
+                    }
+                    if (++g == a.tc_ngrp) break;
+                    if (!wait(&full[b], ph)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (ok) umma_commit(&acc_full[as]);  // the tile's MMAs are done (2 of 2)
             }
             // every MMA issued by this thread completes before TMEM is freed
             umma_commit(&fin_bar);
@@ -360,11 +376,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
         // ---------------- converters ----------------
         const int ct = tid - 64;
         const int npix = rows_in * a.W;
+        int lb = 0, b = 0;
+        uint32_t lph = 0, sph = 0;
         for (int k = 0;; ++k) {
-            const int lb = k % kTcLand, b = k % NS;
-            if (!wait(&land_full[lb], (k / kTcLand) & 1)) break;
+            if (!wait(&land_full[lb], lph)) break;
             const int tile = s_land_tile[lb];
-            if (k >= NS && !wait(&st_empty[b], ((k / NS) - 1) & 1)) break;
+            if (k >= NS && !wait(&st_empty[b], sph ^ 1u)) break;
             if (tile >= 0) {
                 const float *src = reinterpret_cast<const float *>(land(lb));
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
@@ -380,9 +397,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&land_empty[lb]);
-                mbar_arrive(&x_full[b]);
+                mbar_arrive(&full[b]);
             }
             if (tile < 0) break;
+            if (++lb == kTcLand) {
+                lb = 0;
+                lph ^= 1u;
+            }
+            if (++b == NS) {
+                b = 0;
+                sph ^= 1u;
+            }
         }
     } else {
         // ---------------- epilogue ----------------
