@@ -608,6 +608,25 @@ struct Choice {
     double cost = 1e30;
 };
 
+// Row pitch (floats) of the staged input, at least min_pitch and a multiple
+// of 4 (16-byte rows for TMA and bulk copies).  Lane l of a warp reads row
+// l % TR, segment l / TR, so a float4 load's bank group is
+// (pitch/4 * row + RW/4 * segment) mod 8.  With pitch/4 = p (mod 8), p odd,
+// and RW/4 = p * TR (mod 8) that is p * l: the 8 lanes of every quarter
+// warp hit 8 distinct bank groups.  For odd TR, p = RW/4 * TR (odd numbers
+// are their own inverse mod 8).  Otherwise p only needs to be odd (distinct
+// rows of one segment).
+int row_pitch(int min_pitch, int VECW, int RW, int TR) {
+    int pitch = (min_pitch + 3) & ~3;
+    int want = -1;
+    if (VECW == 4 && RW % 4 == 0 && (TR & 1)) {
+        const int pw = ((RW / 4) * TR) & 7;
+        if (pw & 1) want = pw;
+    }
+    while (want >= 0 ? ((pitch / 4) & 7) != want : ((pitch / 4) & 1) == 0) pitch += 4;
+    return pitch;
+}
+
 int pick_wco(int units) {
     for (int c = 8; c >= 1; --c)
         if (units % c == 0) return c;
@@ -675,9 +694,9 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
             // box; otherwise one bulk copy per row plus zeroing of the halo,
             // measured at ~15% of the conv time on the 64-channel transposed conv
             const int cols_in_c = NT * in.RW + K - 1;
-            int pitch_c = std::max(off - in.OFF + (NT - 1) * in.RW + loadw, off + cols_in_c + 3);
-            pitch_c = (pitch_c + 3) & ~3;
-            if (((pitch_c / 4) & 1) == 0) pitch_c += 4;
+            const int pitch_c = row_pitch(
+                std::max(off - in.OFF + (NT - 1) * in.RW + loadw, off + cols_in_c + 3), in.VECW,
+                in.RW, TR);
             const bool tma_c = tma2d && pitch_c <= 256 && TR + K - 1 <= 256;
             const double stage = tma_c ? 1.0 : 1.15;
             const double cost = waste * ratio * balance * occ * spec * stage;
@@ -719,9 +738,8 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.cols_in = a.NT * RW + K - 1;
     // row buffer: the tile's reads reach off - OFF + (NT-1)*RW + LOADW; bulk
     // copies of whole 16-byte groups reach at most off + cols_in + 3.
-    int pitch = std::max(off - in.OFF + (a.NT - 1) * RW + LOADW, off + a.cols_in + 3);
-    pitch = (pitch + 3) & ~3;
-    if (((pitch / 4) & 1) == 0) pitch += 4;  // 4 (mod 8) floats: conflict-free row loads
+    const int pitch = row_pitch(std::max(off - in.OFF + (a.NT - 1) * RW + LOADW, off + a.cols_in + 3),
+                                in.VECW, RW, a.TR);
     a.pitch = pitch;
     // the whole stage as one tensor copy: box (pitch, rows_in, cib, 1)
     a.use_tma = (tma2d && pitch <= 256 && a.rows_in <= 256) ? 1 : 0;
