@@ -239,13 +239,16 @@ class ClockSampler:
 # ---- distributed plumbing ----------------------------------------------------------
 
 def dist_setup(n_gpus):
+    """One process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE): NCCL
+    with GPUs, gloo without (the host-side logic is tested that way)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
@@ -257,13 +260,21 @@ def barrier(world):
 
 
 def max_over_ranks(world, v):
+    """The slowest rank's time: the job finishes when every rank has."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_rate(world, units_per_rank, ms_max):
+    """Whole-job throughput: every rank processes its own batch (weak
+    scaling, no data-path collective), the job takes the slowest rank's time."""
+    return world * units_per_rank / (ms_max / 1e3)
 
 
 # ---- oracle (CPU baseline and the reference arm) --------------------------------------
@@ -394,7 +405,7 @@ def run_cuda(args, spec):
     ms_rank = statistics.mean(times)
     ms = max_over_ranks(world, ms_rank)
     flops = algorithmic_flops(spec)
-    value = world * flops / (ms / 1e3) / 1e9
+    value = job_rate(world, flops, ms) / 1e9
     rl_ms, bound = roofline_ms(spec, pk)
 
     # dominant kernel: the launch with the largest mean device time
