@@ -109,7 +109,8 @@ int pick_variant(const conv_norm_desc &d, int &variant) {
         variant = V_POOL3D;
         return CN_OK;
     }
-    if (d.conv == CN_CONV3D || d.act == CN_ACT_SOFTMAX_C) return CN_ERR_UNSUPPORTED;
+    // full output: Conv2d / ConvTranspose2d, and Conv3d as depth-stacked 2-D samples
+    if (d.act == CN_ACT_SOFTMAX_C) return CN_ERR_UNSUPPORTED;
     variant = V_FULL2D;
     return CN_OK;
 }

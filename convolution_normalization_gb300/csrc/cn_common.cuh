@@ -213,6 +213,16 @@ CN_DEV void tma_load_4d(void *smem_dst, const void *tmap, int c0, int c1, int c2
         "r"(smem_u32(bar))
         : "memory");
 }
+// Tiled 5-D tensor copy global -> shared, completion counted on bar.
+CN_DEV void tma_load_5d(void *smem_dst, const void *tmap, int c0, int c1, int c2, int c3, int c4,
+                        uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+        "r"(smem_u32(bar))
+        : "memory");
+}
 // Contiguous bulk copy global -> shared (16-byte aligned addresses, size a
 // multiple of 16), completion counted on bar.
 CN_DEV void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar) {

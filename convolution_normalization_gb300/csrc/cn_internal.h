@@ -26,6 +26,8 @@ inline void record_launch(const LaunchEvents *e, int i, cudaStream_t s) {
 bool tma_available();
 int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], const uint32_t box[4]);
+int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[5],
+                       const uint64_t strides_bytes[4], const uint32_t box[5]);
 
 // Upper bound on any device-side wait (ns of GPU wall time) before a kernel
 // gives up, records CN_ERR_TIMEOUT in the plan's flag and carries on.
@@ -138,7 +140,12 @@ struct Full2dArgs {
     const float *x, *w, *b, *gamma, *beta;
     float *out;
     int N, Ci, Co, H, W, Ho, Wo;
-    int Cig, Cog;         // conv channels per group (in / out)
+    // Conv3d (full output) runs as 2-D samples (n, d) over depth-stacked
+    // channels (ci, kd): Din input depth, KD depth taps (1 for 2-D), Dv
+    // output depth planes per sample (1 for 2-D).  A stage's channels then
+    // are cib/KD input channels x KD taps.
+    int Din, KD, Dv;
+    int Cig, Cog;         // conv channels per group (in, stacked with the depth taps / out)
     int TR, NT;           // CTA tile: TR output rows x NT row segments
     int row_tiles, col_tiles, ncob, ntiles;
     int wco, wsp;         // warps: channel slices x spatial groups
@@ -153,7 +160,7 @@ struct Full2dArgs {
     int act, norm, NG, affine;
     float eps, post_scale;
     int apply_needed, vec4;
-    long long S;          // Ho * Wo
+    long long S;          // Dv * Ho * Wo: one normalized (n, c) plane
     float4 *partial;      // [N][Co][ntiles * wsp]: per warp and tile (count, K, S1, S2),
                           // shifted sums S1 = sum(v - K), S2 = sum((v - K)^2)
     float4 *coef;         // [N][Co]: (mu, a, bb, 0)

@@ -48,4 +48,19 @@ int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[
     return r == CUDA_SUCCESS ? CN_OK : CN_ERR_CUDA;
 }
 
+// fp32 tensor of rank 5 (dims innermost first, strides in bytes for dims
+// 1..4), tile box `box`, zero fill outside the tensor, no swizzle.
+int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[5],
+                       const uint64_t strides_bytes[4], const uint32_t box[5]) {
+    if (!tma_available()) return CN_ERR_UNSUPPORTED;
+    cuuint64_t gd[5] = {dims[0], dims[1], dims[2], dims[3], dims[4]};
+    cuuint64_t gs[4] = {strides_bytes[0], strides_bytes[1], strides_bytes[2], strides_bytes[3]};
+    cuuint32_t bx[5] = {box[0], box[1], box[2], box[3], box[4]};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, const_cast<float *>(base), gd, gs,
+                          bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? CN_OK : CN_ERR_CUDA;
+}
+
 }  // namespace cn

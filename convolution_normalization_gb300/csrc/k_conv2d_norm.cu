@@ -131,10 +131,12 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
     const int sg = warp / a.wco;
     const int COB = COT * a.wco;
 
-    // tile t -> geometry; tiles are ordered (n, channel block, row tile, col tile)
+    // tile t -> geometry
     struct Geo {
-        int n, cob, rt, ct, co0, ci0, r0, c0, ir0, ic0, xs, off, gc_lo, gc_hi;
+        int n, d, cob, rt, ct, co0, ci0, r0, c0, ir0, ic0, xs, off, gc_lo, gc_hi;
     };
+    // tiles are ordered (sample, channel block, row tile, col tile); a
+    // sample is (n, output depth d) of a Conv3d, or n of a 2-D conv
     auto geo = [&](int t) {
         Geo G;
         G.ct = t % a.col_tiles;
@@ -142,7 +144,9 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
         G.rt = t % a.row_tiles;
         t /= a.row_tiles;
         G.cob = t % a.ncob;
-        G.n = t / a.ncob;
+        const int smp = t / a.ncob;
+        G.n = smp / a.Dv;
+        G.d = smp - G.n * a.Dv;
         G.co0 = G.cob * COB;
         G.ci0 = (G.co0 / a.Cog) * a.Cig;
         G.r0 = G.rt * a.TR;
@@ -156,6 +160,13 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
         G.gc_lo = max(G.ic0, 0) & ~3;
         G.gc_hi = min((G.ic0 + a.cols_in + 3) & ~3, a.W);
         return G;
+    };
+
+    // Input row gr of stacked channel cs (channel cs / KD, depth tap cs % KD)
+    // for output depth d of sample n.
+    auto x_row = [&](int n, int d, int cs, int gr) {
+        const int ci = cs / a.KD, kd = cs - ci * a.KD;
+        return a.x + ((((size_t)n * a.Ci + ci) * a.Din + d + kd) * a.H + gr) * a.W;
     };
 
     // ---- producer (warp 0): one stage = (tile, chunk of cib input channels) ----
@@ -190,7 +201,10 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                 s_tile[buf] = tile;
                 s_chunk[buf] = chunk;
                 mbar_arrive_expect_tx(&full[buf], (uint32_t)(a.xstage + a.wstage) * 4u);
-                tma_load_4d(sxb, &a.xmap, G.xs, G.ir0, G.ci0 + cbase, G.n, &full[buf]);
+                if (a.Din > 1)  // (cib / KD channels) x (KD depth taps) from plane d on
+                    tma_load_5d(sxb, &a.xmap, G.xs, G.ir0, G.d, (G.ci0 + cbase) / a.KD, G.n, &full[buf]);
+                else
+                    tma_load_4d(sxb, &a.xmap, G.xs, G.ir0, G.ci0 + cbase, G.n, &full[buf]);
                 bulk_load(sxb + a.xstage, a.wprep + ((size_t)G.cob * a.nchunk + chunk) * a.wstage,
                           (uint32_t)a.wstage * 4u, &full[buf]);
             }
@@ -226,8 +240,7 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
         __syncwarp();
         for (int q = lane; q < ncl * nr; q += 32) {
             const int cl = q / nr, gr = gr_lo + q % nr;
-            const float *src =
-                a.x + (((size_t)G.n * a.Ci + G.ci0 + cbase + cl) * a.H + gr) * a.W + G.gc_lo;
+            const float *src = x_row(G.n, G.d, G.ci0 + cbase + cl, gr) + G.gc_lo;
             float *dst = sxb + (size_t)(cl * a.rows_in + gr - G.ir0) * a.pitch + (G.gc_lo - G.xs);
             bulk_load(dst, src, row_bytes, &full[buf]);
         }
@@ -326,8 +339,7 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                     const int cl = rI / a.rows_in, rr = rI - cl * a.rows_in;
                     const int gr = H.ir0 + rr;
                     const bool rok = (cbase + cl < a.Cig) && gr >= 0 && gr < a.H;
-                    const float *src = a.x + (((size_t)H.n * a.Ci + H.ci0 + (rok ? cbase + cl : 0)) * a.H +
-                                              (rok ? gr : 0)) * a.W;
+                    const float *src = x_row(H.n, H.d, H.ci0 + (rok ? cbase + cl : 0), rok ? gr : 0);
                     float *dst = sxb + (size_t)rI * a.pitch;
                     for (int cc = lane; cc < a.cols_in; cc += 32) {
                         const int gc = H.ic0 + cc;
@@ -442,7 +454,9 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                         m = act_sums<RW, ACT_NONE>(acc[c], bias, K, nvalid);
                     }
                 }
-                float *op = a.out + (((size_t)G.n * a.Co + co) * a.Ho + (row_ok ? orow : 0)) * a.Wo + ocol0;
+                float *op = a.out +
+                            ((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.Ho + (row_ok ? orow : 0)) * a.Wo +
+                            ocol0;
                 if (nvalid == RW) {
                     if ((RW % 2) == 0 && (reinterpret_cast<uintptr_t>(op) & 7) == 0) {
 #pragma unroll
@@ -459,7 +473,7 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                 }
                 m = warp_sum3(m);
                 if (lane == 0)
-                    a.partial[(((size_t)G.n * a.Co + co) * a.ntiles + tin) * a.wsp + sg] =
+                    a.partial[((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.ntiles + tin) * a.wsp + sg] =
                         make_float4(m.x, K, m.y, m.z);
             }
         }
@@ -508,7 +522,7 @@ __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_c
     __shared__ float sm[kStatsWarps][3];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int cpg = a.Co / a.NG;
-    const int per_c = a.ntiles * a.wsp;
+    const int per_c = a.Dv * a.ntiles * a.wsp;  // a channel's partials: depth planes x tiles x warps
     const bool wide = cpg > 1;
     const int ng = wide ? (int)blockIdx.x : (int)blockIdx.x * kStatsWarps + w;  // (n, group)
     if (ng >= a.N * a.NG) return;  // uniform per block when wide
@@ -642,7 +656,13 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     const int K = d.k;
     const int Ho = T ? d.H + K - 1 : d.H - K + 1;
     const int Wo = T ? d.W + K - 1 : d.W - K + 1;
-    const int Cig = d.C_in / d.groups, Cog = d.C_out / d.groups;
+    // A Conv3d runs as 2-D samples (n, d_out) over depth-stacked channels
+    // (ci, kd): the filter [co][ci][kd][kh][kw] already is [co][ci*K + kd][kh][kw].
+    const bool d3 = d.conv == CN_CONV3D;
+    if (d3 && d.groups != 1) return CN_ERR_UNSUPPORTED;
+    const int KD = d3 ? K : 1;
+    const int Dv = d3 ? d.D - K + 1 : 1;
+    const int Cig = d.C_in / d.groups * KD, Cog = d.C_out / d.groups;
     const bool bulk = (d.W % 4 == 0) && env_int("CN_NO_TMA", 0) == 0;
     const bool tma2d = bulk && tma_available() && env_int("CN_NO_TMA2D", 0) == 0;
     const int f_cot = env_int("CN_FULL2D_COT", 0), f_rw = env_int("CN_FULL2D_RW", 0),
@@ -725,6 +745,9 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.Wo = Wo;
     a.Cig = Cig;
     a.Cog = Cog;
+    a.KD = KD;
+    a.Din = d3 ? d.D : 1;
+    a.Dv = Dv;
     a.wco = best.wco;
     a.wsp = best.wsp;
     a.TR = best.TR;
@@ -742,7 +765,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
                                 in.VECW, RW, a.TR);
     a.pitch = pitch;
     // the whole stage as one tensor copy: box (pitch, rows_in, cib, 1)
-    a.use_tma = (tma2d && pitch <= 256 && a.rows_in <= 256) ? 1 : 0;
+    a.use_tma = (tma2d && pitch <= 256 && a.rows_in <= 256) ? 1 : 0;  // (box extents; KD <= 4)
     a.xmap_base = nullptr;
     const int COB = COT * a.wco;
     const int per_ci = a.rows_in * pitch + K * K * COB;
@@ -751,10 +774,12 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     // channels, fewer otherwise.
     const size_t budget = (in.COT * in.RW <= 64 ? 108 : 216) * 1024;
     int nstage = std::max(2, std::min(kMaxStages, env_int("CN_FULL2D_NSTAGE", 3)));
+    // stages hold whole input channels: cib is a multiple of the depth taps
     int cib = 1;
     for (;; --nstage) {
         cib = std::min(Cig, std::max(1, env_int("CN_FULL2D_CIB", 8)));
-        while (cib > 1 && (size_t)nstage * cib * per_ci * 4 > budget) --cib;
+        cib = std::max(KD, cib / KD * KD);
+        while (cib > KD && (size_t)nstage * cib * per_ci * 4 > budget) cib -= KD;
         if (cib >= std::min(Cig, 2) || nstage == 2) break;
     }
     a.nstage = nstage;
@@ -769,13 +794,13 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.affine = d.affine && d.norm != CN_NORM_NONE;
     a.eps = d.eps;
     a.post_scale = d.post_scale;
-    a.S = (long long)Ho * Wo;
+    a.S = (long long)Dv * Ho * Wo;
     a.apply_needed = !(d.norm == CN_NORM_NONE && d.post_scale == 1.0f);
     a.vec4 = (a.S % 4) == 0;
     const int threads = 32 * a.wco * a.wsp;
     const size_t smem = (size_t)a.nstage * a.stage_floats * 4;
     if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
-    const long long items = (long long)d.N * a.ncob * a.ntiles;
+    const long long items = (long long)d.N * Dv * a.ncob * a.ntiles;
     if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
     a.items = (int)items;
     a.wprep = nullptr;
@@ -802,7 +827,7 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
 }
 
 size_t full2d_workspace(const Full2dArgs &a) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * sizeof(float4);
+    const size_t part = (size_t)a.N * a.Co * a.Dv * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
     const size_t tick = (size_t)(a.N + 2) * sizeof(int);
     const size_t wprep =
@@ -812,7 +837,7 @@ size_t full2d_workspace(const Full2dArgs &a) {
 }
 
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
-    const size_t part = (size_t)a.N * a.Co * a.ntiles * a.wsp * sizeof(float4);
+    const size_t part = (size_t)a.N * a.Co * a.Dv * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
     const size_t tick = (size_t)(a.N + 2) * sizeof(int);
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
@@ -850,11 +875,22 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
         const int st = tc2d_bind_x(a);
         if (st != CN_OK) return st;
     } else if (a.use_tma && a.xmap_base != a.x) {
-        const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Ci, (uint64_t)a.N};
-        const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
-                                     (uint64_t)a.Ci * a.H * a.W * 4};
-        const uint32_t box[4] = {(uint32_t)a.pitch, (uint32_t)a.rows_in, (uint32_t)a.cib, 1u};
-        const int st = encode_tmap_f32_4d(&a.xmap, a.x, dims, strides, box);
+        int st;
+        if (a.Din > 1) {  // x as (W, H, D, C_in, N), box (pitch, rows_in, KD, cib / KD, 1)
+            const uint64_t plane = (uint64_t)a.H * a.W * 4;
+            const uint64_t dims[5] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Din, (uint64_t)a.Ci,
+                                      (uint64_t)a.N};
+            const uint64_t strides[4] = {(uint64_t)a.W * 4, plane, plane * a.Din, plane * a.Din * a.Ci};
+            const uint32_t box[5] = {(uint32_t)a.pitch, (uint32_t)a.rows_in, (uint32_t)a.KD,
+                                     (uint32_t)(a.cib / a.KD), 1u};
+            st = encode_tmap_f32_5d(&a.xmap, a.x, dims, strides, box);
+        } else {
+            const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Ci, (uint64_t)a.N};
+            const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                         (uint64_t)a.Ci * a.H * a.W * 4};
+            const uint32_t box[4] = {(uint32_t)a.pitch, (uint32_t)a.rows_in, (uint32_t)a.cib, 1u};
+            st = encode_tmap_f32_4d(&a.xmap, a.x, dims, strides, box);
+        }
         if (st != CN_OK) return st;
         a.xmap_base = a.x;
     }

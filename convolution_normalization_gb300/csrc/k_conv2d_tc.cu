@@ -542,6 +542,9 @@ int tc2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.Wo = Wo;
     a.Cig = d.C_in;
     a.Cog = d.C_out;
+    a.KD = 1;
+    a.Din = 1;
+    a.Dv = 1;
     a.row_tiles = row_tiles;
     a.col_tiles = 1;
     a.ncob = d.C_out / kTcM;

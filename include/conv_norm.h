@@ -110,7 +110,11 @@ typedef struct {
 
 /* Checks a descriptor.  Returns CN_OK, CN_ERR_INVALID_ARG for a malformed
  * problem (e.g. C_in % groups != 0, kernel larger than the input) or
- * CN_ERR_UNSUPPORTED for a valid problem this library has no kernel for. */
+ * CN_ERR_UNSUPPORTED for a valid problem this library has no kernel for.
+ * Supported: spatial mean after Conv3d (groups 1, k <= 4, C_out % 4 == 0);
+ * the double max pool after Conv3d + channel softmax (C_out = 16, k <= 4, no
+ * norm); the full output after Conv2d, ConvTranspose2d ((C_out/groups) % 4
+ * == 0, k <= 4) or Conv3d (groups 1, k <= 4), any activation but softmax. */
 int conv_norm_desc_validate(const conv_norm_desc *desc);
 
 /* Writes the output shape implied by desc into dims[0..*ndim-1] (ndim <= 5):

@@ -77,6 +77,9 @@ def _base(**kw):
     (dict(act="softmax_c"), -2),              # no full-output softmax kernel
     (dict(C_out=10), -2),                     # channel slices of 4 or 8
     (dict(conv="conv3d", D=6, red="mean_spatial", groups=2, C_in=8), -2),
+    (dict(conv="conv3d", D=6), 0),            # Conv3d with the full output
+    (dict(conv="conv3d", D=6, groups=2, C_in=8), -2),
+    (dict(conv="conv3d", D=6, act="softmax_c"), -2),
     (dict(N=0), 0),                           # empty batch is valid
 ])
 def test_descriptor_validation(B, kw, status):
@@ -89,6 +92,7 @@ def test_output_shapes(B):
     assert B.conv_norm_output_shape(B.make_desc(_base(conv="convt2d"))) == (2, 16, 12, 14)
     d = B.make_desc(_base(conv="conv3d", D=9, act="softmax_c", norm="none", red="maxpool2_x2"))
     assert B.conv_norm_output_shape(d) == (2, 16, 1, 2, 2)  # floor(floor(L/2)/2)
+    assert B.conv_norm_output_shape(B.make_desc(_base(conv="conv3d", D=6))) == (2, 16, 4, 8, 10)
     d = B.make_desc(_base(conv="conv3d", D=5, act="softmax_c", norm="none", red="maxpool2_x2"))
     assert B.conv_norm_output_shape(d) == (2, 16, 0, 2, 2)
 
