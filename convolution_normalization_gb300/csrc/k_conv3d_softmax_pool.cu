@@ -84,9 +84,33 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
         }
         cp_async_commit();
     }
-    // ---- the filter, transposed to [ci][tap][co] ----
-    for (int t = warp; t < a.Ci * KKK; t += nwarps)
-        for (int co = lane; co < CO; co += 32) sw[t * CO + co] = __ldg(a.w + (size_t)co * a.Ci * KKK + t);
+    // ---- the filter, transposed to [ci][tap][co], and the bias ----
+    // Every load of a round is issued before any store, so a CTA waits for
+    // one global round trip per 8 values a thread stages, not one per value.
+    {
+        const int total = a.Ci * KKK * CO;
+        for (int base = tid; base < total + CO; base += 8 * (int)blockDim.x) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = base + u * (int)blockDim.x;
+                float t = 0.0f;
+                if (e < total) {
+                    const int co = e % CO, tap = e / CO;  // e = tap * CO + co
+                    t = __ldg(a.w + (size_t)co * a.Ci * KKK + tap);
+                } else if (e < total + CO && a.b) {
+                    t = __ldg(a.b + (e - total));
+                }
+                v[u] = t;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int e = base + u * (int)blockDim.x;
+                if (e < total + CO) sw[e] = v[u];
+            }
+        }
+    }
+    const float *sbias = sw + (size_t)a.Ci * KKK * CO;
     bool staged = true;
     if (a.use_tma) {
         staged = mbar_wait_bounded(&bar, 0, kWaitLimitNs);
@@ -156,7 +180,7 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
         float m = -INFINITY;
 #pragma unroll
         for (int c = 0; c < CO; ++c) {
-            acc[c][i] += a.b ? __ldg(a.b + c) : 0.0f;
+            acc[c][i] += sbias[c];
             m = fmaxf(m, acc[c][i]);
         }
         float s = 0.0f;
@@ -231,7 +255,7 @@ int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
     a.vox_stride = (d.C_in * P * P * PX + 31) & ~31;
     a.use_tma = (d.W % 4 == 0) && d.C_in <= 256 && env_int("CN_NO_TMA", 0) == 0;
     a.tmap_base = nullptr;
-    const size_t smem = ((size_t)a.vox_per_cta * a.vox_stride + (size_t)d.C_in * K * K * K * in->CO) * 4;
+    const size_t smem = ((size_t)a.vox_per_cta * a.vox_stride + (size_t)d.C_in * K * K * K * in->CO + in->CO) * 4;
     if (smem > 227 * 1024) return CN_ERR_UNSUPPORTED;
     const long long grid = (a.nvox + a.vox_per_cta - 1) / a.vox_per_cta;
     if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
