@@ -167,7 +167,7 @@ def kernel_roofline(spec, name, ms, pk):
     launch / its measured duration against the peak of the unit bounding it."""
     flops = algorithmic_flops(spec)
     base = name.split("<")[0]
-    if base == "k_conv2d_tc":
+    if base in ("k_conv2d_tc", "k_conv3d_tc_mean"):
         work = SPLIT_TF32_PRODUCTS * flops  # tf32 tensor-core flops the split method needs
         peak = pk["bf16_tflops"] * TF32_PER_BF16
         return {"bound": "tensor", "achieved": work / (ms / 1e3) / 1e12, "peak": peak,

@@ -37,6 +37,19 @@ constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 // Variant 0: 3-D conv -> activation -> (GroupNorm | InstanceNorm | none)
 // -> spatial mean.  One launch; the conv tensor is never written.
 struct Mean3dArgs {
+    // Tensor-core kernel (k_conv3d_tc_mean, tc = 1): a stage is one band of
+    // tc_rb output rows of a group of output depth planes; the fields tc_*
+    // describe its staged input and MMA tiles.
+    CUtensorMap tc_xmap;        // x as (W, H, D, N*C_in), box (W, tc_rb + k - 1, planes, C_in)
+    const float *tc_xmap_base;  // x pointer the map was encoded for
+    int tc;
+    int tc_rb;        // output rows per band (tile): 128 / W
+    int tc_nband;     // bands per output plane
+    int tc_pp;        // operand positions per staged input plane
+    int tc_stage;     // bytes of one operand stage (hi and lo, all staged planes)
+    int tc_land;      // bytes of the raw input box of a stage
+    int tc_halo;      // 1: output rows cross 32-lane quadrants (W does not divide 32)
+    uint32_t tc_wmagic;  // ceil(2^32 / W): p / W = umulhi(p, tc_wmagic) for p < 2^16
     CUtensorMap tmap;           // x viewed as (W, H, D, N*C_in), box (pitch, H, planes_max, C_in)
     const float *tmap_base;     // x pointer the map was encoded for
     int use_tma;                // 1: stage with one TMA tensor copy per CTA
@@ -73,6 +86,10 @@ struct Mean3dConfig {
 // Chooses tiling + instantiation; fills the geometry fields of args.
 // Returns CN_OK or CN_ERR_UNSUPPORTED.
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+// The tensor-core plan of the same problem (k_conv3d_tc_mean.cu);
+// CN_ERR_UNSUPPORTED when the problem does not fit it.
+int tc3_mean_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+int tc3_bind_x(Mean3dArgs &a);
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s,

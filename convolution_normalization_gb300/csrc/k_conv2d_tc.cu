@@ -41,6 +41,7 @@
 // core path (k_group_stats, k_norm_apply).
 #include "cn_common.cuh"
 #include "cn_internal.h"
+#include "cn_tcgen05.cuh"
 
 #include <algorithm>
 #include <cstdlib>
@@ -55,54 +56,6 @@ constexpr int kTcMaxStages = 3;
 constexpr int kTcLand = 2;
 constexpr int kScratchFloats = 4 * 32 * 33;  // epilogue transpose, 4 warps
 constexpr int kMaxMmas = 14;                   // MMAs per stage for k <= 3: k*k + ceil(k*k / 2)
-
-// ---- tcgen05 / UMMA helpers (inline PTX) --------------------------------------
-
-// Shared-memory matrix descriptor: start address, leading-dimension byte
-// offset (between the two K core matrices), stride byte offset (between
-// 8-row core-matrix groups), descriptor version 1, no swizzle.
-CN_DEV uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
-}
-// Instruction descriptor of kind::tf32: fp32 accumulator, tf32 A and B, both
-// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
-CN_DEV uint32_t idesc_tf32(int M, int N) {
-    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
-}
-CN_DEV void umma_tf32(uint32_t dtmem, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(dtmem),
-        "l"(ad), "l"(bd), "r"(idesc), "r"(accum));
-}
-// Arrives on bar once every MMA this thread issued so far has completed.
-CN_DEV void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-CN_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
-CN_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
-// 32 lanes x 32 consecutive columns of TMEM: thread i gets lane (base + i).
-CN_DEV void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-        "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-}
-// The tf32 part the tensor cores read (low 13 mantissa bits dropped) and
-// the exact remainder.
-CN_DEV float tf32_trunc(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
-CN_DEV float tf32_rest(float v) { return v - tf32_trunc(v); }
 
 // Filter pre-pass: per (channel block of 128, 4-channel group) one block of
 // [lo | hi] x [tap][128 rows][4 channels], the A operands of that group's
@@ -127,24 +80,6 @@ __global__ void __launch_bounds__(256) k_prep_weights_tc(const float *__restrict
         const int co = cob * kTcM + row, c = 4 * g + j;
         const float v = w[((size_t)co * Ci + c) * T + t];
         wprep[e] = hi ? v : tf32_rest(v);
-    }
-}
-
-// Bounded wait with a CTA-local abort: after one wait gives up, every role
-// stops at its next wait instead of running into further timeouts.
-CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                flag_error(err, ERR_TIMEOUT);
-                *abort = 1;
-                return false;
-            }
-        }
     }
 }
 

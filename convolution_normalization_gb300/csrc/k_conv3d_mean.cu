@@ -25,6 +25,7 @@
 // (vector loads, broadcast across the warp) and issues COT*K*RW FFMAs.
 #include "cn_common.cuh"
 #include "cn_internal.h"
+#include "cn_mean_common.cuh"
 
 #include <algorithm>
 #include <cstdlib>
@@ -310,36 +311,13 @@ __global__ void __launch_bounds__(mean_max_threads(COT, RW), 1)
         if (s_last) {
             __threadfence();
             for (int c = tid; c < a.Co; c += blockDim.x) {
-                Moments<double> m{0.0, 0.0, 0.0};
-                for (int ch = 0; ch < a.nchunks; ++ch) {
-                    const double *p = a.partial + (((size_t)n * a.nchunks + ch) * a.Co + c) * 3;
-                    m = merge(m, Moments<double>{ldcg_f64(p), ldcg_f64(p + 1), ldcg_f64(p + 2)});
-                }
+                const Moments<double> m = mean_chunks_merged(a, n, c);
                 sch[c * 3 + 0] = m.n;
                 sch[c * 3 + 1] = m.mean;
                 sch[c * 3 + 2] = m.m2;
             }
             __syncthreads();
-            for (int c = tid; c < a.Co; c += blockDim.x) {
-                const double mc = sch[c * 3 + 1];
-                double val;
-                if (a.norm == CN_NORM_NONE) {
-                    val = mc;
-                } else {
-                    const int cpg = a.Co / a.G, g = c / cpg;
-                    Moments<double> mg{0.0, 0.0, 0.0};
-                    for (int u = 0; u < cpg; ++u) {
-                        const int cc = g * cpg + u;
-                        mg = merge(mg, Moments<double>{sch[cc * 3], sch[cc * 3 + 1], sch[cc * 3 + 2]});
-                    }
-                    const double var = mg.m2 / mg.n;
-                    const double rstd = 1.0 / sqrt(var + (double)a.eps);
-                    const double ga = a.affine ? (double)a.gamma[c] : 1.0;
-                    const double be = a.affine ? (double)a.beta[c] : 0.0;
-                    val = ga * (mc - mg.mean) * rstd + be;
-                }
-                a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
-            }
+            for (int c = tid; c < a.Co; c += blockDim.x) mean_write_output(a, n, c, sch);
             if (tid == 0) a.tickets[n] = 0;
         }
         __syncthreads();  // buffer b, sred and sch are free for the next item
@@ -375,6 +353,9 @@ int env_int(const char *name, int dflt) {
 }  // namespace
 
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
+    // the tensor-core kernel where the problem fits it
+    if (tc3_mean_plan(d, a, cfg) == CN_OK) return CN_OK;
+    a.tc = 0;
     const int K = d.k;
     const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
     if (d.groups != 1 || d.C_out % 4 != 0) return CN_ERR_UNSUPPORTED;
@@ -514,7 +495,10 @@ int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
 
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
-    if (a.use_tma && a.tmap_base != a.x) {
+    if (a.tc) {
+        const int st = tc3_bind_x(a);
+        if (st != CN_OK) return st;
+    } else if (a.use_tma && a.tmap_base != a.x) {
         const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D,
                                   (uint64_t)a.N * a.Ci};
         const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
