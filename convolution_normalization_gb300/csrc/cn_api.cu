@@ -105,7 +105,9 @@ int pick_variant(const conv_norm_desc &d, int &variant) {
         return CN_OK;
     }
     if (d.red == CN_RED_MAXPOOL2_X2) {
-        if (d.act != CN_ACT_SOFTMAX_C || d.norm != CN_NORM_NONE) return CN_ERR_UNSUPPORTED;
+        // a positive post scale commutes with the max
+        if (d.act != CN_ACT_SOFTMAX_C || d.norm != CN_NORM_NONE || !(d.post_scale > 0.0f))
+            return CN_ERR_UNSUPPORTED;
         variant = V_POOL3D;
         return CN_OK;
     }
@@ -225,8 +227,8 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
             vws = mean3d_workspace(p->mean_args);
             break;
         case V_POOL3D:
-            st = pool3d_prepare(p->pool_cfg);
-            vws = 0;
+            st = pool3d_prepare(p->pool_cfg, p->pool_args);
+            vws = pool3d_workspace(p->pool_args);
             break;
         default:
             st = full2d_prepare(p->full_cfg, p->full_args);
@@ -263,6 +265,7 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
         }
         case V_POOL3D:
             p->pool_args.err = p->err_flag;
+            p->pool_args.t.work = reinterpret_cast<int *>(vbase);  // zero between launches
             break;
         default:
             full2d_bind_workspace(p->full_args, vbase, p->err_flag);

@@ -34,22 +34,52 @@ int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 // ---------------------------------------------------------------------------
+// Tensor-core Conv3d (k_conv3d_tc.cu), used by the spatial-mean and the
+// softmax + pool variants: a stage is one band of rb output rows of a group
+// of output depth planes; the fields describe its staged input and MMA tiles.
+struct Tc3Args {
+    CUtensorMap xmap;        // x as (W, H, D, N*C_in), box (W, rb + k - 1, planes, C_in)
+    const float *xmap_base;  // x pointer the map was encoded for
+    int *err;                // device error flag
+    const float *x, *w, *b, *gamma, *beta;
+    float *out;
+    int N, Ci, Co, D, H, W, Do, Ho, Wo;
+    int k, nu;        // filter extent; staged input planes per stage (plane group + k - 1)
+    int rb;           // output rows per band: 128 / W
+    int nband;        // bands per plane group
+    int pp;           // operand positions per staged input plane
+    int stage;        // bytes of one operand stage (hi and lo, all staged planes)
+    int land;         // bytes of the raw input box of a stage
+    int halo;         // 1: output rows cross 32-lane quadrants (W does not divide 32)
+    uint32_t wmagic;  // ceil(2^32 / W): p / W = umulhi(p, wmagic) for p < 2^16
+    int ngroups;      // plane groups per sample
+    int nsplit;       // items per plane group: 1 (all bands) or nband (one band each)
+    int items;        // N * ngroups * nsplit
+    int act, norm, G, affine;
+    float eps, post_scale;
+    int Pd, Ph, Pw;    // pool: pooled extents
+    double *partial;   // mean: [N][ngroups][Co][3] (count, mean, M2)
+    int *tickets;      // mean: [N] per-sample tickets, zero between launches
+    int *work;         // [2] work / exit counters, zero between launches
+};
+typedef void (*Tc3Kernel)(Tc3Args);
+struct Tc3Config {
+    Tc3Kernel kern;
+    const char *name;
+    int threads, smem, grid;
+};
+// Plans the tensor-core kernel for a spatial-mean or a softmax + pool problem;
+// CN_ERR_UNSUPPORTED when the problem does not fit it.
+int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg);
+int tc3_prepare(Tc3Config &cfg, const Tc3Args &a);  // smem attribute, persistent grid
+int tc3_launch(const Tc3Config &cfg, Tc3Args &a, cudaStream_t s, const LaunchEvents *ev);
+
+// ---------------------------------------------------------------------------
 // Variant 0: 3-D conv -> activation -> (GroupNorm | InstanceNorm | none)
 // -> spatial mean.  One launch; the conv tensor is never written.
 struct Mean3dArgs {
-    // Tensor-core kernel (k_conv3d_tc_mean, tc = 1): a stage is one band of
-    // tc_rb output rows of a group of output depth planes; the fields tc_*
-    // describe its staged input and MMA tiles.
-    CUtensorMap tc_xmap;        // x as (W, H, D, N*C_in), box (W, tc_rb + k - 1, planes, C_in)
-    const float *tc_xmap_base;  // x pointer the map was encoded for
-    int tc;
-    int tc_rb;        // output rows per band (tile): 128 / W
-    int tc_nband;     // bands per output plane
-    int tc_pp;        // operand positions per staged input plane
-    int tc_stage;     // bytes of one operand stage (hi and lo, all staged planes)
-    int tc_land;      // bytes of the raw input box of a stage
-    int tc_halo;      // 1: output rows cross 32-lane quadrants (W does not divide 32)
-    uint32_t tc_wmagic;  // ceil(2^32 / W): p / W = umulhi(p, tc_wmagic) for p < 2^16
+    int tc;           // 1: the tensor-core kernel (t) runs the problem
+    Tc3Args t;
     CUtensorMap tmap;           // x viewed as (W, H, D, N*C_in), box (pitch, H, planes_max, C_in)
     const float *tmap_base;     // x pointer the map was encoded for
     int use_tma;                // 1: stage with one TMA tensor copy per CTA
@@ -77,6 +107,7 @@ struct Mean3dArgs {
 };
 typedef void (*Mean3dKernel)(Mean3dArgs);
 struct Mean3dConfig {
+    Tc3Config tc3;    // the tensor-core kernel's launch, when args.tc
     Mean3dKernel kern;
     const char *name;
     int K, RW, COT;
@@ -86,10 +117,6 @@ struct Mean3dConfig {
 // Chooses tiling + instantiation; fills the geometry fields of args.
 // Returns CN_OK or CN_ERR_UNSUPPORTED.
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
-// The tensor-core plan of the same problem (k_conv3d_tc_mean.cu);
-// CN_ERR_UNSUPPORTED when the problem does not fit it.
-int tc3_mean_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
-int tc3_bind_x(Mean3dArgs &a);
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s,
@@ -108,18 +135,23 @@ struct Pool3dArgs {
     int N, Ci, D, H, W, Do, Ho, Wo;
     int Pd, Ph, Pw;      // pooled extents: floor(Do/4), floor(Ho/4), floor(Wo/4)
     long long nvox;      // N * Pd * Ph * Pw
+    float post_scale;    // > 0: multiplies the pooled value
+    int tc;              // 1: the tensor-core kernel (t) runs the problem
+    Tc3Args t;
     int vox_per_cta;     // pooled voxels per CTA (16 threads each)
     int pw_pitch;        // shared-memory patch row pitch (floats), P rounded up to 4
     int vox_stride;      // floats per staged voxel patch
 };
 typedef void (*Pool3dKernel)(Pool3dArgs);
 struct Pool3dConfig {
+    Tc3Config tc3;       // the tensor-core kernel's launch, when args.tc
     Pool3dKernel kern;
     const char *name;
     int threads, smem, grid;
 };
 int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &args, Pool3dConfig &cfg);
-int pool3d_prepare(const Pool3dConfig &cfg);
+size_t pool3d_workspace(const Pool3dArgs &a);
+int pool3d_prepare(Pool3dConfig &cfg, const Pool3dArgs &a);
 int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s,
                   const LaunchEvents *ev = nullptr);
 

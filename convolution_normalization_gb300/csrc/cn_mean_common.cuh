@@ -14,11 +14,13 @@
 
 namespace cn {
 
-// Moments of channel c of sample n, merged over its chunks in chunk order.
-CN_DEV Moments<double> mean_chunks_merged(const Mean3dArgs &a, int n, int c) {
+// Moments of channel c of sample n, merged over its nchunks chunks in chunk
+// order (partial[N][nchunks][Co][3]).
+template <class Args>
+CN_DEV Moments<double> mean_chunks_merged(const Args &a, int nchunks, int n, int c) {
     Moments<double> m{0.0, 0.0, 0.0};
-    for (int ch = 0; ch < a.nchunks; ++ch) {
-        const double *p = a.partial + (((size_t)n * a.nchunks + ch) * a.Co + c) * 3;
+    for (int ch = 0; ch < nchunks; ++ch) {
+        const double *p = a.partial + (((size_t)n * nchunks + ch) * a.Co + c) * 3;
         m = merge(m, Moments<double>{ldcg_f64(p), ldcg_f64(p + 1), ldcg_f64(p + 2)});
     }
     return m;
@@ -26,7 +28,8 @@ CN_DEV Moments<double> mean_chunks_merged(const Mean3dArgs &a, int n, int c) {
 
 // Output of channel c of sample n from every channel's merged moments,
 // sch[Co][3] = (count, mean, M2).
-CN_DEV void mean_write_output(const Mean3dArgs &a, int n, int c, const double *sch) {
+template <class Args>
+CN_DEV void mean_write_output(const Args &a, int n, int c, const double *sch) {
     const double mc = sch[c * 3 + 1];
     double val;
     if (a.norm == CN_NORM_NONE) {

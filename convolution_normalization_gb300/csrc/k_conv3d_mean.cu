@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(mean_max_threads(COT, RW), 1)
         if (s_last) {
             __threadfence();
             for (int c = tid; c < a.Co; c += blockDim.x) {
-                const Moments<double> m = mean_chunks_merged(a, n, c);
+                const Moments<double> m = mean_chunks_merged(a, a.nchunks, n, c);
                 sch[c * 3 + 0] = m.n;
                 sch[c * 3 + 1] = m.mean;
                 sch[c * 3 + 2] = m.m2;
@@ -354,7 +354,18 @@ int env_int(const char *name, int dflt) {
 
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     // the tensor-core kernel where the problem fits it
-    if (tc3_mean_plan(d, a, cfg) == CN_OK) return CN_OK;
+    if (tc3_plan(d, a.t, cfg.tc3) == CN_OK) {
+        a.tc = 1;
+        a.N = d.N;  // the fields the workspace and the plan's callers read
+        a.Co = d.C_out;
+        a.nchunks = a.t.ngroups;
+        a.items = a.t.items;
+        cfg.name = cfg.tc3.name;
+        cfg.threads = cfg.tc3.threads;
+        cfg.smem = cfg.tc3.smem;
+        cfg.grid = cfg.tc3.grid;
+        return CN_OK;
+    }
     a.tc = 0;
     const int K = d.k;
     const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
@@ -477,6 +488,11 @@ size_t mean3d_workspace(const Mean3dArgs &a) {
 }
 
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
+    if (a.tc) {
+        const int st = tc3_prepare(cfg.tc3, a.t);
+        cfg.grid = cfg.tc3.grid;
+        return st;
+    }
     if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
@@ -496,9 +512,20 @@ int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
     if (a.tc) {
-        const int st = tc3_bind_x(a);
-        if (st != CN_OK) return st;
-    } else if (a.use_tma && a.tmap_base != a.x) {
+        Tc3Args &t = a.t;
+        t.x = a.x;
+        t.w = a.w;
+        t.b = a.b;
+        t.gamma = a.gamma;
+        t.beta = a.beta;
+        t.out = a.out;
+        t.err = a.err;
+        t.partial = a.partial;
+        t.tickets = a.tickets;
+        t.work = a.tickets + a.N;
+        return tc3_launch(cfg.tc3, t, s, ev);
+    }
+    if (a.use_tma && a.tmap_base != a.x) {
         const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D,
                                   (uint64_t)a.N * a.Ci};
         const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,

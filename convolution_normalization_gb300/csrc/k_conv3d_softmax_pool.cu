@@ -31,7 +31,6 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
     constexpr int PX = (P + 3) & ~3;  // patch row pitch
     constexpr int KKK = K * K * K;
     const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int v = tid >> 4, l16 = tid & 15;
     const int dz = l16 >> 2, dy = l16 & 3;
     float *sx = smem;
@@ -209,7 +208,7 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
 #pragma unroll
         for (int c = 0; c < CO; ++c) {
             if ((c % 16) == l16) {
-                a.out[((((size_t)n * CO + c) * a.Pd + pd) * a.Ph + ph) * a.Pw + pw] = best[c];
+                a.out[((((size_t)n * CO + c) * a.Pd + pd) * a.Ph + ph) * a.Pw + pw] = best[c] * a.post_scale;
             }
         }
     }
@@ -237,6 +236,18 @@ int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
         if (i.K == d.k && i.CO == d.C_out) in = &i;
     if (!in || d.groups != 1) return CN_ERR_UNSUPPORTED;
     const int K = d.k, P = 4 + K - 1, PX = (P + 3) & ~3;
+    a.post_scale = d.post_scale;  // > 0 (checked by the caller): commutes with the max
+    // the tensor-core kernel where the problem fits it
+    if (tc3_plan(d, a.t, cfg.tc3) == CN_OK) {
+        a.tc = 1;
+        a.N = d.N;
+        cfg.name = cfg.tc3.name;
+        cfg.threads = cfg.tc3.threads;
+        cfg.smem = cfg.tc3.smem;
+        cfg.grid = cfg.tc3.grid;
+        return CN_OK;
+    }
+    a.tc = 0;
     a.N = d.N;
     a.Ci = d.C_in;
     a.D = d.D;
@@ -267,7 +278,14 @@ int pool3d_plan(const conv_norm_desc &d, Pool3dArgs &a, Pool3dConfig &cfg) {
     return CN_OK;
 }
 
-int pool3d_prepare(const Pool3dConfig &cfg) {
+size_t pool3d_workspace(const Pool3dArgs &a) { return a.tc ? 2 * sizeof(int) : 0; }
+
+int pool3d_prepare(Pool3dConfig &cfg, const Pool3dArgs &a) {
+    if (a.tc) {
+        const int st = tc3_prepare(cfg.tc3, a.t);
+        cfg.grid = cfg.tc3.grid;
+        return st;
+    }
     if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
@@ -276,6 +294,15 @@ int pool3d_prepare(const Pool3dConfig &cfg) {
 
 int pool3d_launch(const Pool3dConfig &cfg, Pool3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
+    if (a.tc) {
+        Tc3Args &t = a.t;
+        t.x = a.x;
+        t.w = a.w;
+        t.b = a.b;
+        t.out = a.out;
+        t.err = a.err;
+        return tc3_launch(cfg.tc3, t, s, ev);
+    }
     if (a.use_tma && a.tmap_base != a.x) {
         const int K = a.D - a.Do + 1, P = 4 + K - 1, PX = (P + 3) & ~3;
         const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D, (uint64_t)a.N * a.Ci};

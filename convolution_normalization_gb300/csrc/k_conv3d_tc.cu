@@ -1,7 +1,10 @@
-// Variant 0, tensor-core conv: Conv3d with up to 4 input channels and 16
-// or 32 output channels -> activation -> GroupNorm / InstanceNorm / none ->
-// mean over D, H, W, as an implicit GEMM on the 5th-generation tensor cores
-// (the l2_p27 problem: Conv3d 3 -> 16, k = 4, HardSwish, GroupNorm(4), mean).
+// Tensor-core Conv3d with up to 4 input channels, as an implicit GEMM on the
+// 5th-generation tensor cores, for two of the fused problems:
+//   mean: Conv3d (16 or 32 output channels) -> activation -> GroupNorm /
+//         InstanceNorm / none -> mean over D, H, W (l2_p27: Conv3d 3 -> 16,
+//         k = 4, HardSwish, GroupNorm(4), mean);
+//   pool: Conv3d (16 output channels) -> softmax over channels -> MaxPool3d(2)
+//         twice = one 4x4x4 stride-4 max (l2_p6: Conv3d 3 -> 16, k = 3).
 //
 // GEMM.  A stage covers one band of RB = 128 / W output rows (M = 128
 // positions p = row * W + x, TMEM lanes) of a group of ZG consecutive output
@@ -13,17 +16,18 @@
 // done by the epilogue with warp shuffles.  Tiles are whole rows, so a shift
 // never reaches a row's next row for a valid output (x + kx < W); where W
 // divides 32 the 32-lane quadrants also hold whole rows, otherwise the k - 1
-// rows past a quadrant come from a small shared halo.
+// rows past a quadrant come from a small shared halo (mean only).
 //
 // Why this shape: a tcgen05.mma with M = 128 and K = 8 costs about the same
-// up to N = 128 (measured ~130 cycles at N = 64 and N = 128 on this GPU,
-// ~185 at N = 256, the full rate), so N is made as wide as it goes: the kx
-// taps and ZG output planes (16 * 4 * 4 = 256 for C_out = 16, k = 4), which
-// reads each staged input plane once for the ZG output planes it feeds.
-// For input plane u the filter operand rows (zg, co, kx) hold taps
+// up to N = 128 (measured ~144 cycles at N = 64, ~162 at N = 128 on this
+// GPU, ~185 at N = 256, the full rate), so N is made as wide as it goes: the
+// kx taps and ZG output planes (16 * 4 * 4 = 256 for C_out = 16, k = 4),
+// which reads each staged input plane once for the ZG output planes it
+// feeds.  For input plane u the filter operand rows (zg, co, kx) hold taps
 // kz = u - zg: consecutive blocks of one sequence stored with kz descending
 // and zero blocks at both ends, so B for every u is a window of that
-// sequence (no copies per u).
+// sequence (no copies per u).  With ZG = 4 a plane group and a band of
+// 4 * (32 / W) rows are exactly whole 4x4x4 pooling windows.
 //
 // Precision: split TF32 as in the 2-D tensor-core kernel (the tensor cores
 // read tf32 by dropping 13 mantissa bits; with v = hi + lo,
@@ -37,20 +41,27 @@
 // channels] fp32, hi part then lo part; a K step of 8 is two 4-channel core
 // matrices, 16 bytes a row.  Tap offsets move the start address only.
 //
-// Warp roles (one persistent CTA per SM, items = (sample, group of ZG
-// output planes) claimed from a counter, each item nband stages):
+// Warp roles (one persistent CTA per SM, items claimed from a counter: for
+// the mean (sample, group of ZG output planes) with all its bands, for the
+// pool (sample, group, band)):
 //   warp 0      producer: one TMA tensor copy per stage (W x (RB + k - 1)
 //               rows x (ZG + k - 1) planes x C_in, zero fill outside x);
 //   warps 2-3   converters: landing [c][u][row][x] -> operand stage hi / lo;
 //   warp 1      MMA issuer (one thread): the stage's MMAs into one of two
 //               TMEM accumulators;
-//   warps 4-19  epilogue, four warps per TMEM lane quadrant (C_out / 4
-//               channels each, all ZG planes): tcgen05.ld of the accumulator
-//               (thread = position), the kx sum, bias + activation,
-//               per-channel shifted sums in registers; at the end of an item
-//               its per-channel moments, then the sample's ticket: the last
-//               item of a sample merges its items and writes the output (the
-//               CUDA-core mean kernel's finish).
+//   warps 4-19  epilogue, four warps per TMEM lane quadrant, thread =
+//               position:
+//     mean: a warp takes C_out / 4 channels of all ZG planes: the kx sum,
+//           bias + activation, per-channel shifted sums in registers; at the
+//           end of an item its per-channel moments, then the sample's
+//           ticket: the last item of a sample merges its items and writes
+//           the output (the CUDA-core mean kernel's finish);
+//     pool: a warp takes the 16 channels of one plane zg: the kx sum, bias,
+//           softmax over the channels in registers, the max over the
+//           window's 4 columns (and rows inside the quadrant) by shuffles,
+//           then across quadrants and planes by shared-memory atomic max
+//           (softmax values are positive, so their bits order as integers);
+//           the stage's pooled values are scaled and stored.
 #include "cn_common.cuh"
 #include "cn_internal.h"
 #include "cn_mean_common.cuh"
@@ -68,6 +79,9 @@ constexpr int kEpiWarp0 = 4;       // epilogue: warps 4-19
 constexpr int kEpiWarps = 16;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kT3SmemLimit = 227 * 1024 - 1024;  // dynamic part (static barriers beside it)
+constexpr int kPoolCells = 8;      // pooled outputs per channel per stage: (RB / 4) (W / 4)
+
+enum { MODE_MEAN = 0, MODE_POOL = 1 };
 
 template <int K, int CO>
 struct T3 {
@@ -81,11 +95,10 @@ struct T3 {
     static constexpr int ZBYTES = (K & 1) ? N * 16 : 0;   // zero block for an odd k
     static constexpr int WBYTES = K * 2 * SLEN + ZBYTES;
     static constexpr int ACC = N <= 128 ? 128 : 256;      // TMEM columns per accumulator
-    static constexpr int CQ = CO / 4;                     // channels per epilogue warp
-    static constexpr int NC = CQ * K;                     // its columns of one plane zg
     static constexpr int HALO = 2 * 4 * (K - 1) * N;      // floats: [parity][quadrant][row][N]
+    static constexpr int RED = 4 * CO * 2;                // floats: mean [quadrant][CO][2] / pool cells
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
-    static_assert(NC % 4 == 0 && NC <= 32, "epilogue columns");
+    static_assert(RED >= CO * kPoolCells, "pool cells");
 };
 
 // The epilogue warps agree on a flag (barrier 1 with an AND reduction), so
@@ -112,8 +125,8 @@ CN_DEV void tmem_ld_cols(uint32_t taddr, uint32_t *v) {
     if (R % 8 >= 4) tmem_ld4(taddr + B8 + (R >= 8 ? 8 : 0), v + B8 + (R >= 8 ? 8 : 0));
 }
 
-template <int K, int CO>
-__global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_constant__ Mean3dArgs a) {
+template <int K, int CO, int MODE>
+CN_DEV void tc3_body(const Tc3Args &a) {
     using P = T3<K, CO>;
     constexpr int N = P::N, ZG = P::ZG, NU = P::NU;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -128,20 +141,22 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int PP = a.tc_pp;
+    const int PP = a.pp;
     unsigned char *stages = smem_raw;
-    auto stage = [&](int b) { return stages + (size_t)b * a.tc_stage; };
-    unsigned char *land = stages + 2 * (size_t)a.tc_stage;
-    unsigned char *wts = land + ((a.tc_land + 127) & ~127);
+    auto stage = [&](int b) { return stages + (size_t)b * a.stage; };
+    unsigned char *land = stages + 2 * (size_t)a.stage;
+    unsigned char *wts = land + ((a.land + 127) & ~127);
     float *halo = reinterpret_cast<float *>(wts + P::WBYTES);
-    float *red = halo + (a.tc_halo ? P::HALO : 0);               // [4 quadrants][CO][2]
-    double *sch = reinterpret_cast<double *>(red + 4 * CO * 2);  // [CO][3]
-    const int rows_in = a.tc_rb + K - 1;
+    float *red = halo + (a.halo ? P::HALO : 0);
+    double *sch = reinterpret_cast<double *>(red + P::RED);  // [CO][3]
+    const int rows_in = a.rb + K - 1;
     const int P0 = rows_in * a.W;  // staged positions per plane
 
+    // item -> (sample n, plane group g, split s of the group's bands)
     auto item_group = [&](int item, int &n, int &g, int &z0, int &nzv) {
-        n = item / a.nchunks;
-        g = item - n * a.nchunks;
+        const int grp = item / a.nsplit;
+        n = grp / a.ngroups;
+        g = grp - n * a.ngroups;
         z0 = g * ZG;
         nzv = min(ZG, a.Do - z0);
     };
@@ -179,6 +194,8 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
             }
             wf[e] = v;
         }
+        if (MODE == MODE_POOL)
+            for (int e = tid; e < P::RED; e += blockDim.x) red[e] = 0.0f;  // pool cells
     }
     if (tid == 0) {
         mbar_init(&land_full, 1);
@@ -215,19 +232,21 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
             bool live = true;
             while (live) {
                 const int item = next < a.items ? next : -1;
-                if (item >= 0) next = (int)gridDim.x + atomicAdd(a.tickets + a.N, 1);
+                if (item >= 0) next = (int)gridDim.x + atomicAdd(a.work, 1);
                 int n = 0, g = 0, z0 = 0, nzv = 0;
                 if (item >= 0) item_group(item, n, g, z0, nzv);
-                const int nb = item >= 0 ? a.tc_nband : 1;  // a stop marker is one stage
-                for (int band = 0; band < nb; ++band) {
+                // bands of this item: all of the group's, or the split's one
+                const int b0 = a.nsplit == 1 ? 0 : item % a.nsplit;
+                const int nb = item < 0 ? 1 : a.nsplit == 1 ? a.nband : 1;  // a stop marker is one stage
+                for (int band = b0; band < b0 + nb; ++band) {
                     if (k >= 1 && !wait(&land_empty, (k - 1) & 1)) {
                         live = false;
                         break;
                     }
-                    s_land_info = make_int4(item, band, band == nb - 1, nzv);
+                    s_land_info = make_int4(item, band, band == b0 + nb - 1, nzv);
                     if (item >= 0) {
-                        mbar_arrive_expect_tx(&land_full, (uint32_t)a.tc_land);
-                        tma_load_4d(land, &a.tc_xmap, 0, band * a.tc_rb, z0, n * a.Ci, &land_full);
+                        mbar_arrive_expect_tx(&land_full, (uint32_t)a.land);
+                        tma_load_4d(land, &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full);
                     } else {
                         mbar_arrive(&land_full);
                     }
@@ -327,14 +346,14 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
             }
             if (info.x < 0) break;
         }
-    } else {
-        // ---------------- epilogue ----------------
-        constexpr int CQ = P::CQ, NC = P::NC;
+    } else if (MODE == MODE_MEAN) {
+        // ---------------- epilogue: activation, moments, mean ----------------
+        constexpr int CQ = CO / 4, NC = CQ * K;  // a warp's channels; its columns of one plane
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
         const int h = (warp - kEpiWarp0) >> 2;  // channel quarter
         const int et = tid - 32 * kEpiWarp0;
         const int r = 32 * q + lane;  // tile row: this thread's position in the band
-        const int ry = (int)__umulhi((uint32_t)r, a.tc_wmagic);
+        const int ry = (int)__umulhi((uint32_t)r, a.wmagic);
         const int rx = r - ry * a.W;
         float bias[CQ], ksh[CQ], s1[CQ], s2[CQ];
 #pragma unroll
@@ -351,7 +370,7 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
             if (got) info = s_acc_info[b];
             const uint32_t tq = tmem + (uint32_t)(b * P::ACC) + ((uint32_t)(q * 32) << 16);
             float *hb = halo + (size_t)(k & 1) * 4 * (K - 1) * N;
-            if (got && info.x >= 0 && a.tc_halo) {
+            if (got && info.x >= 0 && a.halo) {
                 // rows 0 .. k-2 of this quadrant are the shift halo of the one below
                 tc_fence_after();
 #pragma unroll 1
@@ -371,7 +390,7 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
             if (!epi_all(got)) break;
             if (info.x < 0) break;
             tc_fence_after();
-            const bool pos_ok = r < a.tc_rb * a.W && info.y * a.tc_rb + ry < a.Ho && rx < a.Wo;
+            const bool pos_ok = r < a.rb * a.W && info.y * a.rb + ry < a.Ho && rx < a.Wo;
             const float *hq = hb + (size_t)(min(q + 1, 3) * (K - 1)) * N;
 #pragma unroll 1
             for (int zg = 0; zg < ZG; ++zg) {
@@ -389,7 +408,7 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
                         // lanes past the quadrant: the halo (W not dividing
                         // 32), else they are columns x >= Wo and unused
                         float hv = 0.0f;
-                        if (a.tc_halo && q < 3) hv = hq[max(lane + kx - 32, 0) * N + col0 + c * K + kx];
+                        if (a.halo && q < 3) hv = hq[max(lane + kx - 32, 0) * N + col0 + c * K + kx];
                         acc += lane + kx < 32 ? o : hv;
                     }
                     const float y = apply_act(a.act, acc + bias[c]);
@@ -436,19 +455,19 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
                 const float kc = apply_act(a.act, a.b ? __ldg(a.b + et) : 0.0f);
                 const Moments<double> m =
                     moments_from_sums((double)nzv * a.Ho * a.Wo, (double)kc, (double)S1, (double)S2);
-                double *pp = a.partial + (((size_t)n * a.nchunks + g) * a.Co + et) * 3;
+                double *pp = a.partial + (((size_t)n * a.ngroups + g) * a.Co + et) * 3;
                 pp[0] = m.n;
                 pp[1] = m.mean;
                 pp[2] = m.m2;
             }
             __threadfence();
             epi_sync();
-            if (et == 0) s_last = (atomicAdd(a.tickets + n, 1) == a.nchunks - 1);
+            if (et == 0) s_last = (atomicAdd(a.tickets + n, 1) == a.ngroups - 1);
             epi_sync();
             if (s_last) {
                 __threadfence();
                 for (int c = et; c < a.Co; c += kEpiThreads) {
-                    const Moments<double> m = mean_chunks_merged(a, n, c);
+                    const Moments<double> m = mean_chunks_merged(a, a.ngroups, n, c);
                     sch[c * 3 + 0] = m.n;
                     sch[c * 3 + 1] = m.mean;
                     sch[c * 3 + 2] = m.m2;
@@ -456,6 +475,85 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
                 epi_sync();
                 for (int c = et; c < a.Co; c += kEpiThreads) mean_write_output(a, n, c, sch);
                 if (et == 0) a.tickets[n] = 0;
+            }
+        }
+    } else {
+        // ---------------- epilogue: softmax, 4x4x4 max ----------------
+        constexpr int CH = 4;                    // channels per TMEM load
+        const int q = warp & 3;                  // TMEM lane quadrant this warp may read
+        const int zg = (warp - kEpiWarp0) >> 2;  // this warp's output plane of the group
+        const int et = tid - 32 * kEpiWarp0;
+        const int rq = 32 / a.W;                 // rows per quadrant (W divides 32 here)
+        const int row_q = lane / a.W, x = lane - row_q * a.W;
+        const int br = q * rq + row_q;           // row in the band
+        const bool rep = (x & 3) == 0 && (row_q & (min(rq, 4) - 1)) == 0;  // holds its window's max
+        const int cell = (br >> 2) * (a.W >> 2) + (x >> 2);  // pooled (row, column) in the band
+        unsigned *cells = reinterpret_cast<unsigned *>(red);  // [CO][kPoolCells]
+        float bias[CO];
+#pragma unroll
+        for (int c = 0; c < CO; ++c) bias[c] = a.b ? __ldg(a.b + c) : 0.0f;
+        for (int k = 0;; ++k) {
+            const int b = k & 1;
+            const bool got = wait(&acc_full[b], (k >> 1) & 1);
+            int4 info = make_int4(-1, 0, 0, 0);
+            if (got) info = s_acc_info[b];
+            // every epilogue warp got the stage (else all stop); the previous
+            // stage's cells are stored and cleared
+            if (!epi_all(got)) break;
+            if (info.x < 0) break;
+            tc_fence_after();
+            const uint32_t tq = tmem + (uint32_t)(b * P::ACC) + ((uint32_t)(q * 32) << 16);
+            float cv[CO];
+#pragma unroll
+            for (int c0 = 0; c0 < CO; c0 += CH) {
+                uint32_t v[CH * K];
+                tmem_ld_cols<CH * K>(tq + (uint32_t)((zg * CO + c0) * K), v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < CH; ++c) {
+                    float acc = __uint_as_float(v[c * K]);
+                    // lanes past the quadrant are columns x >= W - kx, in no
+                    // window that is stored
+#pragma unroll
+                    for (int kx = 1; kx < K; ++kx)
+                        acc += __shfl_down_sync(0xffffffffu, __uint_as_float(v[c * K + kx]), kx);
+                    cv[c0 + c] = acc + bias[c0 + c];
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+            float m = cv[0];
+#pragma unroll
+            for (int c = 1; c < CO; ++c) m = fmaxf(m, cv[c]);
+            float s = 0.0f;
+#pragma unroll
+            for (int c = 0; c < CO; ++c) {
+                cv[c] = __expf(cv[c] - m);
+                s += cv[c];
+            }
+            const float inv = 1.0f / s;
+#pragma unroll
+            for (int c = 0; c < CO; ++c) {
+                float p = cv[c] * inv;
+                p = fmaxf(p, __shfl_xor_sync(0xffffffffu, p, 1));  // the window's 4 columns
+                p = fmaxf(p, __shfl_xor_sync(0xffffffffu, p, 2));
+                if (rq >= 2) p = fmaxf(p, __shfl_xor_sync(0xffffffffu, p, a.W));  // rows in the quadrant
+                if (rq >= 4) p = fmaxf(p, __shfl_xor_sync(0xffffffffu, p, 2 * a.W));
+                if (rep) atomicMax(&cells[c * kPoolCells + cell], __float_as_uint(p));
+            }
+            epi_sync();
+            if (et < CO * kPoolCells) {
+                const int c = et / kPoolCells, e = et - c * kPoolCells;
+                const int prow = e / (a.W >> 2), pcol = e - prow * (a.W >> 2);
+                const int ph = info.y * (a.rb >> 2) + prow;
+                if (ph < a.Ph && pcol < a.Pw) {
+                    int n, g, z0, nzv;
+                    item_group(info.x, n, g, z0, nzv);
+                    a.out[((((size_t)n * CO + c) * a.Pd + g) * a.Ph + ph) * a.Pw + pcol] =
+                        a.post_scale * __uint_as_float(cells[et]);
+                }
+                cells[et] = 0u;
             }
         }
     }
@@ -469,38 +567,64 @@ __global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_c
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
                      "r"(2 * P::ACC)
                      : "memory");
-    if (tid == 0 && atomicAdd(a.tickets + a.N + 1, 1) == (int)gridDim.x - 1) {
-        a.tickets[a.N] = 0;
-        a.tickets[a.N + 1] = 0;
+    if (tid == 0 && atomicAdd(a.work + 1, 1) == (int)gridDim.x - 1) {
+        a.work[0] = 0;
+        a.work[1] = 0;
     }
 }
 
+template <int K, int CO>
+__global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_mean(const __grid_constant__ Tc3Args a) {
+    tc3_body<K, CO, MODE_MEAN>(a);
+}
+template <int K>
+__global__ void __launch_bounds__(kT3Threads, 1) k_conv3d_tc_pool(const __grid_constant__ Tc3Args a) {
+    tc3_body<K, 16, MODE_POOL>(a);
+}
+
 struct T3Inst {
-    int K, CO, ZG, WBYTES, HALO;
-    Mean3dKernel fn;
+    int mode, K, CO, ZG, WBYTES, HALO, RED;
+    Tc3Kernel fn;
     const char *name;
 };
-#define CN_T3_INST(K, CO)                                                                     \
-    {K, CO, T3<K, CO>::ZG, T3<K, CO>::WBYTES, T3<K, CO>::HALO, k_conv3d_tc_mean<K, CO>, \
-     "k_conv3d_tc_mean<" #K "," #CO ">"}
-const T3Inst kT3Inst[] = {CN_T3_INST(3, 16), CN_T3_INST(4, 16), CN_T3_INST(3, 32), CN_T3_INST(4, 32)};
-#undef CN_T3_INST
+#define CN_T3_MEAN(K, CO)                                                                       \
+    {MODE_MEAN, K, CO, T3<K, CO>::ZG, T3<K, CO>::WBYTES, T3<K, CO>::HALO, T3<K, CO>::RED, \
+     k_conv3d_tc_mean<K, CO>, "k_conv3d_tc_mean<" #K "," #CO ">"}
+#define CN_T3_POOL(K)                                                                           \
+    {MODE_POOL, K, 16, T3<K, 16>::ZG, T3<K, 16>::WBYTES, T3<K, 16>::HALO, T3<K, 16>::RED, \
+     k_conv3d_tc_pool<K>, "k_conv3d_tc_pool<" #K ">"}
+const T3Inst kT3Inst[] = {CN_T3_MEAN(3, 16), CN_T3_MEAN(4, 16), CN_T3_MEAN(3, 32),
+                          CN_T3_MEAN(4, 32), CN_T3_POOL(3),     CN_T3_POOL(4)};
+#undef CN_T3_MEAN
+#undef CN_T3_POOL
 
 }  // namespace
 
-int tc3_mean_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
+int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
+    int mode;
+    if (d.red == CN_RED_MEAN_SPATIAL && d.act != CN_ACT_SOFTMAX_C)
+        mode = MODE_MEAN;
+    else if (d.red == CN_RED_MAXPOOL2_X2 && d.act == CN_ACT_SOFTMAX_C && d.norm == CN_NORM_NONE &&
+             d.post_scale > 0.0f)
+        mode = MODE_POOL;
+    else
+        return CN_ERR_UNSUPPORTED;
     if (d.conv != CN_CONV3D || d.groups != 1 || d.C_in < 1 || d.C_in > 4) return CN_ERR_UNSUPPORTED;
     const T3Inst *inst = nullptr;
     for (const T3Inst &in : kT3Inst)
-        if (in.K == d.k && in.CO == d.C_out) inst = &in;
+        if (in.mode == mode && in.K == d.k && in.CO == d.C_out) inst = &in;
     if (!inst) return CN_ERR_UNSUPPORTED;
-    // whole-row tiles of up to 128 positions; the TMA box is a whole row wide
+    // whole-row tiles of up to 128 positions; the TMA box is a whole row wide;
+    // pooling windows need quadrants of whole rows
     if (d.W % 4 != 0 || d.W > 128 || !tma_available()) return CN_ERR_UNSUPPORTED;
+    if (mode == MODE_POOL && 32 % d.W != 0) return CN_ERR_UNSUPPORTED;
     const char *e = getenv("CN_NO_TC");
     if (e && atoi(e)) return CN_ERR_UNSUPPORTED;
     const int K = d.k, CO = d.C_out, ZG = inst->ZG, NU = ZG + K - 1;
     const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
     if (Do < 1 || Ho < 1 || Wo < 1) return CN_ERR_UNSUPPORTED;
+    const int Pd = Do / 4, Ph = Ho / 4, Pw = Wo / 4;
+    if (mode == MODE_POOL && (Pd < 1 || Ph < 1 || Pw < 1)) return CN_ERR_UNSUPPORTED;
     const int rb = 128 / d.W;
     const int rows_in = rb + K - 1;
     // farthest operand row an MMA reads: tile row 127 + the largest ky offset
@@ -509,28 +633,24 @@ int tc3_mean_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     const int pp = (std::max(rows_in * d.W, far + 1) + 7) & ~7;
     const int stage_bytes = 2 * NU * pp * 16;
     const int land = d.C_in * NU * rows_in * d.W * 4;
-    const int halo = (32 % d.W) != 0;
+    const int halo = mode == MODE_MEAN && (32 % d.W) != 0;
     const int smem = 2 * stage_bytes + ((land + 127) & ~127) + inst->WBYTES +
-                     (halo ? inst->HALO * 4 : 0) + 4 * CO * 2 * 4 + CO * 3 * 8;
+                     (halo ? inst->HALO * 4 : 0) + inst->RED * 4 + CO * 3 * 8;
     if (smem > kT3SmemLimit) return CN_ERR_UNSUPPORTED;
-    // one item = one group of ZG output planes of one sample: a function of
+    // one item = one group of ZG output planes of one sample, a function of
     // the sample's shape only, so a sample's result (its items' merge order)
-    // does not depend on the batch it is part of
-    const int nchunks = (Do + ZG - 1) / ZG;
-    const long long items = (long long)d.N * nchunks;
+    // does not depend on the batch it is part of; the pool needs only the
+    // planes and rows its windows cover
+    const int ngroups = mode == MODE_MEAN ? (Do + ZG - 1) / ZG : Pd;
+    const int rows = mode == MODE_MEAN ? Ho : 4 * Ph;
+    const int nband = (rows + rb - 1) / rb;
+    // the mean keeps an item's moments across its bands; the pool's bands
+    // are independent, so each is an item of its own (finer load balance)
+    const int nsplit = mode == MODE_MEAN ? 1 : nband;
+    const long long items = (long long)d.N * ngroups * nsplit;
     if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
 
-    a.tc = 1;
-    a.tc_xmap_base = nullptr;
-    a.tc_rb = rb;
-    a.tc_nband = (Ho + rb - 1) / rb;
-    a.tc_pp = pp;
-    a.tc_stage = stage_bytes;
-    a.tc_land = land;
-    a.tc_halo = halo;
-    a.tc_wmagic = (uint32_t)(((1ull << 32) + (uint64_t)d.W - 1) / (uint64_t)d.W);
-    a.use_tma = 0;
-    a.tmap_base = nullptr;
+    a.xmap_base = nullptr;
     a.N = d.N;
     a.Ci = d.C_in;
     a.Co = d.C_out;
@@ -540,50 +660,70 @@ int tc3_mean_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     a.Do = Do;
     a.Ho = Ho;
     a.Wo = Wo;
-    a.nseg = 1;
-    a.rows = 0;
-    a.rows_per_cta = 0;
-    a.nchunks = nchunks;
-    a.ncob = 1;
-    a.wco = 0;
-    a.wrows = 0;
-    a.planes_max = NU;
-    a.pitch = d.W;
-    a.nbuf = 2;
-    a.buf_stride = 0;
+    a.k = K;
+    a.nu = NU;
+    a.rb = rb;
+    a.nband = nband;
+    a.nsplit = nsplit;
+    a.pp = pp;
+    a.stage = stage_bytes;
+    a.land = land;
+    a.halo = halo;
+    a.wmagic = (uint32_t)(((1ull << 32) + (uint64_t)d.W - 1) / (uint64_t)d.W);
+    a.ngroups = ngroups;
     a.items = (int)items;
-    a.vec16 = 1;
     a.act = d.act;
     a.norm = d.norm;
     a.G = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
     a.affine = d.affine && d.norm != CN_NORM_NONE;
     a.eps = d.eps;
     a.post_scale = d.post_scale;
+    a.Pd = Pd;
+    a.Ph = Ph;
+    a.Pw = Pw;
     cfg.kern = inst->fn;
     cfg.name = inst->name;
-    cfg.K = K;
-    cfg.RW = 0;
-    cfg.COT = CO;
     cfg.threads = kT3Threads;
     cfg.smem = smem;
-    cfg.grid = (int)std::min<long long>(items, 148);  // refined from the device in mean3d_prepare
+    cfg.grid = (int)std::min<long long>(items, 148);  // refined from the device in tc3_prepare
+    return CN_OK;
+}
+
+int tc3_prepare(Tc3Config &cfg, const Tc3Args &a) {
+    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+        cudaSuccess)
+        return CN_ERR_CUDA;
+    // persistent grid: one CTA per SM, capped by the work items
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, cfg.kern, cfg.threads, cfg.smem) !=
+            cudaSuccess)
+        return CN_ERR_CUDA;
+    if (per_sm < 1) return CN_ERR_UNSUPPORTED;
+    cfg.grid = (int)std::min<long long>((long long)sms, (long long)a.items);
     return CN_OK;
 }
 
 // Encodes the input tensor map for this x (cached while x stays the same):
-// x as (W, H, D, N * C_in), box (W, rb + k - 1 rows, ZG + k - 1 planes, C_in).
-int tc3_bind_x(Mean3dArgs &a) {
-    if (a.tc_xmap_base == a.x) return CN_OK;
-    const int K = a.D - a.Do + 1;
-    const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D, (uint64_t)a.N * a.Ci};
-    const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
-                                 (uint64_t)a.D * a.H * a.W * 4};
-    const uint32_t box[4] = {(uint32_t)a.W, (uint32_t)(a.tc_rb + K - 1), (uint32_t)a.planes_max,
-                             (uint32_t)a.Ci};
-    const int st = encode_tmap_f32_4d(&a.tc_xmap, a.x, dims, strides, box);
-    if (st != CN_OK) return st;
-    a.tc_xmap_base = a.x;
-    return CN_OK;
+// x as (W, H, D, N * C_in), box (W, rb + k - 1 rows, ZG + k - 1 planes,
+// C_in); then launches.
+int tc3_launch(const Tc3Config &cfg, Tc3Args &a, cudaStream_t s, const LaunchEvents *ev) {
+    if (cfg.grid == 0) return CN_OK;
+    if (a.xmap_base != a.x) {
+        const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.D, (uint64_t)a.N * a.Ci};
+        const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                     (uint64_t)a.D * a.H * a.W * 4};
+        const uint32_t box[4] = {(uint32_t)a.W, (uint32_t)(a.rb + a.k - 1), (uint32_t)a.nu,
+                                 (uint32_t)a.Ci};
+        const int st = encode_tmap_f32_4d(&a.xmap, a.x, dims, strides, box);
+        if (st != CN_OK) return st;
+        a.xmap_base = a.x;
+    }
+    record_launch(ev, 0, s);
+    cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+    record_launch(ev, 1, s);
+    return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }
 
 }  // namespace cn

@@ -81,6 +81,11 @@ def _base(**kw):
     (dict(conv="conv3d", D=6, groups=2, C_in=8), -2),
     (dict(conv="conv3d", D=6, act="softmax_c"), -2),
     (dict(N=0), 0),                           # empty batch is valid
+    (dict(conv="conv3d", D=9, act="softmax_c", norm="none", red="maxpool2_x2"), 0),
+    (dict(conv="conv3d", D=9, act="softmax_c", norm="none", red="maxpool2_x2", post_scale=0.5), 0),
+    # a post scale <= 0 does not commute with the max: no kernel
+    (dict(conv="conv3d", D=9, act="softmax_c", norm="none", red="maxpool2_x2", post_scale=-1.0), -2),
+    (dict(conv="conv3d", D=9, act="softmax_c", norm="none", red="maxpool2_x2", post_scale=0.0), -2),
 ])
 def test_descriptor_validation(B, kw, status):
     d = B.make_desc(_base(**kw))

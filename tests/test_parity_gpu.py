@@ -84,6 +84,7 @@ POOL_CASES = [
     dict(N=2, D=10, H=10, W=10, k=2),
     dict(N=17, D=7, H=7, W=7, k=3),                # 1x1x1 pooled per sample, many CTAs
     dict(N=2, D=9, H=12, W=11, k=3, has_bias=0),
+    dict(N=2, D=9, H=12, W=11, k=3, post_scale=0.5),   # the scale applies before the max
 ]
 
 
