@@ -103,12 +103,17 @@ def roofline_ms(s, pk):
 
 # ---- ncu traffic figure (only while the kernel source is unchanged) ------------
 
+_CS = "convolution_normalization_gb300/csrc/"
+# the source files each kernel is built from (its profile is current while
+# their hash is unchanged)
 KERNEL_SOURCES = {
-    "k_conv3d_act_mean": "convolution_normalization_gb300/csrc/k_conv3d_mean.cu",
-    "k_conv3d_softmax_pool4": "convolution_normalization_gb300/csrc/k_conv3d_softmax_pool.cu",
-    "k_conv2d_act_stats": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
-    "k_conv2d_tc": "convolution_normalization_gb300/csrc/k_conv2d_tc.cu",
-    "k_norm_apply": "convolution_normalization_gb300/csrc/k_conv2d_norm.cu",
+    "k_conv3d_act_mean": ("k_conv3d_mean.cu", "cn_mean_common.cuh", "cn_common.cuh"),
+    "k_conv3d_softmax_pool4": ("k_conv3d_softmax_pool.cu", "cn_common.cuh"),
+    "k_conv2d_act_stats": ("k_conv2d_norm.cu", "cn_common.cuh"),
+    "k_conv2d_tc": ("k_conv2d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
+    "k_norm_apply": ("k_conv2d_norm.cu", "cn_common.cuh"),
+    "k_conv3d_tc_mean": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_mean_common.cuh", "cn_common.cuh"),
+    "k_conv3d_tc_pool": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_mean_common.cuh", "cn_common.cuh"),
 }
 # tf32 tensor peak from the measured bf16 one and the nominal dense ratio
 # (1.1 / 2.25 PFLOP/s); split-TF32 runs 3 tf32 products per fp32 product
@@ -141,8 +146,8 @@ def kernel_key(name):
 
 def source_hash(key):
     h = hashlib.sha256()
-    for p in (KERNEL_SOURCES[key], "convolution_normalization_gb300/csrc/cn_common.cuh"):
-        h.update(open(os.path.join(ROOT, p), "rb").read())
+    for p in KERNEL_SOURCES[key]:
+        h.update(open(os.path.join(ROOT, _CS + p), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -167,7 +172,7 @@ def kernel_roofline(spec, name, ms, pk):
     launch / its measured duration against the peak of the unit bounding it."""
     flops = algorithmic_flops(spec)
     base = name.split("<")[0]
-    if base in ("k_conv2d_tc", "k_conv3d_tc_mean"):
+    if base in ("k_conv2d_tc", "k_conv3d_tc_mean", "k_conv3d_tc_pool"):
         work = SPLIT_TF32_PRODUCTS * flops  # tf32 tensor-core flops the split method needs
         peak = pk["bf16_tflops"] * TF32_PER_BF16
         return {"bound": "tensor", "achieved": work / (ms / 1e3) / 1e12, "peak": peak,

@@ -50,15 +50,16 @@ struct Tc3Args {
     int pp;           // operand positions per staged input plane
     int stage;        // bytes of one operand stage (hi and lo, all staged planes)
     int land;         // bytes of the raw input box of a stage
+    int nland;        // landing buffers for it (1 or 2)
     int halo;         // 1: output rows cross 32-lane quadrants (W does not divide 32)
     uint32_t wmagic;  // ceil(2^32 / W): p / W = umulhi(p, wmagic) for p < 2^16
     int ngroups;      // plane groups per sample
-    int nsplit;       // items per plane group: 1 (all bands) or nband (one band each)
+    int nsplit;       // items per plane group, each ceil(nband / nsplit) bands
     int items;        // N * ngroups * nsplit
     int act, norm, G, affine;
     float eps, post_scale;
     int Pd, Ph, Pw;    // pool: pooled extents
-    double *partial;   // mean: [N][ngroups][Co][3] (count, mean, M2)
+    double *partial;   // mean: [N][ngroups * nsplit][Co][3] (count, mean, M2)
     int *tickets;      // mean: [N] per-sample tickets, zero between launches
     int *work;         // [2] work / exit counters, zero between launches
 };

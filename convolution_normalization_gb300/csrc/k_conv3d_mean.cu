@@ -358,7 +358,7 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
         a.tc = 1;
         a.N = d.N;  // the fields the workspace and the plan's callers read
         a.Co = d.C_out;
-        a.nchunks = a.t.ngroups;
+        a.nchunks = a.t.ngroups * a.t.nsplit;
         a.items = a.t.items;
         cfg.name = cfg.tc3.name;
         cfg.threads = cfg.tc3.threads;

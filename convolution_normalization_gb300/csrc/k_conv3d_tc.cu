@@ -45,7 +45,8 @@
 // the mean (sample, group of ZG output planes) with all its bands, for the
 // pool (sample, group, band)):
 //   warp 0      producer: one TMA tensor copy per stage (W x (RB + k - 1)
-//               rows x (ZG + k - 1) planes x C_in, zero fill outside x);
+//               rows x (ZG + k - 1) planes x C_in, zero fill outside x) into
+//               one of two landing buffers (one where two do not fit);
 //   warps 2-3   converters: landing [c][u][row][x] -> operand stage hi / lo;
 //   warp 1      MMA issuer (one thread): the stage's MMAs into one of two
 //               TMEM accumulators;
@@ -130,12 +131,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     using P = T3<K, CO>;
     constexpr int N = P::N, ZG = P::ZG, NU = P::NU;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t land_full, land_empty;
+    __shared__ __align__(8) uint64_t land_full[2], land_empty[2];
     // st_full[b]: the converters wrote stage b; st_empty[b]: its MMAs are done
     __shared__ __align__(8) uint64_t st_full[2], st_empty[2];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
     // stage info: (item or -1 to stop, band, 1 if the item's last band, valid planes)
-    __shared__ int4 s_land_info, s_st_info[2], s_acc_info[2];
+    __shared__ int4 s_land_info[2], s_st_info[2], s_acc_info[2];
     __shared__ uint32_t s_tmem;
     __shared__ int s_last;
     __shared__ volatile int s_abort;
@@ -144,15 +145,19 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     const int PP = a.pp;
     unsigned char *stages = smem_raw;
     auto stage = [&](int b) { return stages + (size_t)b * a.stage; };
-    unsigned char *land = stages + 2 * (size_t)a.stage;
-    unsigned char *wts = land + ((a.land + 127) & ~127);
+    const int land_stride = (a.land + 127) & ~127;
+    unsigned char *land0 = stages + 2 * (size_t)a.stage;
+    auto land = [&](int lb) { return land0 + (size_t)lb * land_stride; };
+    unsigned char *wts = land0 + (size_t)a.nland * land_stride;
     float *halo = reinterpret_cast<float *>(wts + P::WBYTES);
     float *red = halo + (a.halo ? P::HALO : 0);
     double *sch = reinterpret_cast<double *>(red + P::RED);  // [CO][3]
     const int rows_in = a.rb + K - 1;
     const int P0 = rows_in * a.W;  // staged positions per plane
 
-    // item -> (sample n, plane group g, split s of the group's bands)
+    // item -> (sample n, plane group g, split s of the group's bands: bands
+    // s * bpi .. s * bpi + bpi - 1)
+    const int bpi = (a.nband + a.nsplit - 1) / a.nsplit;
     auto item_group = [&](int item, int &n, int &g, int &z0, int &nzv) {
         const int grp = item / a.nsplit;
         n = grp / a.ngroups;
@@ -198,8 +203,10 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             for (int e = tid; e < P::RED; e += blockDim.x) red[e] = 0.0f;  // pool cells
     }
     if (tid == 0) {
-        mbar_init(&land_full, 1);
-        mbar_init(&land_empty, kConvWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&land_full[i], 1);
+            mbar_init(&land_empty[i], kConvWarps);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&st_full[i], kConvWarps);
             mbar_init(&st_empty[i], 1);
@@ -227,7 +234,9 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     if (warp == 0) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            int k = 0;  // stages armed so far (one landing buffer)
+            int k = 0;       // stages armed so far; stage k lands in buffer lb = k % nland
+            int lb = 0;
+            uint32_t lph = 0;  // parity of the current pass over the landing buffers
             int next = (int)blockIdx.x;
             bool live = true;
             while (live) {
@@ -235,27 +244,32 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 if (item >= 0) next = (int)gridDim.x + atomicAdd(a.work, 1);
                 int n = 0, g = 0, z0 = 0, nzv = 0;
                 if (item >= 0) item_group(item, n, g, z0, nzv);
-                // bands of this item: all of the group's, or the split's one
-                const int b0 = a.nsplit == 1 ? 0 : item % a.nsplit;
-                const int nb = item < 0 ? 1 : a.nsplit == 1 ? a.nband : 1;  // a stop marker is one stage
+                // bands of this item (a stop marker is one stage)
+                const int b0 = item < 0 ? 0 : (item % a.nsplit) * bpi;
+                const int nb = item < 0 ? 1 : min(bpi, a.nband - b0);
                 for (int band = b0; band < b0 + nb; ++band) {
-                    if (k >= 1 && !wait(&land_empty, (k - 1) & 1)) {
+                    if (k >= a.nland && !wait(&land_empty[lb], lph ^ 1u)) {
                         live = false;
                         break;
                     }
-                    s_land_info = make_int4(item, band, band == b0 + nb - 1, nzv);
+                    s_land_info[lb] = make_int4(item, band, band == b0 + nb - 1, nzv);
                     if (item >= 0) {
-                        mbar_arrive_expect_tx(&land_full, (uint32_t)a.land);
-                        tma_load_4d(land, &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full);
+                        mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.land);
+                        tma_load_4d(land(lb), &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full[lb]);
                     } else {
-                        mbar_arrive(&land_full);
+                        mbar_arrive(&land_full[lb]);
                     }
                     ++k;
+                    if (++lb == a.nland) {
+                        lb = 0;
+                        lph ^= 1u;
+                    }
                 }
                 if (item < 0) live = false;
             }
             // a copy still in flight (only after an abort) lands before the CTA exits
-            if (k >= 1) mbar_wait_bounded(&land_full, (k - 1) & 1, kWaitLimitNs);
+            for (int j = max(0, k - a.nland); j < k; ++j)
+                mbar_wait_bounded(&land_full[j % a.nland], (j / a.nland) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -315,13 +329,15 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     } else if (warp < kEpiWarp0) {
         // ---------------- converters ----------------
         const int ct = tid - 64;
+        int lb = 0;
+        uint32_t lph = 0;
         for (int k = 0;; ++k) {
-            if (!wait(&land_full, k & 1)) break;
-            const int4 info = s_land_info;
+            if (!wait(&land_full[lb], lph)) break;
+            const int4 info = s_land_info[lb];
             const int b = k & 1;
             if (k >= 2 && !wait(&st_empty[b], ((k >> 1) - 1) & 1)) break;
             if (info.x >= 0) {
-                const float *src = reinterpret_cast<const float *>(land);
+                const float *src = reinterpret_cast<const float *>(land(lb));
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
                 float4 *xl = xh + (size_t)NU * PP;
 #pragma unroll 1
@@ -341,10 +357,14 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             __syncwarp();
             if (lane == 0) {
                 if (warp == 2) s_st_info[b] = info;
-                mbar_arrive(&land_empty);
+                mbar_arrive(&land_empty[lb]);
                 mbar_arrive(&st_full[b]);
             }
             if (info.x < 0) break;
+            if (++lb == a.nland) {
+                lb = 0;
+                lph ^= 1u;
+            }
         }
     } else if (MODE == MODE_MEAN) {
         // ---------------- epilogue: activation, moments, mean ----------------
@@ -425,6 +445,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             // ---- end of the item: its per-channel moments, then the ticket ----
             int n, g, z0, nzv;
             item_group(info.x, n, g, z0, nzv);
+            // the item's slot among the sample's nchunks = ngroups * nsplit,
+            // and its output rows (its bands')
+            const int nchunks = a.ngroups * a.nsplit;
+            const int sp = info.x % a.nsplit;
+            const int chunk = g * a.nsplit + sp;
+            const int rows = min(bpi * a.rb, a.Ho - sp * bpi * a.rb);
 #pragma unroll
             for (int c = 0; c < CQ; ++c) {
 #pragma unroll
@@ -454,20 +480,20 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 }
                 const float kc = apply_act(a.act, a.b ? __ldg(a.b + et) : 0.0f);
                 const Moments<double> m =
-                    moments_from_sums((double)nzv * a.Ho * a.Wo, (double)kc, (double)S1, (double)S2);
-                double *pp = a.partial + (((size_t)n * a.ngroups + g) * a.Co + et) * 3;
+                    moments_from_sums((double)nzv * rows * a.Wo, (double)kc, (double)S1, (double)S2);
+                double *pp = a.partial + (((size_t)n * nchunks + chunk) * a.Co + et) * 3;
                 pp[0] = m.n;
                 pp[1] = m.mean;
                 pp[2] = m.m2;
+                __threadfence();  // the slot is visible before the ticket below
             }
-            __threadfence();
             epi_sync();
-            if (et == 0) s_last = (atomicAdd(a.tickets + n, 1) == a.ngroups - 1);
+            if (et == 0) s_last = (atomicAdd(a.tickets + n, 1) == nchunks - 1);
             epi_sync();
             if (s_last) {
-                __threadfence();
                 for (int c = et; c < a.Co; c += kEpiThreads) {
-                    const Moments<double> m = mean_chunks_merged(a, a.ngroups, n, c);
+                    __threadfence();  // the other items' slots, published before their tickets
+                    const Moments<double> m = mean_chunks_merged(a, nchunks, n, c);
                     sch[c * 3 + 0] = m.n;
                     sch[c * 3 + 1] = m.mean;
                     sch[c * 3 + 2] = m.m2;
@@ -634,19 +660,27 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     const int stage_bytes = 2 * NU * pp * 16;
     const int land = d.C_in * NU * rows_in * d.W * 4;
     const int halo = mode == MODE_MEAN && (32 % d.W) != 0;
-    const int smem = 2 * stage_bytes + ((land + 127) & ~127) + inst->WBYTES +
-                     (halo ? inst->HALO * 4 : 0) + inst->RED * 4 + CO * 3 * 8;
+    // two landing buffers (the next stage's copy in flight while this one is
+    // converted) when they fit, else one
+    const int fixed = 2 * stage_bytes + inst->WBYTES + (halo ? inst->HALO * 4 : 0) + inst->RED * 4 +
+                      CO * 3 * 8;
+    int nland = 2;
+    while (nland > 1 && fixed + nland * ((land + 127) & ~127) > kT3SmemLimit) --nland;
+    const int smem = fixed + nland * ((land + 127) & ~127);
     if (smem > kT3SmemLimit) return CN_ERR_UNSUPPORTED;
-    // one item = one group of ZG output planes of one sample, a function of
-    // the sample's shape only, so a sample's result (its items' merge order)
-    // does not depend on the batch it is part of; the pool needs only the
-    // planes and rows its windows cover
+    // one item = some bands of one group of ZG output planes of one sample:
+    // one band for the pool (no state across bands: finest load balance);
+    // all of the group's bands for the mean, whose item end (moments, ticket,
+    // and for a sample's last item the fp64 merge) is serial latency in the
+    // epilogue (splitting n512's items into 4 measured 0.49 vs 0.39 ms).  A
+    // function of the sample's shape only, so a sample's result (its items'
+    // merge order) does not depend on the batch it is part of.  The pool
+    // needs only the planes and rows its windows cover.
     const int ngroups = mode == MODE_MEAN ? (Do + ZG - 1) / ZG : Pd;
     const int rows = mode == MODE_MEAN ? Ho : 4 * Ph;
     const int nband = (rows + rb - 1) / rb;
-    // the mean keeps an item's moments across its bands; the pool's bands
-    // are independent, so each is an item of its own (finer load balance)
-    const int nsplit = mode == MODE_MEAN ? 1 : nband;
+    const int bpi = mode == MODE_POOL ? 1 : nband;  // bands per item
+    const int nsplit = (nband + bpi - 1) / bpi;
     const long long items = (long long)d.N * ngroups * nsplit;
     if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
 
@@ -668,6 +702,7 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     a.pp = pp;
     a.stage = stage_bytes;
     a.land = land;
+    a.nland = nland;
     a.halo = halo;
     a.wmagic = (uint32_t)(((1ull << 32) + (uint64_t)d.W - 1) / (uint64_t)d.W);
     a.ngroups = ngroups;
