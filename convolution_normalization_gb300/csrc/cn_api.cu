@@ -257,7 +257,7 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
     switch (p->variant) {
         case V_MEAN3D: {
             Mean3dArgs &a = p->mean_args;
-            const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
+            const size_t part = mean3d_partial_bytes(a);
             a.partial = reinterpret_cast<double *>(vbase);
             a.tickets = reinterpret_cast<int *>(vbase + ((part + 255) & ~(size_t)255));
             a.err = p->err_flag;
@@ -309,7 +309,7 @@ int conv_norm_plan_info(conv_norm_plan p, conv_norm_info *info) {
     info->workspace_bytes = p->ws_bytes;
     switch (p->variant) {
         case V_MEAN3D:
-            info->launches_per_forward = p->d.N > 0 ? 1 : 0;
+            info->launches_per_forward = mean3d_launches(p->mean_cfg, p->mean_args);
             info->kernel_names = p->mean_cfg.name;
             info->grid_ctas = p->mean_cfg.grid;
             info->threads_per_cta = p->mean_cfg.threads;
@@ -396,7 +396,7 @@ int conv_norm_plan_set_launch_events(conv_norm_plan p, void *const *events, int 
     int L = 0;
     switch (p->variant) {
         case V_MEAN3D:
-            L = p->d.N > 0 ? 1 : 0;
+            L = mean3d_launches(p->mean_cfg, p->mean_args);
             break;
         case V_POOL3D:
             L = p->pool_cfg.grid > 0 ? 1 : 0;

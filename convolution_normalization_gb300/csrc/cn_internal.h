@@ -59,7 +59,8 @@ struct Tc3Args {
     int act, norm, G, affine;
     float eps, post_scale;
     int Pd, Ph, Pw;    // pool: pooled extents
-    double *partial;   // mean: [N][ngroups * nsplit][Co][3] (count, mean, M2)
+    double inv_cnt, inv_cpg;  // mean: 1 / (Do Ho Wo), 1 / (channels per norm group)
+    float2 *partial;   // mean: [N][ngroups * nsplit][Co] shifted sums (S1, S2) about act(bias)
     int *tickets;      // mean: [N] per-sample tickets, zero between launches
     int *work;         // [2] work / exit counters, zero between launches
 };
@@ -74,6 +75,7 @@ struct Tc3Config {
 int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg);
 int tc3_prepare(Tc3Config &cfg, const Tc3Args &a);  // smem attribute, persistent grid
 int tc3_launch(const Tc3Config &cfg, Tc3Args &a, cudaStream_t s, const LaunchEvents *ev);
+int tc3_launches(const Tc3Config &cfg);  // kernels one forward launches
 
 // ---------------------------------------------------------------------------
 // Variant 0: 3-D conv -> activation -> (GroupNorm | InstanceNorm | none)
@@ -103,7 +105,7 @@ struct Mean3dArgs {
     int vec16;        // 1: 16-byte cp.async staging is legal
     int act, norm, G, affine;
     float eps, post_scale;
-    double *partial;  // [N][nchunks][Co][3]  (count, mean, M2)
+    double *partial;  // [N][nchunks][Co][3]  (count, mean, M2); the tensor-core kernel's float2 sums
     int *tickets;     // [N] per-sample tickets, then [2] work/exit counters; zero between launches
 };
 typedef void (*Mean3dKernel)(Mean3dArgs);
@@ -118,10 +120,14 @@ struct Mean3dConfig {
 // Chooses tiling + instantiation; fills the geometry fields of args.
 // Returns CN_OK or CN_ERR_UNSUPPORTED.
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+// Bytes of the partial-moment slots (the tensor-core kernel's float2 sums or
+// the CUDA-core kernel's fp64 (count, mean, M2)).
+size_t mean3d_partial_bytes(const Mean3dArgs &a);
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s,
                   const LaunchEvents *ev = nullptr);
+int mean3d_launches(const Mean3dConfig &cfg, const Mean3dArgs &a);  // kernels one forward launches
 
 // ---------------------------------------------------------------------------
 // Variant 1: 3-D conv -> channel softmax -> MaxPool3d(2,2) twice (= one

@@ -70,7 +70,7 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     if (st != CN_OK) return st;
     if (d->N == 0) return CN_OK;
     // the scratch this problem needs: moments, then tickets (256-byte aligned)
-    const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
+    const size_t part = cn::mean3d_partial_bytes(a);
     const size_t part_al = (part + 255) & ~(size_t)255;
     if (part_al + (size_t)(a.N + 2) * sizeof(int) > CN_NOALLOC_SCRATCH_BYTES)
         return CN_ERR_UNSUPPORTED;

@@ -482,8 +482,17 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     return CN_OK;
 }
 
+int mean3d_launches(const Mean3dConfig &cfg, const Mean3dArgs &a) {
+    if (a.N == 0) return 0;
+    return a.tc ? tc3_launches(cfg.tc3) : 1;
+}
+
+size_t mean3d_partial_bytes(const Mean3dArgs &a) {
+    return (size_t)a.N * a.nchunks * a.Co * (a.tc ? sizeof(float2) : 3 * sizeof(double));
+}
+
 size_t mean3d_workspace(const Mean3dArgs &a) {
-    const size_t part = (size_t)a.N * a.nchunks * a.Co * 3 * sizeof(double);
+    const size_t part = mean3d_partial_bytes(a);
     return ((part + 255) & ~(size_t)255) + (size_t)(a.N + 2) * sizeof(int);
 }
 
@@ -520,7 +529,7 @@ int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const 
         t.beta = a.beta;
         t.out = a.out;
         t.err = a.err;
-        t.partial = a.partial;
+        t.partial = reinterpret_cast<float2 *>(a.partial);
         t.tickets = a.tickets;
         t.work = a.tickets + a.N;
         return tc3_launch(cfg.tc3, t, s, ev);

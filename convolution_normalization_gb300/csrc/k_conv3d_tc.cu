@@ -54,9 +54,10 @@
 //               position:
 //     mean: a warp takes C_out / 4 channels of all ZG planes: the kx sum,
 //           bias + activation, per-channel shifted sums in registers; at the
-//           end of an item its per-channel moments, then the sample's
-//           ticket: the last item of a sample merges its items and writes
-//           the output (the CUDA-core mean kernel's finish);
+//           end of an item (one band) the sums are posted to warp 0, which
+//           writes them to the item's slot, takes the sample's ticket and,
+//           for the sample's last item, merges the slots and writes the
+//           output;
 //     pool: a warp takes the 16 channels of one plane zg: the kx sum, bias,
 //           softmax over the channels in registers, the max over the
 //           window's 4 columns (and rows inside the quadrant) by shuffles,
@@ -65,7 +66,6 @@
 //           the stage's pooled values are scaled and stored.
 #include "cn_common.cuh"
 #include "cn_internal.h"
-#include "cn_mean_common.cuh"
 #include "cn_tcgen05.cuh"
 
 #include <algorithm>
@@ -78,9 +78,9 @@ constexpr int kT3Threads = 640;    // 20 warps: 5 per SM sub-partition, up to 96
 constexpr int kConvWarps = 2;      // warps 2-3
 constexpr int kEpiWarp0 = 4;       // epilogue: warps 4-19
 constexpr int kEpiWarps = 16;
-constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kT3SmemLimit = 227 * 1024 - 1024;  // dynamic part (static barriers beside it)
 constexpr int kPoolCells = 8;      // pooled outputs per channel per stage: (RB / 4) (W / 4)
+constexpr int kPosts = 4;          // mean: item sums in flight from the epilogue to warp 0
 
 enum { MODE_MEAN = 0, MODE_POOL = 1 };
 
@@ -126,6 +126,62 @@ CN_DEV void tmem_ld_cols(uint32_t taddr, uint32_t *v) {
     if (R % 8 >= 4) tmem_ld4(taddr + B8 + (R >= 8 ? 8 : 0), v + B8 + (R >= 8 ? 8 : 0));
 }
 
+// Finish of one sample of the mean, by one warp (lane = channel).  Every slot of a
+// channel is a sum about the same shift K = act(bias), and every channel of
+// a sample has the same count n, so the statistics need no Chan-merge
+// divisions (slow on this GPU's narrow FP64 pipe): fp64 sums over the slots
+// in slot order, then with one reciprocal 1/n
+//   m_c = K + S1 / n,  M2_c = S2 - S1^2 / n,
+//   mu_g = mean of the group's m_c,  M2_g = sum (M2_c + n (m_c - mu_g)^2),
+// and out = gamma (m_c - mu_g) / sqrt(M2_g / (n C/G) + eps) + beta, times the
+// post scale.
+CN_DEV void tc3_finish_sample(const Tc3Args &a, int n, int c) {
+    const int nchunks = a.ngroups * a.nsplit;
+    const bool on = c < a.Co;
+    double S1 = 0.0, S2 = 0.0;
+    if (on) {
+        // eight slot loads in flight, added in slot order
+        const float2 *pc = a.partial + (size_t)n * nchunks * a.Co + c;
+        for (int ch0 = 0; ch0 < nchunks; ch0 += 8) {
+            float2 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)  // other CTAs' slots: not through L1
+                v[j] = ch0 + j < nchunks ? __ldcg(pc + (size_t)(ch0 + j) * a.Co) : make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                S1 += v[j].x;
+                S2 += v[j].y;
+            }
+        }
+    }
+    const double cnt = (double)a.Do * a.Ho * a.Wo;
+    const double inv_n = a.inv_cnt;  // 1 / cnt and 1 / cpg come from the host
+    const float kc = on ? apply_act(a.act, a.b ? __ldg(a.b + c) : 0.0f) : 0.0f;
+    const double mc = (double)kc + S1 * inv_n;
+    const double m2c = fmax(S2 - S1 * S1 * inv_n, 0.0);
+    double val = mc;
+    if (a.norm != CN_NORM_NONE) {
+        // the group's lanes: cpg consecutive channels (a power of two or not)
+        const int cpg = a.Co / a.G, g0 = (c / cpg) * cpg;
+        const double inv_cpg = a.inv_cpg;
+        double sm = 0.0;
+        for (int u = 0; u < cpg; ++u) sm += __shfl_sync(0xffffffffu, mc, g0 + u);
+        const double mu = sm * inv_cpg;
+        double m2 = 0.0;
+        for (int u = 0; u < cpg; ++u) {
+            const double mu_u = __shfl_sync(0xffffffffu, mc, g0 + u);
+            const double m2_u = __shfl_sync(0xffffffffu, m2c, g0 + u);
+            m2 += m2_u + cnt * (mu_u - mu) * (mu_u - mu);
+        }
+        const double var = m2 * inv_n * inv_cpg;
+        const float rstd = rsqrtf((float)(var + (double)a.eps));
+        const double ga = a.affine && on ? (double)a.gamma[c] : 1.0;
+        const double be = a.affine && on ? (double)a.beta[c] : 0.0;
+        val = ga * (mc - mu) * (double)rstd + be;
+    }
+    if (on) a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
+}
+
 template <int K, int CO, int MODE>
 CN_DEV void tc3_body(const Tc3Args &a) {
     using P = T3<K, CO>;
@@ -137,8 +193,11 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
     // stage info: (item or -1 to stop, band, 1 if the item's last band, valid planes)
     __shared__ int4 s_land_info[2], s_st_info[2], s_acc_info[2];
+    // mean: item sums posted by the epilogue to warp 0 (ring of kPosts)
+    __shared__ __align__(8) uint64_t post_full[kPosts], post_empty[kPosts];
+    __shared__ float2 s_post[kPosts][32];
+    __shared__ int s_post_item[kPosts];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_last;
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -150,8 +209,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     auto land = [&](int lb) { return land0 + (size_t)lb * land_stride; };
     unsigned char *wts = land0 + (size_t)a.nland * land_stride;
     float *halo = reinterpret_cast<float *>(wts + P::WBYTES);
-    float *red = halo + (a.halo ? P::HALO : 0);
-    double *sch = reinterpret_cast<double *>(red + P::RED);  // [CO][3]
+    float *red = halo + (a.halo ? P::HALO : 0);  // mean [quadrant][CO][2] / pool cells
     const int rows_in = a.rb + K - 1;
     const int P0 = rows_in * a.W;  // staged positions per plane
 
@@ -213,6 +271,10 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             mbar_init(&acc_full[i], 2);
             mbar_init(&acc_empty[i], kEpiWarps);
         }
+        for (int i = 0; i < kPosts; ++i) {
+            mbar_init(&post_full[i], 1);
+            mbar_init(&post_empty[i], 1);
+        }
         mbar_init(&fin_bar, 1);
         s_abort = 0;
         fence_barrier_init();
@@ -232,45 +294,121 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     auto wait = [&](uint64_t *bar, uint32_t par) { return tc_wait(bar, par, abort_p, a.err); };
 
     if (warp == 0) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            int k = 0;       // stages armed so far; stage k lands in buffer lb = k % nland
-            int lb = 0;
-            uint32_t lph = 0;  // parity of the current pass over the landing buffers
-            int next = (int)blockIdx.x;
-            bool live = true;
-            while (live) {
-                const int item = next < a.items ? next : -1;
-                if (item >= 0) next = (int)gridDim.x + atomicAdd(a.work, 1);
-                int n = 0, g = 0, z0 = 0, nzv = 0;
-                if (item >= 0) item_group(item, n, g, z0, nzv);
-                // bands of this item (a stop marker is one stage)
-                const int b0 = item < 0 ? 0 : (item % a.nsplit) * bpi;
-                const int nb = item < 0 ? 1 : min(bpi, a.nband - b0);
-                for (int band = b0; band < b0 + nb; ++band) {
-                    if (k >= a.nland && !wait(&land_empty[lb], lph ^ 1u)) {
-                        live = false;
-                        break;
+        // ---------------- producer (+ mean finisher) ----------------
+        // Lane 0 arms the stages' TMA copies.  For the mean the whole warp
+        // also takes the items the epilogue posts: it publishes the item's
+        // sums to its global slot, takes the sample's ticket, and on the
+        // sample's last item merges the slots and writes the output.  Both
+        // are polled, so the work of a merge only delays copies that are
+        // already up to two stages ahead, and never the epilogue.
+        int k = 0, lb = 0;           // stages armed; stage k lands in buffer lb = k % nland
+        uint32_t lph = 0;            // parity of the current pass over the landing buffers
+        int next = (int)blockIdx.x;  // lane 0: the next item to claim
+        int item = 0, band = 0, bend = 0, n = 0, g = 0, z0 = 0, nzv = 0;  // lane 0: current item
+        bool prod_live = true, fin_live = MODE == MODE_MEAN;
+        int pr = 0;
+        uint32_t pph = 0;
+        uint64_t t_idle = 0;
+        for (uint32_t it = 0; prod_live || fin_live; ++it) {
+            bool progress = false;
+            if (prod_live) {
+                bool ready = k < a.nland || mbar_test_wait(&land_empty[lb], lph ^ 1u);
+                ready = __shfl_sync(0xffffffffu, ready, 0);
+                if (ready) {
+                    int stop = 0;
+                    if (lane == 0) {
+                        if (band == bend) {  // claim the next item (a stop marker is one stage)
+                            item = next < a.items ? next : -1;
+                            if (item >= 0) {
+                                next = (int)gridDim.x + atomicAdd(a.work, 1);
+                                item_group(item, n, g, z0, nzv);
+                                band = (item % a.nsplit) * bpi;
+                                bend = min(band + bpi, a.nband);
+                            } else {
+                                band = 0;
+                                bend = 1;
+                            }
+                        }
+                        s_land_info[lb] = make_int4(item, band, band == bend - 1, nzv);
+                        if (item >= 0) {
+                            mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.land);
+                            tma_load_4d(land(lb), &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full[lb]);
+                        } else {
+                            mbar_arrive(&land_full[lb]);
+                            stop = 1;
+                        }
+                        ++band;
                     }
-                    s_land_info[lb] = make_int4(item, band, band == b0 + nb - 1, nzv);
-                    if (item >= 0) {
-                        mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.land);
-                        tma_load_4d(land(lb), &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full[lb]);
-                    } else {
-                        mbar_arrive(&land_full[lb]);
-                    }
+                    if (__shfl_sync(0xffffffffu, stop, 0)) prod_live = false;
                     ++k;
                     if (++lb == a.nland) {
                         lb = 0;
                         lph ^= 1u;
                     }
+                    progress = true;
                 }
-                if (item < 0) live = false;
             }
-            // a copy still in flight (only after an abort) lands before the CTA exits
+            if (MODE == MODE_MEAN && fin_live) {
+                bool got = mbar_test_wait(&post_full[pr], pph);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (got) {
+                    const int pitem = s_post_item[pr];
+                    if (pitem < 0) {
+                        fin_live = false;  // the epilogue is done
+                    } else {
+                        const int grp = pitem / a.nsplit;
+                        const int pn = grp / a.ngroups, pg = grp - pn * a.ngroups;
+                        const int nchunks = a.ngroups * a.nsplit;
+                        const int chunk = pg * a.nsplit + pitem % a.nsplit;
+                        if (lane < CO) {
+                            a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = s_post[pr][lane];
+                            __threadfence();  // the slot is visible before the ticket below
+                        }
+                        __syncwarp();
+                        int last = 0;
+                        if (lane == 0) last = atomicAdd(a.tickets + pn, 1) == nchunks - 1;
+                        if (__shfl_sync(0xffffffffu, last, 0)) {
+                            __threadfence();  // the other items' slots, published before their tickets
+                            tc3_finish_sample(a, pn, lane);
+                            if (lane == 0) a.tickets[pn] = 0;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&post_empty[pr]);
+                    if (++pr == kPosts) {
+                        pr = 0;
+                        pph ^= 1u;
+                    }
+                    progress = true;
+                }
+            }
+            // bounded idling: stop at another role's abort or after the wait limit
+            if (progress) {
+                t_idle = 0;
+            } else {
+                __nanosleep(64);  // leave the issue slots to this sub-partition's epilogue warps
+            }
+            if (!progress && (it & 255u) == 255u) {
+                int quit = 0;
+                if (lane == 0) {
+                    const uint64_t now = globaltimer_ns();
+                    if (*abort_p) {
+                        quit = 1;
+                    } else if (t_idle == 0) {
+                        t_idle = now;
+                    } else if (now - t_idle > kWaitLimitNs) {
+                        flag_error(a.err, ERR_TIMEOUT);
+                        *abort_p = 1;
+                        quit = 1;
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, quit, 0)) break;
+            }
+        }
+        // a copy still in flight (only after an abort) lands before the CTA exits
+        if (lane == 0)
             for (int j = max(0, k - a.nland); j < k; ++j)
                 mbar_wait_bounded(&land_full[j % a.nland], (j / a.nland) & 1, kWaitLimitNs);
-        }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -371,7 +509,6 @@ CN_DEV void tc3_body(const Tc3Args &a) {
         constexpr int CQ = CO / 4, NC = CQ * K;  // a warp's channels; its columns of one plane
         const int q = warp & 3;                 // TMEM lane quadrant this warp may read
         const int h = (warp - kEpiWarp0) >> 2;  // channel quarter
-        const int et = tid - 32 * kEpiWarp0;
         const int r = 32 * q + lane;  // tile row: this thread's position in the band
         const int ry = (int)__umulhi((uint32_t)r, a.wmagic);
         const int rx = r - ry * a.W;
@@ -383,6 +520,9 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             s1[c] = 0.0f;
             s2[c] = 0.0f;
         }
+        int pr = 0, pk = 0;  // post ring (warp kEpiWarp0): slot, posts made
+        uint32_t pph = 0;
+        bool post_ok = true, stop_seen = false;
         for (int k = 0;; ++k) {
             const int b = k & 1;
             const bool got = wait(&acc_full[b], (k >> 1) & 1);
@@ -406,9 +546,13 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                     }
                 }
             }
-            // every epilogue warp got the stage (else all stop), and the halo is written
-            if (!epi_all(got)) break;
-            if (info.x < 0) break;
+            // every epilogue warp got the stage and could post (else all
+            // stop), and the halo is written
+            if (!epi_all(got && post_ok)) break;
+            if (info.x < 0) {
+                stop_seen = true;
+                break;
+            }
             tc_fence_after();
             const bool pos_ok = r < a.rb * a.W && info.y * a.rb + ry < a.Ho && rx < a.Wo;
             const float *hq = hb + (size_t)(min(q + 1, 3) * (K - 1)) * N;
@@ -442,15 +586,8 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             if (lane == 0) mbar_arrive(&acc_empty[b]);
             if (!info.z) continue;
 
-            // ---- end of the item: its per-channel moments, then the ticket ----
-            int n, g, z0, nzv;
-            item_group(info.x, n, g, z0, nzv);
-            // the item's slot among the sample's nchunks = ngroups * nsplit,
-            // and its output rows (its bands')
-            const int nchunks = a.ngroups * a.nsplit;
-            const int sp = info.x % a.nsplit;
-            const int chunk = g * a.nsplit + sp;
-            const int rows = min(bpi * a.rb, a.Ho - sp * bpi * a.rb);
+            // ---- end of the item: its per-channel shifted sums ----
+
 #pragma unroll
             for (int c = 0; c < CQ; ++c) {
 #pragma unroll
@@ -472,35 +609,39 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 s2[c] = 0.0f;
             }
             epi_sync();
-            if (et < CO) {
-                float S1 = 0.0f, S2 = 0.0f;
-                for (int qq = 0; qq < 4; ++qq) {  // fixed quadrant order
-                    S1 += red[(qq * CO + et) * 2 + 0];
-                    S2 += red[(qq * CO + et) * 2 + 1];
+            // one warp posts the item's per-channel sums to warp 0 (which
+            // publishes them and finishes the sample): the epilogue never
+            // waits on global memory
+            if (warp == kEpiWarp0) {
+                post_ok = pk < kPosts || wait(&post_empty[pr], pph ^ 1u);
+                if (post_ok) {
+                    if (lane < CO) {
+                        float S1 = 0.0f, S2 = 0.0f;
+                        for (int qq = 0; qq < 4; ++qq) {  // fixed quadrant order
+                            S1 += red[(qq * CO + lane) * 2 + 0];
+                            S2 += red[(qq * CO + lane) * 2 + 1];
+                        }
+                        s_post[pr][lane] = make_float2(S1, S2);
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        s_post_item[pr] = info.x;
+                        mbar_arrive(&post_full[pr]);
+                    }
+                    ++pk;
+                    if (++pr == kPosts) {
+                        pr = 0;
+                        pph ^= 1u;
+                    }
                 }
-                const float kc = apply_act(a.act, a.b ? __ldg(a.b + et) : 0.0f);
-                const Moments<double> m =
-                    moments_from_sums((double)nzv * rows * a.Wo, (double)kc, (double)S1, (double)S2);
-                double *pp = a.partial + (((size_t)n * nchunks + chunk) * a.Co + et) * 3;
-                pp[0] = m.n;
-                pp[1] = m.mean;
-                pp[2] = m.m2;
-                __threadfence();  // the slot is visible before the ticket below
             }
-            epi_sync();
-            if (et == 0) s_last = (atomicAdd(a.tickets + n, 1) == nchunks - 1);
-            epi_sync();
-            if (s_last) {
-                for (int c = et; c < a.Co; c += kEpiThreads) {
-                    __threadfence();  // the other items' slots, published before their tickets
-                    const Moments<double> m = mean_chunks_merged(a, nchunks, n, c);
-                    sch[c * 3 + 0] = m.n;
-                    sch[c * 3 + 1] = m.mean;
-                    sch[c * 3 + 2] = m.m2;
-                }
-                epi_sync();
-                for (int c = et; c < a.Co; c += kEpiThreads) mean_write_output(a, n, c, sch);
-                if (et == 0) a.tickets[n] = 0;
+            // red is rewritten only after the next stage's barriers
+        }
+        // the stop marker reaches warp 0 too
+        if (warp == kEpiWarp0 && stop_seen && (pk < kPosts || wait(&post_empty[pr], pph ^ 1u))) {
+            if (lane == 0) {
+                s_post_item[pr] = -1;
+                mbar_arrive(&post_full[pr]);
             }
         }
     } else {
@@ -646,7 +787,7 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     if (mode == MODE_POOL && 32 % d.W != 0) return CN_ERR_UNSUPPORTED;
     const char *e = getenv("CN_NO_TC");
     if (e && atoi(e)) return CN_ERR_UNSUPPORTED;
-    const int K = d.k, CO = d.C_out, ZG = inst->ZG, NU = ZG + K - 1;
+    const int K = d.k, ZG = inst->ZG, NU = ZG + K - 1;
     const int Do = d.D - K + 1, Ho = d.H - K + 1, Wo = d.W - K + 1;
     if (Do < 1 || Ho < 1 || Wo < 1) return CN_ERR_UNSUPPORTED;
     const int Pd = Do / 4, Ph = Ho / 4, Pw = Wo / 4;
@@ -662,24 +803,22 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     const int halo = mode == MODE_MEAN && (32 % d.W) != 0;
     // two landing buffers (the next stage's copy in flight while this one is
     // converted) when they fit, else one
-    const int fixed = 2 * stage_bytes + inst->WBYTES + (halo ? inst->HALO * 4 : 0) + inst->RED * 4 +
-                      CO * 3 * 8;
+    const int fixed = 2 * stage_bytes + inst->WBYTES + (halo ? inst->HALO * 4 : 0) + inst->RED * 4;
     int nland = 2;
     while (nland > 1 && fixed + nland * ((land + 127) & ~127) > kT3SmemLimit) --nland;
     const int smem = fixed + nland * ((land + 127) & ~127);
     if (smem > kT3SmemLimit) return CN_ERR_UNSUPPORTED;
-    // one item = some bands of one group of ZG output planes of one sample:
-    // one band for the pool (no state across bands: finest load balance);
-    // all of the group's bands for the mean, whose item end (moments, ticket,
-    // and for a sample's last item the fp64 merge) is serial latency in the
-    // epilogue (splitting n512's items into 4 measured 0.49 vs 0.39 ms).  A
-    // function of the sample's shape only, so a sample's result (its items'
-    // merge order) does not depend on the batch it is part of.  The pool
-    // needs only the planes and rows its windows cover.
+    // one item = some bands of one group of ZG output planes of one sample
+    // (the mean keeps one partial-sum slot per item).  A function of the
+    // sample's shape only, so a sample's result (its items' merge order) does
+    // not depend on the batch it is part of.  The pool needs only the planes
+    // and rows its windows cover.
     const int ngroups = mode == MODE_MEAN ? (Do + ZG - 1) / ZG : Pd;
     const int rows = mode == MODE_MEAN ? Ho : 4 * Ph;
     const int nband = (rows + rb - 1) / rb;
-    const int bpi = mode == MODE_POOL ? 1 : nband;  // bands per item
+    // pool: one band per item; mean: about a quarter of the group's bands
+    // (warp 0 publishes each mean item with a fence and a ticket, ~3 us)
+    const int bpi = mode == MODE_POOL ? 1 : std::max(1, nband / 4);
     const int nsplit = (nband + bpi - 1) / bpi;
     const long long items = (long long)d.N * ngroups * nsplit;
     if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
@@ -716,6 +855,8 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     a.Pd = Pd;
     a.Ph = Ph;
     a.Pw = Pw;
+    a.inv_cnt = 1.0 / ((double)Do * Ho * Wo);
+    a.inv_cpg = 1.0 / (double)(d.C_out / a.G);
     cfg.kern = inst->fn;
     cfg.name = inst->name;
     cfg.threads = kT3Threads;
@@ -760,5 +901,7 @@ int tc3_launch(const Tc3Config &cfg, Tc3Args &a, cudaStream_t s, const LaunchEve
     record_launch(ev, 1, s);
     return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
 }
+
+int tc3_launches(const Tc3Config &cfg) { return cfg.grid == 0 ? 0 : 1; }
 
 }  // namespace cn
