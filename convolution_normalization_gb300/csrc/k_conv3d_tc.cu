@@ -84,6 +84,15 @@ constexpr int kPosts = 4;          // mean: item sums in flight from the epilogu
 
 enum { MODE_MEAN = 0, MODE_POOL = 1 };
 
+// Ticket increment with acquire-release semantics at GPU scope: it publishes
+// the writes the calling thread has observed (the warp's, after __syncwarp)
+// and orders its later reads after the other CTAs' published writes.
+CN_DEV int atomic_add_acq_rel(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 template <int K, int CO>
 struct T3 {
     static constexpr int ZG = CO * K * 4 <= 256 ? 4 : 2;  // output planes per stage
@@ -140,18 +149,27 @@ CN_DEV void tc3_finish_sample(const Tc3Args &a, int n, int c) {
     const bool on = c < a.Co;
     double S1 = 0.0, S2 = 0.0;
     if (on) {
-        // eight slot loads in flight, added in slot order
+        // sixteen slot loads in flight (other CTAs' slots: not through L1),
+        // summed pairwise in a fixed tree, blocks of 16 in slot order
         const float2 *pc = a.partial + (size_t)n * nchunks * a.Co + c;
-        for (int ch0 = 0; ch0 < nchunks; ch0 += 8) {
-            float2 v[8];
+        for (int ch0 = 0; ch0 < nchunks; ch0 += 16) {
+            double v1[16], v2[16];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)  // other CTAs' slots: not through L1
-                v[j] = ch0 + j < nchunks ? __ldcg(pc + (size_t)(ch0 + j) * a.Co) : make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                S1 += v[j].x;
-                S2 += v[j].y;
+            for (int j = 0; j < 16; ++j) {
+                const float2 v = ch0 + j < nchunks ? __ldcg(pc + (size_t)(ch0 + j) * a.Co)
+                                                   : make_float2(0.f, 0.f);
+                v1[j] = v.x;
+                v2[j] = v.y;
             }
+#pragma unroll
+            for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) {
+                    v1[j] += v1[j + w];
+                    v2[j] += v2[j + w];
+                }
+            S1 += v1[0];
+            S2 += v2[0];
         }
     }
     const double cnt = (double)a.Do * a.Ho * a.Wo;
@@ -360,21 +378,20 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         const int pn = grp / a.ngroups, pg = grp - pn * a.ngroups;
                         const int nchunks = a.ngroups * a.nsplit;
                         const int chunk = pg * a.nsplit + pitem % a.nsplit;
-                        if (lane < CO) {
-                            a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = s_post[pr][lane];
-                            __threadfence();  // the slot is visible before the ticket below
-                        }
+                        const float2 sums = lane < CO ? s_post[pr][lane] : make_float2(0.f, 0.f);
                         __syncwarp();
+                        if (lane == 0) mbar_arrive(&post_empty[pr]);  // the ring entry is read
+                        if (lane < CO) a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = sums;
+                        __syncwarp();
+                        // the ticket publishes the warp's slot writes; the last
+                        // item of the sample sees every other item's slot
                         int last = 0;
-                        if (lane == 0) last = atomicAdd(a.tickets + pn, 1) == nchunks - 1;
+                        if (lane == 0) last = atomic_add_acq_rel(a.tickets + pn, 1) == nchunks - 1;
                         if (__shfl_sync(0xffffffffu, last, 0)) {
-                            __threadfence();  // the other items' slots, published before their tickets
                             tc3_finish_sample(a, pn, lane);
                             if (lane == 0) a.tickets[pn] = 0;
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&post_empty[pr]);
                     if (++pr == kPosts) {
                         pr = 0;
                         pph ^= 1u;
