@@ -429,7 +429,6 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            const uint32_t idesc = idesc_tf32(128, N);
             const uint32_t wbase = smem_u32(wts);
             const uint32_t zaddr = wbase + K * 2 * P::SLEN;
             // descriptors are linear in the start address (units of 16 bytes)
@@ -452,15 +451,42 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 const uint32_t sb = smem_u32(stage(b));
                 const uint64_t ac0 = umma_desc(sb, xl_off, 128);                // [Xh | Xl]
                 const uint64_t ap0 = umma_desc(sb, (uint32_t)(a.W * 16), 128);  // [Xh(ky) | Xh(ky+1)]
+                // Input plane u feeds output planes zg in [zlo, zhi] (taps
+                // kz = u - zg in [0, k)): its MMAs cover only those columns
+                // (N = their count x C_out x k, D moved to zlo's first column,
+                // B's window moved past the zero blocks).  A plane's columns
+                // are first written at u = zg, by a cross MMA of its own that
+                // does not accumulate.  Only where a plane's columns are a
+                // multiple of 32 (the TMEM allocation granule), so every D
+                // starts on one; otherwise every MMA spans all ZG planes.
+                constexpr int NZ = CO * K;  // columns of one output plane
+                constexpr bool NARROW = NZ % 32 == 0;
 #pragma unroll
                 for (int u = 0; u < NU; ++u) {
+                    const int zlo = NARROW ? (u - (K - 1) > 0 ? u - (K - 1) : 0) : 0;
+                    const int zhi = NARROW ? (u < ZG - 1 ? u : ZG - 1) : ZG - 1;
+                    const bool fresh = NARROW ? u < ZG : u == 0;  // plane zg = u starts here
+                    const uint32_t id_all = idesc_tf32(128, (zhi - zlo + 1) * NZ);
+                    const uint32_t id_one = idesc_tf32(128, NZ);
+                    const uint32_t id_old = idesc_tf32(128, (u - zlo > 0 ? u - zlo : 1) * NZ);
                     const uint64_t au = (uint64_t)(u * PP);
-                    const int blk = K + ZG - 2 - u;  // window start in the kz sequences
+                    const int blk = K + ZG - 2 - u + zlo;  // first valid block of the kz sequences
+                    const uint32_t dz = d + (uint32_t)(zlo * NZ);
 #pragma unroll
-                    for (int ky = 0; ky < K; ++ky)
-                        umma_tf32(d, ac0 + au + (uint64_t)(ky * a.W),
-                                  bc0 + (uint64_t)((ky * 2 * P::SLEN + blk * P::BLK) >> 4), idesc,
-                                  (u | ky) ? 1u : 0u);
+                    for (int ky = 0; ky < K; ++ky) {
+                        const uint64_t ad = ac0 + au + (uint64_t)(ky * a.W);
+                        const uint64_t bd = bc0 + (uint64_t)((ky * 2 * P::SLEN + blk * P::BLK) >> 4);
+                        if (ky == 0 && fresh && !NARROW) {
+                            umma_tf32(dz, ad, bd, id_all, 0u);  // u = 0 initialises every plane
+                        } else if (ky == 0 && fresh) {
+                            // the new plane u alone (its B rows: u - zlo blocks on), then the others
+                            umma_tf32(d + (uint32_t)(u * NZ), ad,
+                                      bd + (uint64_t)(((u - zlo) * P::BLK) >> 4), id_one, 0u);
+                            if (u > zlo) umma_tf32(dz, ad, bd, id_old, 1u);
+                        } else {
+                            umma_tf32(dz, ad, bd, id_all, 1u);
+                        }
+                    }
 #pragma unroll
                     for (int j = 0; j < P::NPAIR; ++j) {
                         const int ky = 2 * j;
@@ -471,7 +497,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                             const uint32_t ad = wbase + (uint32_t)((ky * 2 + 1) * P::SLEN + blk * P::BLK);
                             bd = umma_desc(ad, zaddr - ad, 128);
                         }
-                        umma_tf32(d, ap0 + au + (uint64_t)(ky * a.W), bd, idesc, 1u);
+                        umma_tf32(dz, ap0 + au + (uint64_t)(ky * a.W), bd, id_all, 1u);
                     }
                 }
                 umma_commit(&st_empty[b]);
