@@ -26,8 +26,10 @@
 // feeds.  For input plane u the filter operand rows (zg, co, kx) hold taps
 // kz = u - zg: consecutive blocks of one sequence stored with kz descending
 // and zero blocks at both ends, so B for every u is a window of that
-// sequence (no copies per u).  With ZG = 4 a plane group and a band of
-// 4 * (32 / W) rows are exactly whole 4x4x4 pooling windows.
+// sequence (no copies per u).  Where a plane's columns are a multiple of
+// 32, an input plane's MMAs span only the planes it feeds (narrower N).
+// With ZG = 4 a plane group and a band of 4 * (32 / W) rows are exactly
+// whole 4x4x4 pooling windows.
 //
 // Precision: split TF32 as in the 2-D tensor-core kernel (the tensor cores
 // read tf32 by dropping 13 mantissa bits; with v = hi + lo,
@@ -35,18 +37,20 @@
 // ~1e-6 relative.  Per (u, ky) one MMA takes both cross terms (A = [Xh |
 // Xl], B = [Wl | Wh]); the hi*hi terms pair two ky taps per MMA (A = Xh at
 // rows ky and ky + 1, B = [Wh(ky) | Wh(ky + 1)]; an odd k pairs its last tap
-// with a zero filter block).  MMAs per stage: (ZG + k - 1) (k + ceil(k/2)).
+// with a zero filter block).  MMAs per stage: (ZG + k - 1) (k + ceil(k/2)),
+// plus one per newly started plane where the MMAs are narrowed.
 //
 // Operands (K-major, no swizzle): a staged input plane is [position][4
 // channels] fp32, hi part then lo part; a K step of 8 is two 4-channel core
 // matrices, 16 bytes a row.  Tap offsets move the start address only.
 //
-// Warp roles (one persistent CTA per SM, items claimed from a counter: for
-// the mean (sample, group of ZG output planes) with all its bands, for the
-// pool (sample, group, band)):
+// Warp roles (one persistent CTA per SM, items claimed from a counter: an
+// item is some bands of one group of ZG output planes of one sample; a
+// quarter of the group's bands for the mean, one band for the pool):
 //   warp 0      producer: one TMA tensor copy per stage (W x (RB + k - 1)
 //               rows x (ZG + k - 1) planes x C_in, zero fill outside x) into
-//               one of two landing buffers (one where two do not fit);
+//               one of two landing buffers (one where two do not fit); for
+//               the mean also the finisher below;
 //   warps 2-3   converters: landing [c][u][row][x] -> operand stage hi / lo;
 //   warp 1      MMA issuer (one thread): the stage's MMAs into one of two
 //               TMEM accumulators;
@@ -54,10 +58,10 @@
 //               position:
 //     mean: a warp takes C_out / 4 channels of all ZG planes: the kx sum,
 //           bias + activation, per-channel shifted sums in registers; at the
-//           end of an item (one band) the sums are posted to warp 0, which
-//           writes them to the item's slot, takes the sample's ticket and,
-//           for the sample's last item, merges the slots and writes the
-//           output;
+//           end of an item the sums are posted through a shared-memory ring
+//           to warp 0, which writes them to the item's slot, takes the
+//           sample's ticket and, for the sample's last item, merges the
+//           slots and writes the output;
 //     pool: a warp takes the 16 channels of one plane zg: the kx sum, bias,
 //           softmax over the channels in registers, the max over the
 //           window's 4 columns (and rows inside the quadrant) by shuffles,
