@@ -246,16 +246,16 @@ CN_DEV void tc3_body(const Tc3Args &a) {
         nzv = min(ZG, a.Do - z0);
     };
 
-    // ---- setup: zero the operand tails, filter sequences, barriers, TMEM ----
-    for (int b = 0; b < 2; ++b) {
-        float4 *xs = reinterpret_cast<float4 *>(stage(b));
-        const int tail = PP - P0;
-        for (int i = tid; i < 2 * NU * tail; i += blockDim.x) {
-            const int pl = i / tail, r = i - pl * tail;
-            xs[(size_t)pl * PP + P0 + r] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
+    // ---- setup: filter sequences, zeroed operand tails, barriers, TMEM ----
     {
+        // the raw filter (C_out x C_in x k^3 floats) lands in the stage
+        // buffers with coalesced loads (they are free until the first stage),
+        // and the blocks are built from there: no dependent global loads
+        float *wraw = reinterpret_cast<float *>(stages);
+        const int nraw = CO * a.Ci * K * K * K;
+#pragma unroll 4
+        for (int e = tid; e < nraw; e += blockDim.x) wraw[e] = __ldg(a.w + e);
+        __syncthreads();
         // [ky][lo | hi][block i: kz = K + ZG - 2 - i][(co, kx) rows][4 channels], zero block
         float *wf = reinterpret_cast<float *>(wts);
         constexpr int ROWS = CO * K;
@@ -273,7 +273,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 const int kz = K + ZG - 2 - i;
                 const int co = row / K, kx = row - co * K;
                 if (c < a.Ci && kz >= 0 && kz < K) {
-                    const float x = __ldg(a.w + ((((size_t)co * a.Ci + c) * K + kz) * K + ky) * K + kx);
+                    const float x = wraw[((((size_t)co * a.Ci + c) * K + kz) * K + ky) * K + kx];
                     v = hi ? x : tf32_rest(x);
                 }
             }
@@ -281,6 +281,15 @@ CN_DEV void tc3_body(const Tc3Args &a) {
         }
         if (MODE == MODE_POOL)
             for (int e = tid; e < P::RED; e += blockDim.x) red[e] = 0.0f;  // pool cells
+        __syncthreads();  // the raw filter is read before the tails below are zeroed
+        for (int b = 0; b < 2; ++b) {
+            float4 *xs = reinterpret_cast<float4 *>(stage(b));
+            const int tail = PP - P0;
+            for (int i = tid; i < 2 * NU * tail; i += blockDim.x) {
+                const int pl = i / tail, r = i - pl * tail;
+                xs[(size_t)pl * PP + P0 + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
     }
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -525,16 +534,29 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 const float *src = reinterpret_cast<const float *>(land(lb));
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
                 float4 *xl = xh + (size_t)NU * PP;
+                constexpr int CT = 32 * kConvWarps;  // converter threads
 #pragma unroll 1
                 for (int u = 0; u < NU; ++u) {
                     const float *su = src + (size_t)u * P0;
-                    for (int p = ct; p < P0; p += 32 * kConvWarps) {
-                        float v[4];
+                    // four positions per thread per pass, their loads in flight together
+                    for (int p0 = ct; p0 < P0; p0 += 4 * CT) {
+                        float v[4][4];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) v[c] = c < a.Ci ? su[(size_t)c * NU * P0 + p] : 0.0f;
-                        xh[(size_t)u * PP + p] = make_float4(v[0], v[1], v[2], v[3]);
-                        xl[(size_t)u * PP + p] = make_float4(tf32_rest(v[0]), tf32_rest(v[1]),
-                                                             tf32_rest(v[2]), tf32_rest(v[3]));
+                        for (int j = 0; j < 4; ++j)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                v[j][c] = (c < a.Ci && p0 + j * CT < P0)
+                                              ? su[(size_t)c * NU * P0 + p0 + j * CT] : 0.0f;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int p = p0 + j * CT;
+                            if (p < P0) {
+                                xh[(size_t)u * PP + p] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
+                                xl[(size_t)u * PP + p] =
+                                    make_float4(tf32_rest(v[j][0]), tf32_rest(v[j][1]),
+                                                tf32_rest(v[j][2]), tf32_rest(v[j][3]));
+                            }
+                        }
                     }
                 }
                 fence_proxy_async();
@@ -846,6 +868,8 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     const int far = 127 + (K - 1 + (K & 1)) * d.W;
     const int pp = (std::max(rows_in * d.W, far + 1) + 7) & ~7;
     const int stage_bytes = 2 * NU * pp * 16;
+    // the raw filter passes through the two stage buffers at setup
+    if ((long long)d.C_out * d.C_in * K * K * K * 4 > 2LL * stage_bytes) return CN_ERR_UNSUPPORTED;
     const int land = d.C_in * NU * rows_in * d.W * 4;
     const int halo = mode == MODE_MEAN && (32 % d.W) != 0;
     // two landing buffers (the next stage's copy in flight while this one is
