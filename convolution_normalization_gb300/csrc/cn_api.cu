@@ -21,15 +21,19 @@ constexpr int kMaxHostChunks = 8;
 // Device staging for conv_norm_forward_host, created on its first call:
 // buffers, per-chunk plans, and the upload / download streams and events
 // that overlap chunk i+1's upload (and chunk i-1's download) with chunk i's
-// kernels.
+// kernels.  Odd chunks compute on a second stream: chunks share no device
+// data (each sub-plan owns its workspace), so chunk i+1's CTAs can take the
+// SMs that chunk i's last work items leave idle instead of waiting for the
+// whole launch to drain.
 struct HostStage {
     float *x = nullptr, *w = nullptr, *b = nullptr, *gamma = nullptr, *beta = nullptr,
           *out = nullptr;
     bool ready = false;
     int nchunk = 1, chunk_n = 0;
     conv_norm_plan_s *sub[kMaxHostChunks] = {};  // one plan per chunk (keeps its tensor map)
-    cudaStream_t up = nullptr, down = nullptr;
+    cudaStream_t up = nullptr, down = nullptr, comp2 = nullptr;
     cudaEvent_t ev_up[kMaxHostChunks] = {}, ev_done[kMaxHostChunks] = {};
+    cudaEvent_t ev_comp2 = nullptr;  // the caller's stream waits for comp2's chunks
 };
 
 }  // namespace
@@ -290,6 +294,8 @@ void conv_norm_plan_destroy(conv_norm_plan p) {
     for (int i = 0; i < kMaxHostChunks; ++i) conv_norm_plan_destroy(p->stage.sub[i]);
     if (p->stage.up) cudaStreamDestroy(p->stage.up);
     if (p->stage.down) cudaStreamDestroy(p->stage.down);
+    if (p->stage.comp2) cudaStreamDestroy(p->stage.comp2);
+    if (p->stage.ev_comp2) cudaEventDestroy(p->stage.ev_comp2);
     for (int i = 0; i < kMaxHostChunks; ++i) {
         if (p->stage.ev_up[i]) cudaEventDestroy(p->stage.ev_up[i]);
         if (p->stage.ev_done[i]) cudaEventDestroy(p->stage.ev_done[i]);
@@ -441,12 +447,13 @@ static int host_stage_setup(conv_norm_plan p) {
     if (st == CN_OK) st = stage_alloc(&hs.out, p->out_numel);
     if (st != CN_OK) return st;
     const int64_t xs = p->x_numel / d.N, os = p->out_numel / d.N;
-    // Measured on GB300 (host copies ~200 GB/s each way): 2 chunks when the
-    // output is small next to the input (only the first chunk's upload stays
-    // exposed), 4 when a large output download can overlap the kernels;
-    // more chunks cost more in per-chunk overhead than they hide.
-    const double xbytes = (double)p->x_numel * 4, obytes = (double)p->out_numel * 4;
-    int nch = xbytes < 16.0 * 1024 * 1024 ? 1 : (obytes > 0.25 * xbytes ? 4 : 2);
+    // Measured on GB300 (host copies ~210 GB/s up, ~190 down, ~330 both
+    // ways at once): about 6 MB of input per chunk, at most 8.  Only the
+    // first chunk's upload and the last chunk's kernels and download stay
+    // exposed, and with two compute streams a chunk's launch ramp overlaps
+    // the previous chunk's tail; at 25 MB of input 4 chunks beat 2 and 8.
+    const double xbytes = (double)p->x_numel * 4;
+    int nch = xbytes < 16.0 * 1024 * 1024 ? 1 : std::min(kMaxHostChunks, (int)(xbytes / 6.0e6));
     if (const char *e = getenv("CN_HOST_CHUNKS")) nch = std::max(1, std::min(kMaxHostChunks, atoi(e)));
     if (xs % 4 != 0 || os % 4 != 0) nch = 1;
     nch = std::min(nch, d.N);
@@ -459,7 +466,9 @@ static int host_stage_setup(conv_norm_plan p) {
             if ((st = conv_norm_plan_create(&dc, &hs.sub[i])) != CN_OK) return st;
         }
         if (cudaStreamCreateWithFlags(&hs.up, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking) != cudaSuccess)
+            cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&hs.comp2, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hs.ev_comp2, cudaEventDisableTiming) != cudaSuccess)
             return CN_ERR_CUDA;
         for (int i = 0; i < hs.nchunk; ++i)
             if (cudaEventCreateWithFlags(&hs.ev_up[i], cudaEventDisableTiming) != cudaSuccess ||
@@ -489,11 +498,15 @@ int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, con
     HostStage &hs = p->stage;
     int st = hs.ready ? CN_OK : host_stage_setup(p);
     bool ok = st == CN_OK;
-    ok = ok && cudaMemcpyAsync(hs.w, w, p->w_numel * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
-    if (b) ok = ok && cudaMemcpyAsync(hs.b, b, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    // The parameters go first on the stream that carries x: queued on a
+    // compute stream instead, these small copies could wait on the copy
+    // engine behind the large x uploads and hold every chunk's kernels back.
+    cudaStream_t ps = hs.nchunk > 1 ? hs.up : s;
+    ok = ok && cudaMemcpyAsync(hs.w, w, p->w_numel * 4, cudaMemcpyHostToDevice, ps) == cudaSuccess;
+    if (b) ok = ok && cudaMemcpyAsync(hs.b, b, d.C_out * 4, cudaMemcpyHostToDevice, ps) == cudaSuccess;
     if (need_aff) {
-        ok = ok && cudaMemcpyAsync(hs.gamma, gamma, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
-        ok = ok && cudaMemcpyAsync(hs.beta, beta, d.C_out * 4, cudaMemcpyHostToDevice, s) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(hs.gamma, gamma, d.C_out * 4, cudaMemcpyHostToDevice, ps) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(hs.beta, beta, d.C_out * 4, cudaMemcpyHostToDevice, ps) == cudaSuccess;
     }
     const float *db = b ? hs.b : nullptr;
     const float *dg = need_aff ? hs.gamma : nullptr, *dbe = need_aff ? hs.beta : nullptr;
@@ -506,30 +519,38 @@ int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, con
         ok = ok && cudaMemcpyAsync(out, hs.out, p->out_numel * 4, cudaMemcpyDeviceToHost, s) == cudaSuccess;
     } else if (ok) {
         const int64_t xs = p->x_numel / d.N, os = p->out_numel / d.N;
-        // uploads run ahead on their own stream
+        // uploads run ahead on their own stream, after the parameters; a
+        // chunk's kernels wait for its upload event, so for the parameters too
         for (int i = 0; ok && i < hs.nchunk; ++i) {
             const int64_t n0 = (int64_t)i * hs.chunk_n, nn = std::min<int64_t>(hs.chunk_n, d.N - n0);
             ok = cudaMemcpyAsync(hs.x + n0 * xs, x + n0 * xs, nn * xs * 4, cudaMemcpyHostToDevice,
                                  hs.up) == cudaSuccess &&
                  cudaEventRecord(hs.ev_up[i], hs.up) == cudaSuccess;
         }
-        // kernels on the caller's stream, each chunk's download on the third
+        // even chunks compute on the caller's stream, odd ones on comp2;
+        // downloads on their own stream
         for (int i = 0; ok && i < hs.nchunk; ++i) {
             const int64_t n0 = (int64_t)i * hs.chunk_n, nn = std::min<int64_t>(hs.chunk_n, d.N - n0);
             conv_norm_plan_s *sp = hs.sub[i];
-            ok = cudaStreamWaitEvent(s, hs.ev_up[i], 0) == cudaSuccess;
+            cudaStream_t cs = (i & 1) ? hs.comp2 : s;
+            ok = cudaStreamWaitEvent(cs, hs.ev_up[i], 0) == cudaSuccess;
             if (ok) {
-                st = forward_impl(sp, hs.x + n0 * xs, hs.w, db, dg, dbe, hs.out + n0 * os, s);
+                st = forward_impl(sp, hs.x + n0 * xs, hs.w, db, dg, dbe, hs.out + n0 * os, cs);
                 ok = st == CN_OK;
             }
-            ok = ok && cudaEventRecord(hs.ev_done[i], s) == cudaSuccess &&
+            ok = ok && cudaEventRecord(hs.ev_done[i], cs) == cudaSuccess &&
                  cudaStreamWaitEvent(hs.down, hs.ev_done[i], 0) == cudaSuccess &&
                  cudaMemcpyAsync(out + n0 * os, hs.out + n0 * os, nn * os * 4, cudaMemcpyDeviceToHost,
                                  hs.down) == cudaSuccess;
         }
-        ok = ok && cudaStreamSynchronize(hs.down) == cudaSuccess;
+        ok = ok && cudaEventRecord(hs.ev_comp2, hs.comp2) == cudaSuccess &&
+             cudaStreamWaitEvent(s, hs.ev_comp2, 0) == cudaSuccess;
     }
-    ok = ok && cudaStreamSynchronize(s) == cudaSuccess;
+    // drain every stream this call used, after an error too, so that the
+    // next call never overwrites staging buffers a queued copy or kernel uses
+    for (cudaStream_t q : {hs.up, hs.comp2, hs.down})
+        if (q && cudaStreamSynchronize(q) != cudaSuccess) ok = false;
+    if (cudaStreamSynchronize(s) != cudaSuccess) ok = false;
     if (!ok) {
         if (st == CN_OK) st = CN_ERR_CUDA;
         cudaGetLastError();
@@ -543,16 +564,24 @@ int conv_norm_plan_check_device(conv_norm_plan p, void *stream) {
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != p->device) cudaSetDevice(p->device);
-    int flag = 0;
     int st = CN_OK;
-    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
-        cudaMemcpy(&flag, p->err_flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         st = CN_ERR_CUDA;
-    } else if (flag != 0) {
-        const int zero = 0;
-        cudaMemcpy(p->err_flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
-        st = flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
+    }
+    // the plan's own flag, then those of the chunk plans conv_norm_forward_host runs
+    for (int i = -1; st != CN_ERR_CUDA && i < kMaxHostChunks; ++i) {
+        const conv_norm_plan_s *q = i < 0 ? p : p->stage.sub[i];
+        if (!q) continue;
+        int flag = 0;
+        if (cudaMemcpy(&flag, q->err_flag, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            st = CN_ERR_CUDA;
+        } else if (flag != 0) {
+            const int zero = 0;
+            cudaMemcpy(q->err_flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+            if (st != CN_ERR_TIMEOUT) st = flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
+        }
     }
     if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     return st;

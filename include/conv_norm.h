@@ -168,12 +168,16 @@ int conv_norm_forward(conv_norm_plan plan, const float *x, const float *w,
  * Same computation with HOST buffers: copies x, w, b, gamma, beta to device
  * buffers owned by the plan, runs the forward on cuda_stream, copies the
  * result back into the host buffer out and synchronizes before returning.
- * Batches of more than about 16 MB of input are cut into up to 8 chunks of
- * whole samples (every step is per sample): chunk i+1 uploads on a
- * plan-owned stream while chunk i computes on cuda_stream, and each chunk's
- * result downloads on a second plan-owned stream as soon as it is done.
+ * Batches of more than about 16 MB of input are cut into chunks of whole
+ * samples, about 6 MB of input each and at most 8 (every step is per
+ * sample): chunk i+1 uploads on a
+ * plan-owned stream while chunk i computes, even chunks on cuda_stream and
+ * odd ones on a plan-owned compute stream (so one chunk's kernels can start
+ * on the SMs the previous chunk's last work leaves idle), and each chunk's
+ * result downloads on a third plan-owned stream as soon as it is done;
+ * cuda_stream waits for the second compute stream before the call returns.
  * The first call allocates the staging buffers, the per-chunk plans, the
- * two streams and their events.  Pinned (page-locked) host memory gives
+ * three streams and their events.  Pinned (page-locked) host memory gives
  * asynchronous full-bandwidth copies; pageable memory works too.  Errors as
  * conv_norm_forward, plus CN_ERR_ALLOC.
  */
@@ -183,7 +187,8 @@ int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
 
 /*
  * Synchronizes cuda_stream, then reads and clears the plan's device error
- * flag.  Returns CN_OK, CN_ERR_TIMEOUT (a bounded device wait gave up; the
+ * flag and those of the chunk plans conv_norm_forward_host created.  Returns
+ * CN_OK, CN_ERR_TIMEOUT (a bounded device wait gave up; the
  * output of that forward is undefined), CN_ERR_DEVICE_CHECK or CN_ERR_CUDA.
  */
 int conv_norm_plan_check_device(conv_norm_plan plan, void *cuda_stream);

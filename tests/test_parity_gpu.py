@@ -197,11 +197,17 @@ def test_forward_host_matches():
         np.testing.assert_array_equal(out2, out.numpy())
 
 
-@pytest.mark.parametrize("name,N", [("conv3d_hswish_gn4_mean_n512", 203),
-                                    ("convt2d_g8_gelu_gn8_n32", 5)])
-def test_forward_host_chunked_matches_device_forward(name, N):
-    # more than 16 MB of input: the host entry point pipelines uneven chunks
-    # (203 samples -> 2 chunks of 102 and 101; 5 large-output samples -> 4 chunks)
+@pytest.mark.parametrize("name,N,chunks", [("conv3d_hswish_gn4_mean_n512", 203, None),
+                                           ("conv3d_hswish_gn4_mean_n512", 203, 3),
+                                           ("conv3d_hswish_gn4_mean_n512", 203, 8),
+                                           ("convt2d_g8_gelu_gn8_n32", 5, None)])
+def test_forward_host_chunked_matches_device_forward(name, N, chunks, monkeypatch):
+    # more than 16 MB of input: the host entry point pipelines chunks of whole
+    # samples, alternating between two compute streams (203 samples: by
+    # default 6 chunks, five of 34 and one of 33; in 3 chunks: 68, 68, 67;
+    # in 8: seven of 26 and one of 21; 5 large samples: one per chunk)
+    if chunks is not None:
+        monkeypatch.setenv("CN_HOST_CHUNKS", str(chunks))
     s = wl.with_overrides(W[name], N=N)
     inp = wl.make_inputs(s)
     dev = {k: to_dev(v) for k, v in inp.items()}
@@ -214,6 +220,7 @@ def test_forward_host_chunked_matches_device_forward(name, N):
             out = torch.full(p.out_shape, float("nan"), dtype=torch.float32).pin_memory()
             p.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], out)
             np.testing.assert_array_equal(out.numpy(), ref.cpu().numpy())
+        assert p.check_device() == B.CN_OK  # the chunk plans' error flags too
     last = [0, N - 1]
     assert_parity(out.numpy()[last], oracle.forward(s, inp, samples=last), name + " chunked")
 
