@@ -83,7 +83,9 @@ int check_wellformed(const conv_norm_desc &d) {
     if (!is_finite(d.eps) || !is_finite(d.post_scale)) return CN_ERR_INVALID_ARG;
     if (d.norm != CN_NORM_NONE && !(d.eps > 0.0f)) return CN_ERR_INVALID_ARG;
     if (d.red == CN_RED_MAXPOOL2_X2 && d.conv != CN_CONV3D) return CN_ERR_INVALID_ARG;
-    // 32-bit index limits of the kernels
+    // element counts must stay far inside int64 (the kernels address memory
+    // with 64-bit offsets; per-axis sizes and TMA coordinates are the
+    // descriptor's 32-bit ints)
     const double big = (double)d.N * d.C_out * d.D * (double)(d.H + d.k) * (d.W + d.k);
     const double bigx = (double)d.N * d.C_in * d.D * (double)d.H * d.W;
     if (big > 4.0e18 || bigx > 4.0e18) return CN_ERR_INVALID_ARG;
@@ -459,21 +461,29 @@ static int host_stage_setup(conv_norm_plan p) {
     nch = std::min(nch, d.N);
     hs.chunk_n = (d.N + nch - 1) / nch;
     hs.nchunk = (d.N + hs.chunk_n - 1) / hs.chunk_n;
+    // Each object is created only if missing, so a call after a failed setup
+    // finishes it without leaking what the failed one made.
+    auto stream = [](cudaStream_t &q) {
+        return q || cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking) == cudaSuccess;
+    };
+    auto event = [](cudaEvent_t &e) {
+        return e || cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+    };
     if (hs.nchunk > 1) {
         conv_norm_desc dc = d;
         for (int i = 0; i < hs.nchunk; ++i) {
             dc.N = std::min(hs.chunk_n, d.N - i * hs.chunk_n);
-            if ((st = conv_norm_plan_create(&dc, &hs.sub[i])) != CN_OK) return st;
+            if (!hs.sub[i] && (st = conv_norm_plan_create(&dc, &hs.sub[i])) != CN_OK) return st;
         }
-        if (cudaStreamCreateWithFlags(&hs.up, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&hs.down, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaStreamCreateWithFlags(&hs.comp2, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&hs.ev_comp2, cudaEventDisableTiming) != cudaSuccess)
+        if (!stream(hs.up) || !stream(hs.down) || !stream(hs.comp2) || !event(hs.ev_comp2)) {
+            cudaGetLastError();
             return CN_ERR_CUDA;
+        }
         for (int i = 0; i < hs.nchunk; ++i)
-            if (cudaEventCreateWithFlags(&hs.ev_up[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&hs.ev_done[i], cudaEventDisableTiming) != cudaSuccess)
+            if (!event(hs.ev_up[i]) || !event(hs.ev_done[i])) {
+                cudaGetLastError();
                 return CN_ERR_CUDA;
+            }
     }
     hs.ready = true;
     return CN_OK;
