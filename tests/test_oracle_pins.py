@@ -305,6 +305,11 @@ SMALL = [
     wl.with_overrides(wl.WORKLOADS[2], N=2, C_in=8, C_out=6, H=11, W=13),
     wl.with_overrides(wl.WORKLOADS[3], N=2, D=9, H=12, W=11),
     wl.with_overrides(wl.WORKLOADS[4], N=2, C_in=16, C_out=16, H=9, W=7),
+    # a post scale before the pool and before the mean (the other cases use 1)
+    wl.with_overrides(wl.WORKLOADS[3], N=2, D=8, H=9, W=12, post_scale=0.5,
+                      name="pool_scaled"),
+    wl.with_overrides(wl.WORKLOADS[1], N=2, D=6, H=8, W=9, post_scale=0.25,
+                      name="mean_scaled"),
 ]
 
 
