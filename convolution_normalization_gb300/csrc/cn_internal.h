@@ -218,7 +218,8 @@ struct Full2dArgs {
     int apply_needed, vec4;
     long long S;          // Dv * Ho * Wo: one normalized (n, c) plane
     float4 *partial;      // [N][Co][ntiles * wsp]: per warp and tile (count, K, S1, S2),
-                          // shifted sums S1 = sum(v - K), S2 = sum((v - K)^2)
+                          // shifted sums S1 = sum(v - K), S2 = sum((v - K)^2) about
+                          // one of the partial's own values K
     float4 *coef;         // [N][Co]: (mu, a, bb, 0)
     int *tickets;         // [N] (unused), then [2] work/exit counters
     int *err;

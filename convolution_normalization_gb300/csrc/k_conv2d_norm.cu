@@ -44,12 +44,16 @@ CN_DEV float act_value(float t) {
     return t;
 }
 
-// Bias + activation of RW values in place, then the shifted sums
-// (count, S1, S2) of the first nvalid of them (all on the common path).
+// Bias + activation of RW values in place.
 template <int RW, int ACT>
-CN_DEV float3 act_sums(float (&v)[RW], float bias, float K, int nvalid) {
+CN_DEV void bias_act(float (&v)[RW], float bias) {
 #pragma unroll
     for (int i = 0; i < RW; ++i) v[i] = act_value<ACT>(v[i] + bias);
+}
+// Shifted sums (count, S1 = sum(v - K), S2 = sum((v - K)^2)) of the first
+// nvalid of RW values (all on the common path).
+template <int RW>
+CN_DEV float3 shifted_sums(const float (&v)[RW], float K, int nvalid) {
     float s1 = 0.0f, s2 = 0.0f;
     if (nvalid == RW) {
 #pragma unroll
@@ -432,28 +436,28 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
             const bool row_ok = item_ok && orow < a.Ho;
             const int nvalid = row_ok ? max(0, min(RW, a.Wo - ocol0)) : 0;
             const int tin = G.rt * a.col_tiles + G.ct;
+            // The shift of a (warp, channel) partial is one of its own values:
+            // the first output of the lowest lane that has a valid one.  The
+            // shifted values then stay within a few standard deviations of 0,
+            // whatever the channel's mean (no cancellation in S2 - S1^2 / n).
+            const unsigned vlanes = __ballot_sync(0xffffffffu, nvalid > 0);
+            const int klane = vlanes ? __ffs(vlanes) - 1 : 0;
 #pragma unroll
             for (int c = 0; c < COT; ++c) {
                 const int co = G.co0 + cs * COT + c;
                 const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-                // shift: the activated bias, a typical value of this channel
-                float3 m;
-                float K;
                 if constexpr (ACTT >= 0) {
-                    K = act_value<ACTT>(bias);
-                    m = act_sums<RW, ACTT>(acc[c], bias, K, nvalid);
+                    bias_act<RW, ACTT>(acc[c], bias);
                 } else {
-                    if (a.act == ACT_HARDSWISH) {
-                        K = act_value<ACT_HARDSWISH>(bias);
-                        m = act_sums<RW, ACT_HARDSWISH>(acc[c], bias, K, nvalid);
-                    } else if (a.act == ACT_GELU) {
-                        K = act_value<ACT_GELU>(bias);
-                        m = act_sums<RW, ACT_GELU>(acc[c], bias, K, nvalid);
-                    } else {
-                        K = bias;
-                        m = act_sums<RW, ACT_NONE>(acc[c], bias, K, nvalid);
-                    }
+                    if (a.act == ACT_HARDSWISH)
+                        bias_act<RW, ACT_HARDSWISH>(acc[c], bias);
+                    else if (a.act == ACT_GELU)
+                        bias_act<RW, ACT_GELU>(acc[c], bias);
+                    else
+                        bias_act<RW, ACT_NONE>(acc[c], bias);
                 }
+                const float K = __shfl_sync(0xffffffffu, acc[c][0], klane);
+                float3 m = shifted_sums<RW>(acc[c], K, nvalid);
                 float *op = a.out +
                             ((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.Ho + (row_ok ? orow : 0)) * a.Wo +
                             ocol0;
@@ -488,34 +492,29 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 
 // Statistics of the normalization groups.  A group of one channel
 // (InstanceNorm) gets one warp, four per block; a wider group gets the four
-// warps of a block, warp w taking channels w, w + 4, ... .  All partials of
-// one channel share that channel's shift K, so per channel the lanes add the
-// shifted sums (count, S1, S2) of every tile, then a butterfly of
-// commutative adds gives every lane the same bits.  Channel moments are
-// merged as (count, mean, M2): within a warp in channel order, then the
-// warps' results in warp order, so the result is deterministic.  The group's
-// coefficients (mu, a = gamma * rstd * scale, bb = beta * scale) go to
-// every channel.  Arithmetic is fp32: its ~1e-6 relative error in mean and
-// variance is far inside the 1e-4 output bound, and the FP64 pipe of this
-// GPU is narrow enough that a few fp64 divisions per group cost more than
-// the pass's memory traffic.
+// warps of a block, warp w taking channels w, w + 4, ... .  Every partial
+// (count, K, S1, S2) is a sum about its own shift K, one of its own values,
+// so it converts to (count, mean = K + S1/n, M2 = S2 - S1^2/n) without
+// cancellation; the lanes merge a channel's partials with the pairwise update
+// of Chan et al. in a fixed order (lane l takes partials l, l + 32, ...),
+// then a butterfly merge gives every lane the same bits.  Channel moments
+// are merged within a warp in channel order, then the warps' results in
+// warp order, so the result is deterministic.  The group's coefficients
+// (mu, a = gamma * rstd * scale, bb = beta * scale) go to every channel.
+// Arithmetic is fp32: its ~1e-6 relative error in mean and variance is far
+// inside the 1e-4 output bound, and the FP64 pipe of this GPU is narrow
+// enough that fp64 divisions per merge cost more than the pass's memory
+// traffic.
 constexpr int kStatsWarps = 4;
+CN_DEV Moments<float> partial_moments(float4 q) {
+    if (!(q.x > 0.0f)) return Moments<float>{0.0f, 0.0f, 0.0f};
+    const float mu_s = q.z / q.x;  // mean - K
+    return Moments<float>{q.x, q.y + mu_s, fmaxf(q.w - q.z * mu_s, 0.0f)};
+}
 CN_DEV Moments<float> channel_moments(const float4 *p, int per_c, int lane) {
-    long long cnt = 0;  // exact count
-    float3 v = make_float3(0.0f, 0.0f, 0.0f);  // (-, S1, S2)
-    for (int i = lane; i < per_c; i += 32) {
-        const float4 q = p[i];
-        cnt += (long long)q.x;
-        v.y += q.z;
-        v.z += q.w;
-    }
-    v = warp_sum3(v);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
-    if (cnt <= 0) return Moments<float>{0.0f, 0.0f, 0.0f};
-    const float fn = (float)cnt;
-    const float mu_s = v.y / fn;  // mean - K
-    return Moments<float>{fn, p[0].y + mu_s, fmaxf(v.z - v.y * mu_s, 0.0f)};
+    Moments<float> m{0.0f, 0.0f, 0.0f};
+    for (int i = lane; i < per_c; i += 32) m = merge(m, partial_moments(p[i]));
+    return warp_merge(m);
 }
 
 __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a) {

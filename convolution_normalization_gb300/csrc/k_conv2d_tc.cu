@@ -34,9 +34,10 @@
 //   warp 1      MMA issuer (one thread): 14 tcgen05.mma per stage into one of
 //               two TMEM accumulators (double buffered across tiles);
 //   warps 6-9   epilogue: tcgen05.ld of the accumulator (thread = channel),
-//               bias + activation, per-channel shifted sums (count, S1, S2)
-//               in registers, then a 32x32 transpose through shared memory so
-//               the pre-norm output is stored with coalesced rows.
+//               bias + activation, per-channel sums (count, S1, S2) about
+//               the tile's first value, in registers, then a 32x32
+//               transpose through shared memory so the pre-norm output is
+//               stored with coalesced rows.
 // The statistics and normalize passes that follow are the ones of the CUDA
 // core path (k_group_stats, k_norm_apply).
 #include "cn_common.cuh"
@@ -362,7 +363,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
             const int r0 = rt * a.tc_R;
             const int co = cob * kTcM + q * 32 + lane;
             const float bias = a.b ? __ldg(a.b + co) : 0.0f;
-            const float Ksh = apply_act(a.act, bias);
+            // shift of the channel's sums: its first value of the tile
+            // (position 0, always valid), so the shifted values stay within a
+            // few standard deviations of 0 whatever the channel's mean
+            float Ksh = 0.0f;
             const int rows_ok = min(a.tc_R, a.Ho - r0);
             float s1 = 0.0f, s2 = 0.0f;
             float *obase = a.out + ((size_t)n * a.Co + cob * kTcM + q * 32) * (size_t)S;
@@ -376,6 +380,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                 const int col = p - rr * a.W;
                 const bool vl = rr < rows_ok && col < a.Wo;
                 const unsigned vmask = __ballot_sync(0xffffffffu, vl);
+                if (i == 0) Ksh = apply_act(a.act, __uint_as_float(v[0]) + bias);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const float y = apply_act(a.act, __uint_as_float(v[j]) + bias);
