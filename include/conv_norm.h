@@ -127,25 +127,46 @@ const char *conv_norm_status_string(int status);
 
 /* ---- plans ---------------------------------------------------------------- */
 
-/* Validates desc, picks the kernel variant and its tiling for the CURRENT
+/* Cites: the module constructor of each problem page, whose arguments fix
+ * the problem: in_channels, out_channels and kernel_size everywhere, the
+ * group count on l2_p27, divide_by on l2_p17, the pool size on l2_p6, and
+ * stride, groups and num_groups on l2_p19.  desc holds those arguments plus
+ * the input extents each page's get_inputs fixes.
+ * Validates desc, picks the kernel variant and its tiling for the CURRENT
  * CUDA device, and allocates the plan's device workspace there (partial
  * statistics, tickets, an error flag).  On success *out_plan owns that
- * memory until conv_norm_plan_destroy. */
+ * memory until conv_norm_plan_destroy; on failure *out_plan is set to NULL.
+ * Errors: CN_ERR_INVALID_ARG (NULL pointers, malformed desc),
+ * CN_ERR_UNSUPPORTED, CN_ERR_CUDA (no device / attribute query failed),
+ * CN_ERR_ALLOC (cudaMalloc or host allocation failed). */
 int conv_norm_plan_create(const conv_norm_desc *desc, conv_norm_plan *out_plan);
 
-/* Frees the plan and its workspace.  NULL is ignored.  The caller must make
+/* Cites: no page passage (the pages' modules own their tensors through
+ * PyTorch); this releases what conv_norm_plan_create acquired.
+ * Frees the plan and its workspace.  NULL is ignored.  The caller must make
  * sure no forward that uses the plan is still running. */
 void conv_norm_plan_destroy(conv_norm_plan plan);
 
-/* Bytes of device workspace the plan owns (0 when none is needed). */
+/* Cites: the buffers of partial statistics that the pages' multi-pass
+ * designs pass between kernels (l2_p19's three-kernel GroupNorm: partial
+ * sums, group statistics, apply; l2_p27's per-block partial moments), kept
+ * here in a plan-owned workspace.
+ * Bytes of device workspace the plan owns (0 when none is needed; 0 for a
+ * NULL plan). */
 size_t conv_norm_workspace_bytes(conv_norm_plan plan);
 
-/* Fills *info; returns CN_ERR_INVALID_ARG for NULL arguments. */
+/* Fills *info with the plan's variant, kernels and workspace size (a
+ * reporting aid; no counterpart on the pages); returns CN_ERR_INVALID_ARG
+ * for NULL arguments. */
 int conv_norm_plan_info(conv_norm_plan plan, conv_norm_info *info);
 
 /* ---- forward -------------------------------------------------------------- */
 
 /*
+ * Cites: ModelNew.forward(x) of each problem page (l2_p27: conv -> HardSwish
+ * -> GroupNorm -> mean over D, H, W; l2_p17: conv -> InstanceNorm2d -> divide
+ * by 2; l2_p6: conv -> Softmax(dim=1) -> MaxPool3d(2) twice; l2_p19:
+ * ConvTranspose2d -> GELU -> GroupNorm), with the module's weights passed in.
  * Runs the fused forward asynchronously on cuda_stream (a cudaStream_t; NULL
  * is the legacy default stream).  All pointers are DEVICE pointers on the
  * plan's device, fp32, contiguous, 16-byte aligned:

@@ -125,3 +125,29 @@ def test_product_package_does_not_import_oracle():
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", src, re.M), f
                 assert "liboracle" not in src, f
+
+
+def _declarations_with_comments():
+    """(function name, the comment block right before its declaration)."""
+    out = {}
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not h.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", h)).read()
+        for m in re.finditer(r"/\*((?:(?!\*/).)*)\*/\s*(?:[\w\s\*]+?)\b(conv_norm_\w+)\s*\(",
+                             src, flags=re.S):
+            out[m.group(2)] = m.group(1)
+    return out
+
+
+def test_boundary_calls_cite_their_passage():
+    # the four calls of the boundary each say which passage of the problem
+    # pages they follow (or that none does); every other call is documented
+    docs = _declarations_with_comments()
+    assert set(docs) == header_functions()
+    for name in ("conv_norm_plan_create", "conv_norm_forward", "conv_norm_workspace_bytes",
+                 "conv_norm_plan_destroy"):
+        assert "Cites:" in docs[name], name
+        assert re.search(r"l2_p\d+|no page passage", docs[name]), name
+    for name, doc in docs.items():
+        assert len(doc.split()) >= 8, name
