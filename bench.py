@@ -39,9 +39,12 @@ sys.path.insert(0, ROOT)
 from convolution_normalization_gb300 import workloads as wl  # noqa: E402
 
 DEFAULT_WORKLOAD = "conv3d_hswish_gn4_mean_n512"
-SMS = 152
+# SM count when no device is visible (host-only runs); the CUDA arm reads the
+# device's own count
+DEFAULT_SMS = 152
 FP32_LANES_PER_SM = 128
 METRIC = "fused conv+norm forward ms & GFLOP/s, % of roofline (FP32 peak vs HBM)"
+DATA = "synthetic (seeded PCG64: x~N(0,1), w,b~U(+-1/sqrt(fan_in)), gamma=1+0.1N, beta=0.1N)"
 
 
 # ---- workload arithmetic (for reporting only) ---------------------------------
@@ -80,7 +83,11 @@ def compulsory_bytes(s):
     return 4.0 * (n + math.prod(out_shape(s)))
 
 
-def peaks():
+def peaks(sms=None):
+    """Roofline denominators: measured HBM copy bandwidth and bf16 GEMM rate
+    (MEASURED_PEAKS.json, else the stated fallback) and the FP32 FMA peak
+    from the SM count (the device's, when given), 128 FP32 lanes per SM and
+    the maximum SM clock."""
     p = {}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -90,9 +97,12 @@ def peaks():
     src = "measured" if hbm else "fallback"
     if not hbm:
         hbm = 6800.0
-    fp32 = SMS * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
+    sms_src = "device" if sms else "default"
+    sms = sms or DEFAULT_SMS
+    fp32 = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s
     bf16 = p.get("bf16_tflops") or 1900.0
-    return dict(hbm_gbs=hbm, fp32_tflops=fp32, sm_max_mhz=sm_mhz, source=src, bf16_tflops=bf16)
+    return dict(hbm_gbs=hbm, fp32_tflops=fp32, sm_max_mhz=sm_mhz, source=src, bf16_tflops=bf16,
+                sms=sms, sms_source=sms_src)
 
 
 def roofline_ms(s, pk):
@@ -119,6 +129,14 @@ KERNEL_SOURCES = {
 # (1.1 / 2.25 PFLOP/s); split-TF32 runs 3 tf32 products per fp32 product
 TF32_PER_BF16 = 1.1 / 2.25
 SPLIT_TF32_PRODUCTS = 3
+TC_KERNELS = ("k_conv2d_tc", "k_conv3d_tc_mean", "k_conv3d_tc_pool")
+
+
+def contraction(kernel_names):
+    """The arithmetic of the conv of a plan's kernel list."""
+    if any(k in kernel_names for k in TC_KERNELS):
+        return "3xTF32 split on tcgen05 tensor cores, fp32 accumulate (fp32 accuracy)"
+    return "fp32 FFMA on CUDA cores"
 
 
 def split_names(s):
@@ -168,18 +186,23 @@ def profiled_traffic(workload, key):
 
 
 def kernel_roofline(spec, name, ms, pk):
-    """Roofline of one kernel launch of the forward: algorithmic work per
-    launch / its measured duration against the peak of the unit bounding it."""
+    """Roofline of one kernel launch of the forward: the method's algorithmic
+    work per launch / its measured duration, against the peak of the unit the
+    kernel runs on (tf32 tensor pipe, HBM, or the FP32 pipe)."""
     flops = algorithmic_flops(spec)
     base = name.split("<")[0]
-    if base in ("k_conv2d_tc", "k_conv3d_tc_mean", "k_conv3d_tc_pool"):
-        work = SPLIT_TF32_PRODUCTS * flops  # tf32 tensor-core flops the split method needs
+    if base in TC_KERNELS:
+        ach = flops / (ms / 1e3) / 1e12
         peak = pk["bf16_tflops"] * TF32_PER_BF16
-        return {"bound": "tensor", "achieved": work / (ms / 1e3) / 1e12, "peak": peak,
-                "unit": "TFLOP/s",
-                "work": f"{SPLIT_TF32_PRODUCTS} tf32 products x 2 x MACs = {work:.4g} flop",
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "work": f"2 x MACs = {flops:.4g} flop (the method's own work)",
                 "peak_source": f"measured bf16 {pk['bf16_tflops']} TFLOP/s x nominal tf32/bf16 "
-                               f"{TF32_PER_BF16:.3f}"}
+                               f"{TF32_PER_BF16:.3f}",
+                # what the tensor pipe executes: the split's 3 tf32 products per MAC
+                "split_tf32": {"achieved": SPLIT_TF32_PRODUCTS * ach,
+                               "frac": SPLIT_TF32_PRODUCTS * ach / peak,
+                               "work": f"{SPLIT_TF32_PRODUCTS} tf32 products x 2 x MACs"},
+                "frac_of_fp32_peak": ach / pk["fp32_tflops"]}
     if base == "k_norm_apply":
         nbytes = 2.0 * 4 * math.prod(out_shape(spec))
         return {"bound": "hbm", "achieved": nbytes / (ms / 1e3) / 1e9, "peak": pk["hbm_gbs"],
@@ -187,8 +210,18 @@ def kernel_roofline(spec, name, ms, pk):
                 "peak_source": f"{pk['source']} HBM {pk['hbm_gbs']} GB/s"}
     return {"bound": "alu", "achieved": flops / (ms / 1e3) / 1e12, "peak": pk["fp32_tflops"],
             "unit": "TFLOP/s", "work": f"2 x MACs = {flops:.4g} flop",
-            "peak_source": f"FP32: {SMS} SMs x {FP32_LANES_PER_SM} lanes x 2 x "
-                           f"{pk['sm_max_mhz']:.0f} MHz"}
+            "peak_source": f"FP32: {pk['sms']} SMs ({pk['sms_source']}) x {FP32_LANES_PER_SM} "
+                           f"lanes x 2 x {pk['sm_max_mhz']:.0f} MHz"}
+
+
+def config_of(spec):
+    """The workload a line is measured on: the same keys and values in both
+    arms (the arithmetic each arm uses is its own top-level key)."""
+    return {"workload": spec["name"], "N": spec["N"], "C_in": spec["C_in"],
+            "C_out": spec["C_out"], "D": spec["D"], "H": spec["H"], "W": spec["W"],
+            "k": spec["k"], "groups": spec["groups"], "per_rank_batch": spec["N"],
+            "l2": "flushed before every timed GPU step (256 MB write)",
+            "precision": "fp32 result, |err| <= 1e-4 + 1e-4|ref| against the fp64 oracle"}
 
 
 # ---- clocks ----------------------------------------------------------------------
@@ -206,7 +239,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "25"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -324,8 +357,9 @@ def run_reference(args, spec):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "GFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64)",
-        "config": {"workload": spec["name"], "samples_per_step": n, "N": spec["N"]},
+        "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": config_of(spec),
+        "contraction": "fp64 loops on the host cores (the oracle)",
         "cpu_baseline": {"value": val, "unit": "GFLOP/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n} of {spec['N']} samples per step"},
         "e2e": {"value": val, "unit": "GFLOP/s", "h2d_bytes_per_step": 0,
@@ -376,6 +410,80 @@ def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf, nla
     return step_ms, launch_ms
 
 
+def measure(B, torch, spec, pk, stream, flush, steps, warmup, world=1, e2e_steps=10,
+            cpu_target_s=None, sampler=None):
+    """One workload on this rank: device step time (mean of `steps`, L2
+    flushed before each), per-launch times, the dominant kernel's roofline,
+    the step roofline of the workload's metric, the end-to-end time through
+    the host-buffer entry point and (if cpu_target_s) the oracle's rate on
+    the host cores."""
+    inp = wl.make_inputs(spec)
+    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
+    plan = B.Plan(spec)
+    info = plan.info()
+    nl = info["launches_per_forward"]
+    out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+    if sampler:
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler.start()
+    times, launch_ms = time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush, nl)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    assert plan.check_device(stream) == B.CN_OK
+    ms_rank = statistics.mean(times)
+    ms = max_over_ranks(world, ms_rank)
+    flops = algorithmic_flops(spec)
+    rl_ms, bound = roofline_ms(spec, pk)
+    names = split_names(info["kernel_names"])[:nl]
+    means = [statistics.mean(v) for v in launch_ms]
+    dom = max(range(nl), key=lambda j: means[j])
+    roofline = kernel_roofline(spec, names[dom], means[dom], pk)
+    roofline["frac"] = roofline["achieved"] / roofline["peak"]
+    roofline.update({
+        "traffic": profiled_traffic(spec["name"], kernel_key(names[dom])),
+        "kernel": names[dom], "kernel_ms": means[dom],
+        "launch_ms": {n: m for n, m in zip(names, means)},
+        # the workload's metric: FP32-peak / HBM roofline time of the whole step
+        "step_roofline_ms": rl_ms, "step_roofline_bound": bound,
+        "frac_of_step_roofline": rl_ms / ms_rank,
+    })
+    del dev, out
+    # end to end through the host-buffer entry point (pinned buffers; the
+    # copies both ways are inside the timed region)
+    hp = {k: (torch.from_numpy(v).pin_memory() if v is not None else None) for k, v in inp.items()}
+    hout = torch.empty(plan.out_shape, dtype=torch.float32).pin_memory()
+    for _ in range(2):
+        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
+    barrier(world)
+    e2e_times = []
+    for _ in range(e2e_steps):
+        t0 = time.perf_counter()
+        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(world, statistics.mean(e2e_times))
+    assert plan.check_device(stream) == B.CN_OK
+    h2d = sum(v.numel() * 4 for v in hp.values() if v is not None)
+    e2e = {"value": world * flops / e2e_s / 1e9, "unit": "GFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 4,
+           "ms_per_step": e2e_s * 1e3, "steps": e2e_steps,
+           "api": "conv_norm_forward_host (C ABI, pinned host buffers)"}
+    plan.close()
+    del hp, hout
+    res = {"workload": spec["name"], "ms": ms, "ms_rank": ms_rank, "steps": steps,
+           "gflops": job_rate(world, flops, ms) / 1e9, "flops_per_step": flops,
+           "roofline_ms": rl_ms, "bound": bound, "frac": rl_ms / ms,
+           "roofline": roofline, "e2e": e2e, "launches": nl, "kernels": info["kernel_names"],
+           "contraction": contraction(info["kernel_names"]), "config": config_of(spec)}
+    if clocks:
+        res["clocks"] = clocks
+    if cpu_target_s:
+        rate, n, dt, thr = oracle_rate(spec, inp, target_s=cpu_target_s)
+        res["cpu_baseline"] = {"value": rate, "unit": "GFLOP/s", "cores": thr, "kind": "oracle",
+                               "sample": f"{n} of {spec['N']} samples, {dt:.1f} s"}
+    return res
+
+
 def run_cuda(args, spec):
     import torch
     world, rank, local = dist_setup(args.gpus)
@@ -386,125 +494,45 @@ def run_cuda(args, spec):
     from convolution_normalization_gb300 import binding as B
 
     torch.cuda.set_device(local)
-    pk = peaks()
-    inp = wl.make_inputs(spec)
-    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
-    plan = B.Plan(spec)
-    info = plan.info()
-    out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
+    pk = peaks(torch.cuda.get_device_properties(local).multi_processor_count)
     stream = torch.cuda.Stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
-    sampler = ClockSampler(torch.cuda.current_device())
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.start()
-    nlaunch = info["launches_per_forward"]
-    times, launch_ms = time_forward(B, torch, plan, dev, out, stream, args.steps, args.warmup,
-                                    flush, nlaunch)
-    torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    assert plan.check_device(stream) == B.CN_OK
-
-    ms_rank = statistics.mean(times)
-    ms = max_over_ranks(world, ms_rank)
-    flops = algorithmic_flops(spec)
-    value = job_rate(world, flops, ms) / 1e9
-    rl_ms, bound = roofline_ms(spec, pk)
-
-    # dominant kernel: the launch with the largest mean device time
-    names = split_names(info["kernel_names"])[:nlaunch]
-    means = [statistics.mean(v) for v in launch_ms]
-    dom = max(range(nlaunch), key=lambda j: means[j])
-    roofline = kernel_roofline(spec, names[dom], means[dom], pk)
-    roofline.update({
-        "traffic": profiled_traffic(spec["name"], kernel_key(names[dom])),
-        "kernel": names[dom], "kernel_ms": means[dom],
-        "launch_ms": {n: m for n, m in zip(names, means)},
-        # the workload's metric: FP32-peak / HBM roofline time of the whole step
-        "step_roofline_ms": rl_ms, "step_roofline_bound": bound,
-        "frac_of_step_roofline": rl_ms / ms_rank,
-    })
-    roofline["frac"] = roofline["achieved"] / roofline["peak"]
-
-    # end to end through the host-buffer entry point
-    hp = {k: (torch.from_numpy(v).pin_memory() if v is not None else None) for k, v in inp.items()}
-    hout = torch.empty(plan.out_shape, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 30))
-    for _ in range(2):
-        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        plan.forward_host(hp["x"], hp["w"], hp["b"], hp["gamma"], hp["beta"], hout, stream)
-    e2e_s = max_over_ranks(world, (time.perf_counter() - t0) / e2e_steps)
-    h2d = sum(v.numel() * 4 for v in hp.values() if v is not None)
-    e2e = {"value": world * flops / e2e_s / 1e9, "unit": "GFLOP/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hout.numel() * 4,
-           "ms_per_step": e2e_s * 1e3}
+    head = measure(B, torch, spec, pk, stream, flush, args.steps, args.warmup, world,
+                   e2e_steps=max(3, min(args.steps, 30)),
+                   cpu_target_s=None if (rank != 0 or args.no_cpu_baseline) else 12.0,
+                   sampler=ClockSampler(torch.cuda.current_device()))
 
     line = {
-        "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": head["gflops"], "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded PCG64: x~N(0,1), w,b~U(+-1/sqrt(fan_in)), gamma=1+0.1N, beta=0.1N)",
-        "config": {"workload": spec["name"], "N": spec["N"], "C_in": spec["C_in"],
-                   "C_out": spec["C_out"], "D": spec["D"], "H": spec["H"], "W": spec["W"],
-                   "k": spec["k"], "per_rank_batch": spec["N"],
-                   "l2": "flushed before every timed step (256 MB write)"},
-        "roofline": roofline,
-        "gpu_launches": args.steps * info["launches_per_forward"],
-        "kernels": info["kernel_names"],
-        "clocks": clocks,
-        "e2e": e2e,
+        "data": DATA, "config": head["config"], "contraction": head["contraction"],
+        "roofline": head["roofline"],
+        "gpu_launches": args.steps * head["launches"],
+        "kernels": head["kernels"],
+        "clocks": head["clocks"],
+        "e2e": head["e2e"],
+        "peaks": {k: pk[k] for k in ("hbm_gbs", "fp32_tflops", "bf16_tflops", "sm_max_mhz",
+                                      "sms", "source")},
     }
-
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
     if rank == 0 and not args.no_extras:
         extras = []
         for s2 in wl.WORKLOADS:
             if s2["name"] == spec["name"]:
                 continue
-            extras.append(measure_extra(B, torch, s2, pk, stream, flush))
+            r = measure(B, torch, s2, pk, stream, flush, 30, 5, 1, e2e_steps=10,
+                        cpu_target_s=None if args.no_cpu_baseline else 3.0)
+            r.pop("config")
+            extras.append(r)
         line["workloads"] = extras
-    if rank == 0 and not args.no_cpu_baseline:
-        rate, n, dt, thr = oracle_rate(spec, inp, target_s=12.0)
-        line["cpu_baseline"] = {"value": rate, "unit": "GFLOP/s", "cores": thr, "kind": "oracle",
-                                "sample": f"{n} of {spec['N']} samples, {dt:.1f} s"}
-    plan.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
-
-
-def measure_extra(B, torch, s, pk, stream, flush):
-    inp = wl.make_inputs(s)
-    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
-    plan = B.Plan(s)
-    info = plan.info()
-    nl = info["launches_per_forward"]
-    out = torch.empty(plan.out_shape, dtype=torch.float32, device="cuda")
-    big = compulsory_bytes(s) > 200e6
-    times, launch_ms = time_forward(B, torch, plan, dev, out, stream, 30, 5, flush, nl)
-    ms = statistics.median(times)
-    rl_ms, bound = roofline_ms(s, pk)
-    names = split_names(info["kernel_names"])[:nl]
-    means = [statistics.mean(v) for v in launch_ms]
-    dom = max(range(nl), key=lambda j: means[j])
-    kr = kernel_roofline(s, names[dom], means[dom], pk)
-    plan.close()
-    del dev, out
-    return {"workload": s["name"], "ms": ms, "gflops": algorithmic_flops(s) / ms / 1e6,
-            "roofline_ms": rl_ms, "bound": bound, "frac": rl_ms / ms,
-            "kernel": names[dom], "kernel_ms": means[dom],
-            "kernel_roofline": {"bound": kr["bound"], "achieved": kr["achieved"],
-                                "peak": kr["peak"], "unit": kr["unit"],
-                                "frac": kr["achieved"] / kr["peak"]},
-            "launch_ms": {n: m for n, m in zip(names, means)},
-            "launches": nl, "kernels": info["kernel_names"],
-            "l2": "flushed" if not big else "flushed (inputs larger than L2)"}
 
 
 def main():

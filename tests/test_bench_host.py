@@ -62,12 +62,16 @@ def test_step_roofline_picks_the_larger_bound():
 
 def test_kernel_roofline_units():
     pk = {"fp32_tflops": 80.0, "hbm_gbs": 8000.0, "bf16_tflops": 2250.0, "sm_max_mhz": 2070.0,
-          "source": "test"}
+          "source": "test", "sms": 152, "sms_source": "test"}
     s = wl.WORKLOAD_BY_NAME["conv3d_hswish_gn4_mean_n512"]
     r = bench.kernel_roofline(s, "k_conv3d_tc_mean<4,16>", 1.0, pk)
-    # three tf32 products per fp32 product, against 2250 x 1.1 / 2.25 = 1100
+    # the method's own work (2 x MACs) against the tf32 peak 2250 x 1.1 / 2.25
+    # = 1100; what the split runs on the tensor pipe (three tf32 products per
+    # fp32 product) is reported beside it
     assert r["bound"] == "tensor" and r["peak"] == pytest.approx(1100.0)
-    assert r["achieved"] == pytest.approx(3 * 34_392_244_224 / 1e-3 / 1e12)
+    assert r["achieved"] == pytest.approx(34_392_244_224 / 1e-3 / 1e12)
+    assert r["split_tf32"]["achieved"] == pytest.approx(3 * r["achieved"])
+    assert r["frac_of_fp32_peak"] == pytest.approx(r["achieved"] / 80.0)
     s2 = wl.WORKLOAD_BY_NAME["convt2d_g8_gelu_gn8_n32"]
     r = bench.kernel_roofline(s2, "k_norm_apply", 1.0, pk)
     # read + write of the 32 x 64 x 258 x 258 output
@@ -88,9 +92,16 @@ def test_reference_arm_prints_one_json_line():
     assert line["impl"] == "reference" and line["metric"] == bench.METRIC
     assert line["unit"] == "GFLOP/s" and line["value"] > 0 and line["higher_is_better"] is True
     assert line["steps"] == 2 and line["warmup"] == 3 and line["n_gpus"] == 1
-    assert line["config"]["workload"] == "conv3d_hswish_gn4_mean_n2"
+    assert line["config"] == bench.config_of(wl.WORKLOAD_BY_NAME["conv3d_hswish_gn4_mean_n2"])
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["cores"] >= 1
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_fp32_peak_follows_the_device_sm_count():
+    assert bench.peaks(148)["fp32_tflops"] == pytest.approx(
+        148 / 152 * bench.peaks(152)["fp32_tflops"])
+    assert bench.peaks(148)["sms_source"] == "device"
+    assert bench.peaks()["sms"] == bench.DEFAULT_SMS
