@@ -124,12 +124,13 @@ KERNEL_SOURCES = {
     "k_norm_apply": ("k_conv2d_norm.cu", "cn_common.cuh"),
     "k_conv3d_tc_mean": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
     "k_conv3d_tc_pool": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
+    "k_convt2d_tc": ("k_convt2d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
 }
 # tf32 tensor peak from the measured bf16 one and the nominal dense ratio
 # (1.1 / 2.25 PFLOP/s); split-TF32 runs 3 tf32 products per fp32 product
 TF32_PER_BF16 = 1.1 / 2.25
 SPLIT_TF32_PRODUCTS = 3
-TC_KERNELS = ("k_conv2d_tc", "k_conv3d_tc_mean", "k_conv3d_tc_pool")
+TC_KERNELS = ("k_conv2d_tc", "k_conv3d_tc_mean", "k_conv3d_tc_pool", "k_convt2d_tc")
 
 
 def contraction(kernel_names):

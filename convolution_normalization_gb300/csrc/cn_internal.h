@@ -30,7 +30,11 @@ int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[
                        const uint64_t strides_bytes[4], const uint32_t box[5]);
 
 // Upper bound on any device-side wait (ns of GPU wall time) before a kernel
-// gives up, records CN_ERR_TIMEOUT in the plan's flag and carries on.
+// gives up, records CN_ERR_TIMEOUT in the plan's flag and carries on.  The
+// tensor-core kernels take their progress-wait limit from their arguments
+// (wait_ns, this value unless conv_norm_plan_set_wait_limit lowered it); the
+// waits that drain copies and MMAs in flight before a CTA exits always use
+// this one.
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 // ---------------------------------------------------------------------------
@@ -41,6 +45,8 @@ struct Tc3Args {
     CUtensorMap xmap;        // x as (W, H, D, N*C_in), box (W, rb + k - 1, planes, C_in)
     const float *xmap_base;  // x pointer the map was encoded for
     int *err;                // device error flag
+    unsigned long long wait_ns;  // progress-wait limit (ns) before a timeout is recorded
+    int stall;               // failure-path test hook: CTA 0 leaves its first copy unissued
     const float *x, *w, *b, *gamma, *beta;
     float *out;
     int N, Ci, Co, D, H, W, Do, Ho, Wo;
@@ -186,6 +192,18 @@ struct Full2dArgs {
     int tc_stages;              // operand stages in shared memory
     int tc_acc_cols;            // TMEM columns per accumulator (two are allocated)
 
+    // Tensor-core grouped transposed conv (k_convt2d_tc, tct = 1): a unit is
+    // 6 output rows x 30 output columns of one (n, group), a tile 4 units of
+    // one group; the CTAs are split evenly over the groups.
+    CUtensorMap tct_xmap;       // x as (W, H, C_in, N), box (36, 8, 8, 1)
+    const float *tct_xmap_base; // x pointer the map was encoded for
+    int tct;
+    int tct_G;                  // conv groups
+    int tct_nseg, tct_nband;    // column units per output row; row bands per plane
+    int tct_U;                  // units per (n, group): nband * nseg
+    int tct_tiles_g;            // tiles per group: ceil(N * U / 4)
+    int tct_ctas_g;             // persistent CTAs per group (full2d_prepare)
+
     // CUDA-core kernel staging: use_tma = one tensor copy per stage (box
     // (pitch, rows_in, cib, 1) of x viewed as (W, H, C_in, N), zero fill
     // outside); else use_bulk = one bulk copy per row; else cp.async.
@@ -221,8 +239,11 @@ struct Full2dArgs {
                           // shifted sums S1 = sum(v - K), S2 = sum((v - K)^2) about
                           // one of the partial's own values K
     float4 *coef;         // [N][Co]: (mu, a, bb, 0)
-    int *tickets;         // [N] (unused), then [2] work/exit counters
+    int *tickets;         // [N] (unused), then work counters (2, or one per group + 1
+                          // for the tensor-core transposed conv), zero between launches
     int *err;
+    unsigned long long wait_ns;  // tensor-core kernels: progress-wait limit (ns)
+    int stall;                   // tensor-core kernels: failure-path test hook (see Tc3Args)
 };
 typedef void (*Full2dKernel)(Full2dArgs);
 struct Full2dConfig {
@@ -239,11 +260,18 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
 // does not fit it), filter-block bytes, x tensor map, filter pre-pass.
 int tc2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
 size_t tc2d_wprep_bytes(const Full2dArgs &a);
+// Tensor-core grouped transposed conv (k_convt2d_tc.cu): plan
+// (CN_ERR_UNSUPPORTED when the problem does not fit it), persistent grid for
+// `sms` SMs, x tensor map.
+int tct_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
+int tct_prepare(Full2dConfig &cfg, Full2dArgs &a, int sms);
+int tct_bind_x(Full2dArgs &a);
 int tc2d_bind_x(Full2dArgs &a);
 int tc2d_prep_launch(const Full2dConfig &cfg, const Full2dArgs &a, cudaStream_t s);
 size_t full2d_workspace(const Full2dArgs &a);
+size_t full2d_counter_bytes(const Full2dArgs &a);  // the tickets / work counters
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag);
-int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a);  // needs a device: smem attribute, grid
+int full2d_prepare(Full2dConfig &cfg, Full2dArgs &a);  // needs a device: smem attribute, grid
 int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a);
 int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s,
                   const LaunchEvents *ev = nullptr);  // may cache a tensor map in a

@@ -461,7 +461,10 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                 float *op = a.out +
                             ((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.Ho + (row_ok ? orow : 0)) * a.Wo +
                             ocol0;
-                if (nvalid == RW) {
+                const size_t o0 = (size_t)(op - a.out);
+                if (!CN_CHECK(nvalid == 0 || o0 + nvalid <= (size_t)a.N * a.Co * a.S, a.err)) {
+                    // (checked build) skip the row
+                } else if (nvalid == RW) {
                     if ((RW % 2) == 0 && (reinterpret_cast<uintptr_t>(op) & 7) == 0) {
 #pragma unroll
                         for (int i = 0; i < RW - 1; i += 2)
@@ -476,9 +479,9 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
                         if (i < nvalid) op[i] = acc[c][i];
                 }
                 m = warp_sum3(m);
-                if (lane == 0)
-                    a.partial[((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.ntiles + tin) * a.wsp + sg] =
-                        make_float4(m.x, K, m.y, m.z);
+                const size_t pi = ((((size_t)G.n * a.Co + co) * a.Dv + G.d) * a.ntiles + tin) * a.wsp + sg;
+                if (lane == 0 && CN_CHECK(pi < (size_t)a.N * a.Co * a.Dv * a.ntiles * a.wsp, a.err))
+                    a.partial[pi] = make_float4(m.x, K, m.y, m.z);
             }
         }
     }
@@ -545,6 +548,7 @@ __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_c
     const float rstd = 1.0f / sqrtf(var + a.eps);
     for (int cl = lane; cl < cpg; cl += 32) {
         const int c = g * cpg + cl;
+        if (!CN_CHECK(c < a.Co, a.err)) break;
         const float ga = a.affine ? a.gamma[c] : 1.0f;
         const float be = a.affine ? a.beta[c] : 0.0f;
         a.coef[(size_t)n * a.Co + c] =
@@ -562,8 +566,9 @@ __global__ void k_fill_scale(float4 *coef, int n, float scale) {
 // Planes run last-written first: the conv pass wrote samples roughly in
 // order, so the newest planes are the ones still in L2.
 __global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *coef, long long S,
-                                                    int vec4) {
+                                                    int vec4, int *err, long long planes) {
     const size_t plane = gridDim.x - 1 - blockIdx.x;
+    if (!CN_CHECK((long long)plane < planes, err)) return;
     const float4 cf = coef[plane];
     float *p = out + plane * (size_t)S;
     const long long step = (long long)gridDim.y * blockDim.x;
@@ -648,9 +653,13 @@ int pick_wco(int units) {
 }  // namespace
 
 int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
-    // dense Conv2d shapes that fit it go to the tensor cores
+    // dense Conv2d shapes and grouped transposed convs that fit them go to
+    // the tensor cores
+    a.tct = 0;
     if (tc2d_plan(d, a, cfg) == CN_OK) return CN_OK;
     a.tc = 0;
+    if (tct_plan(d, a, cfg) == CN_OK) return CN_OK;
+    a.tct = 0;
     const int T = d.conv == CN_CONVT2D ? 1 : 0;
     const int K = d.k;
     const int Ho = T ? d.H + K - 1 : d.H - K + 1;
@@ -825,10 +834,15 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     return CN_OK;
 }
 
+// Work counters after the N per-sample tickets: claim + exit, or one claim
+// counter per group + exit for the tensor-core transposed conv.
+static size_t full2d_tickets(const Full2dArgs &a) { return (size_t)(a.N + 2 + (a.tct ? a.tct_G : 0)); }
+size_t full2d_counter_bytes(const Full2dArgs &a) { return full2d_tickets(a) * sizeof(int); }
+
 size_t full2d_workspace(const Full2dArgs &a) {
     const size_t part = (size_t)a.N * a.Co * a.Dv * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
-    const size_t tick = (size_t)(a.N + 2) * sizeof(int);
+    const size_t tick = full2d_tickets(a) * sizeof(int);
     const size_t wprep =
         a.tc ? tc2d_wprep_bytes(a) : (size_t)a.ncob * a.nchunk * a.wstage * sizeof(float);
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
@@ -838,7 +852,7 @@ size_t full2d_workspace(const Full2dArgs &a) {
 void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
     const size_t part = (size_t)a.N * a.Co * a.Dv * a.ntiles * a.wsp * sizeof(float4);
     const size_t coef = (size_t)a.N * a.Co * sizeof(float4);
-    const size_t tick = (size_t)(a.N + 2) * sizeof(int);
+    const size_t tick = full2d_tickets(a) * sizeof(int);
     auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
     a.partial = reinterpret_cast<float4 *>(base);
     a.coef = reinterpret_cast<float4 *>(base + al(part));
@@ -847,7 +861,7 @@ void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
     a.err = err_flag;
 }
 
-int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a) {
+int full2d_prepare(Full2dConfig &cfg, Full2dArgs &a) {
     if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
@@ -859,18 +873,24 @@ int full2d_prepare(Full2dConfig &cfg, const Full2dArgs &a) {
             cudaSuccess)
         return CN_ERR_CUDA;
     if (per_sm < 1) return CN_ERR_UNSUPPORTED;
+    if (a.tct) return tct_prepare(cfg, a, sms);
     cfg.grid = (int)std::min<long long>((long long)sms * per_sm, (long long)a.items);
     return CN_OK;
 }
 
 int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a) {
     if (cfg.grid == 0 || a.items == 0) return 0;
-    return 2 + (a.apply_needed ? 2 : 0);
+    // the tensor-core transposed conv builds its filter operand itself (no pre-pass)
+    return (a.tct ? 1 : 2) + (a.apply_needed ? 2 : 0);
 }
 
 int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0 || a.items == 0) return CN_OK;
-    if (a.tc) {
+    int li = 0;  // launch index (timing events)
+    if (a.tct) {
+        const int st = tct_bind_x(a);
+        if (st != CN_OK) return st;
+    } else if (a.tc) {
         const int st = tc2d_bind_x(a);
         if (st != CN_OK) return st;
     } else if (a.use_tma && a.xmap_base != a.x) {
@@ -893,19 +913,22 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
         if (st != CN_OK) return st;
         a.xmap_base = a.x;
     }
-    record_launch(ev, 0, s);
-    if (a.tc) {
+    record_launch(ev, li++, s);
+    if (a.tct) {
+        // no filter pre-pass: each CTA builds its group's operand
+    } else if (a.tc) {
         const int st = tc2d_prep_launch(cfg, a, s);
         if (st != CN_OK) return st;
+        record_launch(ev, li++, s);
     } else {
         const int wtotal = a.ncob * a.nchunk * a.wstage;
         k_prep_weights<<<cfg.prep_grid, 256, 0, s>>>(a.w, a.wprep, cfg.K, cfg.transposed, a.Cig,
                                                       a.Cog, cfg.COT * a.wco, a.cib, a.nchunk, wtotal);
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
+        record_launch(ev, li++, s);
     }
-    record_launch(ev, 1, s);
     cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
-    record_launch(ev, 2, s);
+    record_launch(ev, li++, s);
     if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     if (a.apply_needed) {
         if (a.norm == CN_NORM_NONE) {
@@ -916,10 +939,11 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
             k_group_stats<<<blocks, 32 * kStatsWarps, 0, s>>>(a);
         }
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
-        record_launch(ev, 3, s);
+        record_launch(ev, li++, s);
         dim3 grid(cfg.apply_grid_x, cfg.apply_grid_y);
-        k_norm_apply<<<grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4);
-        record_launch(ev, 4, s);
+        k_norm_apply<<<grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4, a.err,
+                                                          (long long)a.N * a.Co);
+        record_launch(ev, li++, s);
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     }
     return CN_OK;

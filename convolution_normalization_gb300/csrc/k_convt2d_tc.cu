@@ -1,0 +1,540 @@
+// Variant 2, tensor-core transposed conv: grouped ConvTranspose2d (stride 1,
+// padding 0, 8 input and 8 output channels per group, k = 3) as an implicit
+// GEMM on the 5th-generation tensor cores, for the l2_p19 problem shape
+// (ConvTranspose2d 64 -> 64, groups 8, k = 3, then GELU and GroupNorm(8)).
+//
+// The transposed conv as a correlation.  With xp = x padded by k - 1 zeros
+// on every side and the filter flipped, wf[ci][co][ky][kx] =
+// w[ci][co][k-1-ky][k-1-kx] (the adjoint derivation of the page),
+//   y[n][co][i][j] = b[co] + sum_{ci in group} sum_{ky,kx} xp[ci][i+ky][j+kx] wf[ci][co][ky][kx],
+// an ordinary stride-1 correlation with Ho = H + k - 1, Wo = W + k - 1.
+//
+// GEMM.  A unit is ZG = 6 output rows (a band) x 30 output columns (a
+// segment) of one (sample, group).  Its input is ZG + k - 1 = 8 padded rows
+// of 32 positions; a tile packs four units (of one group, so of one filter)
+// as the four 32-lane quadrants of M = 128.  Per input row u of the tile,
+//   Dacc[m][(zg, co, kx)] += sum_ci X[u][m][ci] * wf[ci][co][u - zg][kx]
+// (wf = 0 where u - zg is not a tap) with N = (zg, co, kx) = 6 * 8 * 3 = 144
+// columns and K = the group's 8 input channels, and the output is the
+// kx-shifted sum of accumulator rows, done by the epilogue with warp
+// shuffles inside a quadrant:
+//   y[r0 + zg][c0 + m] = sum_kx Dacc[m + kx][(zg, co, kx)],  m < 30.
+// The filter operand of input row u holds taps ky = u - zg: blocks of one
+// sequence stored with ky descending and zero blocks at both ends, so B for
+// every u is a window of it (the same scheme as the tensor-core Conv3d).
+//
+// Precision: split TF32 (v = hi + lo, hi = the tf32 part the tensor core
+// reads, lo = the exact remainder): W X ~= Wh Xh + Wl Xh + Wh Xl, three MMAs
+// of K = 8 per input row: Xh(c0..7) x Wh, [Xh | Xl](c0..3) x [Wl | Wh], and
+// the same for channels 4..7.  The conv then matches an fp32 conv to ~1e-6
+// relative.
+//
+// Operands (K-major, no swizzle, a core matrix is 8 rows x 16 bytes): an
+// operand stage is [input row u][Xh c0-3 | Xh c4-7 | Xl c0-3 | Xl c4-7][128
+// positions][4 channels]; the filter is [Wl c0-3 | Wl c4-7 | Wh c0-3 | Wh
+// c4-7][block][(co, kx) rows][4 channels].  The leading-byte offset of a
+// descriptor picks the second K half anywhere, so the three MMAs differ in
+// their start addresses and offsets only.
+//
+// Warp roles (one persistent CTA per SM; the CTAs are split evenly over the
+// conv groups, each claims tiles of its group from a counter and builds its
+// group's filter operand once):
+//   warp 0      producer: four TMA tensor copies per tile (36 columns x 8
+//               rows x 8 channels each, zero fill outside x: the padding)
+//               into one of two landing buffers;
+//   warps 2-3   converters: landing [unit][c][row][col] -> operand stage;
+//   warp 1      MMA issuer (one thread): 24 MMAs per tile into one of two
+//               TMEM accumulators;
+//   warps 4-11  epilogue, thread = position: warp (q, h) reads quadrant q
+//               (unit q) and output channels 4h .. 4h + 3: the kx sum, bias,
+//               activation, the pre-norm store, and per-channel sums about
+//               the unit's first value, written as the unit's partial
+//               (count, K, S1, S2) for the statistics pass.
+// The statistics and normalize passes that follow are the ones of the other
+// 2-D paths (k_group_stats, k_norm_apply).
+#include "cn_common.cuh"
+#include "cn_internal.h"
+#include "cn_tcgen05.cuh"
+
+#include <algorithm>
+#include <cstdlib>
+
+namespace cn {
+namespace {
+
+constexpr int kK = 3;                       // filter extent
+constexpr int kCig = 8, kCog = 8;           // channels per group
+constexpr int kZG = 6;                      // output rows per unit
+constexpr int kRowsIn = kZG + kK - 1;       // staged input rows per unit
+constexpr int kSegV = 32 - (kK - 1);        // valid output columns per unit
+constexpr int kBoxW = 36;                   // TMA box columns (16-byte aligned start, +3)
+constexpr int kN = kZG * kCog * kK;         // MMA N: (zg, co, kx)
+constexpr int kAccCols = 256;               // TMEM columns per accumulator (two)
+constexpr int kArr = 128 * 16;              // one [128 positions][4 ch] operand array
+constexpr int kRowBytes = 4 * kArr;         // Xh c0-3 | Xh c4-7 | Xl c0-3 | Xl c4-7
+constexpr int kStageBytes = kRowsIn * kRowBytes;
+constexpr int kUnitLand = kCig * kRowsIn * kBoxW * 4;  // one unit's TMA box
+constexpr int kLandBytes = 4 * kUnitLand;
+constexpr int kBlk = kCog * kK * 16;        // one ky block: (co, kx) rows x 4 channels
+constexpr int kNB = 2 * kZG + kK - 2;       // blocks of one ky sequence
+constexpr int kC = kZG + kK - 2;            // block i holds ky = kC - i
+constexpr int kSeq = kNB * kBlk;            // one sequence
+constexpr int kFiltBytes = 4 * kSeq;
+constexpr int kSmemBytes = 2 * kStageBytes + 2 * kLandBytes + kFiltBytes;
+constexpr int kThreads = 384;               // 12 warps
+constexpr int kConvWarps = 2;               // warps 2-3
+constexpr int kEpiWarp0 = 4;                // epilogue: warps 4-11
+constexpr int kEpiWarps = 8;
+static_assert(kN % 16 == 0 && kN <= kAccCols, "MMA N");
+static_assert(kBlk % 128 == 0, "a block is whole 8-row core-matrix groups");
+static_assert(kUnitLand % 128 == 0, "landing units stay 128-byte aligned");
+static_assert(kSmemBytes <= 227 * 1024 - 1024, "shared memory");
+
+template <int ACT>
+CN_DEV float act_v(float t) {
+    if (ACT == ACT_HARDSWISH) return hardswish(t);
+    if (ACT == ACT_GELU) return gelu_erf(t);
+    return t;
+}
+
+// Unit u of a group (over samples, bands, segments) -> its sample, band, segment.
+struct Unit {
+    int n, band, seg;
+};
+CN_DEV Unit unit_of(const Full2dArgs &a, int u) {
+    Unit r;
+    r.n = u / a.tct_U;
+    const int rem = u - r.n * a.tct_U;
+    r.band = rem / a.tct_nseg;
+    r.seg = rem - r.band * a.tct_nseg;
+    return r;
+}
+// First x column of a unit's TMA box: 16-byte aligned, at or left of the
+// unit's first padded column (x column 30 seg - (k - 1)); off = the unit's
+// first column inside the box (0..3).
+CN_DEV int box_col(int seg, int &off) {
+    const int c = seg * kSegV - (kK - 1);
+    const int c4 = c >= 0 ? (c & ~3) : -((-c + 3) & ~3);
+    off = c - c4;
+    return c4;
+}
+
+template <int ACT>
+__global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constant__ Full2dArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t land_full[2], land_empty[2];
+    // st_full[b]: the converters wrote stage b; st_empty[b]: its MMAs are done
+    __shared__ __align__(8) uint64_t st_full[2], st_empty[2];
+    __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
+    __shared__ int s_land_tile[2], s_st_tile[2], s_acc_tile[2];  // tile or -1 to stop
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned char *stage0 = smem_raw;
+    auto stage = [&](int b) { return stage0 + (size_t)b * kStageBytes; };
+    unsigned char *land0 = stage0 + 2 * (size_t)kStageBytes;
+    auto land = [&](int b) { return land0 + (size_t)b * kLandBytes; };
+    unsigned char *filt = land0 + 2 * (size_t)kLandBytes;
+
+    // this CTA's group and its place among the group's CTAs
+    const int g = (int)blockIdx.x / a.tct_ctas_g;
+    const int cta_in_g = (int)blockIdx.x - g * a.tct_ctas_g;
+    const int units_g = a.N * a.tct_U;
+
+    // ---- setup: the group's filter operand, barriers, TMEM ----
+    {
+        // [lo | hi][channel half][block i: ky = kC - i][(co, kx) rows][4 channels]
+        float *wf = reinterpret_cast<float *>(filt);
+        for (int e = tid; e < kFiltBytes / 4; e += blockDim.x) {
+            const int j = e & 3;
+            int r = e >> 2;
+            const int row = r % (kCog * kK);
+            r /= kCog * kK;
+            const int i = r % kNB;
+            const int seq = r / kNB;  // part * 2 + half
+            const int ky = kC - i;
+            float v = 0.0f;
+            if (ky >= 0 && ky < kK) {
+                const int ci = (seq & 1) * 4 + j, co = row / kK, kx = row - co * kK;
+                // PyTorch's transposed-conv weight (C_in, C_out / groups, k, k), flipped
+                const float x = __ldg(a.w + (((size_t)(g * kCig + ci) * kCog + co) * kK + (kK - 1 - ky)) * kK +
+                                      (kK - 1 - kx));
+                v = (seq >> 1) ? x : tf32_rest(x);
+            }
+            wf[e] = v;
+        }
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&land_full[i], 1);
+            mbar_init(&land_empty[i], kConvWarps);
+            mbar_init(&st_full[i], kConvWarps);
+            mbar_init(&st_empty[i], 1);
+            mbar_init(&acc_full[i], 2);
+            mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        mbar_init(&fin_bar, 1);
+        s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(&s_tmem)),
+                     "r"(2 * kAccCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    fence_proxy_async();  // the filter operand is read by the MMAs
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    int *abort_p = const_cast<int *>(&s_abort);
+    auto wait = [&](uint64_t *bar, uint32_t par) {
+        return tc_wait(bar, par, abort_p, a.err, a.wait_ns);
+    };
+    int *work = a.tickets + a.N;  // [G] per-group work counters, then the exit counter
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int k = 0;
+            int next = cta_in_g;  // the first tile; later ones from the group's counter
+            for (;; ++k) {
+                const int lb = k & 1;
+                if (k >= 2 && !wait(&land_empty[lb], ((k >> 1) - 1) & 1)) break;
+                const int tile = next < a.tct_tiles_g ? next : -1;
+                if (tile >= 0) next = a.tct_ctas_g + atomicAdd(work + g, 1);
+                s_land_tile[lb] = tile;
+                if (tile < 0) {
+                    mbar_arrive(&land_full[lb]);
+                    ++k;
+                    break;
+                }
+                // failure-path test hook: the first landing stage of CTA 0
+                // stays unarmed, a phase nothing completes
+                if (a.stall && blockIdx.x == 0 && k == 0) continue;
+                const int nv = min(4, units_g - 4 * tile);
+                mbar_arrive_expect_tx(&land_full[lb], (uint32_t)(nv * kUnitLand));
+                for (int q = 0; q < nv; ++q) {
+                    const Unit U = unit_of(a, 4 * tile + q);
+                    int off;
+                    const int c4 = box_col(U.seg, off);
+                    tma_load_4d(land(lb) + (size_t)q * kUnitLand, &a.tct_xmap, c4,
+                                U.band * kZG - (kK - 1), g * kCig, U.n, &land_full[lb]);
+                }
+            }
+            // copies still in flight (only after an abort) land before the CTA
+            // exits; in a normal run these phases are long complete
+            for (int j = max(0, k - 2); j < k; ++j)
+                if (!(a.stall && blockIdx.x == 0 && j == 0))
+                    mbar_wait_bounded(&land_full[j & 1], (j >> 1) & 1, kWaitLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t idesc = idesc_tf32(128, kN);
+            const uint32_t wb = smem_u32(filt);
+            // B windows: input row u reads blocks kC - u .. kC - u + ZG - 1
+            const uint64_t b_hh = umma_desc(wb + 2 * kSeq + kC * kBlk, kSeq, 128);      // [Wh c0-3 | Wh c4-7]
+            const uint64_t b_c1 = umma_desc(wb + kC * kBlk, 2 * kSeq, 128);             // [Wl c0-3 | Wh c0-3]
+            const uint64_t b_c2 = umma_desc(wb + kSeq + kC * kBlk, 2 * kSeq, 128);      // [Wl c4-7 | Wh c4-7]
+            for (int k = 0;; ++k) {
+                const int b = k & 1;
+                if (!wait(&st_full[b], (k >> 1) & 1)) break;
+                const int tile = s_st_tile[b];
+                if (k >= 2 && !wait(&acc_empty[b], ((k >> 1) - 1) & 1)) break;
+                tc_fence_after();  // the epilogue's reads of this accumulator are done
+                s_acc_tile[b] = tile;
+                mbar_arrive(&acc_full[b]);  // publishes the tile (1 of 2 arrivals)
+                if (tile < 0) {
+                    mbar_arrive(&acc_full[b]);
+                    break;
+                }
+                const uint32_t d = tmem + (uint32_t)(b * kAccCols);
+                const uint32_t sa = smem_u32(stage(b));
+                const uint64_t a_hh = umma_desc(sa, kArr, 128);               // [Xh c0-3 | Xh c4-7]
+                const uint64_t a_c1 = umma_desc(sa, 2 * kArr, 128);           // [Xh c0-3 | Xl c0-3]
+                const uint64_t a_c2 = umma_desc(sa + kArr, 2 * kArr, 128);    // [Xh c4-7 | Xl c4-7]
+#pragma unroll
+                for (int u = 0; u < kRowsIn; ++u) {
+                    // descriptors are linear in the start address (16-byte units)
+                    const uint64_t au = (uint64_t)((u * kRowBytes) >> 4);
+                    const uint64_t bu = (uint64_t)((u * kBlk) >> 4);  // window start kC - u
+                    umma_tf32(d, a_hh + au, b_hh - bu, idesc, u > 0 ? 1u : 0u);
+                    umma_tf32(d, a_c1 + au, b_c1 - bu, idesc, 1u);
+                    umma_tf32(d, a_c2 + au, b_c2 - bu, idesc, 1u);
+                }
+                umma_commit(&st_empty[b]);
+                umma_commit(&acc_full[b]);  // the tile's MMAs are done (2 of 2)
+            }
+            // every MMA issued by this thread completes before TMEM is freed
+            umma_commit(&fin_bar);
+            mbar_wait_bounded(&fin_bar, 0, kWaitLimitNs);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ---------------- converters ----------------
+        const int ct = tid - 64;
+        for (int k = 0;; ++k) {
+            const int lb = k & 1, b = k & 1;
+            if (!wait(&land_full[lb], (k >> 1) & 1)) break;
+            const int tile = s_land_tile[lb];
+            if (k >= 2 && !wait(&st_empty[b], ((k >> 1) - 1) & 1)) break;
+            if (tile >= 0) {
+                const int nv = min(4, units_g - 4 * tile);
+                int offq[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    offq[q] = 0;
+                    if (q < nv) box_col(unit_of(a, 4 * tile + q).seg, offq[q]);
+                }
+                const float *src = reinterpret_cast<const float *>(land(lb));
+                unsigned char *st = stage(b);
+                // position p = (u, q, i): lane = i, so loads and stores of a
+                // warp touch consecutive words / 16-byte rows
+#pragma unroll 2
+                for (int p = ct; p < kRowsIn * 128; p += 32 * kConvWarps) {
+                    const int i = p & 31, q = (p >> 5) & 3, u = p >> 7;
+                    if (q >= nv) continue;
+                    if (!CN_CHECK(q * (kUnitLand / 4) + (kCig - 1) * kRowsIn * kBoxW + u * kBoxW + offq[q] + i <
+                                      kLandBytes / 4,
+                                  a.err))
+                        continue;
+                    const float *s = src + (size_t)q * (kUnitLand / 4) + u * kBoxW + offq[q] + i;
+                    float v[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) v[c] = s[c * kRowsIn * kBoxW];
+                    float4 *row = reinterpret_cast<float4 *>(st + (size_t)u * kRowBytes) + q * 32 + i;
+                    row[0] = make_float4(v[0], v[1], v[2], v[3]);
+                    row[128] = make_float4(v[4], v[5], v[6], v[7]);
+                    row[256] = make_float4(tf32_rest(v[0]), tf32_rest(v[1]), tf32_rest(v[2]), tf32_rest(v[3]));
+                    row[384] = make_float4(tf32_rest(v[4]), tf32_rest(v[5]), tf32_rest(v[6]), tf32_rest(v[7]));
+                }
+                fence_proxy_async();
+            }
+            __syncwarp();
+            if (lane == 0) {
+                if (warp == 2) s_st_tile[b] = tile;
+                mbar_arrive(&land_empty[lb]);
+                mbar_arrive(&st_full[b]);
+            }
+            if (tile < 0) break;
+        }
+    } else {
+        // ---------------- epilogue ----------------
+        const int q = warp & 3;                 // TMEM lane quadrant = unit of the tile
+        const int h = (warp - kEpiWarp0) >> 2;  // output channels 4h .. 4h + 3
+        const int co0 = g * kCog + 4 * h;
+        float bias[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) bias[c] = a.b ? __ldg(a.b + co0 + c) : 0.0f;
+        for (int k = 0;; ++k) {
+            const int b = k & 1;
+            if (!wait(&acc_full[b], (k >> 1) & 1)) break;
+            const int tile = s_acc_tile[b];
+            if (tile < 0) break;
+            tc_fence_after();
+            const int unit = 4 * tile + q;
+            if (unit < units_g) {  // uniform per warp
+                const Unit U = unit_of(a, unit);
+                const int r0 = U.band * kZG, c0 = U.seg * kSegV;
+                const int rows_ok = min(kZG, a.Ho - r0);
+                const int col = c0 + lane;
+                const bool col_ok = lane < kSegV && col < a.Wo;
+                const uint32_t tq = tmem + (uint32_t)(b * kAccCols) + ((uint32_t)(q * 32) << 16);
+                float ksh[4], s1[4], s2[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    ksh[c] = 0.0f;
+                    s1[c] = 0.0f;
+                    s2[c] = 0.0f;
+                }
+                float *obase = a.out + ((size_t)U.n * a.Co + co0) * (size_t)a.S + (size_t)r0 * a.Wo + col;
+#pragma unroll 1
+                for (int zg = 0; zg < kZG; ++zg) {
+                    uint32_t v[12];
+                    const uint32_t ta = tq + (uint32_t)(zg * kCog * kK + 4 * h * kK);
+                    tmem_ld8(ta, v);
+                    tmem_ld4(ta + 8, v + 8);
+                    tmem_wait_ld();
+                    const bool ok = col_ok && zg < rows_ok;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        float acc = __uint_as_float(v[c * kK]);
+#pragma unroll
+                        for (int kx = 1; kx < kK; ++kx)
+                            acc += __shfl_down_sync(0xffffffffu, __uint_as_float(v[c * kK + kx]), kx);
+                        const float y = act_v<ACT>(acc + bias[c]);
+                        // shift of the unit's sums: its first value (row r0,
+                        // column c0: always inside the output)
+                        if (zg == 0) ksh[c] = __shfl_sync(0xffffffffu, y, 0);
+                        const float dl = ok ? y - ksh[c] : 0.0f;
+                        s1[c] += dl;
+                        s2[c] = fmaf(dl, dl, s2[c]);
+                        if (ok && CN_CHECK((size_t)(obase - a.out) + (size_t)c * a.S + (size_t)zg * a.Wo <
+                                               (size_t)a.N * a.Co * a.S,
+                                           a.err))
+                            obase[(size_t)c * a.S + (size_t)zg * a.Wo] = y;
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        s1[c] += __shfl_xor_sync(0xffffffffu, s1[c], o);
+                        s2[c] += __shfl_xor_sync(0xffffffffu, s2[c], o);
+                    }
+                }
+                if (lane == 0) {
+                    const float cnt = (float)(rows_ok * min(kSegV, a.Wo - c0));
+                    const int ui = U.band * a.tct_nseg + U.seg;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        if (CN_CHECK(((size_t)U.n * a.Co + co0 + c) * a.tct_U + ui < (size_t)a.N * a.Co * a.tct_U,
+                                     a.err))
+                            a.partial[((size_t)U.n * a.Co + co0 + c) * a.tct_U + ui] =
+                                make_float4(cnt, ksh[c], s1[c], s2[c]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
+    }
+
+    // ---- teardown ----
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                     "r"(2 * kAccCols)
+                     : "memory");
+    // the last CTA to leave resets the work counters for the next launch
+    if (tid == 0 && atomicAdd(work + a.tct_G, 1) == (int)gridDim.x - 1) {
+        for (int i = 0; i <= a.tct_G; ++i) work[i] = 0;
+    }
+}
+
+}  // namespace
+
+// Plans the tensor-core transposed conv; CN_ERR_UNSUPPORTED when the problem
+// does not fit it (the CUDA-core kernel then takes it).
+int tct_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
+    if (d.conv != CN_CONVT2D) return CN_ERR_UNSUPPORTED;
+    if (d.C_in / d.groups != kCig || d.C_out / d.groups != kCog || d.k != kK) return CN_ERR_UNSUPPORTED;
+    // x rows must be 16-byte multiples for the tensor map
+    if (d.W % 4 != 0 || !tma_available()) return CN_ERR_UNSUPPORTED;
+    const char *e = getenv("CN_NO_TC");
+    if (e && atoi(e)) return CN_ERR_UNSUPPORTED;
+    const int Ho = d.H + kK - 1, Wo = d.W + kK - 1;
+    const int nseg = (Wo + kSegV - 1) / kSegV, nband = (Ho + kZG - 1) / kZG;
+    const long long U = (long long)nseg * nband;
+    const long long units_g = (long long)d.N * U;
+    const long long tiles_g = (units_g + 3) / 4;
+    if (units_g > 0x3fffffffLL || (long long)d.groups * tiles_g > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+
+    a.tc = 0;
+    a.tct = 1;
+    a.tct_xmap_base = nullptr;
+    a.wait_ns = kWaitLimitNs;
+    a.tct_G = d.groups;
+    a.tct_nseg = nseg;
+    a.tct_nband = nband;
+    a.tct_U = (int)U;
+    a.tct_tiles_g = (int)tiles_g;
+    a.tct_ctas_g = 1;  // set from the device by full2d_prepare
+    a.use_bulk = 1;
+    a.use_tma = 0;
+    a.N = d.N;
+    a.Ci = d.C_in;
+    a.Co = d.C_out;
+    a.H = d.H;
+    a.W = d.W;
+    a.Ho = Ho;
+    a.Wo = Wo;
+    a.Cig = kCig;
+    a.Cog = kCog;
+    a.KD = 1;
+    a.Din = 1;
+    a.Dv = 1;
+    a.row_tiles = nband;
+    a.col_tiles = nseg;
+    a.ncob = 0;
+    a.nchunk = 0;
+    a.wstage = 0;
+    a.ntiles = (int)U;  // partials per channel: one per unit
+    a.wsp = 1;
+    a.items = (int)(d.groups * tiles_g);
+    a.wprep = nullptr;
+    a.act = d.act;
+    a.norm = d.norm;
+    a.NG = d.norm == CN_NORM_GROUP ? d.num_groups : d.C_out;
+    a.affine = d.affine && d.norm != CN_NORM_NONE;
+    a.eps = d.eps;
+    a.post_scale = d.post_scale;
+    a.S = (long long)Ho * Wo;
+    a.apply_needed = !(d.norm == CN_NORM_NONE && d.post_scale == 1.0f);
+    a.vec4 = (a.S % 4) == 0;
+
+    switch (d.act) {
+        case CN_ACT_NONE:
+            cfg.kern = k_convt2d_tc<ACT_NONE>;
+            cfg.names = "k_convt2d_tc<0>,k_group_stats,k_norm_apply";
+            break;
+        case CN_ACT_HARDSWISH:
+            cfg.kern = k_convt2d_tc<ACT_HARDSWISH>;
+            cfg.names = "k_convt2d_tc<1>,k_group_stats,k_norm_apply";
+            break;
+        case CN_ACT_GELU_ERF:
+            cfg.kern = k_convt2d_tc<ACT_GELU>;
+            cfg.names = "k_convt2d_tc<2>,k_group_stats,k_norm_apply";
+            break;
+        default:
+            return CN_ERR_UNSUPPORTED;
+    }
+    cfg.K = kK;
+    cfg.RW = 0;
+    cfg.COT = kCog;
+    cfg.VECW = 0;
+    cfg.transposed = 1;
+    cfg.threads = kThreads;
+    cfg.smem = kSmemBytes;
+    cfg.grid = d.groups;  // refined from the device in full2d_prepare
+    cfg.prep_grid = 0;
+    cfg.apply_threads = 256;
+    const long long units = a.vec4 ? a.S / 4 : a.S;
+    const long long gy = (units + 256 * 4 - 1) / (256 * 4);
+    cfg.apply_grid_y = (int)std::max(1LL, std::min(gy, 65535LL));
+    const long long gx = (long long)d.N * d.C_out;
+    if (gx > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.apply_grid_x = (int)gx;
+    return CN_OK;
+}
+
+// Persistent grid: the same number of CTAs for every group (each builds its
+// group's filter once), as many as the SMs allow, capped by the group's tiles.
+int tct_prepare(Full2dConfig &cfg, Full2dArgs &a, int sms) {
+    a.tct_ctas_g = std::max(1, std::min(sms / std::max(1, a.tct_G), a.tct_tiles_g));
+    const long long grid = (long long)a.tct_G * a.tct_ctas_g;
+    if (grid > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.grid = a.tct_tiles_g > 0 ? (int)grid : 0;
+    return CN_OK;
+}
+
+// Encodes the input tensor map for this x (cached while x stays the same):
+// x as (W, H, C_in, N), box (36 columns, 8 rows, 8 channels, 1).
+int tct_bind_x(Full2dArgs &a) {
+    if (a.tct_xmap_base == a.x) return CN_OK;
+    const uint64_t dims[4] = {(uint64_t)a.W, (uint64_t)a.H, (uint64_t)a.Ci, (uint64_t)a.N};
+    const uint64_t strides[3] = {(uint64_t)a.W * 4, (uint64_t)a.H * a.W * 4,
+                                 (uint64_t)a.Ci * a.H * a.W * 4};
+    const uint32_t box[4] = {(uint32_t)kBoxW, (uint32_t)kRowsIn, (uint32_t)kCig, 1u};
+    const int st = encode_tmap_f32_4d(&a.tct_xmap, a.x, dims, strides, box);
+    if (st != CN_OK) return st;
+    a.tct_xmap_base = a.x;
+    return CN_OK;
+}
+
+}  // namespace cn

@@ -87,7 +87,7 @@ NORM_PATHS = {
     "mean_in": (MEAN_IN, "k_conv3d_tc_mean", "k_conv3d_act_mean"),
     "conv2d_in": (CONV2D, "k_conv2d_tc", "k_conv2d_act_stats"),
     "conv2d_gn": (CONV2D_GN, "k_conv2d_act_stats", "k_conv2d_act_stats"),
-    "convt_g8": (CONVT, "k_conv2d_act_stats", "k_conv2d_act_stats"),
+    "convt_g8": (CONVT, "k_convt2d_tc", "k_conv2d_act_stats"),
     "convt_g1": (CONVT_G1, "k_conv2d_act_stats", "k_conv2d_act_stats"),
     "conv3d_full": (CONV3D_FULL, "k_conv2d_act_stats", "k_conv2d_act_stats"),
 }
