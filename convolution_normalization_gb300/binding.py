@@ -15,7 +15,10 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libconv_norm.so")
+# CONV_NORM_LIB=checked loads the bounds-checked build (libconv_norm_checked.so,
+# ``build(checked=True)``) instead of the normal one
+LIB_PATH = os.path.join(_HERE, "libconv_norm_checked.so"
+                        if os.environ.get("CONV_NORM_LIB") == "checked" else "libconv_norm.so")
 
 CN_OK = 0
 CN_ERR_INVALID_ARG = -1
@@ -59,7 +62,8 @@ EXPORTED = ("conv_norm_desc_validate", "conv_norm_output_shape", "conv_norm_stat
             "conv_norm_plan_create", "conv_norm_plan_destroy", "conv_norm_workspace_bytes",
             "conv_norm_plan_info", "conv_norm_forward", "conv_norm_forward_host",
             "conv_norm_plan_check_device", "conv_norm_forward_noalloc",
-            "conv_norm_plan_set_launch_events")
+            "conv_norm_plan_set_launch_events", "conv_norm_plan_set_wait_limit",
+            "conv_norm_plan_inject_stall")
 
 
 def _load():
@@ -94,6 +98,10 @@ def _load():
     lib.conv_norm_forward_noalloc.restype = i
     lib.conv_norm_plan_set_launch_events.argtypes = [vp, ctypes.POINTER(vp), i]
     lib.conv_norm_plan_set_launch_events.restype = i
+    lib.conv_norm_plan_set_wait_limit.argtypes = [vp, ctypes.c_uint64]
+    lib.conv_norm_plan_set_wait_limit.restype = i
+    lib.conv_norm_plan_inject_stall.argtypes = [vp]
+    lib.conv_norm_plan_inject_stall.restype = i
     return lib
 
 
@@ -218,6 +226,16 @@ def conv_norm_plan_check_device(plan, stream=None) -> int:
     return lib.conv_norm_plan_check_device(plan, _stream(stream))
 
 
+def conv_norm_plan_set_wait_limit(plan, ns) -> int:
+    """Status of setting the tensor-core kernel's progress-wait limit (ns)."""
+    return lib.conv_norm_plan_set_wait_limit(plan, int(ns))
+
+
+def conv_norm_plan_inject_stall(plan) -> int:
+    """Status of arming the one-shot stall of the plan's next forward."""
+    return lib.conv_norm_plan_inject_stall(plan)
+
+
 def conv_norm_plan_set_launch_events(plan, events) -> int:
     """events: launches_per_forward + 1 torch.cuda.Event objects (already
     recorded once, so the CUDA events exist), or None/[] to stop."""
@@ -251,6 +269,14 @@ class Plan:
 
     def set_launch_events(self, events):
         return conv_norm_plan_set_launch_events(self.handle, events)
+
+    def set_wait_limit(self, ns):
+        """Limit (ns) of the tensor-core kernel's progress waits; returns the status."""
+        return conv_norm_plan_set_wait_limit(self.handle, ns)
+
+    def inject_stall(self):
+        """The next forward stalls one CTA on purpose (failure-path test hook)."""
+        return conv_norm_plan_inject_stall(self.handle)
 
     def close(self):
         if self.handle:

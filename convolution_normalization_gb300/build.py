@@ -1,7 +1,11 @@
 """Builds the conv_norm C-ABI shared library in-tree with nvcc (sm_103a).
 
 Every ``csrc/*.cu`` translation unit is compiled in parallel into
-``_build/*.o`` and linked into ``libconv_norm.so`` next to this file.  The
+``_build/*.o`` and linked into ``libconv_norm.so`` next to this file.
+``build(checked=True)`` makes the bounds-checked variant
+``libconv_norm_checked.so`` (``-DCN_CHECKS``, objects in ``_build_checked``):
+its kernels test the index of every main store and shared-memory operand
+write and report a failed test as CN_ERR_DEVICE_CHECK instead of making it.  The
 CUDA runtime is linked statically, so the library needs only the driver at
 run time.  Rebuilds are skipped when the library is newer than every source.
 
@@ -21,6 +25,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libconv_norm.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libconv_norm_checked.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -48,23 +54,26 @@ def _deps():
                                                   os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not extra_flags and up_to_date():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    lib_path = LIB_CHECKED if checked else LIB
+    bdir = BUILD_CHECKED if checked else BUILD
+    flags = [*extra_flags] + (["-DCN_CHECKS"] if checked else [])
+    if not force and not extra_flags and up_to_date(lib_path):
+        return lib_path
     nvcc = nvcc_path()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -74,17 +83,18 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     force = "--force" in sys.argv
     verbose = "-v" in sys.argv
     extra = ["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []
-    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra_flags=extra))
+    print(build(force=force or bool(extra), verbose=verbose or bool(extra), extra_flags=extra,
+                checked="--checked" in sys.argv))

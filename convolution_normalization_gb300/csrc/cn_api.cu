@@ -47,6 +47,9 @@ struct conv_norm_plan_s {
     void *ws = nullptr;  // [error flag | variant workspace]
     size_t ws_bytes = 0;
     int *err_flag = nullptr;
+    int *counters = nullptr;  // tickets and work counters: zero between launches
+    size_t counter_bytes = 0;
+    int stall_pending = 0;    // conv_norm_plan_inject_stall: the next forward stalls
     Mean3dArgs mean_args;
     Mean3dConfig mean_cfg;
     Pool3dArgs pool_args;
@@ -267,14 +270,20 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
             a.partial = reinterpret_cast<double *>(vbase);
             a.tickets = reinterpret_cast<int *>(vbase + ((part + 255) & ~(size_t)255));
             a.err = p->err_flag;
+            p->counters = a.tickets;
+            p->counter_bytes = (size_t)(a.N + 2) * sizeof(int);
             break;
         }
         case V_POOL3D:
             p->pool_args.err = p->err_flag;
             p->pool_args.t.work = reinterpret_cast<int *>(vbase);  // zero between launches
+            p->counters = p->pool_args.t.work;
+            p->counter_bytes = pool3d_workspace(p->pool_args);
             break;
         default:
             full2d_bind_workspace(p->full_args, vbase, p->err_flag);
+            p->counters = p->full_args.tickets;
+            p->counter_bytes = full2d_counter_bytes(p->full_args);
             break;
     }
     *out = p;
@@ -363,23 +372,31 @@ static int forward_impl(conv_norm_plan p, const float *x, const float *w, const 
         return CN_ERR_CUDA;
     }
     int st;
+    const int stall = p->stall_pending;  // one forward only
+    p->stall_pending = 0;
     switch (p->variant) {
         case V_MEAN3D: {
             Mean3dArgs &a = p->mean_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
+            a.t.stall = stall;
             st = mean3d_launch(p->mean_cfg, a, s, ev);
+            a.t.stall = 0;
             break;
         }
         case V_POOL3D: {
             Pool3dArgs &a = p->pool_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.out = out;
+            a.t.stall = stall;
             st = pool3d_launch(p->pool_cfg, a, s, ev);
+            a.t.stall = 0;
             break;
         }
         default: {
             Full2dArgs &a = p->full_args;  // keeps the encoded tensor map cached
             a.x = x; a.w = w; a.b = b; a.gamma = gamma; a.beta = beta; a.out = out;
+            a.stall = stall;
             st = full2d_launch(p->full_cfg, a, s, ev);
+            a.stall = 0;
             break;
         }
     }
@@ -569,6 +586,34 @@ int conv_norm_forward_host(conv_norm_plan p, const float *x, const float *w, con
     return st;
 }
 
+static bool has_tc_kernel(const conv_norm_plan_s *p);
+
+int conv_norm_plan_set_wait_limit(conv_norm_plan p, uint64_t ns) {
+    if (!p || ns == 0) return CN_ERR_INVALID_ARG;
+    if (!has_tc_kernel(p)) return CN_ERR_UNSUPPORTED;
+    switch (p->variant) {
+        case V_MEAN3D: p->mean_args.t.wait_ns = ns; break;
+        case V_POOL3D: p->pool_args.t.wait_ns = ns; break;
+        default: p->full_args.wait_ns = ns; break;
+    }
+    return CN_OK;
+}
+
+static bool has_tc_kernel(const conv_norm_plan_s *p) {
+    switch (p->variant) {
+        case V_MEAN3D: return p->mean_args.tc != 0;
+        case V_POOL3D: return p->pool_args.tc != 0;
+        default: return p->full_args.tc || p->full_args.tct;
+    }
+}
+
+int conv_norm_plan_inject_stall(conv_norm_plan p) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    if (!has_tc_kernel(p)) return CN_ERR_UNSUPPORTED;
+    p->stall_pending = 1;
+    return CN_OK;
+}
+
 int conv_norm_plan_check_device(conv_norm_plan p, void *stream) {
     if (!p) return CN_ERR_INVALID_ARG;
     int cur = -1;
@@ -590,6 +635,9 @@ int conv_norm_plan_check_device(conv_norm_plan p, void *stream) {
         } else if (flag != 0) {
             const int zero = 0;
             cudaMemcpy(q->err_flag, &zero, sizeof(int), cudaMemcpyHostToDevice);
+            // a kernel that gave up may have left tickets and work counters
+            // part-way: zero them so the plan's next forward starts clean
+            if (q->counters && q->counter_bytes) cudaMemset(q->counters, 0, q->counter_bytes);
             if (st != CN_ERR_TIMEOUT) st = flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
         }
     }

@@ -215,6 +215,15 @@ CN_DEV bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 CN_DEV void flag_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
+// Bounds checks of the checked build (-DCN_CHECKS, a stand-in for a memory
+// checker): CN_CHECK(cond, err) is cond, and when cond fails it records
+// ERR_CHECK (CN_ERR_DEVICE_CHECK) in the flag, so the caller skips the
+// access.  Normal builds compile every check to true.
+#ifdef CN_CHECKS
+#define CN_CHECK(cond, err) ((cond) ? true : (::cn::flag_error((err), ::cn::ERR_CHECK), false))
+#else
+#define CN_CHECK(cond, err) true
+#endif
 // Tiled 4-D tensor copy global -> shared, completion counted on bar.
 CN_DEV void tma_load_4d(void *smem_dst, const void *tmap, int c0, int c1, int c2, int c3,
                         uint64_t *bar) {

@@ -47,7 +47,7 @@ CN_DEV void mean_write_output(const Args &a, int n, int c, const double *sch) {
         const double be = a.affine ? (double)a.beta[c] : 0.0;
         val = ga * (mc - mg.mean) * rstd + be;
     }
-    a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
+    if (CN_CHECK(n < a.N && c < a.Co, a.err)) a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
 }
 
 }  // namespace cn

@@ -81,16 +81,18 @@ CN_DEV void tmem_ld4(uint32_t taddr, uint32_t *r) {
 CN_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 
-// Bounded wait with a CTA-local abort: after one wait gives up, every role
-// stops at its next wait instead of running into further timeouts.
-CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err) {
+// Bounded wait with a CTA-local abort: after one wait gives up (limit_ns of
+// GPU wall time without the phase completing), every role stops at its next
+// wait instead of running into further timeouts.
+CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                    uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 255u) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 flag_error(err, ERR_TIMEOUT);
                 *abort = 1;
                 return false;

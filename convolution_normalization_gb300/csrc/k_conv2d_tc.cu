@@ -153,7 +153,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     int *abort_p = const_cast<int *>(&s_abort);
-    auto wait = [&](uint64_t *bar, uint32_t par) { return tc_wait(bar, par, abort_p, a.err); };
+    auto wait = [&](uint64_t *bar, uint32_t par) {
+        return tc_wait(bar, par, abort_p, a.err, a.wait_ns);
+    };
 
     const int per_sample = a.row_tiles * a.ncob;
 
@@ -163,6 +165,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
         // slot indices and phase parities advance incrementally.
         if (lane == 0) {
             int kl = 0, kw = 0;  // landing / filter stages armed so far
+            // failure-path test hook: CTA 0 never arms its first landing stage,
+            // a barrier phase nothing completes, so the waits on it run out
+            const bool stall = a.stall && blockIdx.x == 0;
             int lb = 0, b = 0;
             uint32_t lph = 0, sph = 0;  // parity of the current pass over each ring
             int next = (int)blockIdx.x;
@@ -185,7 +190,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                         break;
                     }
                     s_land_tile[lb] = tile;
-                    if (tile >= 0) {
+                    if (stall && kl == 0) {
+                        // left unarmed (never drained below)
+                    } else if (tile >= 0) {
                         mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.tc_land_bytes);
                         tma_load_4d(land(lb), &a.tc_xmap, 0, rt * a.tc_R, 4 * g, n, &land_full[lb]);
                     } else {
@@ -221,7 +228,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
             // copies still in flight (only after an abort) land before the CTA
             // exits; in a normal run these phases are long complete
             for (int j = std::max(0, kl - kTcLand); j < kl; ++j)
-                mbar_wait_bounded(&land_full[j % kTcLand], (j / kTcLand) & 1, kWaitLimitNs);
+                if (!(stall && j == 0))
+                    mbar_wait_bounded(&land_full[j % kTcLand], (j / kTcLand) & 1, kWaitLimitNs);
             for (int j = std::max(0, kw - NS); j < kw; ++j)
                 mbar_wait_bounded(&full[j % NS], (j / NS) & 1, kWaitLimitNs);
         }
@@ -323,6 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
                 float4 *xl = reinterpret_cast<float4 *>(stage(b) + a.tc_xbuf_bytes);
                 for (int p = ct; p < npix; p += 128) {
+                    if (!CN_CHECK(p < a.tc_xbuf_bytes / 16, a.err)) break;
                     const float v0 = src[p], v1 = src[npix + p], v2 = src[2 * npix + p],
                                 v3 = src[3 * npix + p];
                     xh[p] = make_float4(v0, v1, v2, v3);
@@ -392,7 +401,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
                     scr[lane * 33 + j] = y;
                 }
                 __syncwarp();
-                if (vl) {
+                if (vl && CN_CHECK((size_t)(obase - a.out) + (size_t)(r0 + rr) * a.Wo + col +
+                                           31 * (size_t)S < (size_t)a.N * a.Co * S,
+                                       a.err)) {
                     float *op = obase + (size_t)(r0 + rr) * a.Wo + col;
 #pragma unroll 8
                     for (int c = 0; c < 32; ++c) op[(size_t)c * S] = scr[c * 33 + lane];
@@ -403,7 +414,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_conv2d_tc(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[as]);
             const float cnt = (float)(rows_ok * a.Wo);
-            a.partial[((size_t)n * a.Co + co) * a.ntiles + rt] = make_float4(cnt, Ksh, s1, s2);
+            if (CN_CHECK(((size_t)n * a.Co + co) * a.ntiles + rt < (size_t)a.N * a.Co * a.ntiles, a.err))
+                a.partial[((size_t)n * a.Co + co) * a.ntiles + rt] = make_float4(cnt, Ksh, s1, s2);
         }
     }
 
@@ -462,6 +474,7 @@ int tc2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
 
     a.tc = 1;
     a.tc_xmap_base = nullptr;
+    a.wait_ns = kWaitLimitNs;
     a.tc_K = K;
     a.tc_R = R;
     a.tc_npos = npos;

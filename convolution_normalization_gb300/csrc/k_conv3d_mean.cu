@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(mean_max_threads(COT, RW), 1)
                 const double *o = sred + ((size_t)g * COB + c) * 3;
                 m = merge(m, Moments<double>{o[0], o[1], o[2]});
             }
+            if (!CN_CHECK(n < a.N && chunk < a.nchunks && co0 + c < a.Co, a.err)) continue;
             double *p = a.partial + (((size_t)n * a.nchunks + chunk) * a.Co + co0 + c) * 3;
             p[0] = m.n;
             p[1] = m.mean;

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(256) k_conv3d_softmax_pool4(const __grid_const
         const int n = (int)(g / a.Pd);
 #pragma unroll
         for (int c = 0; c < CO; ++c) {
-            if ((c % 16) == l16) {
+            if ((c % 16) == l16 && CN_CHECK(n < a.N, a.err)) {
                 a.out[((((size_t)n * CO + c) * a.Pd + pd) * a.Ph + ph) * a.Pw + pw] = best[c] * a.post_scale;
             }
         }

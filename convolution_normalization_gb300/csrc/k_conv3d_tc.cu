@@ -201,7 +201,7 @@ CN_DEV void tc3_finish_sample(const Tc3Args &a, int n, int c) {
         const double be = a.affine && on ? (double)a.beta[c] : 0.0;
         val = ga * (mc - mu) * (double)rstd + be;
     }
-    if (on) a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
+    if (on && CN_CHECK(n < a.N, a.err)) a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
 }
 
 template <int K, int CO, int MODE>
@@ -322,7 +322,9 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     int *abort_p = const_cast<int *>(&s_abort);
-    auto wait = [&](uint64_t *bar, uint32_t par) { return tc_wait(bar, par, abort_p, a.err); };
+    auto wait = [&](uint64_t *bar, uint32_t par) {
+        return tc_wait(bar, par, abort_p, a.err, a.wait_ns);
+    };
 
     if (warp == 0) {
         // ---------------- producer (+ mean finisher) ----------------
@@ -361,7 +363,10 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                             }
                         }
                         s_land_info[lb] = make_int4(item, band, band == bend - 1, nzv);
-                        if (item >= 0) {
+                        if (a.stall && blockIdx.x == 0 && k == 0) {
+                            // failure-path test hook: the first landing stage of
+                            // CTA 0 stays unarmed, a phase nothing completes
+                        } else if (item >= 0) {
                             mbar_arrive_expect_tx(&land_full[lb], (uint32_t)a.land);
                             tma_load_4d(land(lb), &a.xmap, 0, band * a.rb, z0, n * a.Ci, &land_full[lb]);
                         } else {
@@ -394,7 +399,8 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         const float2 sums = lane < CO ? s_post[pr][lane] : make_float2(0.f, 0.f);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&post_empty[pr]);  // the ring entry is read
-                        if (lane < CO) a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = sums;
+                        if (lane < CO && CN_CHECK(pn < a.N && chunk < nchunks, a.err))
+                            a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = sums;
                         __syncwarp();
                         // the ticket publishes the warp's slot writes; the last
                         // item of the sample sees every other item's slot
@@ -426,7 +432,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         quit = 1;
                     } else if (t_idle == 0) {
                         t_idle = now;
-                    } else if (now - t_idle > kWaitLimitNs) {
+                    } else if (now - t_idle > a.wait_ns) {
                         flag_error(a.err, ERR_TIMEOUT);
                         *abort_p = 1;
                         quit = 1;
@@ -438,7 +444,8 @@ CN_DEV void tc3_body(const Tc3Args &a) {
         // a copy still in flight (only after an abort) lands before the CTA exits
         if (lane == 0)
             for (int j = max(0, k - a.nland); j < k; ++j)
-                mbar_wait_bounded(&land_full[j % a.nland], (j / a.nland) & 1, kWaitLimitNs);
+                if (!(a.stall && blockIdx.x == 0 && j == 0))
+                    mbar_wait_bounded(&land_full[j % a.nland], (j / a.nland) & 1, kWaitLimitNs);
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
@@ -550,7 +557,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const int p = p0 + j * CT;
-                            if (p < P0) {
+                            if (p < P0 && CN_CHECK(P0 <= PP, a.err)) {
                                 xh[(size_t)u * PP + p] = make_float4(v[j][0], v[j][1], v[j][2], v[j][3]);
                                 xl[(size_t)u * PP + p] =
                                     make_float4(tf32_rest(v[j][0]), tf32_rest(v[j][1]),
@@ -786,6 +793,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 if (ph < a.Ph && pcol < a.Pw) {
                     int n, g, z0, nzv;
                     item_group(info.x, n, g, z0, nzv);
+                    if (CN_CHECK(n < a.N && g < a.Pd, a.err))
                     a.out[((((size_t)n * CO + c) * a.Pd + g) * a.Ph + ph) * a.Pw + pcol] =
                         a.post_scale * __uint_as_float(cells[et]);
                 }
@@ -895,6 +903,7 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     if (items > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
 
     a.xmap_base = nullptr;
+    a.wait_ns = kWaitLimitNs;
     a.N = d.N;
     a.Ci = d.C_in;
     a.Co = d.C_out;

@@ -211,8 +211,40 @@ int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
  * flag and those of the chunk plans conv_norm_forward_host created.  Returns
  * CN_OK, CN_ERR_TIMEOUT (a bounded device wait gave up; the
  * output of that forward is undefined), CN_ERR_DEVICE_CHECK or CN_ERR_CUDA.
+ * When a flag was set it also zeroes that plan's tickets and work counters,
+ * which a kernel that gave up can leave part-way, so the plan's next
+ * forward runs normally.
  */
 int conv_norm_plan_check_device(conv_norm_plan plan, void *cuda_stream);
+
+/*
+ * Failure handling (no counterpart in the transcripts).  Every wait of a
+ * kernel on another part of its work (a copy landing, an MMA finishing, a
+ * pipeline slot freeing) is bounded: after the limit it records
+ * CN_ERR_TIMEOUT in the plan's flag, the CTA stops its other roles, waits
+ * (with the fixed 200 ms bound) for its own copies and MMAs in flight,
+ * frees its tensor memory and exits.  This sets the limit of those progress
+ * waits for the plan's tensor-core kernel, in ns of GPU wall time (default
+ * 200 ms); a very short limit makes a forward give up on purpose, which is
+ * how the timeout path is tested.  The CUDA-core kernels keep the fixed
+ * limit.  The chunk plans of conv_norm_forward_host keep the default.
+ * Errors: CN_ERR_INVALID_ARG (NULL plan, ns == 0), CN_ERR_UNSUPPORTED (the
+ * plan runs no tensor-core kernel).
+ */
+int conv_norm_plan_set_wait_limit(conv_norm_plan plan, uint64_t ns);
+
+/*
+ * Failure-path test hook (no counterpart in the transcripts): the plan's
+ * next forward runs its tensor-core kernel with the first input copy of
+ * CTA 0 left unissued, a barrier phase that nothing completes.  That CTA's
+ * waits run out after the plan's wait limit, it stops and exits as above,
+ * the other CTAs finish their own work, and conv_norm_plan_check_device
+ * then returns CN_ERR_TIMEOUT; the output of that forward is undefined.
+ * Nothing faults and no wait is unbounded.  One forward only.
+ * Errors: CN_ERR_INVALID_ARG (NULL plan), CN_ERR_UNSUPPORTED (the plan
+ * runs no tensor-core kernel).
+ */
+int conv_norm_plan_inject_stall(conv_norm_plan plan);
 
 /*
  * Optional per-launch timing (a measurement aid; no counterpart in the
