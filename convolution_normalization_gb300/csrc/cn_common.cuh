@@ -71,6 +71,42 @@ CN_DEV float gelu_erf(float v) {
     const float e = ex2_approx(v * (v * (-0.5f * 1.4426950408889634f)));
     return fmaf(-av, y * e, fmaxf(v, 0.0f));
 }
+// ---- packed fp32 pairs (one instruction for two lanes of a float2) -----------
+// Each lane is rounded as the scalar operation rounds it (round to nearest;
+// fma fused), so pairs give the same bits as two scalar operations.
+CN_DEV uint64_t f2_bits(float2 a) { return (uint64_t)__float_as_uint(a.x) | ((uint64_t)__float_as_uint(a.y) << 32); }
+CN_DEV float2 f2_of(uint64_t r) { return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32))); }
+CN_DEV float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)), "l"(f2_bits(c)));
+    return f2_of(r);
+}
+CN_DEV float2 add2(float2 a, float2 b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_of(r);
+}
+CN_DEV float2 mul2(float2 a, float2 b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+    return f2_of(r);
+}
+CN_DEV float2 f2(float v) { return make_float2(v, v); }
+// gelu_erf of two values, with the same operations (and so the same bits)
+// as gelu_erf on each.
+CN_DEV float2 gelu_erf2(float2 v) {
+    const float2 av = make_float2(fabsf(v.x), fabsf(v.y));
+    const float2 d = fma2(f2(CN_AS_P * 0.70710678118654752f), av, f2(1.0f));
+    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 y = fma2(t, f2(0.5f * CN_AS_A5), f2(0.5f * CN_AS_A4));
+    y = fma2(t, y, f2(0.5f * CN_AS_A3));
+    y = fma2(t, y, f2(0.5f * CN_AS_A2));
+    y = fma2(t, y, f2(0.5f * CN_AS_A1));
+    y = mul2(y, t);
+    const float2 q = mul2(v, mul2(v, f2(-0.5f * 1.4426950408889634f)));
+    const float2 e = make_float2(ex2_approx(q.x), ex2_approx(q.y));
+    return fma2(make_float2(-av.x, -av.y), mul2(y, e), make_float2(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f)));
+}
 CN_DEV float apply_act(int act, float v) {
     if (act == ACT_HARDSWISH) return hardswish(v);
     if (act == ACT_GELU) return gelu_erf(v);
@@ -181,6 +217,19 @@ CN_DEV bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// try_wait that lets the hardware suspend the thread until the phase
+// completes or about hint_ns pass, instead of returning at once: a waiting
+// warp then takes no issue slots from the warps that work.
+CN_DEV bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }

@@ -193,9 +193,9 @@ struct Full2dArgs {
     int tc_acc_cols;            // TMEM columns per accumulator (two are allocated)
 
     // Tensor-core grouped transposed conv (k_convt2d_tc, tct = 1): a unit is
-    // 6 output rows x 30 output columns of one (n, group), a tile 4 units of
+    // 4 output rows x 30 output columns of one (n, group), a tile 4 units of
     // one group; the CTAs are split evenly over the groups.
-    CUtensorMap tct_xmap;       // x as (W, H, C_in, N), box (36, 8, 8, 1)
+    CUtensorMap tct_xmap;       // x as (W, H, C_in, N), box (36, 6, 8, 1)
     const float *tct_xmap_base; // x pointer the map was encoded for
     int tct;
     int tct_G;                  // conv groups

@@ -78,6 +78,12 @@ CN_DEV void tmem_ld4(uint32_t taddr, uint32_t *r) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(taddr));
 }
+// 32 lanes x 2 consecutive columns, without the wait (tmem_wait_ld).
+CN_DEV void tmem_ld2(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];\n"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(taddr));
+}
 CN_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 
@@ -97,6 +103,26 @@ CN_DEV bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort, int *er
                 *abort = 1;
                 return false;
             }
+        }
+    }
+}
+
+// The same bounded wait with the thread suspended in hardware between polls
+// (up to 20 us each, woken when the phase completes): for roles that wait
+// most of the time, so their polling does not take issue slots from the
+// warps that work.  The abort flag and the limit are checked after every
+// poll.
+CN_DEV bool tc_wait_sleep(uint64_t *bar, uint32_t parity, volatile int *abort, int *err,
+                          uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            flag_error(err, ERR_TIMEOUT);
+            *abort = 1;
+            return false;
         }
     }
 }

@@ -499,8 +499,9 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 // (count, K, S1, S2) is a sum about its own shift K, one of its own values,
 // so it converts to (count, mean = K + S1/n, M2 = S2 - S1^2/n) without
 // cancellation; the lanes merge a channel's partials with the pairwise update
-// of Chan et al. in a fixed order (lane l takes partials l, l + 32, ...),
-// then a butterfly merge gives every lane the same bits.  Channel moments
+// of Chan et al. in a fixed order (lane l takes partials l, l + 32, ...: 16
+// at a time, loaded together and merged as a balanced tree, the batches in
+// order), then a butterfly merge gives every lane the same bits.  Channel moments
 // are merged within a warp in channel order, then the warps' results in
 // warp order, so the result is deterministic.  The group's coefficients
 // (mu, a = gamma * rstd * scale, bb = beta * scale) go to every channel.
@@ -515,8 +516,21 @@ CN_DEV Moments<float> partial_moments(float4 q) {
     return Moments<float>{q.x, q.y + mu_s, fmaxf(q.w - q.z * mu_s, 0.0f)};
 }
 CN_DEV Moments<float> channel_moments(const float4 *p, int per_c, int lane) {
+    constexpr int B = 16;  // partials per lane and batch
     Moments<float> m{0.0f, 0.0f, 0.0f};
-    for (int i = lane; i < per_c; i += 32) m = merge(m, partial_moments(p[i]));
+    for (int i0 = lane; i0 < per_c; i0 += 32 * B) {
+        Moments<float> t[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            const int i = i0 + 32 * j;
+            t[j] = partial_moments(i < per_c ? p[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f));
+        }
+#pragma unroll
+        for (int w = B / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) t[j] = merge(t[j], t[j + w]);
+        m = merge(m, t[0]);
+    }
     return warp_merge(m);
 }
 

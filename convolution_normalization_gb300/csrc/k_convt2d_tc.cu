@@ -41,15 +41,20 @@
 // group's filter operand once):
 //   warp 0      producer: four TMA tensor copies per tile (36 columns x 8
 //               rows x 8 channels each, zero fill outside x: the padding)
-//               into one of two landing buffers;
-//   warps 2-3   converters: landing [unit][c][row][col] -> operand stage;
+//               into one of two landing buffers; tiles are claimed two
+//               ahead, so the claim's round trip is off the critical path;
+//   warps 2-5   converters, warp 2 + q for unit q: landing [c][row][col]
+//               -> the unit's quadrant of the operand stage;
 //   warp 1      MMA issuer (one thread): 24 MMAs per tile into one of two
 //               TMEM accumulators;
-//   warps 4-11  epilogue, thread = position: warp (q, h) reads quadrant q
-//               (unit q) and output channels 4h .. 4h + 3: the kx sum, bias,
-//               activation, the pre-norm store, and per-channel sums about
-//               the unit's first value, written as the unit's partial
-//               (count, K, S1, S2) for the statistics pass.
+//   warps 6-21  epilogue, thread = position: warp (q, h) reads quadrant q
+//               (unit q) and output channels 2h, 2h + 1 of all its rows
+//               (every column it needs with one TMEM wait, after which the
+//               accumulator is released; the channel pair in packed fp32x2
+//               arithmetic): the kx sum, bias, activation, the pre-norm
+//               store, and per-channel sums about the unit's first value,
+//               written as the unit's partial (count, K, S1, S2) for the
+//               statistics pass.
 // The statistics and normalize passes that follow are the ones of the other
 // 2-D paths (k_group_stats, k_norm_apply).
 #include "cn_common.cuh"
@@ -80,20 +85,26 @@ constexpr int kNB = 2 * kZG + kK - 2;       // blocks of one ky sequence
 constexpr int kC = kZG + kK - 2;            // block i holds ky = kC - i
 constexpr int kSeq = kNB * kBlk;            // one sequence
 constexpr int kFiltBytes = 4 * kSeq;
-constexpr int kSmemBytes = 2 * kStageBytes + 2 * kLandBytes + kFiltBytes;
-constexpr int kThreads = 384;               // 12 warps
-constexpr int kConvWarps = 2;               // warps 2-3
-constexpr int kEpiWarp0 = 4;                // epilogue: warps 4-11
-constexpr int kEpiWarps = 8;
+constexpr int kNLand = 2;                   // landing buffers
+constexpr int kSmemBytes = 2 * kStageBytes + kNLand * kLandBytes + kFiltBytes;
+constexpr int kConvWarps = 4;               // warps 2-5, one unit of a tile each
+constexpr int kEpiWarp0 = 2 + kConvWarps;   // epilogue: warps 6-21
+constexpr int kEpiRows = kZG;               // output rows per epilogue warp
+constexpr int kEpiCo = 2;                   // output channels per epilogue warp
+constexpr int kRowParts = kZG / kEpiRows;   // a unit's rows split over this many warps
+constexpr int kEpiWarps = 4 * kRowParts * (kCog / kEpiCo);  // six per TMEM lane quadrant
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+static_assert(kZG % kEpiRows == 0 && kCog % kEpiCo == 0 && kEpiCo % 2 == 0, "epilogue split");
+static_assert(kEpiCo * kK == 6 || kEpiCo * kK == 12, "TMEM loads of a warp's row columns");
 static_assert(kN % 16 == 0 && kN <= kAccCols, "MMA N");
 static_assert(kBlk % 128 == 0, "a block is whole 8-row core-matrix groups");
 static_assert(kUnitLand % 128 == 0, "landing units stay 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024 - 1024, "shared memory");
 
 template <int ACT>
-CN_DEV float act_v(float t) {
-    if (ACT == ACT_HARDSWISH) return hardswish(t);
-    if (ACT == ACT_GELU) return gelu_erf(t);
+CN_DEV float2 act_v2(float2 t) {
+    if (ACT == ACT_HARDSWISH) return make_float2(hardswish(t.x), hardswish(t.y));
+    if (ACT == ACT_GELU) return gelu_erf2(t);
     return t;
 }
 
@@ -122,11 +133,11 @@ CN_DEV int box_col(int seg, int &off) {
 template <int ACT>
 __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constant__ Full2dArgs a) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t land_full[2], land_empty[2];
+    __shared__ __align__(8) uint64_t land_full[kNLand], land_empty[kNLand];
     // st_full[b]: the converters wrote stage b; st_empty[b]: its MMAs are done
     __shared__ __align__(8) uint64_t st_full[2], st_empty[2];
     __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], fin_bar;
-    __shared__ int s_land_tile[2], s_st_tile[2], s_acc_tile[2];  // tile or -1 to stop
+    __shared__ int s_land_tile[kNLand], s_st_tile[2], s_acc_tile[2];  // tile or -1 to stop
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
 
@@ -135,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
     auto stage = [&](int b) { return stage0 + (size_t)b * kStageBytes; };
     unsigned char *land0 = stage0 + 2 * (size_t)kStageBytes;
     auto land = [&](int b) { return land0 + (size_t)b * kLandBytes; };
-    unsigned char *filt = land0 + 2 * (size_t)kLandBytes;
+    unsigned char *filt = land0 + kNLand * (size_t)kLandBytes;
 
     // this CTA's group and its place among the group's CTAs
     const int g = (int)blockIdx.x / a.tct_ctas_g;
@@ -166,9 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
         }
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kNLand; ++i) {
             mbar_init(&land_full[i], 1);
             mbar_init(&land_empty[i], kConvWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&st_full[i], kConvWarps);
             mbar_init(&st_empty[i], 1);
             mbar_init(&acc_full[i], 2);
@@ -191,26 +204,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
     const uint32_t tmem = s_tmem;
     int *abort_p = const_cast<int *>(&s_abort);
     auto wait = [&](uint64_t *bar, uint32_t par) {
-        return tc_wait(bar, par, abort_p, a.err, a.wait_ns);
+        return tc_wait_sleep(bar, par, abort_p, a.err, a.wait_ns);
     };
     int *work = a.tickets + a.N;  // [G] per-group work counters, then the exit counter
 
     if (warp == 0) {
         // ---------------- producer ----------------
+        // Lane 0 claims tiles two ahead of the one it arms (the claim's round
+        // trip overlaps a whole tile) and issues the four copies of each.
         if (lane == 0) {
             int k = 0;
-            int next = cta_in_g;  // the first tile; later ones from the group's counter
+            int cur = cta_in_g;  // the tile armed next; later ones from the group's counter
+            int nxt = a.tct_ctas_g + atomicAdd(work + g, 1);  // past the last tile: a stop
             for (;; ++k) {
-                const int lb = k & 1;
-                if (k >= 2 && !wait(&land_empty[lb], ((k >> 1) - 1) & 1)) break;
-                const int tile = next < a.tct_tiles_g ? next : -1;
-                if (tile >= 0) next = a.tct_ctas_g + atomicAdd(work + g, 1);
+                const int lb = k % kNLand;
+                if (k >= kNLand && !wait(&land_empty[lb], ((k / kNLand) - 1) & 1)) break;
+                const int tile = cur < a.tct_tiles_g ? cur : -1;
                 s_land_tile[lb] = tile;
                 if (tile < 0) {
                     mbar_arrive(&land_full[lb]);
                     ++k;
                     break;
                 }
+                cur = nxt;
+                if (cur < a.tct_tiles_g) nxt = a.tct_ctas_g + atomicAdd(work + g, 1);
                 // failure-path test hook: the first landing stage of CTA 0
                 // stays unarmed, a phase nothing completes
                 if (a.stall && blockIdx.x == 0 && k == 0) continue;
@@ -220,15 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
                     const Unit U = unit_of(a, 4 * tile + q);
                     int off;
                     const int c4 = box_col(U.seg, off);
-                    tma_load_4d(land(lb) + (size_t)q * kUnitLand, &a.tct_xmap, c4,
-                                U.band * kZG - (kK - 1), g * kCig, U.n, &land_full[lb]);
+                    tma_load_4d(land(lb) + (size_t)q * kUnitLand, &a.tct_xmap, c4, U.band * kZG - (kK - 1),
+                                g * kCig, U.n, &land_full[lb]);
                 }
             }
             // copies still in flight (only after an abort) land before the CTA
             // exits; in a normal run these phases are long complete
-            for (int j = max(0, k - 2); j < k; ++j)
+            for (int j = max(0, k - kNLand); j < k; ++j)
                 if (!(a.stall && blockIdx.x == 0 && j == 0))
-                    mbar_wait_bounded(&land_full[j & 1], (j >> 1) & 1, kWaitLimitNs);
+                    mbar_wait_bounded(&land_full[j % kNLand], (j / kNLand) & 1, kWaitLimitNs);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -274,44 +291,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
         }
     } else if (warp < kEpiWarp0) {
         // ---------------- converters ----------------
-        const int ct = tid - 64;
+        // Warp 2 + c converts units c and c + 2 of each tile: lane i takes
+        // position i of the unit's 8 staged rows (loads of a warp: 32
+        // consecutive words; stores: 32 consecutive 16-byte rows).
+        const int cw = warp - 2;
         for (int k = 0;; ++k) {
-            const int lb = k & 1, b = k & 1;
-            if (!wait(&land_full[lb], (k >> 1) & 1)) break;
+            const int lb = k % kNLand, b = k & 1;
+            if (!wait(&land_full[lb], (k / kNLand) & 1)) break;
             const int tile = s_land_tile[lb];
             if (k >= 2 && !wait(&st_empty[b], ((k >> 1) - 1) & 1)) break;
-            if (tile >= 0) {
-                const int nv = min(4, units_g - 4 * tile);
-                int offq[4];
+            bool wrote = false;
+#pragma unroll 1
+            for (int q = cw; q < 4; q += kConvWarps) {
+                if (tile < 0 || 4 * tile + q >= units_g) continue;
+                int off;
+                box_col(unit_of(a, 4 * tile + q).seg, off);
+                const float *s = reinterpret_cast<const float *>(land(lb)) + (size_t)q * (kUnitLand / 4) + off + lane;
+                float4 *dst = reinterpret_cast<float4 *>(stage(b)) + q * 32 + lane;
+                if (!CN_CHECK(q * (kUnitLand / 4) + (kCig - 1) * kRowsIn * kBoxW + (kRowsIn - 1) * kBoxW + off + lane <
+                                  kLandBytes / 4,
+                              a.err))
+                    continue;
+                // all 64 loads in flight before the first store
+                float v[kRowsIn][8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    offq[q] = 0;
-                    if (q < nv) box_col(unit_of(a, 4 * tile + q).seg, offq[q]);
-                }
-                const float *src = reinterpret_cast<const float *>(land(lb));
-                unsigned char *st = stage(b);
-                // position p = (u, q, i): lane = i, so loads and stores of a
-                // warp touch consecutive words / 16-byte rows
-#pragma unroll 2
-                for (int p = ct; p < kRowsIn * 128; p += 32 * kConvWarps) {
-                    const int i = p & 31, q = (p >> 5) & 3, u = p >> 7;
-                    if (q >= nv) continue;
-                    if (!CN_CHECK(q * (kUnitLand / 4) + (kCig - 1) * kRowsIn * kBoxW + u * kBoxW + offq[q] + i <
-                                      kLandBytes / 4,
-                                  a.err))
-                        continue;
-                    const float *s = src + (size_t)q * (kUnitLand / 4) + u * kBoxW + offq[q] + i;
-                    float v[8];
+                for (int u = 0; u < kRowsIn; ++u)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) v[c] = s[c * kRowsIn * kBoxW];
-                    float4 *row = reinterpret_cast<float4 *>(st + (size_t)u * kRowBytes) + q * 32 + i;
-                    row[0] = make_float4(v[0], v[1], v[2], v[3]);
-                    row[128] = make_float4(v[4], v[5], v[6], v[7]);
-                    row[256] = make_float4(tf32_rest(v[0]), tf32_rest(v[1]), tf32_rest(v[2]), tf32_rest(v[3]));
-                    row[384] = make_float4(tf32_rest(v[4]), tf32_rest(v[5]), tf32_rest(v[6]), tf32_rest(v[7]));
+                    for (int c = 0; c < 8; ++c) v[u][c] = s[c * kRowsIn * kBoxW + u * kBoxW];
+#pragma unroll
+                for (int u = 0; u < kRowsIn; ++u) {
+                    float4 *row = dst + u * (kRowBytes / 16);
+                    row[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                    row[128] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+                    row[256] = make_float4(tf32_rest(v[u][0]), tf32_rest(v[u][1]), tf32_rest(v[u][2]),
+                                           tf32_rest(v[u][3]));
+                    row[384] = make_float4(tf32_rest(v[u][4]), tf32_rest(v[u][5]), tf32_rest(v[u][6]),
+                                           tf32_rest(v[u][7]));
                 }
-                fence_proxy_async();
+                wrote = true;
             }
+            if (wrote) fence_proxy_async();
             __syncwarp();
             if (lane == 0) {
                 if (warp == 2) s_st_tile[b] = tile;
@@ -322,12 +341,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
         }
     } else {
         // ---------------- epilogue ----------------
-        const int q = warp & 3;                 // TMEM lane quadrant = unit of the tile
-        const int h = (warp - kEpiWarp0) >> 2;  // output channels 4h .. 4h + 3
-        const int co0 = g * kCog + 4 * h;
-        float bias[4];
+        const int e = warp - kEpiWarp0;
+        const int q = warp & 3;                  // TMEM lane quadrant = unit of the tile
+        const int rp = (e >> 2) % kRowParts;     // output rows kEpiRows rp ..
+        const int h = (e >> 2) / kRowParts;      // output channels kEpiCo h ..
+        const int co0 = g * kCog + kEpiCo * h;
+        constexpr int NV = kEpiCo * kK;          // a warp's columns of one output row
+        constexpr int NP = kEpiCo / 2;           // channel pairs
+        float2 bias2[NP];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) bias[c] = a.b ? __ldg(a.b + co0 + c) : 0.0f;
+        for (int c = 0; c < NP; ++c)
+            bias2[c] = a.b ? make_float2(__ldg(a.b + co0 + 2 * c), __ldg(a.b + co0 + 2 * c + 1))
+                           : make_float2(0.0f, 0.0f);
         for (int k = 0;; ++k) {
             const int b = k & 1;
             if (!wait(&acc_full[b], (k >> 1) & 1)) break;
@@ -337,68 +362,100 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
             const int unit = 4 * tile + q;
             if (unit < units_g) {  // uniform per warp
                 const Unit U = unit_of(a, unit);
-                const int r0 = U.band * kZG, c0 = U.seg * kSegV;
-                const int rows_ok = min(kZG, a.Ho - r0);
+                const int r0 = U.band * kZG + kEpiRows * rp, c0 = U.seg * kSegV;
+                const int rows_ok = max(0, min(kEpiRows, a.Ho - r0));
                 const int col = c0 + lane;
                 const bool col_ok = lane < kSegV && col < a.Wo;
                 const uint32_t tq = tmem + (uint32_t)(b * kAccCols) + ((uint32_t)(q * 32) << 16);
-                float ksh[4], s1[4], s2[4];
+                // every column this warp needs, then one wait
+                uint32_t v[kEpiRows][NV];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    ksh[c] = 0.0f;
-                    s1[c] = 0.0f;
-                    s2[c] = 0.0f;
+                for (int zi = 0; zi < kEpiRows; ++zi) {
+                    const uint32_t ta = tq + (uint32_t)((kEpiRows * rp + zi) * kCog * kK + kEpiCo * h * kK);
+                    if (NV == 12) {
+                        tmem_ld8(ta, v[zi]);
+                        tmem_ld4(ta + 8, v[zi] + 8);
+                    } else {
+                        tmem_ld4(ta, v[zi]);
+                        tmem_ld2(ta + 4, v[zi] + 4);
+                    }
                 }
-                float *obase = a.out + ((size_t)U.n * a.Co + co0) * (size_t)a.S + (size_t)r0 * a.Wo + col;
-#pragma unroll 1
-                for (int zg = 0; zg < kZG; ++zg) {
-                    uint32_t v[12];
-                    const uint32_t ta = tq + (uint32_t)(zg * kCog * kK + 4 * h * kK);
-                    tmem_ld8(ta, v);
-                    tmem_ld4(ta + 8, v + 8);
-                    tmem_wait_ld();
-                    const bool ok = col_ok && zg < rows_ok;
+                tmem_wait_ld();
+                // the accumulator is in registers: release it for the tile
+                // after next, whose MMAs then overlap this tile's arithmetic
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[b]);
+                // kx sums by lane shifts (the next two positions' columns),
+                // then the channel pairs in packed arithmetic
+                float2 y[kEpiRows][NP];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        float acc = __uint_as_float(v[c * kK]);
+                for (int zi = 0; zi < kEpiRows; ++zi)
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        const uint32_t *w0 = v[zi] + 2 * c * kK, *w1 = w0 + kK;
+                        float2 acc = make_float2(__uint_as_float(w0[0]), __uint_as_float(w1[0]));
 #pragma unroll
                         for (int kx = 1; kx < kK; ++kx)
-                            acc += __shfl_down_sync(0xffffffffu, __uint_as_float(v[c * kK + kx]), kx);
-                        const float y = act_v<ACT>(acc + bias[c]);
-                        // shift of the unit's sums: its first value (row r0,
-                        // column c0: always inside the output)
-                        if (zg == 0) ksh[c] = __shfl_sync(0xffffffffu, y, 0);
-                        const float dl = ok ? y - ksh[c] : 0.0f;
-                        s1[c] += dl;
-                        s2[c] = fmaf(dl, dl, s2[c]);
-                        if (ok && CN_CHECK((size_t)(obase - a.out) + (size_t)c * a.S + (size_t)zg * a.Wo <
-                                               (size_t)a.N * a.Co * a.S,
-                                           a.err))
-                            obase[(size_t)c * a.S + (size_t)zg * a.Wo] = y;
+                            acc = add2(acc, make_float2(__shfl_down_sync(0xffffffffu, __uint_as_float(w0[kx]), kx),
+                                                        __shfl_down_sync(0xffffffffu, __uint_as_float(w1[kx]), kx)));
+                        y[zi][c] = act_v2<ACT>(add2(acc, bias2[c]));
+                    }
+                // shift of the warp's sums: its first value (row r0, column
+                // c0: inside the output whenever the warp has rows)
+                float2 ksh[NP], s1[NP], s2[NP];
+                float *obase = a.out + ((size_t)U.n * a.Co + co0) * (size_t)a.S + (size_t)r0 * a.Wo + col;
+#pragma unroll
+                for (int c = 0; c < NP; ++c) {
+                    ksh[c] = make_float2(__shfl_sync(0xffffffffu, y[0][c].x, 0),
+                                         __shfl_sync(0xffffffffu, y[0][c].y, 0));
+                    s1[c] = make_float2(0.0f, 0.0f);
+                    s2[c] = s1[c];
+                }
+#pragma unroll
+                for (int zi = 0; zi < kEpiRows; ++zi) {
+                    const bool ok = col_ok && zi < rows_ok;
+#pragma unroll
+                    for (int c = 0; c < NP; ++c) {
+                        float2 dl = add2(y[zi][c], make_float2(-ksh[c].x, -ksh[c].y));
+                        if (!ok) dl = make_float2(0.0f, 0.0f);
+                        s1[c] = add2(s1[c], dl);
+                        s2[c] = fma2(dl, dl, s2[c]);
+                        float *o = obase + (size_t)(2 * c) * a.S + (size_t)zi * a.Wo;
+                        if (ok && CN_CHECK((size_t)(o - a.out) + (size_t)a.S < (size_t)a.N * a.Co * a.S, a.err)) {
+                            o[0] = y[zi][c].x;
+                            o[a.S] = y[zi][c].y;
+                        }
                     }
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < NP; ++c)
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) {
-                        s1[c] += __shfl_xor_sync(0xffffffffu, s1[c], o);
-                        s2[c] += __shfl_xor_sync(0xffffffffu, s2[c], o);
+                        s1[c] = add2(s1[c], make_float2(__shfl_xor_sync(0xffffffffu, s1[c].x, o),
+                                                        __shfl_xor_sync(0xffffffffu, s1[c].y, o)));
+                        s2[c] = add2(s2[c], make_float2(__shfl_xor_sync(0xffffffffu, s2[c].x, o),
+                                                        __shfl_xor_sync(0xffffffffu, s2[c].y, o)));
                     }
-                }
                 if (lane == 0) {
                     const float cnt = (float)(rows_ok * min(kSegV, a.Wo - c0));
                     const int ui = U.band * a.tct_nseg + U.seg;
+                    // partials [n][channel][unit][row part]
+                    const size_t pi = (((size_t)U.n * a.Co + co0) * a.tct_U + ui) * kRowParts + rp;
+                    const size_t pc = (size_t)a.tct_U * kRowParts;  // one channel's partials
+                    if (CN_CHECK(pi + (kEpiCo - 1) * pc < (size_t)a.N * a.Co * pc, a.err)) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        if (CN_CHECK(((size_t)U.n * a.Co + co0 + c) * a.tct_U + ui < (size_t)a.N * a.Co * a.tct_U,
-                                     a.err))
-                            a.partial[((size_t)U.n * a.Co + co0 + c) * a.tct_U + ui] =
-                                make_float4(cnt, ksh[c], s1[c], s2[c]);
+                        for (int c = 0; c < NP; ++c) {
+                            a.partial[pi + (2 * c) * pc] = make_float4(cnt, ksh[c].x, s1[c].x, s2[c].x);
+                            a.partial[pi + (2 * c + 1) * pc] = make_float4(cnt, ksh[c].y, s1[c].y, s2[c].y);
+                        }
+                    }
                 }
+            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[b]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
     }
 
@@ -464,8 +521,8 @@ int tct_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     a.ncob = 0;
     a.nchunk = 0;
     a.wstage = 0;
-    a.ntiles = (int)U;  // partials per channel: one per unit
-    a.wsp = 1;
+    a.ntiles = (int)U;  // partials per channel: one per unit and row part
+    a.wsp = kRowParts;
     a.items = (int)(d.groups * tiles_g);
     a.wprep = nullptr;
     a.act = d.act;
