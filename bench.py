@@ -11,7 +11,7 @@ time per step; the roofline is max(FLOPs / FP32 peak, compulsory bytes /
 HBM bandwidth).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                  [--impl reference] [--no-extras]
+                  [--impl reference] [--no-extras] [--no-cpu-baseline] [--batch N]
 
 Under torchrun each rank runs its own full batch (weak scaling, no
 collective on the data path); the value is the sum of FLOPs over ranks
@@ -373,8 +373,9 @@ def run_reference(args, spec):
 
 def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf, nlaunch):
     """Times `steps` forwards (L2 flushed before each) with CUDA events on the
-    forward's stream; every step also records one event before each kernel
-    launch and one after the last.  Returns (step ms list, per-launch ms
+    forward's stream: the plan records one event before each kernel launch and
+    one after the last, so a step is the time from its first event to its last
+    (no events of its own beside them).  Returns (step ms list, per-launch ms
     lists)."""
     def fwd():
         plan.forward(dev["x"], dev["w"], dev["b"], dev["gamma"], dev["beta"], out, stream)
@@ -399,13 +400,19 @@ def time_forward(B, torch, plan, dev, out, stream, steps, warmup, flush_buf, nla
         torch.cuda._sleep(int(min(2e9, 2e5 * steps + 2e7)))
         for i in range(steps):
             flush_buf.zero_()
-            plan.set_launch_events(lev[i] if nlaunch else None)
-            starts[i].record(stream)
-            fwd()
-            ends[i].record(stream)
+            if nlaunch:
+                plan.set_launch_events(lev[i])
+                fwd()
+            else:  # an empty problem launches nothing
+                starts[i].record(stream)
+                fwd()
+                ends[i].record(stream)
     stream.synchronize()
     plan.set_launch_events(None)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    if nlaunch:
+        step_ms = [row[0].elapsed_time(row[-1]) for row in lev]
+    else:
+        step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     launch_ms = [[lev[i][j].elapsed_time(lev[i][j + 1]) for i in range(steps)]
                  for j in range(nlaunch)]
     return step_ms, launch_ms
@@ -545,9 +552,13 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     spec = wl.WORKLOAD_BY_NAME[args.workload]
+    if args.batch is not None:
+        spec = wl.with_overrides(spec, N=args.batch, name=f"{spec['name']}_batch{args.batch}")
     if args.impl == "reference":
         run_reference(args, spec)
     else:

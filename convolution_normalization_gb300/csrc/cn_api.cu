@@ -271,7 +271,7 @@ int conv_norm_plan_create(const conv_norm_desc *d, conv_norm_plan *out) {
             a.tickets = reinterpret_cast<int *>(vbase + ((part + 255) & ~(size_t)255));
             a.err = p->err_flag;
             p->counters = a.tickets;
-            p->counter_bytes = (size_t)(a.N + 2) * sizeof(int);
+            p->counter_bytes = mean3d_tickets(a) * sizeof(int);
             break;
         }
         case V_POOL3D:

@@ -146,6 +146,54 @@ CN_DEV float3 warp_sum3(float3 v) {
     }
     return v;
 }
+// (count, mean, M2) of one channel from its per_c partials (count, K, S1,
+// S2), each a sum about its own shift K, one of its own values: the partials
+// move to one common shift K0 (the first non-empty partial's, a value of the
+// channel's data) by the exact identities S1' = S1 + n d, S2' = S2 + d (2 S1
+// + n d), d = K - K0, which stay well conditioned since every K lies within
+// a few standard deviations of the data; lanes add them in a fixed order, a
+// butterfly of commutative adds gives every lane the same bits, and one
+// division gives mean = K0 + S1'/n, M2 = S2' - S1'^2/n.  Deterministic.
+CN_DEV Moments<float> channel_moments(const float4 *p, int per_c, int lane) {
+    // common shift: the first non-empty partial's (lowest lane of the first 32)
+    const float4 f = lane < per_c ? p[lane] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const unsigned has = __ballot_sync(0xffffffffu, f.x > 0.0f);
+    if (!has) {
+        // no non-empty partial among the first 32: take the first anywhere
+        // (serially; only for channels that are empty at the start)
+        float K0 = 0.0f;
+        for (int i = 0; i < per_c; ++i)
+            if (p[i].x > 0.0f) {
+                K0 = p[i].y;
+                break;
+            }
+        float3 v = make_float3(0.0f, 0.0f, 0.0f);
+        for (int i = lane; i < per_c; i += 32) {
+            const float4 q = p[i];
+            const float d = q.y - K0;
+            v.x += q.x;
+            v.y += fmaf(q.x, d, q.z);
+            v.z += fmaf(d, fmaf(q.x, d, 2.0f * q.z), q.w);
+        }
+        v = warp_sum3(v);
+        if (!(v.x > 0.0f)) return Moments<float>{0.0f, 0.0f, 0.0f};
+        const float mu_s = v.y / v.x;
+        return Moments<float>{v.x, K0 + mu_s, fmaxf(v.z - v.y * mu_s, 0.0f)};
+    }
+    const float K0 = __shfl_sync(0xffffffffu, f.y, __ffs(has) - 1);
+    float3 v = make_float3(0.0f, 0.0f, 0.0f);  // (count, S1', S2') about K0
+    for (int i = lane; i < per_c; i += 32) {
+        const float4 q = i == lane ? f : p[i];
+        const float d = q.y - K0;
+        v.x += q.x;
+        v.y += fmaf(q.x, d, q.z);
+        v.z += fmaf(d, fmaf(q.x, d, 2.0f * q.z), q.w);
+    }
+    v = warp_sum3(v);
+    const float mu_s = v.y / v.x;  // mean - K0
+    return Moments<float>{v.x, K0 + mu_s, fmaxf(v.z - v.y * mu_s, 0.0f)};
+}
+
 CN_DEV Moments<double> moments_from_sums(double n, double K, double s1, double s2) {
     if (n <= 0.0) return Moments<double>{0.0, 0.0, 0.0};
     const double m2 = s2 - s1 * s1 / n;

@@ -88,6 +88,10 @@ int tc3_launches(const Tc3Config &cfg);  // kernels one forward launches
 // -> spatial mean.  One launch; the conv tensor is never written.
 struct Mean3dArgs {
     int tc;           // 1: the tensor-core kernel (t) runs the problem
+    int small;        // 1: the small-problem kernel (one CTA per (n, norm group)) runs it
+    int sm_cpg;       // small: channels per normalization group (one CTA's channels)
+    int sm_ngrp;      // small: normalization groups per sample
+    int sm_nsplit;    // small: CTAs per (sample, normalization group), by output rows
     Tc3Args t;
     CUtensorMap tmap;           // x viewed as (W, H, D, N*C_in), box (pitch, H, planes_max, C_in)
     const float *tmap_base;     // x pointer the map was encoded for
@@ -112,7 +116,8 @@ struct Mean3dArgs {
     int act, norm, G, affine;
     float eps, post_scale;
     double *partial;  // [N][nchunks][Co][3]  (count, mean, M2); the tensor-core kernel's float2 sums
-    int *tickets;     // [N] per-sample tickets, then [2] work/exit counters; zero between launches
+    int *tickets;     // [N] per-sample tickets (small kernel: [N * groups] per-group
+                      // ones), then [2] work/exit counters; zero between launches
 };
 typedef void (*Mean3dKernel)(Mean3dArgs);
 struct Mean3dConfig {
@@ -126,9 +131,14 @@ struct Mean3dConfig {
 // Chooses tiling + instantiation; fills the geometry fields of args.
 // Returns CN_OK or CN_ERR_UNSUPPORTED.
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+// The small-problem kernel (k_conv3d_mean_small.cu); CN_ERR_UNSUPPORTED when
+// the problem is too large for it.
+int small3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
+size_t small3d_partial_bytes(const Mean3dArgs &a);
 // Bytes of the partial-moment slots (the tensor-core kernel's float2 sums or
 // the CUDA-core kernel's fp64 (count, mean, M2)).
 size_t mean3d_partial_bytes(const Mean3dArgs &a);
+size_t mean3d_tickets(const Mean3dArgs &a);  // ints after the partial slots
 size_t mean3d_workspace(const Mean3dArgs &a);
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a);  // needs a device: smem attribute, grid
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s,

@@ -72,7 +72,8 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     // the scratch this problem needs: moments, then tickets (256-byte aligned)
     const size_t part = cn::mean3d_partial_bytes(a);
     const size_t part_al = (part + 255) & ~(size_t)255;
-    if (part_al + (size_t)(a.N + 2) * sizeof(int) > CN_NOALLOC_SCRATCH_BYTES)
+    const size_t tick_bytes = cn::mean3d_tickets(a) * sizeof(int);
+    if (part_al + tick_bytes > CN_NOALLOC_SCRATCH_BYTES)
         return CN_ERR_UNSUPPORTED;
     const bool need_aff = d->affine && d->norm != CN_NORM_NONE;
     if (!x || !w || !out) return CN_ERR_INVALID_ARG;
@@ -95,7 +96,7 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     // The array keeps the previous call's contents: the tickets and work
     // counters must start at zero (every partial-moment slot is overwritten
     // before it is read).
-    if (cudaMemsetAsync(a.tickets, 0, (size_t)(a.N + 2) * sizeof(int), s) != cudaSuccess) {
+    if (cudaMemsetAsync(a.tickets, 0, tick_bytes, s) != cudaSuccess) {
         cudaGetLastError();
         return CN_ERR_CUDA;
     }

@@ -494,58 +494,35 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 }
 
 // Statistics of the normalization groups.  A group of one channel
-// (InstanceNorm) gets one warp, four per block; a wider group gets the four
-// warps of a block, warp w taking channels w, w + 4, ... .  Every partial
-// (count, K, S1, S2) is a sum about its own shift K, one of its own values,
-// so it converts to (count, mean = K + S1/n, M2 = S2 - S1^2/n) without
-// cancellation; the lanes merge a channel's partials with the pairwise update
-// of Chan et al. in a fixed order (lane l takes partials l, l + 32, ...: 16
-// at a time, loaded together and merged as a balanced tree, the batches in
-// order), then a butterfly merge gives every lane the same bits.  Channel moments
-// are merged within a warp in channel order, then the warps' results in
-// warp order, so the result is deterministic.  The group's coefficients
-// (mu, a = gamma * rstd * scale, bb = beta * scale) go to every channel.
-// Arithmetic is fp32: its ~1e-6 relative error in mean and variance is far
-// inside the 1e-4 output bound, and the FP64 pipe of this GPU is narrow
-// enough that fp64 divisions per merge cost more than the pass's memory
-// traffic.
-constexpr int kStatsWarps = 4;
-CN_DEV Moments<float> partial_moments(float4 q) {
-    if (!(q.x > 0.0f)) return Moments<float>{0.0f, 0.0f, 0.0f};
-    const float mu_s = q.z / q.x;  // mean - K
-    return Moments<float>{q.x, q.y + mu_s, fmaxf(q.w - q.z * mu_s, 0.0f)};
-}
-CN_DEV Moments<float> channel_moments(const float4 *p, int per_c, int lane) {
-    constexpr int B = 16;  // partials per lane and batch
-    Moments<float> m{0.0f, 0.0f, 0.0f};
-    for (int i0 = lane; i0 < per_c; i0 += 32 * B) {
-        Moments<float> t[B];
-#pragma unroll
-        for (int j = 0; j < B; ++j) {
-            const int i = i0 + 32 * j;
-            t[j] = partial_moments(i < per_c ? p[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f));
-        }
-#pragma unroll
-        for (int w = B / 2; w > 0; w >>= 1)
-#pragma unroll
-            for (int j = 0; j < w; ++j) t[j] = merge(t[j], t[j + w]);
-        m = merge(m, t[0]);
-    }
-    return warp_merge(m);
-}
-
+// (InstanceNorm) gets one warp, eight per block; a wider group gets a block
+// of min(channels, 8) warps, warp w taking channels w, w + warps, ... .
+// Every partial (count, K, S1, S2) is a sum about its own shift K, one of
+// its own values.  A channel's partials are moved to one common shift K0,
+// the shift of the channel's first non-empty partial (a value of the
+// channel's data), by the exact identities
+//   S1' = S1 + n d,  S2' = S2 + d (2 S1 + n d),  d = K - K0,
+// which stay well conditioned because every K and K0 lie within a few
+// standard deviations of the data; then lanes add them in a fixed order and a
+// butterfly of commutative adds gives every lane the same bits, and the
+// channel's (count, mean = K0 + S1'/n, M2 = S2' - S1'^2/n) follows with one
+// division.  Channel moments are merged (Chan et al.) within a warp in
+// channel order, then the warps' results in warp order, so the result is
+// deterministic.  The group's coefficients (mu, a = gamma * rstd * scale,
+// bb = beta * scale) go to every channel.  Arithmetic is fp32: its ~1e-6
+// relative error in mean and variance is far inside the 1e-4 output bound.
+constexpr int kStatsWarps = 8;  // most warps of a statistics block
 __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a) {
     __shared__ float sm[kStatsWarps][3];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int cpg = a.Co / a.NG;
     const int per_c = a.Dv * a.ntiles * a.wsp;  // a channel's partials: depth planes x tiles x warps
     const bool wide = cpg > 1;
-    const int ng = wide ? (int)blockIdx.x : (int)blockIdx.x * kStatsWarps + w;  // (n, group)
+    const int ng = wide ? (int)blockIdx.x : (int)blockIdx.x * nw + w;  // (n, group)
     if (ng >= a.N * a.NG) return;  // uniform per block when wide
     const int n = ng / a.NG, g = ng % a.NG;
     const float4 *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c;
     Moments<float> m{0.0f, 0.0f, 0.0f};
-    for (int cl = wide ? w : 0; cl < cpg; cl += wide ? kStatsWarps : 1)
+    for (int cl = wide ? w : 0; cl < cpg; cl += wide ? nw : 1)
         m = merge(m, channel_moments(p0 + (size_t)cl * per_c, per_c, lane));
     if (wide) {
         if (lane == 0) {
@@ -556,7 +533,7 @@ __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_c
         __syncthreads();
         if (w != 0) return;
         m = Moments<float>{sm[0][0], sm[0][1], sm[0][2]};
-        for (int j = 1; j < kStatsWarps; ++j) m = merge(m, Moments<float>{sm[j][0], sm[j][1], sm[j][2]});
+        for (int j = 1; j < nw; ++j) m = merge(m, Moments<float>{sm[j][0], sm[j][1], sm[j][2]});
     }
     const float var = m.n > 0.0f ? m.m2 / m.n : 0.0f;
     const float rstd = 1.0f / sqrtf(var + a.eps);
@@ -949,8 +926,9 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
             k_fill_scale<<<(a.N * a.Co + 255) / 256, 256, 0, s>>>(a.coef, a.N * a.Co, a.post_scale);
         } else {
             const int cpg = a.Co / a.NG;
-            const int blocks = cpg > 1 ? a.N * a.NG : (a.N * a.NG + kStatsWarps - 1) / kStatsWarps;
-            k_group_stats<<<blocks, 32 * kStatsWarps, 0, s>>>(a);
+            const int nw = cpg > 1 ? std::min(cpg, kStatsWarps) : kStatsWarps;
+            const int blocks = cpg > 1 ? a.N * a.NG : (a.N * a.NG + nw - 1) / nw;
+            k_group_stats<<<blocks, 32 * nw, 0, s>>>(a);
         }
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
         record_launch(ev, li++, s);

@@ -354,6 +354,9 @@ int env_int(const char *name, int dflt) {
 }  // namespace
 
 int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
+    // small batches: one CTA per (sample, normalization group)
+    if (small3d_plan(d, a, cfg) == CN_OK) return CN_OK;
+    a.small = 0;
     // the tensor-core kernel where the problem fits it
     if (tc3_plan(d, a.t, cfg.tc3) == CN_OK) {
         a.tc = 1;
@@ -489,15 +492,25 @@ int mean3d_launches(const Mean3dConfig &cfg, const Mean3dArgs &a) {
 }
 
 size_t mean3d_partial_bytes(const Mean3dArgs &a) {
+    if (a.small) return small3d_partial_bytes(a);
     return (size_t)a.N * a.nchunks * a.Co * (a.tc ? sizeof(float2) : 3 * sizeof(double));
+}
+
+size_t mean3d_tickets(const Mean3dArgs &a) {
+    return (a.small ? (size_t)a.N * a.sm_ngrp : (size_t)a.N) + 2;
 }
 
 size_t mean3d_workspace(const Mean3dArgs &a) {
     const size_t part = mean3d_partial_bytes(a);
-    return ((part + 255) & ~(size_t)255) + (size_t)(a.N + 2) * sizeof(int);
+    return ((part + 255) & ~(size_t)255) + mean3d_tickets(a) * sizeof(int);
 }
 
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
+    if (a.small)  // the grid is one CTA per (sample, normalization group)
+        return cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) ==
+                       cudaSuccess
+                   ? CN_OK
+                   : CN_ERR_CUDA;
     if (a.tc) {
         const int st = tc3_prepare(cfg.tc3, a.t);
         cfg.grid = cfg.tc3.grid;
@@ -521,6 +534,12 @@ int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
 
 int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const LaunchEvents *ev) {
     if (cfg.grid == 0) return CN_OK;
+    if (a.small) {
+        record_launch(ev, 0, s);
+        cfg.kern<<<cfg.grid, cfg.threads, cfg.smem, s>>>(a);
+        record_launch(ev, 1, s);
+        return cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
+    }
     if (a.tc) {
         Tc3Args &t = a.t;
         t.x = a.x;

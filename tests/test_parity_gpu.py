@@ -69,8 +69,13 @@ MEAN_CASES = [
 ]
 
 
+@pytest.mark.parametrize("small", [True, False], ids=["small_kernel", "persistent_kernels"])
 @pytest.mark.parametrize("kw", MEAN_CASES, ids=[str(i) for i in range(len(MEAN_CASES))])
-def test_mean_variant_shapes(kw):
+def test_mean_variant_shapes(kw, small, monkeypatch):
+    # these batches fit the one-CTA-per-group kernel; CN_NO_SMALL=1 runs them
+    # on the persistent (tensor-core or CUDA-core) kernels instead
+    if not small:
+        monkeypatch.setenv("CN_NO_SMALL", "1")
     check(wl.with_overrides(W["conv3d_hswish_gn4_mean_n2"], seed=100, **kw))
 
 
