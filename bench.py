@@ -125,6 +125,7 @@ KERNEL_SOURCES = {
     "k_conv3d_tc_mean": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
     "k_conv3d_tc_pool": ("k_conv3d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
     "k_convt2d_tc": ("k_convt2d_tc.cu", "cn_tcgen05.cuh", "cn_common.cuh"),
+    "k_conv3d_mean_small": ("k_conv3d_mean_small.cu", "cn_common.cuh"),
 }
 # tf32 tensor peak from the measured bf16 one and the nominal dense ratio
 # (1.1 / 2.25 PFLOP/s); split-TF32 runs 3 tf32 products per fp32 product

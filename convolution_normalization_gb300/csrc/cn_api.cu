@@ -615,7 +615,7 @@ int conv_norm_plan_inject_stall(conv_norm_plan p) {
 }
 
 int conv_norm_plan_check_device(conv_norm_plan p, void *stream) {
-    if (!p) return CN_ERR_INVALID_ARG;
+    if (!p) return noalloc_check_device(static_cast<cudaStream_t>(stream));
     int cur = -1;
     cudaGetDevice(&cur);
     if (cur != p->device) cudaSetDevice(p->device);

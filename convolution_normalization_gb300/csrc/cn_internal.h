@@ -286,4 +286,8 @@ int full2d_launches(const Full2dConfig &cfg, const Full2dArgs &a);
 int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s,
                   const LaunchEvents *ev = nullptr);  // may cache a tensor map in a
 
+// Reads and clears the error flag of conv_norm_forward_noalloc on the current
+// device after synchronizing the stream (cn_noalloc.cu).
+int noalloc_check_device(cudaStream_t stream);
+
 }  // namespace cn

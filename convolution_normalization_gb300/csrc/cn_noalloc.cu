@@ -25,27 +25,34 @@
 // name is only a host-side stand-in: the device address must come from
 // cudaGetSymbolAddress (scratch_device_address below).
 static __device__ __align__(256) unsigned char g_cn_noalloc_scratch[CN_NOALLOC_SCRATCH_BYTES];
+// Error flag of those calls (a bounded wait that gave up), read and cleared
+// by conv_norm_plan_check_device(NULL, stream).  Same host-side caveat.
+static __device__ int g_cn_noalloc_err;
 
 namespace {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void *g_scratch_ptr[kMaxDevices] = {};
+void *g_err_ptr[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (with that device current) and cached.
-int scratch_device_address(int dev, void **out) {
+// Device addresses of the scratch array and the error flag on the current
+// device, looked up once per device (with that device current) and cached.
+int scratch_device_address(int dev, void **out, int **err) {
     if (dev < 0 || dev >= kMaxDevices) return CN_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_cn_noalloc_scratch) != cudaSuccess || !p) {
+        void *p = nullptr, *e = nullptr;
+        if (cudaGetSymbolAddress(&p, g_cn_noalloc_scratch) != cudaSuccess || !p ||
+            cudaGetSymbolAddress(&e, g_cn_noalloc_err) != cudaSuccess || !e) {
             cudaGetLastError();
             return CN_ERR_CUDA;
         }
         g_scratch_ptr[dev] = p;
+        g_err_ptr[dev] = e;
     }
     *out = g_scratch_ptr[dev];
+    *err = static_cast<int *>(g_err_ptr[dev]);
     return CN_OK;
 }
 
@@ -87,12 +94,13 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
         return CN_ERR_CUDA;
     }
     void *base = nullptr;
-    st = scratch_device_address(dev, &base);
+    int *err = nullptr;
+    st = scratch_device_address(dev, &base, &err);
     if (st != CN_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     a.partial = static_cast<double *>(base);
     a.tickets = reinterpret_cast<int *>(static_cast<char *>(base) + part_al);
-    a.err = nullptr;  // no plan, so device-side timeouts are not recorded
+    a.err = err;
     // The array keeps the previous call's contents: the tickets and work
     // counters must start at zero (every partial-moment slot is overwritten
     // before it is read).
@@ -114,4 +122,33 @@ extern "C" int conv_norm_forward_noalloc(const conv_norm_desc *d, const float *x
     st = cn::mean3d_launch(cfg, a, s);
     if (st != CN_OK) cudaGetLastError();
     return st;
+}
+
+// conv_norm_plan_check_device(NULL, stream): the flag of the no-allocation
+// calls on the current device, after synchronizing the stream.
+int cn::noalloc_check_device(cudaStream_t stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    void *base = nullptr;
+    int *err = nullptr;
+    int st = scratch_device_address(dev, &base, &err);
+    if (st != CN_OK) return st;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    int flag = 0;
+    if (cudaMemcpy(&flag, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    if (flag == 0) return CN_OK;
+    // clear it, and the scratch's tickets and counters (every call zeroes
+    // the ones it uses before its kernel runs, so nothing else is needed)
+    const int zero = 0;
+    cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    return flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
 }

@@ -211,6 +211,8 @@ int conv_norm_forward_host(conv_norm_plan plan, const float *x, const float *w,
  * flag and those of the chunk plans conv_norm_forward_host created.  Returns
  * CN_OK, CN_ERR_TIMEOUT (a bounded device wait gave up; the
  * output of that forward is undefined), CN_ERR_DEVICE_CHECK or CN_ERR_CUDA.
+ * With plan == NULL it reads and clears the flag of the
+ * conv_norm_forward_noalloc calls on the current device instead.
  * When a flag was set it also zeroes that plan's tickets and work counters,
  * which a kernel that gave up can leave part-way, so the plan's next
  * forward runs normally.
@@ -283,12 +285,20 @@ int conv_norm_plan_set_launch_events(conv_norm_plan plan, void *const *events, i
  * pointers.  The call is asynchronous on cuda_stream.
  *
  * Limits and errors:
- *  - a problem needing more than 4 MiB of scratch returns CN_ERR_UNSUPPORTED;
- *    it needs about N * ceil(rows/32) * C_out * 24 bytes + 4 N bytes, where
- *    rows = D_out * H_out (for example 2.4 MB for N=512, 16x32x32, k=4);
+ *  - the scratch a problem needs is the workspace conv_norm_plan_create would
+ *    allocate for it, less the plan's 256-byte flag (conv_norm_workspace_bytes
+ *    of such a plan, minus 256); more than 4 MiB returns CN_ERR_UNSUPPORTED.
+ *    It depends on the kernel the problem runs on: small batches (up to about
+ *    16 M multiply-adds) 16 bytes per (sample, channel, row split) plus 4
+ *    bytes per (sample, normalization group); the tensor-core kernel 8 bytes
+ *    per (sample, item, channel) plus 4 bytes per sample (1 MB for N=512,
+ *    16x32x32, k=4: 16 items a sample); the CUDA-core kernel 24 bytes per
+ *    (sample, row chunk, channel) plus 4 bytes per sample;
  *  - other problem kinds return CN_ERR_UNSUPPORTED; malformed descriptors or
  *    null/misaligned pointers CN_ERR_INVALID_ARG; a failed launch CN_ERR_CUDA;
- *  - device-side wait timeouts are not recorded (there is no plan flag).
+ *  - a bounded device wait that gives up is recorded in a flag of the
+ *    library's device globals, which conv_norm_plan_check_device(NULL,
+ *    stream) reads and clears.
  * All calls share the one array: calls whose work overlaps on the GPU (two
  * streams, or two host threads) race and give wrong results; order them.
  * Each call clears the tickets it needs before its kernel runs.

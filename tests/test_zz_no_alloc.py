@@ -54,6 +54,8 @@ def test_noalloc_matches_plan_forward_twice(spec):
         B.conv_norm_forward_noalloc(desc, dev["x"], dev["w"], dev["b"], dev["gamma"],
                                     dev["beta"], out)
         torch.cuda.synchronize()
+        # no bounded wait gave up (the calls' flag, read with a NULL plan)
+        assert B.lib.conv_norm_plan_check_device(None, None) == B.CN_OK
         assert_parity(out.cpu().numpy(), ref, f"{spec['name']} no-alloc call {call + 1}")
 
 
