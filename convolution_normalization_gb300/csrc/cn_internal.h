@@ -261,11 +261,13 @@ struct Full2dConfig {
     const char *names;
     int K, RW, COT, VECW, transposed;
     int threads, smem, grid;
-    int apply_threads, apply_grid_x, apply_grid_y;
+    int apply_threads, apply_grid, apply_slices;  // normalize pass: 1-D grid, slices per plane
     int prep_grid;
     int fin_threads;
 };
 int full2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);
+// Launch shape of the normalize pass (k_conv2d_norm.cu), shared by every 2-D plan.
+int apply_config(const conv_norm_desc &d, const Full2dArgs &a, Full2dConfig &cfg);
 // Tensor-core path (k_conv2d_tc.cu): plan (CN_ERR_UNSUPPORTED when the problem
 // does not fit it), filter-block bytes, x tensor map, filter pre-pass.
 int tc2d_plan(const conv_norm_desc &d, Full2dArgs &args, Full2dConfig &cfg);

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 
 // Statistics of the normalization groups.  A group of one channel
 // (InstanceNorm) gets one warp, eight per block; a wider group gets a block
-// of min(channels, 8) warps, warp w taking channels w, w + warps, ... .
+// of min(channels, 8) x parts warps (below).
 // Every partial (count, K, S1, S2) is a sum about its own shift K, one of
 // its own values.  A channel's partials are moved to one common shift K0,
 // the shift of the channel's first non-empty partial (a value of the
@@ -510,8 +510,13 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 // deterministic.  The group's coefficients (mu, a = gamma * rstd * scale,
 // bb = beta * scale) go to every channel.  Arithmetic is fp32: its ~1e-6
 // relative error in mean and variance is far inside the 1e-4 output bound.
-constexpr int kStatsWarps = 8;  // most warps of a statistics block
-__global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a) {
+// With parts > 1 (wide groups with many partials) each channel's partials
+// are split into `parts` contiguous ranges, one warp each: warp w takes
+// range w % parts of channels w / parts, w / parts + warps / parts, ...;
+// the warps' results still merge in warp order.
+constexpr int kStatsWarps = 16;  // most warps of a statistics block
+constexpr int kStatsGroupsPerBlock = 8;  // one-channel groups: one warp each
+__global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a, int parts) {
     __shared__ float sm[kStatsWarps][3];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int cpg = a.Co / a.NG;
@@ -522,8 +527,15 @@ __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_c
     const int n = ng / a.NG, g = ng % a.NG;
     const float4 *p0 = a.partial + ((size_t)n * a.Co + (size_t)g * cpg) * per_c;
     Moments<float> m{0.0f, 0.0f, 0.0f};
-    for (int cl = wide ? w : 0; cl < cpg; cl += wide ? nw : 1)
-        m = merge(m, channel_moments(p0 + (size_t)cl * per_c, per_c, lane));
+    if (wide) {
+        const int slot = w / parts, part = w - slot * parts;
+        const int lo = (int)((long long)per_c * part / parts);
+        const int hi = (int)((long long)per_c * (part + 1) / parts);
+        for (int cl = slot; cl < cpg; cl += nw / parts)
+            m = merge(m, channel_moments(p0 + (size_t)cl * per_c + lo, hi - lo, lane));
+    } else {
+        m = channel_moments(p0, per_c, lane);
+    }
     if (wide) {
         if (lane == 0) {
             sm[w][0] = m.n;
@@ -554,29 +566,45 @@ __global__ void k_fill_scale(float4 *coef, int n, float scale) {
 }
 
 // Normalize pass: out = (y - mu) * a + bb per (n, c) plane, in place.
-// Planes run last-written first: the conv pass wrote samples roughly in
-// order, so the newest planes are the ones still in L2.
-__global__ void __launch_bounds__(256) k_norm_apply(float *out, const float4 *coef, long long S,
-                                                    int vec4, int *err, long long planes) {
-    const size_t plane = gridDim.x - 1 - blockIdx.x;
-    if (!CN_CHECK((long long)plane < planes, err)) return;
+// Block b takes slice b % slices of plane planes - 1 - b / slices: the
+// planes run last-written first and whole (the conv pass wrote samples
+// roughly in order, so the newest planes are the ones still in L2).  A
+// thread loads all its kApplyVec values before it stores any, which keeps
+// enough reads in flight to run near the memory bandwidth.
+constexpr int kApplyThreads = 256, kApplyVec = 4;
+__global__ void __launch_bounds__(kApplyThreads) k_norm_apply(float *out, const float4 *coef, long long S,
+                                                              int vec4, int *err, long long planes, int slices) {
+    const long long pb = (long long)blockIdx.x / slices;
+    const int slice = (int)((long long)blockIdx.x - pb * slices);
+    const long long plane = planes - 1 - pb;
+    if (!CN_CHECK(plane >= 0 && plane < planes, err)) return;
     const float4 cf = coef[plane];
-    float *p = out + plane * (size_t)S;
-    const long long step = (long long)gridDim.y * blockDim.x;
+    const long long i0 = (long long)slice * (kApplyThreads * kApplyVec) + threadIdx.x;
     if (vec4) {
-        float4 *p4 = reinterpret_cast<float4 *>(p);
+        float4 *p4 = reinterpret_cast<float4 *>(out + plane * S);
         const long long n4 = S >> 2;
-        for (long long i = (long long)blockIdx.y * blockDim.x + threadIdx.x; i < n4; i += step) {
-            float4 v = p4[i];
-            v.x = (v.x - cf.x) * cf.y + cf.z;
-            v.y = (v.y - cf.x) * cf.y + cf.z;
-            v.z = (v.z - cf.x) * cf.y + cf.z;
-            v.w = (v.w - cf.x) * cf.y + cf.z;
-            p4[i] = v;
-        }
+        float4 v[kApplyVec];
+#pragma unroll
+        for (int j = 0; j < kApplyVec; ++j)
+            if (i0 + j * kApplyThreads < n4) v[j] = p4[i0 + j * kApplyThreads];
+#pragma unroll
+        for (int j = 0; j < kApplyVec; ++j)
+            if (i0 + j * kApplyThreads < n4) {
+                v[j].x = (v[j].x - cf.x) * cf.y + cf.z;
+                v[j].y = (v[j].y - cf.x) * cf.y + cf.z;
+                v[j].z = (v[j].z - cf.x) * cf.y + cf.z;
+                v[j].w = (v[j].w - cf.x) * cf.y + cf.z;
+                p4[i0 + j * kApplyThreads] = v[j];
+            }
     } else {
-        for (long long i = (long long)blockIdx.y * blockDim.x + threadIdx.x; i < S; i += step)
-            p[i] = (p[i] - cf.x) * cf.y + cf.z;
+        float *p = out + plane * S;
+        float v[kApplyVec];
+#pragma unroll
+        for (int j = 0; j < kApplyVec; ++j)
+            if (i0 + j * kApplyThreads < S) v[j] = p[i0 + j * kApplyThreads];
+#pragma unroll
+        for (int j = 0; j < kApplyVec; ++j)
+            if (i0 + j * kApplyThreads < S) p[i0 + j * kApplyThreads] = (v[j] - cf.x) * cf.y + cf.z;
     }
 }
 
@@ -815,13 +843,17 @@ int full2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     cfg.grid = (int)std::min<long long>(items, 148);  // refined from the device in full2d_prepare
     const long long wtotal = (long long)a.ncob * a.nchunk * a.wstage;
     cfg.prep_grid = (int)std::max(1LL, std::min((wtotal + 255) / 256, 1024LL));
-    cfg.apply_threads = 256;
+    return apply_config(d, a, cfg);
+}
+
+int apply_config(const conv_norm_desc &d, const Full2dArgs &a, Full2dConfig &cfg) {
+    cfg.apply_threads = kApplyThreads;
     const long long units = a.vec4 ? a.S / 4 : a.S;
-    long long gy = (units + 256 * 4 - 1) / (256 * 4);
-    cfg.apply_grid_y = (int)std::max(1LL, std::min(gy, 65535LL));
-    const long long gx = (long long)d.N * d.C_out;
-    if (gx > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
-    cfg.apply_grid_x = (int)gx;
+    const long long slices = std::max(1LL, (units + kApplyThreads * kApplyVec - 1) / (kApplyThreads * kApplyVec));
+    const long long blocks = (long long)d.N * d.C_out * slices;
+    if (blocks > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
+    cfg.apply_slices = (int)slices;
+    cfg.apply_grid = (int)blocks;
     return CN_OK;
 }
 
@@ -926,15 +958,16 @@ int full2d_launch(const Full2dConfig &cfg, Full2dArgs &a, cudaStream_t s, const 
             k_fill_scale<<<(a.N * a.Co + 255) / 256, 256, 0, s>>>(a.coef, a.N * a.Co, a.post_scale);
         } else {
             const int cpg = a.Co / a.NG;
-            const int nw = cpg > 1 ? std::min(cpg, kStatsWarps) : kStatsWarps;
+            const int per_c = a.Dv * a.ntiles * a.wsp;
+            const int parts = (cpg > 1 && per_c >= 128) ? 2 : 1;
+            const int nw = cpg > 1 ? std::min(cpg, kStatsWarps / 2) * parts : kStatsGroupsPerBlock;
             const int blocks = cpg > 1 ? a.N * a.NG : (a.N * a.NG + nw - 1) / nw;
-            k_group_stats<<<blocks, 32 * nw, 0, s>>>(a);
+            k_group_stats<<<blocks, 32 * nw, 0, s>>>(a, parts);
         }
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
         record_launch(ev, li++, s);
-        dim3 grid(cfg.apply_grid_x, cfg.apply_grid_y);
-        k_norm_apply<<<grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4, a.err,
-                                                          (long long)a.N * a.Co);
+        k_norm_apply<<<cfg.apply_grid, cfg.apply_threads, 0, s>>>(a.out, a.coef, a.S, a.vec4, a.err,
+                                                                   (long long)a.N * a.Co, cfg.apply_slices);
         record_launch(ev, li++, s);
         if (cudaGetLastError() != cudaSuccess) return CN_ERR_CUDA;
     }

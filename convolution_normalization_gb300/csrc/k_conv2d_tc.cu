@@ -527,14 +527,7 @@ int tc2d_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     cfg.grid = (int)std::min<long long>(items, 148);
     const long long wtotal = (long long)a.ncob * a.tc_ngrp * wblk / 4;
     cfg.prep_grid = (int)std::max(1LL, std::min((wtotal + 255) / 256, 1024LL));
-    cfg.apply_threads = 256;
-    const long long units = a.vec4 ? a.S / 4 : a.S;
-    const long long gy = (units + 256 * 4 - 1) / (256 * 4);
-    cfg.apply_grid_y = (int)std::max(1LL, std::min(gy, 65535LL));
-    const long long gx = (long long)d.N * d.C_out;
-    if (gx > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
-    cfg.apply_grid_x = (int)gx;
-    return CN_OK;
+    return apply_config(d, a, cfg);
 }
 
 size_t tc2d_wprep_bytes(const Full2dArgs &a) { return (size_t)a.ncob * a.tc_ngrp * a.tc_wblk_bytes; }

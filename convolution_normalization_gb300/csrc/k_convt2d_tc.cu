@@ -291,44 +291,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
         }
     } else if (warp < kEpiWarp0) {
         // ---------------- converters ----------------
-        // Warp 2 + c converts units c and c + 2 of each tile: lane i takes
-        // position i of the unit's 8 staged rows (loads of a warp: 32
-        // consecutive words; stores: 32 consecutive 16-byte rows).
-        const int cw = warp - 2;
+        // Warp 2 + q converts unit q of each tile: lane i takes position i
+        // of the unit's 8 staged rows (loads of a warp: 32 consecutive words;
+        // stores: 32 consecutive 16-byte rows).  The landing buffer and the
+        // operand stage are both released after the stores (releasing the
+        // landing buffer right after the loads measured slower).
+        static_assert(kConvWarps == 4, "one unit of a tile per converter warp");
+        const int q = warp - 2;
         for (int k = 0;; ++k) {
             const int lb = k % kNLand, b = k & 1;
             if (!wait(&land_full[lb], (k / kNLand) & 1)) break;
             const int tile = s_land_tile[lb];
             if (k >= 2 && !wait(&st_empty[b], ((k >> 1) - 1) & 1)) break;
             bool wrote = false;
-#pragma unroll 1
-            for (int q = cw; q < 4; q += kConvWarps) {
-                if (tile < 0 || 4 * tile + q >= units_g) continue;
+            if (tile >= 0 && 4 * tile + q < units_g) {
                 int off;
                 box_col(unit_of(a, 4 * tile + q).seg, off);
                 const float *s = reinterpret_cast<const float *>(land(lb)) + (size_t)q * (kUnitLand / 4) + off + lane;
                 float4 *dst = reinterpret_cast<float4 *>(stage(b)) + q * 32 + lane;
-                if (!CN_CHECK(q * (kUnitLand / 4) + (kCig - 1) * kRowsIn * kBoxW + (kRowsIn - 1) * kBoxW + off + lane <
-                                  kLandBytes / 4,
-                              a.err))
-                    continue;
-                // all 64 loads in flight before the first store
-                float v[kRowsIn][8];
+                if (CN_CHECK(q * (kUnitLand / 4) + (kCig - 1) * kRowsIn * kBoxW + (kRowsIn - 1) * kBoxW + off + lane <
+                                 kLandBytes / 4,
+                             a.err)) {
+                    // all 64 loads in flight before the first store
+                    float v[kRowsIn][8];
 #pragma unroll
-                for (int u = 0; u < kRowsIn; ++u)
+                    for (int u = 0; u < kRowsIn; ++u)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) v[u][c] = s[c * kRowsIn * kBoxW + u * kBoxW];
+                        for (int c = 0; c < 8; ++c) v[u][c] = s[c * kRowsIn * kBoxW + u * kBoxW];
 #pragma unroll
-                for (int u = 0; u < kRowsIn; ++u) {
-                    float4 *row = dst + u * (kRowBytes / 16);
-                    row[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
-                    row[128] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
-                    row[256] = make_float4(tf32_rest(v[u][0]), tf32_rest(v[u][1]), tf32_rest(v[u][2]),
-                                           tf32_rest(v[u][3]));
-                    row[384] = make_float4(tf32_rest(v[u][4]), tf32_rest(v[u][5]), tf32_rest(v[u][6]),
-                                           tf32_rest(v[u][7]));
+                    for (int u = 0; u < kRowsIn; ++u) {
+                        float4 *row = dst + u * (kRowBytes / 16);
+                        row[0] = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                        row[128] = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+                        row[256] = make_float4(tf32_rest(v[u][0]), tf32_rest(v[u][1]), tf32_rest(v[u][2]),
+                                               tf32_rest(v[u][3]));
+                        row[384] = make_float4(tf32_rest(v[u][4]), tf32_rest(v[u][5]), tf32_rest(v[u][6]),
+                                               tf32_rest(v[u][7]));
+                    }
+                    wrote = true;
                 }
-                wrote = true;
             }
             if (wrote) fence_proxy_async();
             __syncwarp();
@@ -428,28 +429,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
                         }
                     }
                 }
+                // Warp sums of the four values (S1, S2 of the two channels) by
+                // reduce-scatter: halve the values each lane carries (xor 16,
+                // then xor 8), then a butterfly over the last three lane bits.
+                // Lane 0 ends with S1 of channel co0, lane 8 S1 of co0 + 1,
+                // lane 16 and 24 the S2 values.
+                static_assert(NP == 1, "reduce-scatter of one channel pair");
+                const bool hi16 = lane & 16, hi8 = lane & 8;
+                float2 keep = hi16 ? s2[0] : s1[0];
+                const float2 send = hi16 ? s1[0] : s2[0];
+                keep.x += __shfl_xor_sync(0xffffffffu, send.x, 16);
+                keep.y += __shfl_xor_sync(0xffffffffu, send.y, 16);
+                float r = hi8 ? keep.y : keep.x;
+                r += __shfl_xor_sync(0xffffffffu, hi8 ? keep.x : keep.y, 8);
 #pragma unroll
-                for (int c = 0; c < NP; ++c)
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        s1[c] = add2(s1[c], make_float2(__shfl_xor_sync(0xffffffffu, s1[c].x, o),
-                                                        __shfl_xor_sync(0xffffffffu, s1[c].y, o)));
-                        s2[c] = add2(s2[c], make_float2(__shfl_xor_sync(0xffffffffu, s2[c].x, o),
-                                                        __shfl_xor_sync(0xffffffffu, s2[c].y, o)));
-                    }
-                if (lane == 0) {
+                for (int o = 4; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+                const float r2 = __shfl_down_sync(0xffffffffu, r, 16);  // the S2 of lanes 0 and 8
+                if ((lane & ~8) == 0) {
                     const float cnt = (float)(rows_ok * min(kSegV, a.Wo - c0));
                     const int ui = U.band * a.tct_nseg + U.seg;
                     // partials [n][channel][unit][row part]
-                    const size_t pi = (((size_t)U.n * a.Co + co0) * a.tct_U + ui) * kRowParts + rp;
-                    const size_t pc = (size_t)a.tct_U * kRowParts;  // one channel's partials
-                    if (CN_CHECK(pi + (kEpiCo - 1) * pc < (size_t)a.N * a.Co * pc, a.err)) {
-#pragma unroll
-                        for (int c = 0; c < NP; ++c) {
-                            a.partial[pi + (2 * c) * pc] = make_float4(cnt, ksh[c].x, s1[c].x, s2[c].x);
-                            a.partial[pi + (2 * c + 1) * pc] = make_float4(cnt, ksh[c].y, s1[c].y, s2[c].y);
-                        }
-                    }
+                    const size_t pi = (((size_t)U.n * a.Co + co0 + (hi8 ? 1 : 0)) * a.tct_U + ui) * kRowParts + rp;
+                    if (CN_CHECK(pi < (size_t)a.N * a.Co * a.tct_U * kRowParts, a.err))
+                        a.partial[pi] = make_float4(cnt, hi8 ? ksh[0].y : ksh[0].x, r, r2);
                 }
             } else {
                 tc_fence_before();
@@ -560,14 +562,7 @@ int tct_plan(const conv_norm_desc &d, Full2dArgs &a, Full2dConfig &cfg) {
     cfg.smem = kSmemBytes;
     cfg.grid = d.groups;  // refined from the device in full2d_prepare
     cfg.prep_grid = 0;
-    cfg.apply_threads = 256;
-    const long long units = a.vec4 ? a.S / 4 : a.S;
-    const long long gy = (units + 256 * 4 - 1) / (256 * 4);
-    cfg.apply_grid_y = (int)std::max(1LL, std::min(gy, 65535LL));
-    const long long gx = (long long)d.N * d.C_out;
-    if (gx > 0x7fffffffLL) return CN_ERR_UNSUPPORTED;
-    cfg.apply_grid_x = (int)gx;
-    return CN_OK;
+    return apply_config(d, a, cfg);
 }
 
 // Persistent grid: the same number of CTAs for every group (each builds its
