@@ -66,7 +66,8 @@ struct Tc3Args {
     float eps, post_scale;
     int Pd, Ph, Pw;    // pool: pooled extents
     double inv_cnt, inv_cpg;  // mean: 1 / (Do Ho Wo), 1 / (channels per norm group)
-    float2 *partial;   // mean: [N][ngroups * nsplit][Co] shifted sums (S1, S2) about act(bias)
+    float4 *partial;   // mean: [N][ngroups * nsplit][Co] (count, K, S1, S2): an item's sums about
+                       // K, its first value of the channel
     int *tickets;      // mean: [N] per-sample tickets, zero between launches
     int *work;         // [2] work / exit counters, zero between launches
 };
@@ -115,7 +116,7 @@ struct Mean3dArgs {
     int vec16;        // 1: 16-byte cp.async staging is legal
     int act, norm, G, affine;
     float eps, post_scale;
-    double *partial;  // [N][nchunks][Co][3]  (count, mean, M2); the tensor-core kernel's float2 sums
+    double *partial;  // [N][nchunks][Co][3]  (count, mean, M2); the tensor-core kernel's float4 sums
     int *tickets;     // [N] per-sample tickets (small kernel: [N * groups] per-group
                       // ones), then [2] work/exit counters; zero between launches
 };
@@ -135,7 +136,7 @@ int mean3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
 // the problem is too large for it.
 int small3d_plan(const conv_norm_desc &d, Mean3dArgs &args, Mean3dConfig &cfg);
 size_t small3d_partial_bytes(const Mean3dArgs &a);
-// Bytes of the partial-moment slots (the tensor-core kernel's float2 sums or
+// Bytes of the partial-moment slots (the tensor-core kernel's float4 sums or
 // the CUDA-core kernel's fp64 (count, mean, M2)).
 size_t mean3d_partial_bytes(const Mean3dArgs &a);
 size_t mean3d_tickets(const Mean3dArgs &a);  // ints after the partial slots

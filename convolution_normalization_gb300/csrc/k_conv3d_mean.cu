@@ -493,7 +493,7 @@ int mean3d_launches(const Mean3dConfig &cfg, const Mean3dArgs &a) {
 
 size_t mean3d_partial_bytes(const Mean3dArgs &a) {
     if (a.small) return small3d_partial_bytes(a);
-    return (size_t)a.N * a.nchunks * a.Co * (a.tc ? sizeof(float2) : 3 * sizeof(double));
+    return (size_t)a.N * a.nchunks * a.Co * (a.tc ? sizeof(float4) : 3 * sizeof(double));
 }
 
 size_t mean3d_tickets(const Mean3dArgs &a) {
@@ -549,7 +549,7 @@ int mean3d_launch(const Mean3dConfig &cfg, Mean3dArgs &a, cudaStream_t s, const 
         t.beta = a.beta;
         t.out = a.out;
         t.err = a.err;
-        t.partial = reinterpret_cast<float2 *>(a.partial);
+        t.partial = reinterpret_cast<float4 *>(a.partial);
         t.tickets = a.tickets;
         t.work = a.tickets + a.N;
         return tc3_launch(cfg.tc3, t, s, ev);

@@ -110,7 +110,7 @@ struct T3 {
     static constexpr int WBYTES = K * 2 * SLEN + ZBYTES;
     static constexpr int ACC = N <= 128 ? 128 : 256;      // TMEM columns per accumulator
     static constexpr int HALO = 2 * 4 * (K - 1) * N;      // floats: [parity][quadrant][row][N]
-    static constexpr int RED = 4 * CO * 2;                // floats: mean [quadrant][CO][2] / pool cells
+    static constexpr int RED = 4 * CO * 4;                // floats: mean [quadrant][CO] float4 / pool cells
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(RED >= CO * kPoolCells, "pool cells");
 };
@@ -139,31 +139,36 @@ CN_DEV void tmem_ld_cols(uint32_t taddr, uint32_t *v) {
     if (R % 8 >= 4) tmem_ld4(taddr + B8 + (R >= 8 ? 8 : 0), v + B8 + (R >= 8 ? 8 : 0));
 }
 
-// Finish of one sample of the mean, by one warp (lane = channel).  Every slot of a
-// channel is a sum about the same shift K = act(bias), and every channel of
-// a sample has the same count n, so the statistics need no Chan-merge
-// divisions (slow on this GPU's narrow FP64 pipe): fp64 sums over the slots
-// in slot order, then with one reciprocal 1/n
-//   m_c = K + S1 / n,  M2_c = S2 - S1^2 / n,
+// Finish of one sample of the mean, by one warp (lane = channel).  Slot i of
+// a channel holds an item's (count n_i, K_i, S1_i, S2_i): sums about K_i, a
+// value of the item's data.  The slots move to one shift K0 (slot 0's) by
+// the exact identities
+//   S1 += S1_i + n_i d,  S2 += S2_i + d (2 S1_i + n_i d),  d = K_i - K0,
+// summed in a fixed tree, and with one reciprocal 1/n of the sample's count
+//   m_c = K0 + S1 / n,  M2_c = S2 - S1^2 / n,
 //   mu_g = mean of the group's m_c,  M2_g = sum (M2_c + n (m_c - mu_g)^2),
 // and out = gamma (m_c - mu_g) / sqrt(M2_g / (n C/G) + eps) + beta, times the
-// post scale.
+// post scale.  All in fp32: every shift is within a few standard deviations
+// of the data, so nothing cancels (and this GPU's FP64 pipe is slow enough
+// that fp64 here cost the kernel ~8%).
 CN_DEV void tc3_finish_sample(const Tc3Args &a, int n, int c) {
     const int nchunks = a.ngroups * a.nsplit;
     const bool on = c < a.Co;
-    double S1 = 0.0, S2 = 0.0;
+    float S1 = 0.0f, S2 = 0.0f, K0 = 0.0f;
     if (on) {
         // sixteen slot loads in flight (other CTAs' slots: not through L1),
         // summed pairwise in a fixed tree, blocks of 16 in slot order
-        const float2 *pc = a.partial + (size_t)n * nchunks * a.Co + c;
+        const float4 *pc = a.partial + (size_t)n * nchunks * a.Co + c;
+        K0 = __ldcg(pc).y;  // slot 0 (the first bands of the first planes) is never empty
         for (int ch0 = 0; ch0 < nchunks; ch0 += 16) {
-            double v1[16], v2[16];
+            float v1[16], v2[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float2 v = ch0 + j < nchunks ? __ldcg(pc + (size_t)(ch0 + j) * a.Co)
-                                                   : make_float2(0.f, 0.f);
-                v1[j] = v.x;
-                v2[j] = v.y;
+                const float4 v = ch0 + j < nchunks ? __ldcg(pc + (size_t)(ch0 + j) * a.Co)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float d = v.x > 0.0f ? v.y - K0 : 0.0f;
+                v1[j] = fmaf(v.x, d, v.z);
+                v2[j] = fmaf(d, fmaf(v.x, d, 2.0f * v.z), v.w);
             }
 #pragma unroll
             for (int w = 8; w > 0; w >>= 1)
@@ -176,32 +181,29 @@ CN_DEV void tc3_finish_sample(const Tc3Args &a, int n, int c) {
             S2 += v2[0];
         }
     }
-    const double cnt = (double)a.Do * a.Ho * a.Wo;
-    const double inv_n = a.inv_cnt;  // 1 / cnt and 1 / cpg come from the host
-    const float kc = on ? apply_act(a.act, a.b ? __ldg(a.b + c) : 0.0f) : 0.0f;
-    const double mc = (double)kc + S1 * inv_n;
-    const double m2c = fmax(S2 - S1 * S1 * inv_n, 0.0);
-    double val = mc;
+    const float cnt = (float)a.Do * a.Ho * a.Wo;
+    const float inv_n = (float)a.inv_cnt;  // 1 / cnt and 1 / cpg come from the host
+    const float mc = fmaf(S1, inv_n, K0);
+    const float m2c = fmaxf(fmaf(-S1, S1 * inv_n, S2), 0.0f);
+    float val = mc;
     if (a.norm != CN_NORM_NONE) {
         // the group's lanes: cpg consecutive channels (a power of two or not)
         const int cpg = a.Co / a.G, g0 = (c / cpg) * cpg;
-        const double inv_cpg = a.inv_cpg;
-        double sm = 0.0;
+        const float inv_cpg = (float)a.inv_cpg;
+        float sm = 0.0f;
         for (int u = 0; u < cpg; ++u) sm += __shfl_sync(0xffffffffu, mc, g0 + u);
-        const double mu = sm * inv_cpg;
-        double m2 = 0.0;
+        const float mu = sm * inv_cpg;
+        float m2 = 0.0f;
         for (int u = 0; u < cpg; ++u) {
-            const double mu_u = __shfl_sync(0xffffffffu, mc, g0 + u);
-            const double m2_u = __shfl_sync(0xffffffffu, m2c, g0 + u);
-            m2 += m2_u + cnt * (mu_u - mu) * (mu_u - mu);
+            const float dm = __shfl_sync(0xffffffffu, mc, g0 + u) - mu;
+            m2 += fmaf(cnt * dm, dm, __shfl_sync(0xffffffffu, m2c, g0 + u));
         }
-        const double var = m2 * inv_n * inv_cpg;
-        const float rstd = rsqrtf((float)(var + (double)a.eps));
-        const double ga = a.affine && on ? (double)a.gamma[c] : 1.0;
-        const double be = a.affine && on ? (double)a.beta[c] : 0.0;
-        val = ga * (mc - mu) * (double)rstd + be;
+        const float rstd = rsqrtf(m2 * inv_n * inv_cpg + a.eps);
+        const float ga = a.affine && on ? a.gamma[c] : 1.0f;
+        const float be = a.affine && on ? a.beta[c] : 0.0f;
+        val = fmaf(ga * (mc - mu), rstd, be);
     }
-    if (on && CN_CHECK(n < a.N, a.err)) a.out[(size_t)n * a.Co + c] = (float)(val * (double)a.post_scale);
+    if (on && CN_CHECK(n < a.N, a.err)) a.out[(size_t)n * a.Co + c] = val * a.post_scale;
 }
 
 template <int K, int CO, int MODE>
@@ -217,7 +219,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     __shared__ int4 s_land_info[2], s_st_info[2], s_acc_info[2];
     // mean: item sums posted by the epilogue to warp 0 (ring of kPosts)
     __shared__ __align__(8) uint64_t post_full[kPosts], post_empty[kPosts];
-    __shared__ float2 s_post[kPosts][32];
+    __shared__ float4 s_post[kPosts][32];  // per channel (unused, K, S1, S2)
     __shared__ int s_post_item[kPosts];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -231,7 +233,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     auto land = [&](int lb) { return land0 + (size_t)lb * land_stride; };
     unsigned char *wts = land0 + (size_t)a.nland * land_stride;
     float *halo = reinterpret_cast<float *>(wts + P::WBYTES);
-    float *red = halo + (a.halo ? P::HALO : 0);  // mean [quadrant][CO][2] / pool cells
+    float *red = halo + (a.halo ? P::HALO : 0);  // mean [quadrant][CO] (n, K, S1, S2) / pool cells
     const int rows_in = a.rb + K - 1;
     const int P0 = rows_in * a.W;  // staged positions per plane
 
@@ -396,9 +398,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         const int pn = grp / a.ngroups, pg = grp - pn * a.ngroups;
                         const int nchunks = a.ngroups * a.nsplit;
                         const int chunk = pg * a.nsplit + pitem % a.nsplit;
-                        const float2 sums = lane < CO ? s_post[pr][lane] : make_float2(0.f, 0.f);
+                        float4 sums = lane < CO ? s_post[pr][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&post_empty[pr]);  // the ring entry is read
+                        // the item's count: its valid rows x Wo x valid planes
+                        const int b0 = (pitem % a.nsplit) * bpi, b1 = min(b0 + bpi, a.nband);
+                        sums.x = (float)((min(b1 * a.rb, a.Ho) - b0 * a.rb) * a.Wo * min(ZG, a.Do - pg * ZG));
                         if (lane < CO && CN_CHECK(pn < a.N && chunk < nchunks, a.err))
                             a.partial[((size_t)pn * nchunks + chunk) * a.Co + lane] = sums;
                         __syncwarp();
@@ -599,6 +604,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
         int pr = 0, pk = 0;  // post ring (warp kEpiWarp0): slot, posts made
         uint32_t pph = 0;
         bool post_ok = true, stop_seen = false;
+        // A thread's sums of an item are taken about its own first value of
+        // the item (plane 0 of the item's first stage: every thread with any
+        // valid value of the item has that one), so they never cancel; at the
+        // item's end they move to one shift per warp and then per item.
+        bool item_first = true;
+        int cnt_t = 0;  // the thread's values of the item (per channel)
         for (int k = 0;; ++k) {
             const int b = k & 1;
             const bool got = wait(&acc_full[b], (k >> 1) & 1);
@@ -631,6 +642,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             }
             tc_fence_after();
             const bool pos_ok = r < a.rb * a.W && info.y * a.rb + ry < a.Ho && rx < a.Wo;
+            if (pos_ok) cnt_t += info.w;
             const float *hq = hb + (size_t)(min(q + 1, 3) * (K - 1)) * N;
 #pragma unroll 1
             for (int zg = 0; zg < ZG; ++zg) {
@@ -652,18 +664,39 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         acc += lane + kx < 32 ? o : hv;
                     }
                     const float y = apply_act(a.act, acc + bias[c]);
+                    if (item_first && zg == 0) ksh[c] = valid ? y : 0.0f;
                     const float dl = valid ? y - ksh[c] : 0.0f;
                     s1[c] += dl;
                     s2[c] = fmaf(dl, dl, s2[c]);
                 }
             }
+            item_first = false;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);
             if (!info.z) continue;
 
             // ---- end of the item: its per-channel shifted sums ----
-
+            // Each thread's sums move from its shift to the warp's (that of
+            // its lowest lane with values) by the exact identities
+            //   S1' = S1 + n d,  S2' = S2 + d (2 S1 + n d),  d = K_t - K_w,
+            // then plain adds over the warp.
+            item_first = true;
+            {
+                const unsigned has = __ballot_sync(0xffffffffu, cnt_t > 0);
+                const int src = has ? __ffs(has) - 1 : 0;
+                const float nt = (float)cnt_t;
+#pragma unroll
+                for (int c = 0; c < CQ; ++c) {
+                    const float kw = __shfl_sync(0xffffffffu, ksh[c], src);
+                    const float d = cnt_t > 0 ? ksh[c] - kw : 0.0f;
+                    s2[c] += d * fmaf(nt, d, 2.0f * s1[c]);
+                    s1[c] = fmaf(nt, d, s1[c]);
+                    ksh[c] = kw;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) cnt_t += __shfl_xor_sync(0xffffffffu, cnt_t, off);
 #pragma unroll
             for (int c = 0; c < CQ; ++c) {
 #pragma unroll
@@ -674,16 +707,16 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             }
             if (lane == 0) {
 #pragma unroll
-                for (int c = 0; c < CQ; ++c) {
-                    red[(q * CO + h * CQ + c) * 2 + 0] = s1[c];
-                    red[(q * CO + h * CQ + c) * 2 + 1] = s2[c];
-                }
+                for (int c = 0; c < CQ; ++c)
+                    reinterpret_cast<float4 *>(red)[q * CO + h * CQ + c] =
+                        make_float4((float)cnt_t, ksh[c], s1[c], s2[c]);
             }
 #pragma unroll
             for (int c = 0; c < CQ; ++c) {
                 s1[c] = 0.0f;
                 s2[c] = 0.0f;
             }
+            cnt_t = 0;
             epi_sync();
             // one warp posts the item's per-channel sums to warp 0 (which
             // publishes them and finishes the sample): the epilogue never
@@ -692,12 +725,20 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 post_ok = pk < kPosts || wait(&post_empty[pr], pph ^ 1u);
                 if (post_ok) {
                     if (lane < CO) {
-                        float S1 = 0.0f, S2 = 0.0f;
-                        for (int qq = 0; qq < 4; ++qq) {  // fixed quadrant order
-                            S1 += red[(qq * CO + lane) * 2 + 0];
-                            S2 += red[(qq * CO + lane) * 2 + 1];
+                        // the quadrants' sums moved to the first non-empty
+                        // quadrant's shift, in fixed quadrant order
+                        float K0 = 0.0f, S1 = 0.0f, S2 = 0.0f;
+                        bool have = false;
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float4 t = reinterpret_cast<const float4 *>(red)[qq * CO + lane];
+                            if (!(t.x > 0.0f)) continue;
+                            if (!have) K0 = t.y;
+                            have = true;
+                            const float d = t.y - K0;
+                            S2 += t.w + d * fmaf(t.x, d, 2.0f * t.z);
+                            S1 += fmaf(t.x, d, t.z);
                         }
-                        s_post[pr][lane] = make_float2(S1, S2);
+                        s_post[pr][lane] = make_float4(0.0f, K0, S1, S2);
                     }
                     __syncwarp();
                     if (lane == 0) {

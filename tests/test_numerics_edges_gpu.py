@@ -17,7 +17,9 @@ same problem, the plan's kernel list is checked first):
   * softmax logits x 50 (channel spreads of ~100: exp underflows for all but
     the largest channels);
   * pooling windows full of exact ties (constant x; x and w quantised so
-    that many conv outputs are bitwise equal).
+    that many conv outputs are bitwise equal);
+  * (spatial mean) groups whose channels share one large DC level, so the
+    group statistics must resolve a small spread under a large mean.
 
 Tolerance: |gpu - ref| <= 1e-4 + 1e-4 |ref| per element, the bound of the
 fused forward, with the fp64 oracle on the same inputs as reference.
@@ -114,6 +116,42 @@ def test_norm_large_dc_offset(path, scale, offset, cuda_cores, monkeypatch):
     inp = affine_input(wl.make_inputs(spec), scale, offset)
     check(spec, inp, k_cc if cuda_cores else k_tc, f"{path} x*{scale}+{offset}",
           monkeypatch, cuda_cores)
+
+
+# Channels of a group that share one large DC level and differ by little:
+# filters equal within each group up to +-1e-3 perturbations, x + offset.
+# The group's variance is then mostly within-channel and (m_c - mu_g) * rstd
+# is O(1), so the statistics must resolve a spread some 300x below the
+# channels' common mean: sums about a fixed shift far from the data (such as
+# act(bias)) lose that to cancellation, sums about a value of the data do
+# not.  The spatial-mean kernels, GroupNorm(4) of 16 channels, no activation
+# (so no group is clipped to a constant).
+SHARED_DC = wl.with_overrides(MEAN, act="none", seed=910)
+SHARED_DC_SMALL = wl.with_overrides(W["conv3d_hswish_gn4_mean_n2"], act="none", seed=911)
+
+
+def shared_dc_input(spec, offset):
+    inp = dict(wl.make_inputs(spec))
+    w = inp["w"]
+    cpg = spec["C_out"] // spec["num_groups"]
+    rng = np.random.default_rng(912)
+    base = np.repeat(w[::cpg], cpg, axis=0)
+    inp["w"] = (base + rng.uniform(-1e-3, 1e-3, size=w.shape)).astype(np.float32)
+    inp["x"] = (inp["x"] + np.float32(offset)).astype(np.float32)
+    return inp
+
+
+@pytest.mark.parametrize("offset", [100.0, 300.0])
+@pytest.mark.parametrize("kernel", ["k_conv3d_tc_mean", "k_conv3d_act_mean", "k_conv3d_mean_small"])
+def test_mean_group_with_shared_dc_level(kernel, offset, monkeypatch):
+    spec = SHARED_DC_SMALL if kernel == "k_conv3d_mean_small" else SHARED_DC
+    if kernel == "k_conv3d_act_mean":
+        monkeypatch.setenv("CN_NO_TC", "1")
+    inp = shared_dc_input(spec, offset)
+    ref = oracle.forward(spec, inp)
+    # the case is the intended one: outputs of order one, not all beta
+    assert float(np.max(np.abs(ref - np.repeat(inp["beta"][None, :], spec["N"], axis=0)))) > 0.3
+    check(spec, inp, kernel, f"{kernel} shared DC x+{offset:g}")
 
 
 @pytest.mark.parametrize("cuda_cores", [False, True], ids=["default", "cuda_cores"])
