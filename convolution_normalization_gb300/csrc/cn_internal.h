@@ -54,6 +54,8 @@ struct Tc3Args {
     int rb;           // output rows per band: 128 / W
     int nband;        // bands per plane group
     int pp;           // operand positions per staged input plane
+    int pad;          // 1: operand planes leave a 16-byte gap after every 8 positions (W % 8 == 0)
+    int ppu;          // 16-byte units per staged operand plane: pp, or pp / 8 * 9 with pad
     int stage;        // bytes of one operand stage (hi and lo, all staged planes)
     int land;         // bytes of the raw input box of a stage
     int nland;        // landing buffers for it (1 or 2)

@@ -103,7 +103,12 @@ struct T3 {
     static constexpr int N = ZG * CO * K;                 // MMA N: (zg, co, kx) columns
     static constexpr int NU = ZG + K - 1;                 // staged input planes
     static constexpr int NPAIR = (K + 1) / 2;             // hi*hi MMAs per input plane
-    static constexpr int NB = K + 2 * (ZG - 1);           // blocks of one kz sequence
+    // Narrow MMAs (a plane's columns a multiple of 32, see the MMA issuer)
+    // read only the K nonzero blocks of a kz sequence; the others also read
+    // the ZG - 1 zero blocks at each end.
+    static constexpr bool NARROW = (CO * K) % 32 == 0;
+    static constexpr int NB = NARROW ? K : K + 2 * (ZG - 1);  // stored blocks of one kz sequence
+    static constexpr int B0 = NARROW ? ZG - 1 : 0;            // leading zero blocks not stored
     static constexpr int BLK = CO * K * 16;               // one kz block: (co, kx) rows x 4 channels
     static constexpr int SLEN = NB * BLK;                 // one (ky, lo | hi) kz sequence
     static constexpr int ZBYTES = (K & 1) ? N * 16 : 0;   // zero block for an odd k
@@ -225,7 +230,10 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int PP = a.pp;
+    const int PP = a.pp, PPU = a.ppu;
+    // position p of a staged plane -> its 16-byte unit (a gap after every 8
+    // positions with pad: the converters' strided stores then miss no bank)
+    auto unit = [&](int p) { return a.pad ? p + (p >> 3) : p; };
     unsigned char *stages = smem_raw;
     auto stage = [&](int b) { return stages + (size_t)b * a.stage; };
     const int land_stride = (a.land + 127) & ~127;
@@ -258,7 +266,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
 #pragma unroll 4
         for (int e = tid; e < nraw; e += blockDim.x) wraw[e] = __ldg(a.w + e);
         __syncthreads();
-        // [ky][lo | hi][block i: kz = K + ZG - 2 - i][(co, kx) rows][4 channels], zero block
+        // [ky][lo | hi][block i: kz = K + ZG - 2 - B0 - i][(co, kx) rows][4 channels], zero block
         float *wf = reinterpret_cast<float *>(wts);
         constexpr int ROWS = CO * K;
         constexpr int NW = K * 2 * P::NB * ROWS * 4;
@@ -272,7 +280,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 const int i = r % P::NB;
                 r /= P::NB;
                 const int hi = r & 1, ky = r >> 1;
-                const int kz = K + ZG - 2 - i;
+                const int kz = K + ZG - 2 - P::B0 - i;
                 const int co = row / K, kx = row - co * K;
                 if (c < a.Ci && kz >= 0 && kz < K) {
                     const float x = wraw[((((size_t)co * a.Ci + c) * K + kz) * K + ky) * K + kx];
@@ -289,7 +297,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             const int tail = PP - P0;
             for (int i = tid; i < 2 * NU * tail; i += blockDim.x) {
                 const int pl = i / tail, r = i - pl * tail;
-                xs[(size_t)pl * PP + P0 + r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                xs[(size_t)pl * PPU + unit(P0 + r)] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
     }
@@ -459,7 +467,9 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             // descriptors are linear in the start address (units of 16 bytes)
             const uint64_t bc0 = umma_desc(wbase, P::SLEN, 128);                 // [Wl | Wh](ky)
             const uint64_t bp0 = umma_desc(wbase + P::SLEN, 2 * P::SLEN, 128);  // [Wh(ky) | Wh(ky+1)]
-            const uint32_t xl_off = (uint32_t)(NU * PP * 16);
+            const uint32_t xl_off = (uint32_t)(NU * PPU * 16);
+            const uint32_t sbo = a.pad ? 144u : 128u;  // bytes between 8-position groups
+            const int WU = unit(a.W);                  // units per input row (W % 8 == 0 with pad)
             for (int k = 0;; ++k) {
                 const int b = k & 1;
                 if (!wait(&st_full[b], (k >> 1) & 1)) break;
@@ -474,8 +484,8 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 }
                 const uint32_t d = tmem + (uint32_t)(b * P::ACC);
                 const uint32_t sb = smem_u32(stage(b));
-                const uint64_t ac0 = umma_desc(sb, xl_off, 128);                // [Xh | Xl]
-                const uint64_t ap0 = umma_desc(sb, (uint32_t)(a.W * 16), 128);  // [Xh(ky) | Xh(ky+1)]
+                const uint64_t ac0 = umma_desc(sb, xl_off, sbo);                // [Xh | Xl]
+                const uint64_t ap0 = umma_desc(sb, (uint32_t)(WU * 16), sbo);   // [Xh(ky) | Xh(ky+1)]
                 // Input plane u feeds output planes zg in [zlo, zhi] (taps
                 // kz = u - zg in [0, k)): its MMAs cover only those columns
                 // (N = their count x C_out x k, D moved to zlo's first column,
@@ -485,7 +495,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 // multiple of 32 (the TMEM allocation granule), so every D
                 // starts on one; otherwise every MMA spans all ZG planes.
                 constexpr int NZ = CO * K;  // columns of one output plane
-                constexpr bool NARROW = NZ % 32 == 0;
+                constexpr bool NARROW = P::NARROW;
 #pragma unroll
                 for (int u = 0; u < NU; ++u) {
                     const int zlo = NARROW ? (u - (K - 1) > 0 ? u - (K - 1) : 0) : 0;
@@ -494,12 +504,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                     const uint32_t id_all = idesc_tf32(128, (zhi - zlo + 1) * NZ);
                     const uint32_t id_one = idesc_tf32(128, NZ);
                     const uint32_t id_old = idesc_tf32(128, (u - zlo > 0 ? u - zlo : 1) * NZ);
-                    const uint64_t au = (uint64_t)(u * PP);
-                    const int blk = K + ZG - 2 - u + zlo;  // first valid block of the kz sequences
+                    const uint64_t au = (uint64_t)(u * PPU);
+                    const int blk = K + ZG - 2 - u + zlo - P::B0;  // first valid block of the kz sequences
                     const uint32_t dz = d + (uint32_t)(zlo * NZ);
 #pragma unroll
                     for (int ky = 0; ky < K; ++ky) {
-                        const uint64_t ad = ac0 + au + (uint64_t)(ky * a.W);
+                        const uint64_t ad = ac0 + au + (uint64_t)(ky * WU);
                         const uint64_t bd = bc0 + (uint64_t)((ky * 2 * P::SLEN + blk * P::BLK) >> 4);
                         if (ky == 0 && fresh && !NARROW) {
                             umma_tf32(dz, ad, bd, id_all, 0u);  // u = 0 initialises every plane
@@ -522,7 +532,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                             const uint32_t ad = wbase + (uint32_t)((ky * 2 + 1) * P::SLEN + blk * P::BLK);
                             bd = umma_desc(ad, zaddr - ad, 128);
                         }
-                        umma_tf32(dz, ap0 + au + (uint64_t)(ky * a.W), bd, id_all, 1u);
+                        umma_tf32(dz, ap0 + au + (uint64_t)(ky * WU), bd, id_all, 1u);
                     }
                 }
                 umma_commit(&st_empty[b]);
@@ -545,8 +555,39 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             if (info.x >= 0) {
                 const float *src = reinterpret_cast<const float *>(land(lb));
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
-                float4 *xl = xh + (size_t)NU * PP;
+                float4 *xl = xh + (size_t)NU * PPU;
                 constexpr int CT = 32 * kConvWarps;  // converter threads
+                if (a.pad) {
+                    // a thread takes 4 consecutive positions of a plane: one
+                    // 16-byte load per channel; its i-th stores of a warp land
+                    // 64 bytes apart, on distinct banks thanks to the gaps
+                    const int nq = P0 >> 2;
+#pragma unroll 1
+                    for (int u = 0; u < NU; ++u) {
+                        for (int q = ct; q < nq; q += CT) {
+                            float4 cv[4];
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                cv[c] = c < a.Ci ? *reinterpret_cast<const float4 *>(
+                                                       src + ((size_t)c * NU + u) * P0 + 4 * q)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int o = u * PPU + unit(4 * q);  // 4q % 8 is 0 or 4: one group
+                            if (!CN_CHECK(4 * q + 3 < PP, a.err)) continue;
+                            xh[o + 0] = make_float4(cv[0].x, cv[1].x, cv[2].x, cv[3].x);
+                            xh[o + 1] = make_float4(cv[0].y, cv[1].y, cv[2].y, cv[3].y);
+                            xh[o + 2] = make_float4(cv[0].z, cv[1].z, cv[2].z, cv[3].z);
+                            xh[o + 3] = make_float4(cv[0].w, cv[1].w, cv[2].w, cv[3].w);
+                            xl[o + 0] = make_float4(tf32_rest(cv[0].x), tf32_rest(cv[1].x), tf32_rest(cv[2].x),
+                                                    tf32_rest(cv[3].x));
+                            xl[o + 1] = make_float4(tf32_rest(cv[0].y), tf32_rest(cv[1].y), tf32_rest(cv[2].y),
+                                                    tf32_rest(cv[3].y));
+                            xl[o + 2] = make_float4(tf32_rest(cv[0].z), tf32_rest(cv[1].z), tf32_rest(cv[2].z),
+                                                    tf32_rest(cv[3].z));
+                            xl[o + 3] = make_float4(tf32_rest(cv[0].w), tf32_rest(cv[1].w), tf32_rest(cv[2].w),
+                                                    tf32_rest(cv[3].w));
+                        }
+                    }
+                } else
 #pragma unroll 1
                 for (int u = 0; u < NU; ++u) {
                     const float *su = src + (size_t)u * P0;
@@ -916,7 +957,11 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     // (+1 row for the zero-padded pair of an odd k)
     const int far = 127 + (K - 1 + (K & 1)) * d.W;
     const int pp = (std::max(rows_in * d.W, far + 1) + 7) & ~7;
-    const int stage_bytes = 2 * NU * pp * 16;
+    const int pad = d.W % 8 == 0;
+    const int ppu = pad ? pp / 8 * 9 : pp;
+    // stage buffers and the landing buffers after them start on 128 bytes
+    // (TMA destinations): the padded planes are only 32-byte multiples
+    const int stage_bytes = (2 * NU * ppu * 16 + 127) & ~127;
     // the raw filter passes through the two stage buffers at setup
     if ((long long)d.C_out * d.C_in * K * K * K * 4 > 2LL * stage_bytes) return CN_ERR_UNSUPPORTED;
     const int land = d.C_in * NU * rows_in * d.W * 4;
@@ -960,6 +1005,8 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
     a.nband = nband;
     a.nsplit = nsplit;
     a.pp = pp;
+    a.pad = pad;
+    a.ppu = ppu;
     a.stage = stage_bytes;
     a.land = land;
     a.nland = nland;
