@@ -115,7 +115,7 @@ struct T3 {
     static constexpr int WBYTES = K * 2 * SLEN + ZBYTES;
     static constexpr int ACC = N <= 128 ? 128 : 256;      // TMEM columns per accumulator
     static constexpr int HALO = 2 * 4 * (K - 1) * N;      // floats: [parity][quadrant][row][N]
-    static constexpr int RED = 4 * CO * 4;                // floats: mean [quadrant][CO] float4 / pool cells
+    static constexpr int RED = kPosts * 4 * CO * 4;       // floats: mean post ring [slot][quadrant][CO] float4 / pool cells
     static_assert(N % 16 == 0 && N <= 256, "MMA N");
     static_assert(RED >= CO * kPoolCells, "pool cells");
 };
@@ -224,7 +224,6 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     __shared__ int4 s_land_info[2], s_st_info[2], s_acc_info[2];
     // mean: item sums posted by the epilogue to warp 0 (ring of kPosts)
     __shared__ __align__(8) uint64_t post_full[kPosts], post_empty[kPosts];
-    __shared__ float4 s_post[kPosts][32];  // per channel (unused, K, S1, S2)
     __shared__ int s_post_item[kPosts];
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
@@ -241,7 +240,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
     auto land = [&](int lb) { return land0 + (size_t)lb * land_stride; };
     unsigned char *wts = land0 + (size_t)a.nland * land_stride;
     float *halo = reinterpret_cast<float *>(wts + P::WBYTES);
-    float *red = halo + (a.halo ? P::HALO : 0);  // mean [quadrant][CO] (n, K, S1, S2) / pool cells
+    float *red = halo + (a.halo ? P::HALO : 0);  // mean post ring [slot][quadrant][CO] (n, K, S1, S2) / pool cells
     const int rows_in = a.rb + K - 1;
     const int P0 = rows_in * a.W;  // staged positions per plane
 
@@ -406,7 +405,24 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         const int pn = grp / a.ngroups, pg = grp - pn * a.ngroups;
                         const int nchunks = a.ngroups * a.nsplit;
                         const int chunk = pg * a.nsplit + pitem % a.nsplit;
-                        float4 sums = lane < CO ? s_post[pr][lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+                        // the quadrants' sums moved to the first non-empty
+                        // quadrant's shift, in fixed quadrant order
+                        float K0 = 0.0f, S1 = 0.0f, S2 = 0.0f;
+                        if (lane < CO) {
+                            bool have = false;
+                            const float4 *ring = reinterpret_cast<const float4 *>(red) + (size_t)pr * 4 * CO + lane;
+#pragma unroll
+                            for (int qq = 0; qq < 4; ++qq) {
+                                const float4 t = ring[qq * CO];
+                                if (!(t.x > 0.0f)) continue;
+                                if (!have) K0 = t.y;
+                                have = true;
+                                const float d = t.y - K0;
+                                S2 += t.w + d * fmaf(t.x, d, 2.0f * t.z);
+                                S1 += fmaf(t.x, d, t.z);
+                            }
+                        }
+                        float4 sums = make_float4(0.0f, K0, S1, S2);
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&post_empty[pr]);  // the ring entry is read
                         // the item's count: its valid rows x Wo x valid planes
@@ -642,7 +658,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             s1[c] = 0.0f;
             s2[c] = 0.0f;
         }
-        int pr = 0, pk = 0;  // post ring (warp kEpiWarp0): slot, posts made
+        int pr = 0, pk = 0;  // post ring: slot, items posted (every epilogue warp keeps them)
         uint32_t pph = 0;
         bool post_ok = true, stop_seen = false;
         // A thread's sums of an item are taken about its own first value of
@@ -746,10 +762,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                     s2[c] += __shfl_xor_sync(0xffffffffu, s2[c], off);
                 }
             }
+            // straight into the post ring's slot pr (free: the posting warp
+            // saw it consumed before the stage's first barrier)
             if (lane == 0) {
 #pragma unroll
                 for (int c = 0; c < CQ; ++c)
-                    reinterpret_cast<float4 *>(red)[q * CO + h * CQ + c] =
+                    reinterpret_cast<float4 *>(red)[((size_t)pr * 4 + q) * CO + h * CQ + c] =
                         make_float4((float)cnt_t, ksh[c], s1[c], s2[c]);
             }
 #pragma unroll
@@ -759,41 +777,21 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             }
             cnt_t = 0;
             epi_sync();
-            // one warp posts the item's per-channel sums to warp 0 (which
-            // publishes them and finishes the sample): the epilogue never
-            // waits on global memory
-            if (warp == kEpiWarp0) {
-                post_ok = pk < kPosts || wait(&post_empty[pr], pph ^ 1u);
-                if (post_ok) {
-                    if (lane < CO) {
-                        // the quadrants' sums moved to the first non-empty
-                        // quadrant's shift, in fixed quadrant order
-                        float K0 = 0.0f, S1 = 0.0f, S2 = 0.0f;
-                        bool have = false;
-                        for (int qq = 0; qq < 4; ++qq) {
-                            const float4 t = reinterpret_cast<const float4 *>(red)[qq * CO + lane];
-                            if (!(t.x > 0.0f)) continue;
-                            if (!have) K0 = t.y;
-                            have = true;
-                            const float d = t.y - K0;
-                            S2 += t.w + d * fmaf(t.x, d, 2.0f * t.z);
-                            S1 += fmaf(t.x, d, t.z);
-                        }
-                        s_post[pr][lane] = make_float4(0.0f, K0, S1, S2);
-                    }
-                    __syncwarp();
-                    if (lane == 0) {
-                        s_post_item[pr] = info.x;
-                        mbar_arrive(&post_full[pr]);
-                    }
-                    ++pk;
-                    if (++pr == kPosts) {
-                        pr = 0;
-                        pph ^= 1u;
-                    }
-                }
+            // one warp posts the item (its quadrants' sums are in ring slot
+            // pr) to warp 0, which merges, publishes and finishes the sample:
+            // the epilogue never waits on global memory
+            if (warp == kEpiWarp0 && lane == 0) {
+                s_post_item[pr] = info.x;
+                mbar_arrive(&post_full[pr]);
             }
-            // red is rewritten only after the next stage's barriers
+            ++pk;
+            if (++pr == kPosts) {
+                pr = 0;
+                pph ^= 1u;
+            }
+            // the next slot must be consumed before any warp writes it: the
+            // posting warp checks before the next stage's barrier
+            if (warp == kEpiWarp0) post_ok = pk < kPosts || wait(&post_empty[pr], pph ^ 1u);
         }
         // the stop marker reaches warp 0 too
         if (warp == kEpiWarp0 && stop_seen && (pk < kPosts || wait(&post_empty[pr], pph ^ 1u))) {
