@@ -12,7 +12,8 @@
 // output rows over `nsplit` CTAs, so the grid spreads over the SMs: a CTA
 // stages the input planes its rows need and the group's filter in shared
 // memory, computes the group's channels at its positions, and keeps
-// per-channel sums about its first position's values.  Its partial (count,
+// per-channel sums about values of its own data (each thread's first one,
+// then the warp's and the CTA's, moved by the identities below).  Its partial (count,
 // K, S1, S2) goes to a slot; the CTA that takes the group's last ticket
 // (acquire-release) moves every partial to the first one's shift by the exact
 // identities
@@ -28,7 +29,6 @@ namespace cn {
 namespace {
 
 constexpr int kSmallThreads = 128;
-constexpr int kSmallMaxCpg = 8;  // channels per normalization group a CTA takes
 
 CN_DEV int small_ticket(int *p) {
     int old;
@@ -39,8 +39,7 @@ CN_DEV int small_ticket(int *p) {
 template <int K, int CPG>
 __global__ void __launch_bounds__(kSmallThreads) k_conv3d_mean_small(const __grid_constant__ Mean3dArgs a) {
     extern __shared__ __align__(16) float sm[];
-    __shared__ float s_red[kSmallThreads / 32][CPG][2];
-    __shared__ float s_k[CPG];
+    __shared__ float4 s_red[kSmallThreads / 32][CPG];  // per warp (count, K, S1, S2)
     __shared__ int s_last;
     constexpr int T = K * K * K;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -90,67 +89,79 @@ __global__ void __launch_bounds__(kSmallThreads) k_conv3d_mean_small(const __gri
 #pragma unroll
     for (int c = 0; c < CPG; ++c) bias[c] = a.b ? __ldg(a.b + c0 + c) : 0.0f;
     const int P0 = r0 * a.Wo, P1 = r1 * a.Wo;  // this CTA's positions
-    auto conv_at = [&](int p, float (&acc)[CPG]) {
+    // Two threads per position (lanes 2i and 2i + 1 of a warp): thread h
+    // takes the (input channel, kd) slices h, h + 2, ... of the taps, so each
+    // chain of dependent multiply-adds is half as long; the halves are added
+    // by one shuffle.
+    auto conv_half = [&](int p, int h, float (&acc)[CPG]) {
         const int ow = p % a.Wo, t = p / a.Wo, oh = t % a.Ho, od = t / a.Ho;
 #pragma unroll
-        for (int c = 0; c < CPG; ++c) acc[c] = bias[c];
-        for (int ci = 0; ci < a.Ci; ++ci) {
-            const float *xb = xs + ((size_t)ci * np + (od - pl0)) * plane + oh * a.W + ow;
-            const float *wb = ws + (size_t)ci * T * CPG;
-#pragma unroll
-            for (int kd = 0; kd < K; ++kd)
-#pragma unroll
-                for (int kh = 0; kh < K; ++kh)
-#pragma unroll
-                    for (int kw = 0; kw < K; ++kw) {
-                        const float xv = xb[kd * plane + kh * a.W + kw];
-                        const int tap = (kd * K + kh) * K + kw;
-#pragma unroll
-                        for (int c = 0; c < CPG; ++c) acc[c] = fmaf(xv, wb[tap * CPG + c], acc[c]);
-                    }
-        }
-#pragma unroll
-        for (int c = 0; c < CPG; ++c) acc[c] = apply_act(a.act, acc[c]);
-    };
-    // shift of this CTA's sums: its first position's values (output row r0,
-    // column 0), the taps split over warp 0's lanes and added by a butterfly
-    if (warp == 0) {
-        const int od = r0 / a.Ho, oh = r0 - od * a.Ho;
-        float acc[CPG];
-#pragma unroll
         for (int c = 0; c < CPG; ++c) acc[c] = 0.0f;
-        for (int ct = lane; ct < a.Ci * T; ct += 32) {
-            const int ci = ct / T, tap = ct - ci * T;
-            const int kd = tap / (K * K), kh = (tap / K) % K, kw = tap % K;
-            const float xv = xs[((size_t)ci * np + (od - pl0 + kd)) * plane + (oh + kh) * a.W + kw];
+        for (int j = h; j < a.Ci * K; j += 2) {
+            const int ci = j / K, kd = j - ci * K;
+            const float *xb = xs + ((size_t)ci * np + (od - pl0 + kd)) * plane + oh * a.W + ow;
+            const float *wb = ws + ((size_t)ci * T + kd * K * K) * CPG;
 #pragma unroll
-            for (int c = 0; c < CPG; ++c) acc[c] = fmaf(xv, ws[ct * CPG + c], acc[c]);
+            for (int kh = 0; kh < K; ++kh)
+#pragma unroll
+                for (int kw = 0; kw < K; ++kw) {
+                    const float xv = xb[kh * a.W + kw];
+#pragma unroll
+                    for (int c = 0; c < CPG; ++c) acc[c] = fmaf(xv, wb[(kh * K + kw) * CPG + c], acc[c]);
+                }
         }
-#pragma unroll
-        for (int c = 0; c < CPG; ++c) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], o);
-            if (lane == 0) s_k[c] = apply_act(a.act, acc[c] + bias[c]);
-        }
-    }
-    __syncthreads();
-    float K0[CPG], s1[CPG], s2[CPG];
+    };
+    // Each thread sums about its own first value (a value of the data, so
+    // nothing cancels); the sums then move to the warp's shift (its lowest
+    // lane with values) and the CTA's (its first warp with values) by the
+    // exact identities S1' = S1 + n d, S2' = S2 + d (2 S1 + n d), d = K - K'.
+    float kt[CPG], s1[CPG], s2[CPG];
 #pragma unroll
     for (int c = 0; c < CPG; ++c) {
-        K0[c] = s_k[c];
+        kt[c] = 0.0f;
         s1[c] = 0.0f;
         s2[c] = 0.0f;
     }
-    for (int p = P0 + tid; p < P1; p += blockDim.x) {
+    int nt = 0;
+    const int h = tid & 1;
+    for (int pb = P0; pb < P1; pb += (int)(blockDim.x >> 1)) {  // uniform: every lane shuffles
+        const int p = pb + (tid >> 1);
         float acc[CPG];
-        conv_at(p, acc);
+        if (p < P1) {
+            conv_half(p, h, acc);
+        } else {
 #pragma unroll
-        for (int c = 0; c < CPG; ++c) {
-            const float d = acc[c] - K0[c];
-            s1[c] += d;
-            s2[c] = fmaf(d, d, s2[c]);
+            for (int c = 0; c < CPG; ++c) acc[c] = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < CPG; ++c) acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 1);
+        if (p < P1 && h == 0) {
+#pragma unroll
+            for (int c = 0; c < CPG; ++c) acc[c] = apply_act(a.act, acc[c] + bias[c]);
+            if (nt == 0)
+#pragma unroll
+                for (int c = 0; c < CPG; ++c) kt[c] = acc[c];
+            ++nt;
+#pragma unroll
+            for (int c = 0; c < CPG; ++c) {
+                const float d = acc[c] - kt[c];
+                s1[c] += d;
+                s2[c] = fmaf(d, d, s2[c]);
+            }
         }
     }
+    const unsigned has = __ballot_sync(0xffffffffu, nt > 0);
+    const int src = has ? __ffs(has) - 1 : 0;
+#pragma unroll
+    for (int c = 0; c < CPG; ++c) {
+        const float kw = __shfl_sync(0xffffffffu, kt[c], src);
+        const float d = nt > 0 ? kt[c] - kw : 0.0f;
+        s2[c] += d * fmaf((float)nt, d, 2.0f * s1[c]);
+        s1[c] = fmaf((float)nt, d, s1[c]);
+        kt[c] = kw;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nt += __shfl_xor_sync(0xffffffffu, nt, o);
 #pragma unroll
     for (int c = 0; c < CPG; ++c)
 #pragma unroll
@@ -160,27 +171,29 @@ __global__ void __launch_bounds__(kSmallThreads) k_conv3d_mean_small(const __gri
         }
     if (lane == 0)
 #pragma unroll
-        for (int c = 0; c < CPG; ++c) {
-            s_red[warp][c][0] = s1[c];
-            s_red[warp][c][1] = s2[c];
-        }
+        for (int c = 0; c < CPG; ++c) s_red[warp][c] = make_float4((float)nt, kt[c], s1[c], s2[c]);
     __syncthreads();
     // the CTA's partial per channel (warps added in order), then its ticket
     float4 *part = reinterpret_cast<float4 *>(a.partial) + (size_t)ng * ns * CPG;
     if (tid < CPG) {
-        float S1 = 0.0f, S2 = 0.0f;
+        float Kc = 0.0f, S1 = 0.0f, S2 = 0.0f;
+        bool have = false;
         for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-            S1 += s_red[w][tid][0];
-            S2 += s_red[w][tid][1];
+            const float4 t = s_red[w][tid];
+            if (!(t.x > 0.0f)) continue;
+            if (!have) Kc = t.y;
+            have = true;
+            const float d = t.y - Kc;
+            S2 += t.w + d * fmaf(t.x, d, 2.0f * t.z);
+            S1 += fmaf(t.x, d, t.z);
         }
         if (CN_CHECK(ng < a.N * a.sm_ngrp, a.err))
-            part[(size_t)split * CPG + tid] = make_float4((float)(P1 - P0), K0[tid], S1, S2);
+            part[(size_t)split * CPG + tid] = make_float4((float)(P1 - P0), Kc, S1, S2);
     }
     __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        s_last = small_ticket(a.tickets + ng) == ns - 1;
-    }
+    // the acquire-release ticket publishes the partial (ordered before it by
+    // the barrier) and, for the last CTA, makes every other partial visible
+    if (tid == 0) s_last = small_ticket(a.tickets + ng) == ns - 1;
     __syncthreads();
     if (!s_last) return;
     // ---- the group's last CTA: merge the splits, write the results ----
@@ -246,8 +259,9 @@ const SmallInst kSmall[] = {CN_SMALL(1, 1), CN_SMALL(2, 1), CN_SMALL(3, 1), CN_S
 // Plans the small-problem kernel: Conv3d (groups 1) -> mean with 1, 2, 4 or 8
 // channels per normalization group (InstanceNorm and no norm: one channel per
 // CTA), up to ~16 M multiply-adds in all (beyond that the persistent kernels
-// are faster).  The splits give each CTA at least 64 positions and the grid
-// about two CTAs per SM.
+// are faster).  The splits give each CTA at most 64 positions where the rows
+// allow (one pass of its 64 thread pairs), and the grid at most about two
+// CTAs per SM.
 int small3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     if (d.conv != CN_CONV3D || d.groups != 1 || d.red != CN_RED_MEAN_SPATIAL || d.act == CN_ACT_SOFTMAX_C)
         return CN_ERR_UNSUPPORTED;
@@ -265,7 +279,9 @@ int small3d_plan(const conv_norm_desc &d, Mean3dArgs &a, Mean3dConfig &cfg) {
     if (macs > 16.0e6) return CN_ERR_UNSUPPORTED;
     const long long groups = (long long)d.N * (d.C_out / cpg);
     const int rows = Do * Ho;
-    const long long by_pos = std::max(1LL, (long long)rows * Wo / 64);
+    // at most 64 positions a CTA where rows allow (one pass of 64 thread pairs)
+    const int rows_per = std::max(1, 64 / Wo);
+    const long long by_pos = (rows + rows_per - 1) / rows_per;
     // about two CTAs per SM of a 152-SM GPU (a heuristic fixed at plan time,
     // since the workspace depends on it)
     const long long by_grid = std::max(1LL, (2LL * 152 + groups - 1) / std::max(1LL, groups));
