@@ -701,10 +701,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             const bool pos_ok = r < a.rb * a.W && info.y * a.rb + ry < a.Ho && rx < a.Wo;
             if (pos_ok) cnt_t += info.w;
             const float *hq = hb + (size_t)(min(q + 1, 3) * (K - 1)) * N;
-            // one plane's columns: the kx sum (lane shifts, the halo past a
-            // quadrant), bias + activation, the thread's shifted sums
-            auto plane_sums = [&](int zg, const uint32_t (&v)[NC]) {
+#pragma unroll 1
+            for (int zg = 0; zg < ZG; ++zg) {
+                uint32_t v[NC];
                 const int col0 = (zg * CO + h * CQ) * K;
+                tmem_ld_cols<NC>(tq + (uint32_t)col0, v);
+                tmem_wait_ld();
                 const bool valid = pos_ok && zg < info.w;
 #pragma unroll
                 for (int c = 0; c < CQ; ++c) {
@@ -724,13 +726,6 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                     s1[c] += dl;
                     s2[c] = fmaf(dl, dl, s2[c]);
                 }
-            };
-#pragma unroll 1
-            for (int zg = 0; zg < ZG; ++zg) {
-                uint32_t v[NC];
-                tmem_ld_cols<NC>(tq + (uint32_t)((zg * CO + h * CQ) * K), v);
-                tmem_wait_ld();
-                plane_sums(zg, v);
             }
             item_first = false;
             tc_fence_before();
