@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the fused convolution + normalization forward.
+"""fp64 CPU oracle for the fused convolution + normalization forward, and
+for its backward pass (the gradients of a loss through the same layers).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
 CPU-baseline leg may import this package; the library itself never does.
@@ -59,6 +60,13 @@ def _load():
         lib.ocn_scale.argtypes = [_dp, L, d]
         lib.ocn_mean_spatial.argtypes = [_dp, i, i, L, _dp]
         lib.ocn_maxpool3d_2.argtypes = [_dp, i, i, i, i, i, _dp]
+        lib.ocn_conv3d_grad_input.argtypes = [_dp, i, i, i, i, i, _dp, i, i, i, i, i, _dp]
+        lib.ocn_conv3d_grad_weight.argtypes = [_dp, i, i, i, i, i, _dp, i, i, i, i, i, _dp, _dp]
+        lib.ocn_conv_transpose2d_grad_input.argtypes = [_dp, i, i, i, i, _dp, i, i, i, _dp]
+        lib.ocn_conv_transpose2d_grad_weight.argtypes = [_dp, i, i, i, i, _dp, i, i, i, _dp, _dp]
+        lib.ocn_hardswish_grad.argtypes = [_dp, _dp, L]
+        lib.ocn_gelu_erf_grad.argtypes = [_dp, _dp, L]
+        lib.ocn_group_norm_grad.argtypes = [_dp, i, i, L, i, d, _dp, _dp, _dp, _dp, _dp]
         lib.ocn_num_threads.restype = i
         lib.ocn_set_num_threads.argtypes = [i]
         _lib = lib
@@ -206,3 +214,128 @@ def forward(s, inputs, samples=None):
     elif red == "maxpool2_x2":
         y = maxpool3d_2(maxpool3d_2(y))
     return y
+
+
+# ---- the backward pass ------------------------------------------------------
+# Gradients of a loss L through the forward above, given dout = dL/d(output).
+# Each primitive is the derivative of the forward primitive of the same name.
+
+def conv3d_grad_input(dy, w, groups=1):
+    dy, w = _f64(dy), _f64(w)
+    N, Co, Do, Ho, Wo = dy.shape
+    _, Cig, kd, kh, kw = w.shape
+    Ci = Cig * groups
+    dx = np.empty((N, Ci, Do + kd - 1, Ho + kh - 1, Wo + kw - 1))
+    _load().ocn_conv3d_grad_input(_p(dy), N, Co, Do, Ho, Wo, _p(w), Ci, kd, kh, kw, groups, _p(dx))
+    return dx
+
+
+def conv3d_grad_weight(x, dy, w_shape, groups=1):
+    x, dy = _f64(x), _f64(dy)
+    N, Ci, D, H, W = x.shape
+    Co, Cig, kd, kh, kw = w_shape
+    dw = np.empty(w_shape)
+    db = np.empty(Co)
+    _load().ocn_conv3d_grad_weight(_p(x), N, Ci, D, H, W, _p(dy), Co, kd, kh, kw, groups, _p(dw), _p(db))
+    return dw, db
+
+
+def conv2d_grad_input(dy, w, groups=1):
+    N, Co, Ho, Wo = dy.shape
+    Co_, Cig, kh, kw = w.shape
+    dx = conv3d_grad_input(np.asarray(dy).reshape(N, Co, 1, Ho, Wo),
+                           np.asarray(w).reshape(Co_, Cig, 1, kh, kw), groups)
+    return dx.reshape(N, Cig * groups, Ho + kh - 1, Wo + kw - 1)
+
+
+def conv2d_grad_weight(x, dy, w_shape, groups=1):
+    N, Ci, H, W = x.shape
+    Co, Cig, kh, kw = w_shape
+    dw, db = conv3d_grad_weight(np.asarray(x).reshape(N, Ci, 1, H, W),
+                                np.asarray(dy).reshape(dy.shape[0], dy.shape[1], 1, *dy.shape[2:]),
+                                (Co, Cig, 1, kh, kw), groups)
+    return dw.reshape(w_shape), db
+
+
+def conv_transpose2d_grad_input(dy, w, groups=1):
+    dy, w = _f64(dy), _f64(w)
+    N, Co, Ho, Wo = dy.shape
+    Ci, _, k, _ = w.shape
+    H, W = Ho - k + 1, Wo - k + 1
+    dx = np.empty((N, Ci, H, W))
+    _load().ocn_conv_transpose2d_grad_input(_p(dy), N, Co, H, W, _p(w), Ci, k, groups, _p(dx))
+    return dx
+
+
+def conv_transpose2d_grad_weight(x, dy, w_shape, groups=1):
+    x, dy = _f64(x), _f64(dy)
+    N, Ci, H, W = x.shape
+    _, Cog, k, _ = w_shape
+    Co = Cog * groups
+    dw = np.empty(w_shape)
+    db = np.empty(Co)
+    _load().ocn_conv_transpose2d_grad_weight(_p(x), N, Ci, H, W, _p(dy), Co, k, groups, _p(dw), _p(db))
+    return dw, db
+
+
+def hardswish_grad(v, g):
+    g = np.array(g, dtype=np.float64, order="C", copy=True)
+    _load().ocn_hardswish_grad(_p(_f64(v)), _p(g), g.size)
+    return g
+
+
+def gelu_erf_grad(v, g):
+    g = np.array(g, dtype=np.float64, order="C", copy=True)
+    _load().ocn_gelu_erf_grad(_p(_f64(v)), _p(g), g.size)
+    return g
+
+
+def group_norm_grad(y, dout, G, eps=1e-5, gamma=None):
+    """(dy, dgamma, dbeta) of group_norm(y, G, eps, gamma, beta) for dout."""
+    y, dout = _f64(y), _f64(dout)
+    N, C = y.shape[:2]
+    S = int(np.prod(y.shape[2:]))
+    dy = np.empty_like(y)
+    dgamma, dbeta = np.empty(C), np.empty(C)
+    _load().ocn_group_norm_grad(_p(y), N, C, S, G, eps, _p(_f64(gamma)), _p(dout), _p(dy),
+                                _p(dgamma), _p(dbeta))
+    return dy, dgamma, dbeta
+
+
+def backward(s, inputs, dout):
+    """Gradients of the whole fused block for workload dict ``s`` (spatial
+    reductions none or the spatial mean; activations none, HardSwish or
+    GELU): dict with dx, dw, db (None without bias), dgamma and dbeta (None
+    without an affine norm).  The forward's intermediates are recomputed."""
+    act, norm, red = s["act"], s["norm"], s["red"]
+    assert red in ("none", "mean_spatial") and act in ("none", "hardswish", "gelu_erf")
+    x, w, G = inputs["x"], inputs["w"], s["groups"]
+    a = conv_stage(s, inputs)                       # pre-activation
+    y = a if act == "none" else (hardswish(a) if act == "hardswish" else gelu_erf(a))
+    g = np.asarray(dout, dtype=np.float64)
+    if red == "mean_spatial":                       # d(mean)/dv = 1/S for every position
+        S = int(np.prod(a.shape[2:]))
+        g = np.broadcast_to((g / S).reshape(g.shape + (1,) * (a.ndim - 2)), a.shape).copy()
+    if s["post_scale"] != 1.0:
+        g = scale(g, s["post_scale"])
+    dgamma = dbeta = None
+    aff = bool(s["affine"]) and norm != "none"
+    if norm != "none":
+        Gn = s["num_groups"] if norm == "group" else a.shape[1]
+        g, dgamma, dbeta = group_norm_grad(y, g, Gn, s["eps"], inputs["gamma"] if aff else None)
+        if not aff:
+            dgamma = dbeta = None
+    if act == "hardswish":
+        g = hardswish_grad(a, g)
+    elif act == "gelu_erf":
+        g = gelu_erf_grad(a, g)
+    if s["conv"] == "conv3d":
+        dx = conv3d_grad_input(g, w, G)
+        dw, db = conv3d_grad_weight(x, g, w.shape, G)
+    elif s["conv"] == "conv2d":
+        dx = conv2d_grad_input(g, w, G)
+        dw, db = conv2d_grad_weight(x, g, w.shape, G)
+    else:
+        dx = conv_transpose2d_grad_input(g, w, G)
+        dw, db = conv_transpose2d_grad_weight(x, g, w.shape, G)
+    return {"dx": dx, "dw": dw, "db": db if s["has_bias"] else None, "dgamma": dgamma, "dbeta": dbeta}

@@ -18,6 +18,7 @@
  */
 #include <math.h>
 #include <stddef.h>
+#include <stdlib.h>
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
@@ -243,4 +244,235 @@ void ocn_maxpool3d_2(const double *v, int N, int C, int D, int H, int W,
                     out[((t * Dp + d) * (long)Hp + h) * Wp + w] = m;
                 }
     }
+}
+
+/* ---------------------------------------------------------------------------
+ * Backward pass (the gradient of a scalar loss L through the same layers).
+ * The pages treat only the forward; each routine below is the derivative of
+ * the forward routine it names, written out as plain loops, with dy the
+ * gradient of L with respect to that routine's output.
+ * ------------------------------------------------------------------------- */
+
+/* Gradient of ocn_conv3d with respect to its input:
+ *   dx[n,ci,z,h,w] = sum_{co in group(ci)} sum_{a,p,q} dy[n,co,z-a,h-p,w-q] * w[co, ci - g*Cig, a, p, q]
+ * over the output positions that exist (0 <= z-a < Do, ...). */
+void ocn_conv3d_grad_input(const double *dy, int N, int Co, int Do, int Ho, int Wo,
+                           const double *w, int Ci, int kd, int kh, int kw, int groups,
+                           double *dx) {
+    const int D = Do + kd - 1, H = Ho + kh - 1, W = Wo + kw - 1;
+    const int Cig = Ci / groups, Cog = Co / groups;
+    long nci = (long)N * Ci;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < nci; ++t) {
+        const int n = (int)(t / Ci), ci = (int)(t % Ci);
+        const int g = ci / Cig, cl = ci - g * Cig;
+        for (int z = 0; z < D; ++z)
+            for (int h = 0; h < H; ++h)
+                for (int x = 0; x < W; ++x) {
+                    double acc = 0.0;
+                    for (int j = 0; j < Cog; ++j) {
+                        const int co = g * Cog + j;
+                        for (int a = 0; a < kd; ++a) {
+                            const int zo = z - a;
+                            if (zo < 0 || zo >= Do) continue;
+                            for (int p = 0; p < kh; ++p) {
+                                const int ho = h - p;
+                                if (ho < 0 || ho >= Ho) continue;
+                                for (int q = 0; q < kw; ++q) {
+                                    const int xo = x - q;
+                                    if (xo < 0 || xo >= Wo) continue;
+                                    acc += dy[((((long)n * Co + co) * Do + zo) * Ho + ho) * Wo + xo] *
+                                           w[((((long)co * Cig + cl) * kd + a) * kh + p) * kw + q];
+                                }
+                            }
+                        }
+                    }
+                    dx[((((long)n * Ci + ci) * D + z) * H + h) * W + x] = acc;
+                }
+    }
+}
+
+/* Gradient of ocn_conv3d with respect to its weight and bias:
+ *   dw[co, cl, a, p, q] = sum_{n, z, h, x} dy[n,co,z,h,x] * x[n, g*Cig + cl, z+a, h+p, x+q]
+ *   db[co] = sum_{n, z, h, x} dy[n,co,z,h,x]            (db may be NULL) */
+void ocn_conv3d_grad_weight(const double *x, int N, int Ci, int D, int H, int W,
+                            const double *dy, int Co, int kd, int kh, int kw, int groups,
+                            double *dw, double *db) {
+    const int Do = D - kd + 1, Ho = H - kh + 1, Wo = W - kw + 1;
+    const int Cig = Ci / groups, Cog = Co / groups;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int co = 0; co < Co; ++co) {
+        const int g = co / Cog;
+        for (int cl = 0; cl < Cig; ++cl) {
+            const int ci = g * Cig + cl;
+            for (int a = 0; a < kd; ++a)
+                for (int p = 0; p < kh; ++p)
+                    for (int q = 0; q < kw; ++q) {
+                        double acc = 0.0;
+                        for (int n = 0; n < N; ++n)
+                            for (int z = 0; z < Do; ++z)
+                                for (int h = 0; h < Ho; ++h)
+                                    for (int xo = 0; xo < Wo; ++xo)
+                                        acc += dy[((((long)n * Co + co) * Do + z) * Ho + h) * Wo + xo] *
+                                               x[((((long)n * Ci + ci) * D + z + a) * H + h + p) * W + xo + q];
+                        dw[((((long)co * Cig + cl) * kd + a) * kh + p) * kw + q] = acc;
+                    }
+        }
+        if (db) {
+            double s = 0.0;
+            for (int n = 0; n < N; ++n)
+                for (long i = 0; i < (long)Do * Ho * Wo; ++i) s += dy[((long)n * Co + co) * Do * Ho * Wo + i];
+            db[co] = s;
+        }
+    }
+}
+
+/* Gradient of ocn_conv_transpose2d with respect to its input:
+ *   dx[n,ci,ii,jj] = sum_{co in group(ci)} sum_{p,q} dy[n,co,ii+p,jj+q] * w[ci, co - g*Cog, p, q] */
+void ocn_conv_transpose2d_grad_input(const double *dy, int N, int Co, int H, int W,
+                                     const double *w, int Ci, int k, int groups, double *dx) {
+    const int Ho = H + k - 1, Wo = W + k - 1;
+    const int Cig = Ci / groups, Cog = Co / groups;
+    long nci = (long)N * Ci;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < nci; ++t) {
+        const int n = (int)(t / Ci), ci = (int)(t % Ci);
+        const int g = ci / Cig;
+        for (int ii = 0; ii < H; ++ii)
+            for (int jj = 0; jj < W; ++jj) {
+                double acc = 0.0;
+                for (int col = 0; col < Cog; ++col) {
+                    const int co = g * Cog + col;
+                    for (int p = 0; p < k; ++p)
+                        for (int q = 0; q < k; ++q)
+                            acc += dy[(((long)n * Co + co) * Ho + ii + p) * Wo + jj + q] *
+                                   w[(((long)ci * Cog + col) * k + p) * k + q];
+                }
+                dx[(((long)n * Ci + ci) * H + ii) * W + jj] = acc;
+            }
+    }
+}
+
+/* Gradient of ocn_conv_transpose2d with respect to its weight and bias:
+ *   dw[ci, col, p, q] = sum_{n, ii, jj} x[n,ci,ii,jj] * dy[n, g*Cog + col, ii+p, jj+q]
+ *   db[co] = sum_{n, i, j} dy[n,co,i,j]                  (db may be NULL) */
+void ocn_conv_transpose2d_grad_weight(const double *x, int N, int Ci, int H, int W,
+                                      const double *dy, int Co, int k, int groups,
+                                      double *dw, double *db) {
+    const int Ho = H + k - 1, Wo = W + k - 1;
+    const int Cig = Ci / groups, Cog = Co / groups;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int ci = 0; ci < Ci; ++ci) {
+        const int g = ci / Cig;
+        for (int col = 0; col < Cog; ++col) {
+            const int co = g * Cog + col;
+            for (int p = 0; p < k; ++p)
+                for (int q = 0; q < k; ++q) {
+                    double acc = 0.0;
+                    for (int n = 0; n < N; ++n)
+                        for (int ii = 0; ii < H; ++ii)
+                            for (int jj = 0; jj < W; ++jj)
+                                acc += x[(((long)n * Ci + ci) * H + ii) * W + jj] *
+                                       dy[(((long)n * Co + co) * Ho + ii + p) * Wo + jj + q];
+                    dw[(((long)ci * Cog + col) * k + p) * k + q] = acc;
+                }
+        }
+    }
+    if (db) {
+#pragma omp parallel for schedule(static)
+        for (int co = 0; co < Co; ++co) {
+            double s = 0.0;
+            for (int n = 0; n < N; ++n)
+                for (long i = 0; i < (long)Ho * Wo; ++i) s += dy[((long)n * Co + co) * Ho * Wo + i];
+            db[co] = s;
+        }
+    }
+}
+
+/* g *= hardswish'(v): 0 below -3, v/3 + 1/2 on [-3, 3], 1 above (the
+ * one-sided values PyTorch uses at the two kinks). */
+void ocn_hardswish_grad(const double *v, double *g, long n) {
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < n; ++i) {
+        const double a = v[i];
+        const double d = a < -3.0 ? 0.0 : (a <= 3.0 ? a / 3.0 + 0.5 : 1.0);
+        g[i] *= d;
+    }
+}
+
+/* g *= gelu'(v) for the erf form: Phi(v) + v * phi(v), with Phi the normal
+ * CDF 0.5 (1 + erf(v / sqrt(2))) and phi its density exp(-v^2/2)/sqrt(2 pi). */
+void ocn_gelu_erf_grad(const double *v, double *g, long n) {
+    const double inv_sqrt2pi = 0.39894228040143267794;
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < n; ++i) {
+        const double a = v[i];
+        g[i] *= 0.5 * (1.0 + erf(a / sqrt(2.0))) + a * inv_sqrt2pi * exp(-0.5 * a * a);
+    }
+}
+
+/*
+ * Gradient of ocn_group_norm.  Per (n, g), with M = (C/G) S values, mu and
+ * var as in the forward (two passes), r = 1/sqrt(var + eps), xh = (y - mu) r
+ * and dxh = dout * gamma[c]:
+ *   dy = r (dxh - mean(dxh) - xh mean(dxh xh))
+ *   dgamma[c] = sum_{n, s} dout xh,   dbeta[c] = sum_{n, s} dout
+ * gamma NULL means 1; dgamma and dbeta may be NULL.
+ */
+void ocn_group_norm_grad(const double *y, int N, int C, long S, int G, double eps,
+                         const double *gamma, const double *dout, double *dy,
+                         double *dgamma, double *dbeta) {
+    const int cpg = C / G;
+    const long cnt = (long)cpg * S;
+    double *xh_all = (double *)malloc(sizeof(double) * (size_t)N * C * S);
+    long ng = (long)N * G;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < ng; ++t) {
+        const long n = t / G, g = t % G;
+        const long base = (n * C + g * cpg) * S;
+        double s = 0.0;
+        for (long i = 0; i < cnt; ++i) s += y[base + i];
+        const double mu = s / (double)cnt;
+        double q = 0.0;
+        for (long i = 0; i < cnt; ++i) {
+            const double d = y[base + i] - mu;
+            q += d * d;
+        }
+        const double r = 1.0 / sqrt(q / (double)cnt + eps);
+        double m1 = 0.0, m2 = 0.0;
+        for (int cl = 0; cl < cpg; ++cl) {
+            const double ga = gamma ? gamma[g * cpg + cl] : 1.0;
+            for (long i = 0; i < S; ++i) {
+                const long idx = base + (long)cl * S + i;
+                const double xh = (y[idx] - mu) * r;
+                xh_all[idx] = xh;
+                m1 += dout[idx] * ga;
+                m2 += dout[idx] * ga * xh;
+            }
+        }
+        m1 /= (double)cnt;
+        m2 /= (double)cnt;
+        for (int cl = 0; cl < cpg; ++cl) {
+            const double ga = gamma ? gamma[g * cpg + cl] : 1.0;
+            for (long i = 0; i < S; ++i) {
+                const long idx = base + (long)cl * S + i;
+                dy[idx] = r * (dout[idx] * ga - m1 - xh_all[idx] * m2);
+            }
+        }
+    }
+    if (dgamma || dbeta) {
+#pragma omp parallel for schedule(static)
+        for (int c = 0; c < C; ++c) {
+            double sg = 0.0, sb = 0.0;
+            for (int n = 0; n < N; ++n)
+                for (long i = 0; i < S; ++i) {
+                    const long idx = ((long)n * C + c) * S + i;
+                    sg += dout[idx] * xh_all[idx];
+                    sb += dout[idx];
+                }
+            if (dgamma) dgamma[c] = sg;
+            if (dbeta) dbeta[c] = sb;
+        }
+    }
+    free(xh_all);
 }
