@@ -63,7 +63,9 @@ EXPORTED = ("conv_norm_desc_validate", "conv_norm_output_shape", "conv_norm_stat
             "conv_norm_plan_info", "conv_norm_forward", "conv_norm_forward_host",
             "conv_norm_plan_check_device", "conv_norm_forward_noalloc",
             "conv_norm_plan_set_launch_events", "conv_norm_plan_set_wait_limit",
-            "conv_norm_plan_inject_stall")
+            "conv_norm_plan_inject_stall", "conv_norm_bwd_plan_create", "conv_norm_backward",
+            "conv_norm_bwd_workspace_bytes", "conv_norm_bwd_check_device",
+            "conv_norm_bwd_plan_destroy")
 
 
 def _load():
@@ -102,6 +104,16 @@ def _load():
     lib.conv_norm_plan_set_wait_limit.restype = i
     lib.conv_norm_plan_inject_stall.argtypes = [vp]
     lib.conv_norm_plan_inject_stall.restype = i
+    lib.conv_norm_bwd_plan_create.argtypes = [pd, ctypes.POINTER(vp)]
+    lib.conv_norm_bwd_plan_create.restype = i
+    lib.conv_norm_backward.argtypes = [vp] * 13
+    lib.conv_norm_backward.restype = i
+    lib.conv_norm_bwd_workspace_bytes.argtypes = [vp]
+    lib.conv_norm_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.conv_norm_bwd_check_device.argtypes = [vp, vp]
+    lib.conv_norm_bwd_check_device.restype = i
+    lib.conv_norm_bwd_plan_destroy.argtypes = [vp]
+    lib.conv_norm_bwd_plan_destroy.restype = None
     return lib
 
 
@@ -247,6 +259,30 @@ def conv_norm_plan_set_launch_events(plan, events) -> int:
                   "conv_norm_plan_set_launch_events")
 
 
+def conv_norm_bwd_plan_create(desc: conv_norm_desc) -> int:
+    h = ctypes.c_void_p()
+    _check(lib.conv_norm_bwd_plan_create(ctypes.byref(desc), ctypes.byref(h)), "conv_norm_bwd_plan_create")
+    return h.value
+
+
+def conv_norm_bwd_plan_destroy(plan: int) -> None:
+    lib.conv_norm_bwd_plan_destroy(plan)
+
+
+def conv_norm_bwd_workspace_bytes(plan: int) -> int:
+    return int(lib.conv_norm_bwd_workspace_bytes(plan))
+
+
+def conv_norm_backward(plan, x, w, b, gamma, beta, dout, dx, dw, db, dgamma, dbeta, stream=None) -> int:
+    return _check(lib.conv_norm_backward(plan, _ptr(x), _ptr(w), _ptr(b), _ptr(gamma), _ptr(beta),
+                                         _ptr(dout), _ptr(dx), _ptr(dw), _ptr(db), _ptr(dgamma),
+                                         _ptr(dbeta), _stream(stream)), "conv_norm_backward")
+
+
+def conv_norm_bwd_check_device(plan, stream=None) -> int:
+    return lib.conv_norm_bwd_check_device(plan, _stream(stream))
+
+
 class Plan:
     """Owns one conv_norm plan; a convenience wrapper over the C calls."""
 
@@ -294,3 +330,37 @@ class Plan:
 
     def __exit__(self, *exc):
         self.close()
+
+
+class BwdPlan:
+    """Owns one backward plan (full-output 2-D blocks); a convenience wrapper."""
+
+    def __init__(self, spec=None, **kw):
+        self.desc = make_desc(spec, **kw)
+        self.handle = conv_norm_bwd_plan_create(self.desc)
+
+    def backward(self, x, w, b, gamma, beta, dout, dx, dw, db, dgamma, dbeta, stream=None):
+        return conv_norm_backward(self.handle, x, w, b, gamma, beta, dout, dx, dw, db, dgamma, dbeta, stream)
+
+    def check_device(self, stream=None):
+        return conv_norm_bwd_check_device(self.handle, stream)
+
+    def workspace_bytes(self):
+        return conv_norm_bwd_workspace_bytes(self.handle)
+
+    def close(self):
+        if self.handle:
+            conv_norm_bwd_plan_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,480 @@
+// Backward pass of the full-output 2-D block: Conv2d or ConvTranspose2d
+// (groups) -> activation (none, HardSwish, GELU) -> GroupNorm / InstanceNorm
+// / none -> post scale.  The pages state only the forward; the gradients are
+// the derivatives of that forward (the chain rule through each layer).
+//
+// Given dout = dL/d(out), with A the conv output (pre-activation), y = act(A),
+// per (n, group) mu, r = 1/sqrt(var + eps), xh = (y - mu) r, and s the post
+// scale:
+//   dxh   = s gamma_c dout
+//   dy    = r (dxh - mean(dxh) - xh mean(dxh xh))        (mean over the group)
+//   dA    = dy act'(A)
+//   dgamma_c = s sum_{n,p} dout xh,  dbeta_c = s sum_{n,p} dout,  db_co = sum dA
+//   dx    = the adjoint conv of dA with the same weights (a transposed conv for
+//           Conv2d, a conv for ConvTranspose2d)
+//   dw    = the correlation of dA with x over every sample and position.
+//
+// Steps (one stream, all deterministic):
+//   1. A: the forward plan of the conv alone (no activation, norm or scale);
+//   2. k_bwd_plane_sums: per (n, c) plane, sums about the plane's first value
+//      y0: count, sum(y - y0), sum (y - y0)^2, sum dout, sum dout (y - y0);
+//   3. k_bwd_group: per (n, group) the planes merge at one shift (exact
+//      identities), giving mu, r and the two group means above; per (n, c)
+//      the coefficients of dy = a dout + b + c (y - mu) and the plane's
+//      dgamma / dbeta terms;
+//   4. k_bwd_dA: dA in place of A, and per-plane-slice sums for db;
+//   5. dx: the forward plan of the adjoint conv on dA;
+//   6. k_bwd_weight: dw as a GEMM over all positions (split over the
+//      positions, fixed-order sum of the splits in k_bwd_weight_sum);
+//   7. k_bwd_channel_sums: dgamma, dbeta and db, summed over n in order.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "cn_common.cuh"
+#include "cn_internal.h"
+
+namespace cn {
+namespace {
+
+constexpr int kBwdThreads = 256;
+
+// act'(a): HardSwish 0 below -3, a/3 + 1/2 on [-3, 3], 1 above; GELU (erf
+// form) Phi(a) + a phi(a), erf by Abramowitz & Stegun 7.1.26 as in the
+// forward (|error| <= 1.5e-7).
+CN_DEV float act_grad(int act, float a) {
+    if (act == ACT_HARDSWISH) return a < -3.0f ? 0.0f : (a <= 3.0f ? fmaf(a, 1.0f / 3.0f, 0.5f) : 1.0f);
+    if (act == ACT_GELU) {
+        const float z = fabsf(a) * 0.70710678118654752f;
+        const float t = 1.0f / fmaf(CN_AS_P, z, 1.0f);
+        float y = fmaf(t, CN_AS_A5, CN_AS_A4);
+        y = fmaf(t, y, CN_AS_A3);
+        y = fmaf(t, y, CN_AS_A2);
+        y = fmaf(t, y, CN_AS_A1);
+        const float e = expf(-0.5f * a * a);
+        const float q = y * t * e;  // erfc(|a| / sqrt 2)
+        const float Phi = a >= 0.0f ? 1.0f - 0.5f * q : 0.5f * q;
+        return fmaf(a * 0.39894228040143268f, e, Phi);
+    }
+    return 1.0f;
+}
+
+// Block sum of kBwdThreads values in a fixed order (warp butterflies, then
+// the warps' results in warp order); every thread gets the result.
+template <int NV>
+CN_DEV void block_sum(float (&v)[NV]) {
+    __shared__ float red[kBwdThreads / 32][NV];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < NV; ++j)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v[j] += __shfl_xor_sync(0xffffffffu, v[j], o);
+    if (lane == 0)
+#pragma unroll
+        for (int j = 0; j < NV; ++j) red[warp][j] = v[j];
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        float s = 0.0f;
+        for (int w = 0; w < kBwdThreads / 32; ++w) s += red[w][j];
+        v[j] = s;
+    }
+    __syncthreads();
+}
+
+// Step 2: one block per (n, c) plane.
+__global__ void __launch_bounds__(kBwdThreads) k_bwd_plane_sums(const float *A, const float *dout, long long S,
+                                                                int act, float4 *ps) {
+    const long long plane = blockIdx.x;
+    const float *ap = A + plane * S, *gp = dout + plane * S;
+    const float K = apply_act(act, ap[0]);
+    float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // sum d, sum d^2, sum g, sum g d
+    for (long long i = threadIdx.x; i < S; i += kBwdThreads) {
+        const float d = apply_act(act, ap[i]) - K, g = gp[i];
+        v[0] += d;
+        v[1] = fmaf(d, d, v[1]);
+        v[2] += g;
+        v[3] = fmaf(g, d, v[3]);
+    }
+    block_sum<4>(v);
+    if (threadIdx.x == 0) {
+        ps[2 * plane] = make_float4((float)S, K, v[0], v[1]);
+        ps[2 * plane + 1] = make_float4(v[2], v[3], 0.0f, 0.0f);
+    }
+}
+
+// Step 3: one thread per (n, group), planes in channel order.
+__global__ void k_bwd_group(const float4 *ps, int N, int C, int G, int norm, float eps, float scale,
+                            const float *gamma, float4 *coef, float2 *gpart) {
+    const int ng = blockIdx.x * blockDim.x + threadIdx.x;
+    if (ng >= N * G) return;
+    const int n = ng / G, g = ng - n * G, cpg = C / G;
+    const int c0 = g * cpg;
+    if (norm == CN_NORM_NONE) {
+        for (int cl = 0; cl < cpg; ++cl) {
+            coef[(size_t)n * C + c0 + cl] = make_float4(scale, 0.0f, 0.0f, 0.0f);
+            gpart[(size_t)n * C + c0 + cl] = make_float2(0.0f, 0.0f);
+        }
+        return;
+    }
+    // (count, K, S1, S2) of the planes moved to the first plane's shift K0
+    const float K0 = ps[2 * ((size_t)n * C + c0)].y;
+    float M = 0.0f, S1 = 0.0f, S2 = 0.0f;
+    for (int cl = 0; cl < cpg; ++cl) {
+        const float4 p = ps[2 * ((size_t)n * C + c0 + cl)];
+        const float d = p.y - K0;
+        S2 += p.w + d * fmaf(p.x, d, 2.0f * p.z);
+        S1 += fmaf(p.x, d, p.z);
+        M += p.x;
+    }
+    const float mu_s = S1 / M;  // mu - K0
+    const float r = 1.0f / sqrtf(fmaxf(fmaf(-S1, mu_s, S2), 0.0f) / M + eps);
+    const float mu = K0 + mu_s;
+    // T1 = sum dxh, T2 = sum dxh (y - mu); a plane's sum dout (y - mu) is
+    // sum dout (y - K_c) + (K_c - mu) sum dout
+    float T1 = 0.0f, T2 = 0.0f;
+    for (int cl = 0; cl < cpg; ++cl) {
+        const size_t pl = (size_t)n * C + c0 + cl;
+        const float4 p0 = ps[2 * pl], p1 = ps[2 * pl + 1];
+        const float ga = gamma ? gamma[c0 + cl] : 1.0f;
+        const float gy = fmaf(p0.y - mu, p1.x, p1.y);
+        T1 = fmaf(scale * ga, p1.x, T1);
+        T2 = fmaf(scale * ga, gy, T2);
+        gpart[pl] = make_float2(scale * r * gy, scale * p1.x);  // this plane's dgamma, dbeta terms
+    }
+    const float m1 = T1 / M, m2 = r * T2 / M;  // mean(dxh), mean(dxh xh)
+    for (int cl = 0; cl < cpg; ++cl) {
+        const float ga = gamma ? gamma[c0 + cl] : 1.0f;
+        // dy = r dxh - r m1 - r^2 m2 (y - mu)
+        coef[(size_t)n * C + c0 + cl] = make_float4(r * scale * ga, -r * m1, -r * r * m2, mu);
+    }
+}
+
+// Step 4: dA in place of A over `slices` blocks per plane; each block's sum of dA.
+__global__ void __launch_bounds__(kBwdThreads) k_bwd_dA(float *A, const float *dout, const float4 *coef,
+                                                        long long S, int act, int slices, float *dbpart) {
+    const long long plane = blockIdx.x / slices;
+    const int slice = (int)(blockIdx.x - plane * slices);
+    const float4 cf = coef[plane];
+    const long long i0 = S * slice / slices, i1 = S * (slice + 1) / slices;
+    float *ap = A + plane * S;
+    const float *gp = dout + plane * S;
+    float v[1] = {0.0f};
+    for (long long i = i0 + threadIdx.x; i < i1; i += kBwdThreads) {
+        const float a = ap[i];
+        const float y = act == ACT_NONE ? a : apply_act(act, a);
+        const float dy = fmaf(cf.x, gp[i], fmaf(cf.z, y - cf.w, cf.y));
+        const float da = act == ACT_NONE ? dy : dy * act_grad(act, a);
+        ap[i] = da;
+        v[0] += da;
+    }
+    block_sum<1>(v);
+    if (threadIdx.x == 0) dbpart[plane * slices + slice] = v[0];
+}
+
+// Step 6: R[g][m][nn] over positions pos = (n, i, j) of U's planes:
+//   R = sum_pos U[n][g CUg + m][i][j] * V[n][g CVg + c][i + p][j + q],  nn = (c, p, q)
+// (Conv2d: U = dA, V = x, R = dw[co][ci][p][q]; ConvTranspose2d: U = x, V = dA,
+// R = dw[ci][co][p][q]).  A block takes a 64 x 64 tile of (m, nn) and one
+// split of the positions; 16 positions per step staged in shared memory; a
+// thread owns 4 x 4 outputs.  Its split's sums go to part[split][g][m][nn].
+constexpr int kWBM = 64, kWBN = 64, kWBK = 16;
+__global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, const float *V, int N, int CU, int CV,
+                                                            int PH, int PW, int k, int groups, long long kchunk,
+                                                            float *part) {
+    __shared__ __align__(16) float Us[kWBK][kWBM + 4];
+    __shared__ __align__(16) float Vs[kWBK][kWBN + 4];
+    const int tid = threadIdx.x;
+    const int CUg = CU / groups, CVg = CV / groups, kk2 = k * k, NN = CVg * kk2;
+    const int mtiles = (CUg + kWBM - 1) / kWBM, ntiles = (NN + kWBN - 1) / kWBN;
+    int bx = blockIdx.x;
+    const int mt = bx % mtiles;
+    bx /= mtiles;
+    const int nt = bx % ntiles;
+    const int g = bx / ntiles;
+    const long long P = (long long)PH * PW, Ktot = (long long)N * P;
+    const long long kbeg = (long long)blockIdx.y * kchunk, kend = Ktot < kbeg + kchunk ? Ktot : kbeg + kchunk;
+    const int VH = PH + k - 1, VW = PW + k - 1;
+    // this thread's loads: position lane kk, tile rows tid/16 + 16 t
+    const int kk = tid & (kWBK - 1);
+    long long ub[4], vb[4];
+    bool uok[4], vok[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int m = mt * kWBM + (tid >> 4) + 16 * t;
+        uok[t] = m < CUg;
+        ub[t] = (long long)(g * CUg + (uok[t] ? m : 0)) * P;
+        const int nn = nt * kWBN + (tid >> 4) + 16 * t;
+        vok[t] = nn < NN;
+        const int c = vok[t] ? nn / kk2 : 0, pq = vok[t] ? nn - c * kk2 : 0;
+        const int p = pq / k, q = pq - p * k;
+        vb[t] = ((long long)(g * CVg + c) * VH + p) * VW + q;
+    }
+    // the thread's position k0 + kk as (n, i, j), advanced by kWBK each step
+    long long pos = kbeg + kk;
+    int n = (int)(pos / P);
+    long long rr = pos - (long long)n * P;
+    int i = (int)(rr / PW), j = (int)(rr - (long long)i * PW);
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[4][4] = {};
+    for (long long k0 = kbeg; k0 < kend; k0 += kWBK) {
+        const bool pok = pos < kend;
+        const long long uo = (long long)n * CU * P + (long long)i * PW + j;
+        const long long vo = (long long)n * CV * VH * VW + (long long)i * VW + j;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            Us[kk][(tid >> 4) + 16 * t] = pok && uok[t] ? __ldg(U + ub[t] + uo) : 0.0f;
+            Vs[kk][(tid >> 4) + 16 * t] = pok && vok[t] ? __ldg(V + vb[t] + vo) : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int s = 0; s < kWBK; ++s) {
+            const float4 a = *reinterpret_cast<const float4 *>(&Us[s][ty * 4]);
+            const float4 b = *reinterpret_cast<const float4 *>(&Vs[s][tx * 4]);
+            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], bv[y], acc[x][y]);
+        }
+        __syncthreads();
+        pos += kWBK;
+        j += kWBK;
+        while (j >= PW) {
+            j -= PW;
+            if (++i == PH) {
+                i = 0;
+                ++n;
+            }
+        }
+    }
+    float *pp = part + ((size_t)blockIdx.y * groups + g) * (size_t)CUg * NN;
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int m = mt * kWBM + ty * 4 + x;
+        if (m >= CUg) continue;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int nn = nt * kWBN + tx * 4 + y;
+            if (nn < NN) pp[(size_t)m * NN + nn] = acc[x][y];
+        }
+    }
+}
+
+// dw[e] = sum over the splits of part[split][e], in split order.
+__global__ void k_bwd_weight_sum(const float *part, int splits, long long total, float *dw) {
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= total) return;
+    float s = 0.0f;
+    for (int q = 0; q < splits; ++q) s += part[(size_t)q * total + e];
+    dw[e] = s;
+}
+
+// Step 7: per channel, sums over n (and the db slices) in order.
+__global__ void k_bwd_channel_sums(const float2 *gpart, const float *dbpart, int N, int C, int slices,
+                                   float *dgamma, float *dbeta, float *db) {
+    const int c = blockIdx.x * blockDim.x + threadIdx.x;
+    if (c >= C) return;
+    float sg = 0.0f, sb = 0.0f, sd = 0.0f;
+    for (int n = 0; n < N; ++n) {
+        const size_t pl = (size_t)n * C + c;
+        sg += gpart[pl].x;
+        sb += gpart[pl].y;
+        for (int s = 0; s < slices; ++s) sd += dbpart[pl * slices + s];
+    }
+    if (dgamma) dgamma[c] = sg;
+    if (dbeta) dbeta[c] = sb;
+    if (db) db[c] = sd;
+}
+
+}  // namespace
+}  // namespace cn
+
+using namespace cn;
+
+struct conv_norm_bwd_plan_s {
+    conv_norm_desc d;
+    int device = -1;
+    conv_norm_plan conv_fwd = nullptr;  // A = conv(x) + b
+    conv_norm_plan conv_adj = nullptr;  // dx = the adjoint conv of dA
+    int Ho = 0, Wo = 0;
+    long long S = 0, planes = 0;
+    int slices = 1;
+    int wsplits = 1;
+    long long wchunk = 0, wtotal = 0;
+    int wgrid = 0;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    float *A = nullptr;      // [N][C_out][S]: A, then dA
+    float4 *ps = nullptr;    // [planes][2]
+    float4 *coef = nullptr;  // [planes]
+    float2 *gpart = nullptr; // [planes]
+    float *dbpart = nullptr; // [planes][slices]
+    float *wpart = nullptr;  // [wsplits][w numel]
+};
+
+namespace {
+
+size_t al256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+}  // namespace
+
+extern "C" {
+
+int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) {
+    if (!d || !out) return CN_ERR_INVALID_ARG;
+    *out = nullptr;
+    int st = conv_norm_desc_validate(d);
+    if (st != CN_OK) return st;
+    if ((d->conv != CN_CONV2D && d->conv != CN_CONVT2D) || d->red != CN_RED_NONE ||
+        d->act == CN_ACT_SOFTMAX_C || d->N < 1)
+        return CN_ERR_UNSUPPORTED;
+    conv_norm_bwd_plan_s *p = new (std::nothrow) conv_norm_bwd_plan_s();
+    if (!p) return CN_ERR_ALLOC;
+    p->d = *d;
+    auto fail = [&](int s) {
+        conv_norm_bwd_plan_destroy(p);
+        return s;
+    };
+    if (cudaGetDevice(&p->device) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CN_ERR_CUDA);
+    }
+    const bool T = d->conv == CN_CONVT2D;
+    p->Ho = T ? d->H + d->k - 1 : d->H - d->k + 1;
+    p->Wo = T ? d->W + d->k - 1 : d->W - d->k + 1;
+    p->S = (long long)p->Ho * p->Wo;
+    p->planes = (long long)d->N * d->C_out;
+    // the conv alone, and its adjoint (C_in and C_out swapped, dA's extent in)
+    conv_norm_desc f = *d;
+    f.act = CN_ACT_NONE;
+    f.norm = CN_NORM_NONE;
+    f.affine = 0;
+    f.post_scale = 1.0f;
+    f.red = CN_RED_NONE;
+    if ((st = conv_norm_plan_create(&f, &p->conv_fwd)) != CN_OK) return fail(st);
+    conv_norm_desc j = f;
+    j.conv = T ? CN_CONV2D : CN_CONVT2D;
+    j.C_in = d->C_out;
+    j.C_out = d->C_in;
+    j.H = p->Ho;
+    j.W = p->Wo;
+    j.has_bias = 0;
+    if ((st = conv_norm_plan_create(&j, &p->conv_adj)) != CN_OK) return fail(st);
+    // db slices: about 16 K values per block
+    p->slices = (int)std::max(1LL, std::min(64LL, p->S / 16384));
+    // dw: enough position splits for ~4 blocks per SM
+    int sms = 152;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+    const int G = d->groups;
+    const int CU = T ? d->C_in : d->C_out, CV = T ? d->C_out : d->C_in;
+    const int CUg = CU / G, NN = (CV / G) * d->k * d->k;
+    const int tiles = ((CUg + kWBM - 1) / kWBM) * ((NN + kWBN - 1) / kWBN) * G;
+    const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
+    p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
+    p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + kWBK - 1) / kWBK * kWBK;
+    p->wsplits = (int)((Ktot + p->wchunk - 1) / p->wchunk);
+    p->wgrid = tiles;
+    p->wtotal = (long long)CU * NN;
+    if (p->wsplits > 65535) return fail(CN_ERR_UNSUPPORTED);
+    const size_t bA = al256((size_t)p->planes * p->S * 4), bps = al256((size_t)p->planes * 32),
+                 bcoef = al256((size_t)p->planes * 16), bg = al256((size_t)p->planes * 8),
+                 bdb = al256((size_t)p->planes * p->slices * 4), bw = al256((size_t)p->wsplits * p->wtotal * 4);
+    p->ws_bytes = bA + bps + bcoef + bg + bdb + bw;
+    if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(CN_ERR_ALLOC);
+    }
+    char *b = static_cast<char *>(p->ws);
+    p->A = reinterpret_cast<float *>(b);
+    p->ps = reinterpret_cast<float4 *>(b + bA);
+    p->coef = reinterpret_cast<float4 *>(b + bA + bps);
+    p->gpart = reinterpret_cast<float2 *>(b + bA + bps + bcoef);
+    p->dbpart = reinterpret_cast<float *>(b + bA + bps + bcoef + bg);
+    p->wpart = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb);
+    *out = p;
+    return CN_OK;
+}
+
+void conv_norm_bwd_plan_destroy(conv_norm_bwd_plan p) {
+    if (!p) return;
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
+    conv_norm_plan_destroy(p->conv_fwd);
+    conv_norm_plan_destroy(p->conv_adj);
+    cudaFree(p->ws);
+    if (cur >= 0 && p->device >= 0 && cur != p->device) cudaSetDevice(cur);
+    cudaGetLastError();
+    delete p;
+}
+
+size_t conv_norm_bwd_workspace_bytes(conv_norm_bwd_plan p) {
+    if (!p) return 0;
+    return p->ws_bytes + conv_norm_workspace_bytes(p->conv_fwd) + conv_norm_workspace_bytes(p->conv_adj);
+}
+
+int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, const float *b,
+                       const float *gamma, const float *beta, const float *dout, float *dx, float *dw,
+                       float *db, float *dgamma, float *dbeta, void *stream) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    const conv_norm_desc &d = p->d;
+    const bool aff = d.affine && d.norm != CN_NORM_NONE;
+    (void)beta;  // the gradients do not depend on beta
+    if (!x || !w || !dout || !dx || !dw) return CN_ERR_INVALID_ARG;
+    if ((b != nullptr) != (d.has_bias == 1) || (db != nullptr) != (d.has_bias == 1)) return CN_ERR_INVALID_ARG;
+    if (aff && (!gamma || !dgamma || !dbeta)) return CN_ERR_INVALID_ARG;
+    if (!aff && (dgamma || dbeta)) return CN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(dout) % 16 || reinterpret_cast<uintptr_t>(dx) % 16) return CN_ERR_INVALID_ARG;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    if (cur != p->device && cudaSetDevice(p->device) != cudaSuccess) {
+        cudaGetLastError();
+        return CN_ERR_CUDA;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = conv_norm_forward(p->conv_fwd, x, w, b, nullptr, nullptr, p->A, stream);
+    if (st == CN_OK) {
+        const int act = d.act == CN_ACT_HARDSWISH ? ACT_HARDSWISH : (d.act == CN_ACT_GELU_ERF ? ACT_GELU : ACT_NONE);
+        const int G = d.norm == CN_NORM_GROUP ? d.num_groups : (d.norm == CN_NORM_INSTANCE ? d.C_out : 1);
+        if (d.norm != CN_NORM_NONE)
+            k_bwd_plane_sums<<<(unsigned)p->planes, kBwdThreads, 0, s>>>(p->A, dout, p->S, act, p->ps);
+        const int ng = d.N * G;
+        k_bwd_group<<<(ng + 127) / 128, 128, 0, s>>>(p->ps, d.N, d.C_out, G, d.norm, d.eps, d.post_scale,
+                                                     aff ? gamma : nullptr, p->coef, p->gpart);
+        k_bwd_dA<<<(unsigned)(p->planes * p->slices), kBwdThreads, 0, s>>>(p->A, dout, p->coef, p->S, act,
+                                                                           p->slices, p->dbpart);
+        if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
+    }
+    if (st == CN_OK) st = conv_norm_forward(p->conv_adj, p->A, w, nullptr, nullptr, nullptr, dx, stream);
+    if (st == CN_OK) {
+        const bool T = d.conv == CN_CONVT2D;
+        const float *U = T ? x : p->A, *V = T ? p->A : x;
+        const int CU = T ? d.C_in : d.C_out, CV = T ? d.C_out : d.C_in;
+        const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
+        k_bwd_weight<<<dim3((unsigned)p->wgrid, (unsigned)p->wsplits), kBwdThreads, 0, s>>>(
+            U, V, d.N, CU, CV, PH, PW, d.k, d.groups, p->wchunk, p->wpart);
+        k_bwd_weight_sum<<<(unsigned)((p->wtotal + 255) / 256), 256, 0, s>>>(p->wpart, p->wsplits, p->wtotal, dw);
+        k_bwd_channel_sums<<<(d.C_out + 127) / 128, 128, 0, s>>>(p->gpart, p->dbpart, d.N, d.C_out, p->slices,
+                                                                 aff ? dgamma : nullptr, aff ? dbeta : nullptr, db);
+        if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
+    }
+    if (st != CN_OK) cudaGetLastError();
+    if (cur != p->device) cudaSetDevice(cur);
+    return st;
+}
+
+int conv_norm_bwd_check_device(conv_norm_bwd_plan p, void *stream) {
+    if (!p) return CN_ERR_INVALID_ARG;
+    const int a = conv_norm_plan_check_device(p->conv_fwd, stream);
+    const int c = conv_norm_plan_check_device(p->conv_adj, stream);
+    return a != CN_OK ? a : c;
+}
+
+}  // extern "C"

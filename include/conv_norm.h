@@ -310,6 +310,61 @@ int conv_norm_forward_noalloc(const conv_norm_desc *desc, const float *x, const 
                               const float *b, const float *gamma, const float *beta,
                               float *out, void *cuda_stream);
 
+/* ---- backward pass ----------------------------------------------------------- */
+
+typedef struct conv_norm_bwd_plan_s *conv_norm_bwd_plan;
+
+/* Cites: no page passage: the pages implement the forward only (l2_p27 notes
+ * that its problem asks for no gradient).  The backward is the derivative of
+ * the forward each page states (the chain rule through its layers).
+ * A backward plan for the full-output 2-D block: desc with conv = CN_CONV2D
+ * or CN_CONVT2D (any groups the forward takes), act none / HardSwish / GELU,
+ * any norm, any post scale, red = CN_RED_NONE, N >= 1, and a forward that the
+ * library supports for desc (the adjoint conv, C_in and C_out swapped, must
+ * also be one: (C_in / groups) % 4 == 0).  Allocates, on the CURRENT device,
+ * a workspace of N C_out H_out W_out floats (the conv output, then its
+ * gradient) plus small per-plane and per-split buffers, and two forward plans
+ * (the conv alone and its adjoint).
+ * Errors: CN_ERR_INVALID_ARG, CN_ERR_UNSUPPORTED, CN_ERR_CUDA, CN_ERR_ALLOC. */
+int conv_norm_bwd_plan_create(const conv_norm_desc *desc, conv_norm_bwd_plan *out_plan);
+
+/* Cites: as conv_norm_bwd_plan_create.
+ * Gradients of a loss L through the block, given dout = dL/d(out) (the
+ * forward output's shape, NCHW fp32, 16-byte aligned) and the forward's
+ * inputs x, w, b, gamma, beta (layouts as conv_norm_forward):
+ *   dx (x's shape, 16-byte aligned), dw (w's shape), db (C_out; required
+ *   iff has_bias), dgamma and dbeta (C_out; required iff the norm is affine,
+ *   NULL otherwise).  All device pointers, written in full.
+ * With A the conv output, y = act(A), mu and r = 1/sqrt(var + eps) per
+ * (sample, norm group), xh = (y - mu) r and s the post scale:
+ *   dy = r (s gamma dout - mean(s gamma dout) - xh mean(s gamma dout xh)),
+ *   dA = dy act'(A) (HardSwish' = 0 / a/3 + 1/2 / 1 below -3 / on [-3, 3] /
+ *   above 3), dgamma = s sum dout xh, dbeta = s sum dout, db = sum dA,
+ *   dx = the adjoint conv of dA, dw = the correlation of dA with x.
+ * Asynchronous on cuda_stream; allocates nothing; deterministic (fixed-order
+ * sums).  Calls on one plan must not overlap.  Errors: CN_ERR_INVALID_ARG
+ * (NULL plan or tensor, a gradient pointer given or missing against desc,
+ * misalignment), CN_ERR_CUDA. */
+int conv_norm_backward(conv_norm_bwd_plan plan, const float *x, const float *w, const float *b,
+                       const float *gamma, const float *beta, const float *dout, float *dx,
+                       float *dw, float *db, float *dgamma, float *dbeta, void *cuda_stream);
+
+/* Cites: as conv_norm_bwd_plan_create.
+ * Bytes of device memory the backward plan holds (its workspace and its two
+ * forward plans'); 0 for NULL. */
+size_t conv_norm_bwd_workspace_bytes(conv_norm_bwd_plan plan);
+
+/* Cites: as conv_norm_plan_check_device.
+ * Synchronizes cuda_stream and reads and clears the error flags of the
+ * backward plan's forward plans (CN_OK, CN_ERR_TIMEOUT, CN_ERR_DEVICE_CHECK,
+ * CN_ERR_CUDA); CN_ERR_INVALID_ARG for NULL. */
+int conv_norm_bwd_check_device(conv_norm_bwd_plan plan, void *cuda_stream);
+
+/* Cites: as conv_norm_plan_destroy.
+ * Frees the backward plan and its forward plans; NULL is ignored; no call on
+ * the plan may still be running. */
+void conv_norm_bwd_plan_destroy(conv_norm_bwd_plan plan);
+
 #ifdef __cplusplus
 }
 #endif

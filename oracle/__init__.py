@@ -302,11 +302,13 @@ def group_norm_grad(y, dout, G, eps=1e-5, gamma=None):
     return dy, dgamma, dbeta
 
 
-def backward(s, inputs, dout):
+def backward(s, inputs, dout, intermediates=False):
     """Gradients of the whole fused block for workload dict ``s`` (spatial
     reductions none or the spatial mean; activations none, HardSwish or
     GELU): dict with dx, dw, db (None without bias), dgamma and dbeta (None
-    without an affine norm).  The forward's intermediates are recomputed."""
+    without an affine norm).  The forward's intermediates are recomputed;
+    with ``intermediates`` the dict also holds dA, the gradient with respect
+    to the conv output."""
     act, norm, red = s["act"], s["norm"], s["red"]
     assert red in ("none", "mean_spatial") and act in ("none", "hardswish", "gelu_erf")
     x, w, G = inputs["x"], inputs["w"], s["groups"]
@@ -338,4 +340,7 @@ def backward(s, inputs, dout):
     else:
         dx = conv_transpose2d_grad_input(g, w, G)
         dw, db = conv_transpose2d_grad_weight(x, g, w.shape, G)
-    return {"dx": dx, "dw": dw, "db": db if s["has_bias"] else None, "dgamma": dgamma, "dbeta": dbeta}
+    res = {"dx": dx, "dw": dw, "db": db if s["has_bias"] else None, "dgamma": dgamma, "dbeta": dbeta}
+    if intermediates:
+        res["dA"] = g
+    return res
