@@ -493,6 +493,74 @@ def measure(B, torch, spec, pk, stream, flush, steps, warmup, world=1, e2e_steps
     return res
 
 
+BACKWARD_METRIC = "fused conv+norm backward ms & GFLOP/s (dx and dw work), % of roofline (FP32 peak vs HBM)"
+BACKWARD_WORKLOADS = ("conv2d_in_half_n32", "convt2d_g8_gelu_gn8_n32")
+
+
+def backward_flops(s):
+    """The gradients' own work: dx and dw are each one conv's multiply-adds
+    (2 x the forward conv's FLOPs together); the conv output the backward
+    recomputes is not counted."""
+    return 2.0 * algorithmic_flops(s)
+
+
+def backward_bytes(s):
+    """Compulsory bytes of one backward: read x, w, dout (and b, gamma,
+    beta), write dx, dw (and db, dgamma, dbeta)."""
+    shp = wl.input_shapes(s)
+    n = sum(math.prod(v) for v in shp.values() if v)
+    return 4.0 * (2 * n + math.prod(out_shape(s)))
+
+
+def measure_backward(B, torch, spec, pk, stream, flush, steps, warmup):
+    """Backward step time (mean of `steps`, L2 flushed before each, CUDA
+    events on the stream) through conv_norm_backward, for a full-output 2-D
+    workload; dout is seeded N(0, 1)."""
+    import numpy as np
+    inp = wl.make_inputs(spec)
+    dev = {k: (torch.from_numpy(v).cuda() if v is not None else None) for k, v in inp.items()}
+    dout = torch.from_numpy(np.random.default_rng(spec["seed"] + 100).standard_normal(
+        out_shape(spec)).astype(np.float32)).cuda()
+    aff = bool(spec["affine"]) and spec["norm"] != "none"
+    g = {"dx": torch.empty_like(dev["x"]), "dw": torch.empty_like(dev["w"]),
+         "db": torch.empty_like(dev["b"]) if spec["has_bias"] else None,
+         "dgamma": torch.empty(spec["C_out"], device="cuda") if aff else None,
+         "dbeta": torch.empty(spec["C_out"], device="cuda") if aff else None}
+    plan = B.BwdPlan(spec)
+
+    def bwd():
+        plan.backward(dev["x"], dev["w"], dev["b"], dev["gamma"] if aff else None,
+                      dev["beta"] if aff else None, dout, g["dx"], g["dw"], g["db"], g["dgamma"],
+                      g["dbeta"], stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            bwd()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(min(2e9, 2e6 * steps + 2e7)))
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            bwd()
+            e1.record(stream)
+    stream.synchronize()
+    assert plan.check_device(stream) == B.CN_OK
+    ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in ev)
+    ws = plan.workspace_bytes()
+    plan.close()
+    flops, nbytes = backward_flops(spec), backward_bytes(spec)
+    rl_ms = max(flops / (pk["fp32_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9)) * 1e3
+    return {"workload": spec["name"], "ms": ms, "steps": steps, "gflops": flops / ms / 1e6,
+            "flops_per_step": flops, "roofline_ms": rl_ms, "frac": rl_ms / ms,
+            "bound": "alu" if flops / (pk["fp32_tflops"] * 1e12) >= nbytes / (pk["hbm_gbs"] * 1e9) else "hbm",
+            "workspace_bytes": ws,
+            "api": "conv_norm_backward (C ABI): conv recompute, plane sums, group coefficients, dA, "
+                   "adjoint conv (dx), split-K correlation (dw), channel sums"}
+
+
 def run_cuda(args, spec):
     import torch
     world, rank, local = dist_setup(args.gpus)
@@ -507,6 +575,15 @@ def run_cuda(args, spec):
     stream = torch.cuda.Stream()
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
 
+    if args.backward:
+        r = measure_backward(B, torch, spec, pk, stream, flush, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"metric": BACKWARD_METRIC, "value": r["gflops"], "unit": "GFLOP/s",
+                              "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                              "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+                              "vs_baseline": None, "dtype": "f32", "data": DATA, "config": config_of(spec),
+                              "backward": r}), flush=True)
+        return
     head = measure(B, torch, spec, pk, stream, flush, args.steps, args.warmup, world,
                    e2e_steps=max(3, min(args.steps, 30)),
                    cpu_target_s=None if (rank != 0 or args.no_cpu_baseline) else 12.0,
@@ -537,6 +614,8 @@ def run_cuda(args, spec):
             r.pop("config")
             extras.append(r)
         line["workloads"] = extras
+        line["backward"] = [measure_backward(B, torch, wl.WORKLOAD_BY_NAME[n], pk, stream, flush, 20, 3)
+                            for n in BACKWARD_WORKLOADS]
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -553,6 +632,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass of the workload instead (full-output 2-D workloads)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiling)")
     args = ap.parse_args()

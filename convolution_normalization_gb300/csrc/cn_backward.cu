@@ -178,18 +178,25 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_dA(float *A, const float *d
 // Step 6: R[g][m][nn] over positions pos = (n, i, j) of U's planes:
 //   R = sum_pos U[n][g CUg + m][i][j] * V[n][g CVg + c][i + p][j + q],  nn = (c, p, q)
 // (Conv2d: U = dA, V = x, R = dw[co][ci][p][q]; ConvTranspose2d: U = x, V = dA,
-// R = dw[ci][co][p][q]).  A block takes a 64 x 64 tile of (m, nn) and one
+// R = dw[ci][co][p][q]).  A block takes a BM x BN tile of (m, nn) and one
 // split of the positions; 16 positions per step staged in shared memory; a
-// thread owns 4 x 4 outputs.  Its split's sums go to part[split][g][m][nn].
-constexpr int kWBM = 64, kWBN = 64, kWBK = 16;
+// thread owns TM x TN outputs (64 x 64 tiles of 4 x 4 for wide problems,
+// 8 x 128 tiles of 1 x 4 for groups of at most 8 channels).  Its split's
+// sums go to part[split][g][m][nn].
+constexpr int kWBK = 16;
+template <int BM, int BN, int TM, int TN>
 __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, const float *V, int N, int CU, int CV,
                                                             int PH, int PW, int k, int groups, long long kchunk,
                                                             float *part) {
-    __shared__ __align__(16) float Us[kWBK][kWBM + 4];
-    __shared__ __align__(16) float Vs[kWBK][kWBN + 4];
+    static_assert((BM / TM) * (BN / TN) == kBwdThreads, "one output tile per thread");
+    constexpr int RU = (BM * kWBK + kBwdThreads - 1) / kBwdThreads;  // U rows a thread loads
+    constexpr int RV = BN * kWBK / kBwdThreads;                      // V rows a thread loads
+    constexpr int RS = kBwdThreads / kWBK;                           // rows a load step covers
+    __shared__ __align__(16) float Us[kWBK][BM + 4];
+    __shared__ __align__(16) float Vs[kWBK][BN + 4];
     const int tid = threadIdx.x;
     const int CUg = CU / groups, CVg = CV / groups, kk2 = k * k, NN = CVg * kk2;
-    const int mtiles = (CUg + kWBM - 1) / kWBM, ntiles = (NN + kWBN - 1) / kWBN;
+    const int mtiles = (CUg + BM - 1) / BM, ntiles = (NN + BN - 1) / BN;
     int bx = blockIdx.x;
     const int mt = bx % mtiles;
     bx /= mtiles;
@@ -198,16 +205,19 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
     const long long P = (long long)PH * PW, Ktot = (long long)N * P;
     const long long kbeg = (long long)blockIdx.y * kchunk, kend = Ktot < kbeg + kchunk ? Ktot : kbeg + kchunk;
     const int VH = PH + k - 1, VW = PW + k - 1;
-    // this thread's loads: position lane kk, tile rows tid/16 + 16 t
-    const int kk = tid & (kWBK - 1);
-    long long ub[4], vb[4];
-    bool uok[4], vok[4];
+    // this thread's loads: position lane kk, tile rows tid/16 + RS t
+    const int kk = tid & (kWBK - 1), r0 = tid / kWBK;
+    long long ub[RU], vb[RV];
+    bool uok[RU], vok[RV];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const int m = mt * kWBM + (tid >> 4) + 16 * t;
-        uok[t] = m < CUg;
+    for (int t = 0; t < RU; ++t) {
+        const int ml = r0 + RS * t, m = mt * BM + ml;
+        uok[t] = ml < BM && m < CUg;
         ub[t] = (long long)(g * CUg + (uok[t] ? m : 0)) * P;
-        const int nn = nt * kWBN + (tid >> 4) + 16 * t;
+    }
+#pragma unroll
+    for (int t = 0; t < RV; ++t) {
+        const int nn = nt * BN + r0 + RS * t;
         vok[t] = nn < NN;
         const int c = vok[t] ? nn / kk2 : 0, pq = vok[t] ? nn - c * kk2 : 0;
         const int p = pq / k, q = pq - p * k;
@@ -218,27 +228,35 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
     int n = (int)(pos / P);
     long long rr = pos - (long long)n * P;
     int i = (int)(rr / PW), j = (int)(rr - (long long)i * PW);
-    const int ty = tid >> 4, tx = tid & 15;
-    float acc[4][4] = {};
+    const int ty = tid / (BN / TN), tx = tid % (BN / TN);
+    float acc[TM][TN] = {};
     for (long long k0 = kbeg; k0 < kend; k0 += kWBK) {
         const bool pok = pos < kend;
         const long long uo = (long long)n * CU * P + (long long)i * PW + j;
         const long long vo = (long long)n * CV * VH * VW + (long long)i * VW + j;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            Us[kk][(tid >> 4) + 16 * t] = pok && uok[t] ? __ldg(U + ub[t] + uo) : 0.0f;
-            Vs[kk][(tid >> 4) + 16 * t] = pok && vok[t] ? __ldg(V + vb[t] + vo) : 0.0f;
-        }
+        for (int t = 0; t < RU; ++t)
+            if (r0 + RS * t < BM) Us[kk][r0 + RS * t] = pok && uok[t] ? __ldg(U + ub[t] + uo) : 0.0f;
+#pragma unroll
+        for (int t = 0; t < RV; ++t) Vs[kk][r0 + RS * t] = pok && vok[t] ? __ldg(V + vb[t] + vo) : 0.0f;
         __syncthreads();
 #pragma unroll
         for (int s = 0; s < kWBK; ++s) {
-            const float4 a = *reinterpret_cast<const float4 *>(&Us[s][ty * 4]);
-            const float4 b = *reinterpret_cast<const float4 *>(&Vs[s][tx * 4]);
-            const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            float av[TM], bv[TN];
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
+            for (int x = 0; x < TM; ++x) av[x] = Us[s][ty * TM + x];
 #pragma unroll
-                for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(av[x], bv[y], acc[x][y]);
+            for (int y = 0; y < TN; y += 4) {
+                const float4 b4 = *reinterpret_cast<const float4 *>(&Vs[s][tx * TN + y]);
+                bv[y] = b4.x;
+                bv[y + 1] = b4.y;
+                bv[y + 2] = b4.z;
+                bv[y + 3] = b4.w;
+            }
+#pragma unroll
+            for (int x = 0; x < TM; ++x)
+#pragma unroll
+                for (int y = 0; y < TN; ++y) acc[x][y] = fmaf(av[x], bv[y], acc[x][y]);
         }
         __syncthreads();
         pos += kWBK;
@@ -253,12 +271,12 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
     }
     float *pp = part + ((size_t)blockIdx.y * groups + g) * (size_t)CUg * NN;
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int m = mt * kWBM + ty * 4 + x;
+    for (int x = 0; x < TM; ++x) {
+        const int m = mt * BM + ty * TM + x;
         if (m >= CUg) continue;
 #pragma unroll
-        for (int y = 0; y < 4; ++y) {
-            const int nn = nt * kWBN + tx * 4 + y;
+        for (int y = 0; y < TN; ++y) {
+            const int nn = nt * BN + tx * TN + y;
             if (nn < NN) pp[(size_t)m * NN + nn] = acc[x][y];
         }
     }
@@ -306,6 +324,7 @@ struct conv_norm_bwd_plan_s {
     int wsplits = 1;
     long long wchunk = 0, wtotal = 0;
     int wgrid = 0;
+    bool wsmall = false;  // dw tiles of 8 x 128 (groups of at most 8 channels) instead of 64 x 64
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *A = nullptr;      // [N][C_out][S]: A, then dA
@@ -372,7 +391,9 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     const int G = d->groups;
     const int CU = T ? d->C_in : d->C_out, CV = T ? d->C_out : d->C_in;
     const int CUg = CU / G, NN = (CV / G) * d->k * d->k;
-    const int tiles = ((CUg + kWBM - 1) / kWBM) * ((NN + kWBN - 1) / kWBN) * G;
+    p->wsmall = CUg <= 8;
+    const int BM = p->wsmall ? 8 : 64, BN = p->wsmall ? 128 : 64;
+    const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
     const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
     p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
     p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + kWBK - 1) / kWBK * kWBK;
@@ -458,8 +479,13 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
         const float *U = T ? x : p->A, *V = T ? p->A : x;
         const int CU = T ? d.C_in : d.C_out, CV = T ? d.C_out : d.C_in;
         const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
-        k_bwd_weight<<<dim3((unsigned)p->wgrid, (unsigned)p->wsplits), kBwdThreads, 0, s>>>(
-            U, V, d.N, CU, CV, PH, PW, d.k, d.groups, p->wchunk, p->wpart);
+        const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits);
+        if (p->wsmall)
+            k_bwd_weight<8, 128, 1, 4><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k, d.groups,
+                                                                   p->wchunk, p->wpart);
+        else
+            k_bwd_weight<64, 64, 4, 4><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k, d.groups,
+                                                                   p->wchunk, p->wpart);
         k_bwd_weight_sum<<<(unsigned)((p->wtotal + 255) / 256), 256, 0, s>>>(p->wpart, p->wsplits, p->wtotal, dw);
         k_bwd_channel_sums<<<(d.C_out + 127) / 128, 128, 0, s>>>(p->gpart, p->dbpart, d.N, d.C_out, p->slices,
                                                                  aff ? dgamma : nullptr, aff ? dbeta : nullptr, db);
