@@ -179,21 +179,21 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_dA(float *A, const float *d
 //   R = sum_pos U[n][g CUg + m][i][j] * V[n][g CVg + c][i + p][j + q],  nn = (c, p, q)
 // (Conv2d: U = dA, V = x, R = dw[co][ci][p][q]; ConvTranspose2d: U = x, V = dA,
 // R = dw[ci][co][p][q]).  A block takes a BM x BN tile of (m, nn) and one
-// split of the positions; 16 positions per step staged in shared memory; a
+// split of the positions; BK positions per step staged in shared memory; a
 // thread owns TM x TN outputs (64 x 64 tiles of 4 x 4 for wide problems,
 // 8 x 128 tiles of 1 x 4 for groups of at most 8 channels).  Its split's
 // sums go to part[split][g][m][nn].
-constexpr int kWBK = 16;
-template <int BM, int BN, int TM, int TN>
+template <int BM, int BN, int TM, int TN, int BK>
 __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, const float *V, int N, int CU, int CV,
                                                             int PH, int PW, int k, int groups, long long kchunk,
                                                             float *part) {
     static_assert((BM / TM) * (BN / TN) == kBwdThreads, "one output tile per thread");
-    constexpr int RU = (BM * kWBK + kBwdThreads - 1) / kBwdThreads;  // U rows a thread loads
-    constexpr int RV = BN * kWBK / kBwdThreads;                      // V rows a thread loads
-    constexpr int RS = kBwdThreads / kWBK;                           // rows a load step covers
-    __shared__ __align__(16) float Us[kWBK][BM + 4];
-    __shared__ __align__(16) float Vs[kWBK][BN + 4];
+    constexpr int RU = (BM * BK + kBwdThreads - 1) / kBwdThreads;  // U rows a thread loads
+    constexpr int RV = BN * BK / kBwdThreads;                      // V rows a thread loads
+    constexpr int RS = kBwdThreads / BK;                           // rows a load step covers
+    static_assert(kBwdThreads % BK == 0 && (BN * BK) % kBwdThreads == 0, "load mapping");
+    __shared__ __align__(16) float Us[BK][BM + 4];
+    __shared__ __align__(16) float Vs[BK][BN + 4];
     const int tid = threadIdx.x;
     const int CUg = CU / groups, CVg = CV / groups, kk2 = k * k, NN = CVg * kk2;
     const int mtiles = (CUg + BM - 1) / BM, ntiles = (NN + BN - 1) / BN;
@@ -205,8 +205,8 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
     const long long P = (long long)PH * PW, Ktot = (long long)N * P;
     const long long kbeg = (long long)blockIdx.y * kchunk, kend = Ktot < kbeg + kchunk ? Ktot : kbeg + kchunk;
     const int VH = PH + k - 1, VW = PW + k - 1;
-    // this thread's loads: position lane kk, tile rows tid/16 + RS t
-    const int kk = tid & (kWBK - 1), r0 = tid / kWBK;
+    // this thread's loads: position lane kk, tile rows tid / BK + RS t
+    const int kk = tid % BK, r0 = tid / BK;
     long long ub[RU], vb[RV];
     bool uok[RU], vok[RV];
 #pragma unroll
@@ -223,14 +223,14 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
         const int p = pq / k, q = pq - p * k;
         vb[t] = ((long long)(g * CVg + c) * VH + p) * VW + q;
     }
-    // the thread's position k0 + kk as (n, i, j), advanced by kWBK each step
+    // the thread's position k0 + kk as (n, i, j), advanced by BK each step
     long long pos = kbeg + kk;
     int n = (int)(pos / P);
     long long rr = pos - (long long)n * P;
     int i = (int)(rr / PW), j = (int)(rr - (long long)i * PW);
     const int ty = tid / (BN / TN), tx = tid % (BN / TN);
     float acc[TM][TN] = {};
-    for (long long k0 = kbeg; k0 < kend; k0 += kWBK) {
+    for (long long k0 = kbeg; k0 < kend; k0 += BK) {
         const bool pok = pos < kend;
         const long long uo = (long long)n * CU * P + (long long)i * PW + j;
         const long long vo = (long long)n * CV * VH * VW + (long long)i * VW + j;
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
         for (int t = 0; t < RV; ++t) Vs[kk][r0 + RS * t] = pok && vok[t] ? __ldg(V + vb[t] + vo) : 0.0f;
         __syncthreads();
 #pragma unroll
-        for (int s = 0; s < kWBK; ++s) {
+        for (int s = 0; s < BK; ++s) {
             float av[TM], bv[TN];
 #pragma unroll
             for (int x = 0; x < TM; ++x) av[x] = Us[s][ty * TM + x];
@@ -259,8 +259,8 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
                 for (int y = 0; y < TN; ++y) acc[x][y] = fmaf(av[x], bv[y], acc[x][y]);
         }
         __syncthreads();
-        pos += kWBK;
-        j += kWBK;
+        pos += BK;
+        j += BK;
         while (j >= PW) {
             j -= PW;
             if (++i == PH) {
@@ -281,6 +281,9 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
         }
     }
 }
+
+// positions a step (measured on the l2_p19 and l2_p17 blocks: 16 and 32)
+constexpr int kWBKSmall = 16, kWBKWide = 32;
 
 // dw[e] = sum over the splits of part[split][e], in split order.
 __global__ void k_bwd_weight_sum(const float *part, int splits, long long total, float *dw) {
@@ -396,7 +399,7 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
     const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
     p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
-    p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + kWBK - 1) / kWBK * kWBK;
+    p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + 63) / 64 * 64;
     p->wsplits = (int)((Ktot + p->wchunk - 1) / p->wchunk);
     p->wgrid = tiles;
     p->wtotal = (long long)CU * NN;
@@ -481,11 +484,11 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
         const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
         const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits);
         if (p->wsmall)
-            k_bwd_weight<8, 128, 1, 4><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k, d.groups,
-                                                                   p->wchunk, p->wpart);
+            k_bwd_weight<8, 128, 1, 4, kWBKSmall><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
+                                                                              d.groups, p->wchunk, p->wpart);
         else
-            k_bwd_weight<64, 64, 4, 4><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k, d.groups,
-                                                                   p->wchunk, p->wpart);
+            k_bwd_weight<64, 64, 4, 4, kWBKWide><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
+                                                                             d.groups, p->wchunk, p->wpart);
         k_bwd_weight_sum<<<(unsigned)((p->wtotal + 255) / 256), 256, 0, s>>>(p->wpart, p->wsplits, p->wtotal, dw);
         k_bwd_channel_sums<<<(d.C_out + 127) / 128, 128, 0, s>>>(p->gpart, p->dbpart, d.N, d.C_out, p->slices,
                                                                  aff ? dgamma : nullptr, aff ? dbeta : nullptr, db);
