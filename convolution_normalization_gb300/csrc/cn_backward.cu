@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_dA(float *A, const float *d
 // (Conv2d: U = dA, V = x, R = dw[co][ci][p][q]; ConvTranspose2d: U = x, V = dA,
 // R = dw[ci][co][p][q]).  A block takes a BM x BN tile of (m, nn) and one
 // split of the positions; BK positions per step staged in shared memory; a
-// thread owns TM x TN outputs (64 x 64 tiles of 4 x 4 for wide problems,
-// 8 x 128 tiles of 1 x 4 for groups of at most 8 channels).  Its split's
+// thread owns TM x TN outputs (128 x 128 tiles of 8 x 8 for at least 96
+// channels a group, 64 x 64 tiles of 4 x 4 below that, 8 x 128 tiles of
+// 1 x 4 for groups of at most 8 channels).  Its split's
 // sums go to part[split][g][m][nn].
 template <int BM, int BN, int TM, int TN, int BK>
 __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, const float *V, int N, int CU, int CV,
@@ -243,8 +244,19 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
 #pragma unroll
         for (int s = 0; s < BK; ++s) {
             float av[TM], bv[TN];
+            if (TM % 4 == 0) {
 #pragma unroll
-            for (int x = 0; x < TM; ++x) av[x] = Us[s][ty * TM + x];
+                for (int x = 0; x < TM; x += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&Us[s][ty * TM + x]);
+                    av[x] = a4.x;
+                    av[x + 1] = a4.y;
+                    av[x + 2] = a4.z;
+                    av[x + 3] = a4.w;
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < TM; ++x) av[x] = Us[s][ty * TM + x];
+            }
 #pragma unroll
             for (int y = 0; y < TN; y += 4) {
                 const float4 b4 = *reinterpret_cast<const float4 *>(&Vs[s][tx * TN + y]);
@@ -327,7 +339,7 @@ struct conv_norm_bwd_plan_s {
     int wsplits = 1;
     long long wchunk = 0, wtotal = 0;
     int wgrid = 0;
-    bool wsmall = false;  // dw tiles of 8 x 128 (groups of at most 8 channels) instead of 64 x 64
+    int wtile = 1;  // dw tiles: 0 = 8 x 128 (groups of at most 8 channels), 1 = 64 x 64, 2 = 128 x 128
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *A = nullptr;      // [N][C_out][S]: A, then dA
@@ -394,8 +406,8 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     const int G = d->groups;
     const int CU = T ? d->C_in : d->C_out, CV = T ? d->C_out : d->C_in;
     const int CUg = CU / G, NN = (CV / G) * d->k * d->k;
-    p->wsmall = CUg <= 8;
-    const int BM = p->wsmall ? 8 : 64, BN = p->wsmall ? 128 : 64;
+    p->wtile = CUg <= 8 ? 0 : (CUg < 96 ? 1 : 2);
+    const int BM = p->wtile == 0 ? 8 : (p->wtile == 1 ? 64 : 128), BN = p->wtile == 1 ? 64 : 128;
     const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
     const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
     p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
@@ -483,12 +495,15 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
         const int CU = T ? d.C_in : d.C_out, CV = T ? d.C_out : d.C_in;
         const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
         const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits);
-        if (p->wsmall)
+        if (p->wtile == 0)
             k_bwd_weight<8, 128, 1, 4, kWBKSmall><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
                                                                               d.groups, p->wchunk, p->wpart);
-        else
+        else if (p->wtile == 1)
             k_bwd_weight<64, 64, 4, 4, kWBKWide><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
                                                                              d.groups, p->wchunk, p->wpart);
+        else
+            k_bwd_weight<128, 128, 8, 8, kWBKSmall><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
+                                                                                d.groups, p->wchunk, p->wpart);
         k_bwd_weight_sum<<<(unsigned)((p->wtotal + 255) / 256), 256, 0, s>>>(p->wpart, p->wsplits, p->wtotal, dw);
         k_bwd_channel_sums<<<(d.C_out + 127) / 128, 128, 0, s>>>(p->gpart, p->dbpart, d.N, d.C_out, p->slices,
                                                                  aff ? dgamma : nullptr, aff ? dbeta : nullptr, db);
