@@ -92,12 +92,24 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_plane_sums(const float *A, 
     const float *ap = A + plane * S, *gp = dout + plane * S;
     const float K = apply_act(act, ap[0]);
     float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // sum d, sum d^2, sum g, sum g d
-    for (long long i = threadIdx.x; i < S; i += kBwdThreads) {
-        const float d = apply_act(act, ap[i]) - K, g = gp[i];
+    auto add = [&](float a, float g) {
+        const float d = apply_act(act, a) - K;
         v[0] += d;
         v[1] = fmaf(d, d, v[1]);
         v[2] += g;
         v[3] = fmaf(g, d, v[3]);
+    };
+    if ((S & 3) == 0) {  // planes start on 16 bytes: four values a load
+        const float4 *a4 = reinterpret_cast<const float4 *>(ap), *g4 = reinterpret_cast<const float4 *>(gp);
+        for (long long i = threadIdx.x; i < S / 4; i += kBwdThreads) {
+            const float4 a = a4[i], g = g4[i];
+            add(a.x, g.x);
+            add(a.y, g.y);
+            add(a.z, g.z);
+            add(a.w, g.w);
+        }
+    } else {
+        for (long long i = threadIdx.x; i < S; i += kBwdThreads) add(ap[i], gp[i]);
     }
     block_sum<4>(v);
     if (threadIdx.x == 0) {
@@ -159,17 +171,32 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_dA(float *A, const float *d
     const long long plane = blockIdx.x / slices;
     const int slice = (int)(blockIdx.x - plane * slices);
     const float4 cf = coef[plane];
-    const long long i0 = S * slice / slices, i1 = S * (slice + 1) / slices;
+    // slice bounds on multiples of 4 (the last one ends at S)
+    const long long i0 = (S * slice / slices) & ~3LL, i1 = slice + 1 == slices ? S : (S * (slice + 1) / slices) & ~3LL;
     float *ap = A + plane * S;
     const float *gp = dout + plane * S;
     float v[1] = {0.0f};
-    for (long long i = i0 + threadIdx.x; i < i1; i += kBwdThreads) {
-        const float a = ap[i];
+    auto grad = [&](float a, float g) {
         const float y = act == ACT_NONE ? a : apply_act(act, a);
-        const float dy = fmaf(cf.x, gp[i], fmaf(cf.z, y - cf.w, cf.y));
+        const float dy = fmaf(cf.x, g, fmaf(cf.z, y - cf.w, cf.y));
         const float da = act == ACT_NONE ? dy : dy * act_grad(act, a);
-        ap[i] = da;
         v[0] += da;
+        return da;
+    };
+    if ((S & 3) == 0 && (i0 & 3) == 0 && (i1 & 3) == 0) {  // four values a load
+        float4 *a4 = reinterpret_cast<float4 *>(ap);
+        const float4 *g4 = reinterpret_cast<const float4 *>(gp);
+        for (long long i = i0 / 4 + threadIdx.x; i < i1 / 4; i += kBwdThreads) {
+            float4 a = a4[i];
+            const float4 g = g4[i];
+            a.x = grad(a.x, g.x);
+            a.y = grad(a.y, g.y);
+            a.z = grad(a.z, g.z);
+            a.w = grad(a.w, g.w);
+            a4[i] = a;
+        }
+    } else {
+        for (long long i = i0 + threadIdx.x; i < i1; i += kBwdThreads) ap[i] = grad(ap[i], gp[i]);
     }
     block_sum<1>(v);
     if (threadIdx.x == 0) dbpart[plane * slices + slice] = v[0];
