@@ -74,6 +74,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <type_traits>
 
 namespace cn {
 namespace {
@@ -510,13 +511,22 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 // does not accumulate.  Only where a plane's columns are a
                 // multiple of 32 (the TMEM allocation granule), so every D
                 // starts on one; otherwise every MMA spans all ZG planes.
+                // With narrow MMAs, a group with fewer than ZG output planes
+                // left (the depth's last) gets MMAs only for its planes: the
+                // same code with the window's end and the fresh planes taken
+                // at run time.
                 constexpr int NZ = CO * K;  // columns of one output plane
                 constexpr bool NARROW = P::NARROW;
+                auto stage_mmas = [&](auto partial_tag) {
+                constexpr bool PARTIAL = decltype(partial_tag)::value;
+                const int nzv = info.w;  // valid output planes of the group
 #pragma unroll
                 for (int u = 0; u < NU; ++u) {
                     const int zlo = NARROW ? (u - (K - 1) > 0 ? u - (K - 1) : 0) : 0;
-                    const int zhi = NARROW ? (u < ZG - 1 ? u : ZG - 1) : ZG - 1;
-                    const bool fresh = NARROW ? u < ZG : u == 0;  // plane zg = u starts here
+                    const int zhi_g = NARROW ? (u < ZG - 1 ? u : ZG - 1) : ZG - 1;
+                    const int zhi = PARTIAL ? min(zhi_g, nzv - 1) : zhi_g;
+                    if (PARTIAL && zhi < zlo) continue;  // feeds no valid plane
+                    const bool fresh = NARROW ? (u < ZG && (!PARTIAL || u < nzv)) : u == 0;  // plane zg = u starts here
                     const uint32_t id_all = idesc_tf32(128, (zhi - zlo + 1) * NZ);
                     const uint32_t id_one = idesc_tf32(128, NZ);
                     const uint32_t id_old = idesc_tf32(128, (u - zlo > 0 ? u - zlo : 1) * NZ);
@@ -551,6 +561,11 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                         umma_tf32(dz, ap0 + au + (uint64_t)(ky * WU), bd, id_all, 1u);
                     }
                 }
+                };
+                if (NARROW && info.w < ZG)
+                    stage_mmas(std::true_type{});
+                else
+                    stage_mmas(std::false_type{});
                 umma_commit(&st_empty[b]);
                 umma_commit(&acc_full[b]);  // the stage's MMAs are done (2 of 2)
             }
@@ -573,13 +588,16 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 float4 *xh = reinterpret_cast<float4 *>(stage(b));
                 float4 *xl = xh + (size_t)NU * PPU;
                 constexpr int CT = 32 * kConvWarps;  // converter threads
+                // narrow MMAs of a partial group read only the planes that
+                // feed its valid output planes
+                const int nuc = P::NARROW ? min(NU, info.w + K - 1) : NU;
                 if (a.pad) {
                     // a thread takes 4 consecutive positions of a plane: one
                     // 16-byte load per channel; its i-th stores of a warp land
                     // 64 bytes apart, on distinct banks thanks to the gaps
                     const int nq = P0 >> 2;
 #pragma unroll 1
-                    for (int u = 0; u < NU; ++u) {
+                    for (int u = 0; u < nuc; ++u) {
                         for (int q = ct; q < nq; q += CT) {
                             float4 cv[4];
 #pragma unroll
@@ -605,7 +623,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                     }
                 } else
 #pragma unroll 1
-                for (int u = 0; u < NU; ++u) {
+                for (int u = 0; u < nuc; ++u) {
                     const float *su = src + (size_t)u * P0;
                     // four positions per thread per pass, their loads in flight together
                     for (int p0 = ct; p0 < P0; p0 += 4 * CT) {
@@ -678,7 +696,7 @@ CN_DEV void tc3_body(const Tc3Args &a) {
                 // rows 0 .. k-2 of this quadrant are the shift halo of the one below
                 tc_fence_after();
 #pragma unroll 1
-                for (int zg = 0; zg < ZG; ++zg) {
+                for (int zg = 0; zg < info.w; ++zg) {
                     uint32_t v[NC];
                     const int col0 = (zg * CO + h * CQ) * K;
                     tmem_ld_cols<NC>(tq + (uint32_t)col0, v);
@@ -702,12 +720,12 @@ CN_DEV void tc3_body(const Tc3Args &a) {
             if (pos_ok) cnt_t += info.w;
             const float *hq = hb + (size_t)(min(q + 1, 3) * (K - 1)) * N;
 #pragma unroll 1
-            for (int zg = 0; zg < ZG; ++zg) {
+            for (int zg = 0; zg < info.w; ++zg) {
                 uint32_t v[NC];
                 const int col0 = (zg * CO + h * CQ) * K;
                 tmem_ld_cols<NC>(tq + (uint32_t)col0, v);
                 tmem_wait_ld();
-                const bool valid = pos_ok && zg < info.w;
+                const bool valid = pos_ok;  // planes past the group's valid ones are not computed
 #pragma unroll
                 for (int c = 0; c < CQ; ++c) {
                     float acc = __uint_as_float(v[c * K]);
