@@ -25,12 +25,15 @@
 //   4. k_bwd_dA: dA in place of A, and per-plane-slice sums for db;
 //   5. dx: the forward plan of the adjoint conv on dA;
 //   6. k_bwd_weight: dw as a GEMM over all positions (split over the
-//      positions, fixed-order sum of the splits in k_bwd_weight_sum);
+//      positions), or k_bwd_weight_win for groups of 8 channels (the k x k
+//      window slid along rows); fixed-order sum of the splits in
+//      k_bwd_weight_sum;
 //   7. k_bwd_channel_sums: dgamma, dbeta and db, summed over n in order.
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -324,6 +327,145 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_weight(const float *U, cons
 // positions a step (measured on the l2_p19 and l2_p17 blocks: 16 and 32)
 constexpr int kWBKSmall = 16, kWBKWide = 32;
 
+// Step 6 for narrow groups (8 V channels and at most 8 U channels a group,
+// k <= 3; the l2_p19 block's ConvTranspose2d: U = x, V = dA): the same R,
+// computed with the window slid along the rows instead of as a GEMM.  A
+// block takes one (group, sample) and a run of bands of kWinRB U rows; per
+// band it stages the band's U rows and the V rows they reach in shared
+// memory.  Lane (c, r) of a warp owns the CUG x k x k outputs of V channel c
+// for the positions of band row r in the warp's 32-column segments, so a
+// position costs CUG + k shared loads (the U values, the same for the
+// warp's 8 channels, and the new column of the k x k V window) for CUG k^2
+// multiply-adds.  The pitches put a warp's loads on distinct banks: U rows
+// 4 banks apart, V rows 8 and V channels an odd number of words apart.  At
+// the end the block sums its threads' outputs per channel in a fixed order
+// and writes them to part[(n, run)][w numel].
+constexpr int kWinRB = 4, kWinSeg = 32;
+CN_DEV int win_upitch(int PW) { return (PW + 31) / 32 * 32 + 4; }
+CN_DEV int win_vpitch(int VW) { return (VW + 31) / 32 * 32 + 8; }
+
+template <int K, int CUG>
+__global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *U, const float *V, int N, int CU,
+                                                                   int CV, int PH, int PW, int nrun, int bpr,
+                                                                   float *part) {
+    constexpr int CVG = 8, KK = K * K, NO = CUG * KK, RP = NO + 1, NW = kBwdThreads / 32;
+    extern __shared__ __align__(16) float wsm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = lane >> 2, r = lane & 3;
+    const int VH = PH + K - 1, VW = PW + K - 1, VR = kWinRB + K - 1;
+    const int up = win_upitch(PW), vp = win_vpitch(VW), vcs = VR * vp + 1;
+    float *us = wsm;                       // [CUG][kWinRB][up]
+    float *vs = wsm + CUG * kWinRB * up;   // [CVG][vcs]: rows vp apart
+    int bx = blockIdx.x;
+    const int run = bx % nrun;
+    bx /= nrun;
+    const int n = bx % N, g = bx / N;
+    const int nband = (PH + kWinRB - 1) / kWinRB;
+    const int band0 = run * bpr, band1 = min(band0 + bpr, nband);
+    const float *Ub = U + ((size_t)n * CU + (size_t)g * CUG) * PH * PW;
+    const float *Vb = V + ((size_t)n * CV + (size_t)g * CVG) * VH * VW;
+    const int nseg = (PW + kWinSeg - 1) / kWinSeg;
+    const bool u4 = (PW & 3) == 0 && (reinterpret_cast<uintptr_t>(U) & 15) == 0;
+    float acc[CUG][KK];
+#pragma unroll
+    for (int m = 0; m < CUG; ++m)
+#pragma unroll
+        for (int e = 0; e < KK; ++e) acc[m][e] = 0.0f;
+    for (int band = band0; band < band1; ++band) {
+        const int i0 = band * kWinRB;
+        // stage with asynchronous copies (all in flight at once; zero fill
+        // past the edges): rows spread over the warps, coalesced
+        for (int row = warp; row < CUG * kWinRB; row += NW) {
+            const int m = row / kWinRB, rr = row - m * kWinRB;
+            float *dst = us + (size_t)row * up;
+            const bool ok = i0 + rr < PH;
+            const float *src = Ub + ((size_t)m * PH + (ok ? i0 + rr : 0)) * PW;
+            if (u4) {
+                for (int j = 4 * lane; j < PW; j += 128) cp_async16(dst + j, src + j, ok);
+            } else {
+                for (int j = lane; j < PW; j += 32) cp_async4(dst + j, src + j, ok);
+            }
+        }
+        for (int row = warp; row < CVG * VR; row += NW) {
+            const int cc = row / VR, rr = row - cc * VR;
+            float *dst = vs + (size_t)cc * vcs + (size_t)rr * vp;
+            const bool ok = i0 + rr < VH;
+            const float *src = Vb + ((size_t)cc * VH + (ok ? i0 + rr : 0)) * VW;
+            for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+        if (i0 + r < PH) {
+            for (int seg = warp; seg < nseg; seg += NW) {
+                const int j0 = seg * kWinSeg, jn = min(kWinSeg, PW - j0);
+                const float *ur = us + (size_t)r * up + j0;
+                const float *vr = vs + (size_t)c * vcs + (size_t)r * vp + j0;
+                float win[K][K];
+#pragma unroll
+                for (int p = 0; p < K; ++p)
+#pragma unroll
+                    for (int q = 0; q + 1 < K; ++q) win[p][q] = vr[p * vp + q];
+#pragma unroll 4
+                for (int t = 0; t < jn; ++t) {
+#pragma unroll
+                    for (int p = 0; p < K; ++p) win[p][K - 1] = vr[p * vp + t + K - 1];
+                    float u[CUG];
+#pragma unroll
+                    for (int m = 0; m < CUG; ++m) u[m] = ur[(size_t)m * kWinRB * up + t];
+#pragma unroll
+                    for (int m = 0; m < CUG; ++m)
+#pragma unroll
+                        for (int p = 0; p < K; ++p)
+#pragma unroll
+                            for (int q = 0; q < K; ++q) acc[m][p * K + q] = fmaf(u[m], win[p][q], acc[m][p * K + q]);
+#pragma unroll
+                    for (int p = 0; p < K; ++p)
+#pragma unroll
+                        for (int q = 0; q + 1 < K; ++q) win[p][q] = win[p][q + 1];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    // the block's sums per (m, c, p, q): threads of channel c in warp, then
+    // band-row order
+    float *red = wsm;  // [kBwdThreads][RP]
+#pragma unroll
+    for (int m = 0; m < CUG; ++m)
+#pragma unroll
+        for (int e = 0; e < KK; ++e) red[(size_t)tid * RP + m * KK + e] = acc[m][e];
+    __syncthreads();
+    float *pp = part + ((size_t)n * nrun + run) * ((size_t)CU * CVG * KK) + (size_t)g * CUG * CVG * KK;
+    for (int e = tid; e < CUG * CVG * KK; e += kBwdThreads) {
+        const int m = e / (CVG * KK), rem = e - m * (CVG * KK), cc = rem / KK, pq = rem - cc * KK;
+        float sum = 0.0f;
+        for (int w = 0; w < NW; ++w)
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) sum += red[(size_t)(w * 32 + cc * 4 + rr) * RP + m * KK + pq];
+        pp[e] = sum;
+    }
+}
+
+// Dynamic shared memory of k_bwd_weight_win: the staged rows, or the
+// threads' sums at the end, whichever is larger.
+size_t win_smem_bytes(int CUG, int K, int PW) {
+    const int up = (PW + 31) / 32 * 32 + 4, vp = (PW + K - 1 + 31) / 32 * 32 + 8;
+    const size_t tiles = (size_t)CUG * kWinRB * up + (size_t)8 * ((kWinRB + K - 1) * vp + 1);
+    const size_t red = (size_t)kBwdThreads * (CUG * K * K + 1);
+    return 4 * std::max(tiles, red);
+}
+typedef void (*WinKernel)(const float *, const float *, int, int, int, int, int, int, int, float *);
+WinKernel win_kernel(int CUG, int K) {
+#define CN_WIN(KK_, CC_) \
+    if (K == KK_ && CUG == CC_) return k_bwd_weight_win<KK_, CC_>;
+    CN_WIN(1, 1) CN_WIN(1, 2) CN_WIN(1, 4) CN_WIN(1, 8)
+    CN_WIN(2, 1) CN_WIN(2, 2) CN_WIN(2, 4) CN_WIN(2, 8)
+    CN_WIN(3, 1) CN_WIN(3, 2) CN_WIN(3, 4) CN_WIN(3, 8)
+#undef CN_WIN
+    return nullptr;
+}
+
 // dw[e] = sum over the splits of part[split][e], in split order.
 __global__ void k_bwd_weight_sum(const float *part, int splits, long long total, float *dw) {
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -366,7 +508,9 @@ struct conv_norm_bwd_plan_s {
     int wsplits = 1;
     long long wchunk = 0, wtotal = 0;
     int wgrid = 0;
-    int wtile = 1;  // dw tiles: 0 = 8 x 128 (groups of at most 8 channels), 1 = 64 x 64, 2 = 128 x 128
+    int wtile = 1;  // dw: 0 = 8 x 128 tiles (groups of at most 8 channels), 1 = 64 x 64, 2 = 128 x 128, 3 = sliding window
+    int wrun = 1, wbpr = 1;  // sliding window: runs of bands per (group, sample), bands a run
+    size_t wsmem = 0;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *A = nullptr;      // [N][C_out][S]: A, then dA
@@ -434,15 +578,37 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     const int CU = T ? d->C_in : d->C_out, CV = T ? d->C_out : d->C_in;
     const int CUg = CU / G, NN = (CV / G) * d->k * d->k;
     p->wtile = CUg <= 8 ? 0 : (CUg < 96 ? 1 : 2);
-    const int BM = p->wtile == 0 ? 8 : (p->wtile == 1 ? 64 : 128), BN = p->wtile == 1 ? 64 : 128;
-    const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
-    const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
-    p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
-    p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + 63) / 64 * 64;
-    p->wsplits = (int)((Ktot + p->wchunk - 1) / p->wchunk);
-    p->wgrid = tiles;
+    const int PHw = T ? d->H : p->Ho, PWw = T ? d->W : p->Wo;
     p->wtotal = (long long)CU * NN;
-    if (p->wsplits > 65535) return fail(CN_ERR_UNSUPPORTED);
+    const char *nowin = getenv("CN_NO_WIN");
+    if (CV / G == 8 && d->k <= 3 && win_kernel(CUg, d->k) && !(nowin && atoi(nowin))) {
+        // sliding window: about four blocks' worth per SM slot (two a SM)
+        p->wtile = 3;
+        const int nband = (PHw + kWinRB - 1) / kWinRB;
+        const long long gn = (long long)G * d->N;
+        p->wrun = (int)std::max(1LL, std::min((long long)nband, (8LL * sms + gn - 1) / gn));
+        p->wbpr = (nband + p->wrun - 1) / p->wrun;
+        p->wrun = (nband + p->wbpr - 1) / p->wbpr;
+        p->wgrid = (int)(gn * p->wrun);
+        p->wsplits = d->N * p->wrun;
+        p->wsmem = win_smem_bytes(CUg, d->k, PWw);
+        if (gn * p->wrun > 0x7fffffffLL || p->wsmem > 200 * 1024 ||
+            cudaFuncSetAttribute(win_kernel(CUg, d->k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)p->wsmem) != cudaSuccess) {
+            cudaGetLastError();
+            p->wtile = 0;
+        }
+    }
+    if (p->wtile != 3) {
+        const int BM = p->wtile == 0 ? 8 : (p->wtile == 1 ? 64 : 128), BN = p->wtile == 1 ? 64 : 128;
+        const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
+        const long long Ktot = (long long)d->N * (T ? (long long)d->H * d->W : p->S);
+        p->wsplits = (int)std::max(1LL, std::min((long long)(4 * sms + tiles - 1) / tiles, (Ktot + 4095) / 4096));
+        p->wchunk = ((Ktot + p->wsplits - 1) / p->wsplits + 63) / 64 * 64;
+        p->wsplits = (int)((Ktot + p->wchunk - 1) / p->wchunk);
+        p->wgrid = tiles;
+        if (p->wsplits > 65535) return fail(CN_ERR_UNSUPPORTED);
+    }
     const size_t bA = al256((size_t)p->planes * p->S * 4), bps = al256((size_t)p->planes * 32),
                  bcoef = al256((size_t)p->planes * 16), bg = al256((size_t)p->planes * 8),
                  bdb = al256((size_t)p->planes * p->slices * 4), bw = al256((size_t)p->wsplits * p->wtotal * 4);
@@ -522,7 +688,10 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
         const int CU = T ? d.C_in : d.C_out, CV = T ? d.C_out : d.C_in;
         const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
         const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits);
-        if (p->wtile == 0)
+        if (p->wtile == 3)
+            win_kernel(CU / d.groups, d.k)<<<(unsigned)p->wgrid, kBwdThreads, p->wsmem, s>>>(
+                U, V, d.N, CU, CV, PH, PW, p->wrun, p->wbpr, p->wpart);
+        else if (p->wtile == 0)
             k_bwd_weight<8, 128, 1, 4, kWBKSmall><<<grid, kBwdThreads, 0, s>>>(U, V, d.N, CU, CV, PH, PW, d.k,
                                                                               d.groups, p->wchunk, p->wpart);
         else if (p->wtile == 1)
