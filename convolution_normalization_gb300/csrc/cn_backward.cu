@@ -333,16 +333,20 @@ constexpr int kWBKSmall = 16, kWBKWide = 32;
 // block takes one (group, sample) and a run of bands of kWinRB U rows; per
 // band it stages the band's U rows and the V rows they reach in shared
 // memory.  Lane (c, r) of a warp owns the CUG x k x k outputs of V channel c
-// for the positions of band row r in the warp's 32-column segments, so a
-// position costs CUG + k shared loads (the U values, the same for the
-// warp's 8 channels, and the new column of the k x k V window) for CUG k^2
-// multiply-adds.  The pitches put a warp's loads on distinct banks: U rows
-// 4 banks apart, V rows 8 and V channels an odd number of words apart.  At
-// the end the block sums its threads' outputs per channel in a fixed order
-// and writes them to part[(n, run)][w numel].
+// for the positions of band row r in the warp's 32-column segments, four
+// positions at a time: 16-byte loads of the four positions' U values (the
+// same for the warp's 8 channels) and of the k x k V window's four new
+// columns feed 4 CUG k^2 multiply-adds.  V rows start k - 1 columns before a
+// 16-byte boundary, so those loads are aligned; the pitches put the 16-byte
+// loads of every quarter warp on distinct banks (U rows 1 bank group apart,
+// V rows 2 and V channels an odd number of groups apart).  Columns the
+// staging never writes are zeroed once, so the positions past a row's end
+// add zeros.  At the end the block sums its threads' outputs per channel in
+// a fixed order and writes them to part[(n, run)][w numel].
 constexpr int kWinRB = 4, kWinSeg = 32;
 CN_DEV int win_upitch(int PW) { return (PW + 31) / 32 * 32 + 4; }
 CN_DEV int win_vpitch(int VW) { return (VW + 31) / 32 * 32 + 8; }
+CN_DEV int win_vpad(int K) { return (4 - (K - 1) % 4) % 4; }  // zero columns before a V row
 
 template <int K, int CUG>
 __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *U, const float *V, int N, int CU,
@@ -353,9 +357,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = lane >> 2, r = lane & 3;
     const int VH = PH + K - 1, VW = PW + K - 1, VR = kWinRB + K - 1;
-    const int up = win_upitch(PW), vp = win_vpitch(VW), vcs = VR * vp + 1;
+    const int up = win_upitch(PW), vp = win_vpitch(VW), vcs = VR * vp + 4, vpad = win_vpad(K);
     float *us = wsm;                       // [CUG][kWinRB][up]
-    float *vs = wsm + CUG * kWinRB * up;   // [CVG][vcs]: rows vp apart
+    float *vs = wsm + CUG * kWinRB * up;   // [CVG][vcs]: rows vp apart, column j at vpad + j
     int bx = blockIdx.x;
     const int run = bx % nrun;
     bx /= nrun;
@@ -371,6 +375,14 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
     for (int m = 0; m < CUG; ++m)
 #pragma unroll
         for (int e = 0; e < KK; ++e) acc[m][e] = 0.0f;
+    // the columns no staging writes: U past PW, V before vpad and past vpad + VW
+    for (int row = warp; row < CUG * kWinRB; row += NW)
+        for (int j = PW + lane; j < up; j += 32) us[(size_t)row * up + j] = 0.0f;
+    for (int row = warp; row < CVG * VR; row += NW) {
+        float *dst = vs + (size_t)(row / VR) * vcs + (size_t)(row % VR) * vp;
+        for (int j = lane; j < vp; j += 32)
+            if (j < vpad || j >= vpad + VW) dst[j] = 0.0f;
+    }
     for (int band = band0; band < band1; ++band) {
         const int i0 = band * kWinRB;
         // stage with asynchronous copies (all in flight at once; zero fill
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
         }
         for (int row = warp; row < CVG * VR; row += NW) {
             const int cc = row / VR, rr = row - cc * VR;
-            float *dst = vs + (size_t)cc * vcs + (size_t)rr * vp;
+            float *dst = vs + (size_t)cc * vcs + (size_t)rr * vp + vpad;
             const bool ok = i0 + rr < VH;
             const float *src = Vb + ((size_t)cc * VH + (ok ? i0 + rr : 0)) * VW;
             for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
@@ -400,29 +412,38 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
             for (int seg = warp; seg < nseg; seg += NW) {
                 const int j0 = seg * kWinSeg, jn = min(kWinSeg, PW - j0);
                 const float *ur = us + (size_t)r * up + j0;
-                const float *vr = vs + (size_t)c * vcs + (size_t)r * vp + j0;
-                float win[K][K];
+                const float *vr = vs + (size_t)c * vcs + (size_t)r * vp + vpad + j0;
+                // W[p][e]: V row r + p, columns t + e, e < k + 3
+                float W[K][K + 3];
 #pragma unroll
                 for (int p = 0; p < K; ++p)
 #pragma unroll
-                    for (int q = 0; q + 1 < K; ++q) win[p][q] = vr[p * vp + q];
-#pragma unroll 4
-                for (int t = 0; t < jn; ++t) {
+                    for (int q = 0; q + 1 < K; ++q) W[p][q] = vr[p * vp + q];
+                for (int t = 0; t < jn; t += 4) {
 #pragma unroll
-                    for (int p = 0; p < K; ++p) win[p][K - 1] = vr[p * vp + t + K - 1];
-                    float u[CUG];
+                    for (int p = 0; p < K; ++p) {
+                        const float4 v4 = *reinterpret_cast<const float4 *>(vr + p * vp + t + K - 1);
+                        W[p][K - 1] = v4.x;
+                        W[p][K] = v4.y;
+                        W[p][K + 1] = v4.z;
+                        W[p][K + 2] = v4.w;
+                    }
 #pragma unroll
-                    for (int m = 0; m < CUG; ++m) u[m] = ur[(size_t)m * kWinRB * up + t];
+                    for (int m = 0; m < CUG; ++m) {
+                        const float4 u4 = *reinterpret_cast<const float4 *>(ur + (size_t)m * kWinRB * up + t);
+                        const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-                    for (int m = 0; m < CUG; ++m)
+                        for (int tt = 0; tt < 4; ++tt)
 #pragma unroll
-                        for (int p = 0; p < K; ++p)
+                            for (int p = 0; p < K; ++p)
 #pragma unroll
-                            for (int q = 0; q < K; ++q) acc[m][p * K + q] = fmaf(u[m], win[p][q], acc[m][p * K + q]);
+                                for (int q = 0; q < K; ++q)
+                                    acc[m][p * K + q] = fmaf(uu[tt], W[p][tt + q], acc[m][p * K + q]);
+                    }
 #pragma unroll
                     for (int p = 0; p < K; ++p)
 #pragma unroll
-                        for (int q = 0; q + 1 < K; ++q) win[p][q] = win[p][q + 1];
+                        for (int q = 0; q + 1 < K; ++q) W[p][q] = W[p][q + 4];
                 }
             }
         }
@@ -451,7 +472,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
 // threads' sums at the end, whichever is larger.
 size_t win_smem_bytes(int CUG, int K, int PW) {
     const int up = (PW + 31) / 32 * 32 + 4, vp = (PW + K - 1 + 31) / 32 * 32 + 8;
-    const size_t tiles = (size_t)CUG * kWinRB * up + (size_t)8 * ((kWinRB + K - 1) * vp + 1);
+    const size_t tiles = (size_t)CUG * kWinRB * up + (size_t)8 * ((kWinRB + K - 1) * vp + 4);
     const size_t red = (size_t)kBwdThreads * (CUG * K * K + 1);
     return 4 * std::max(tiles, red);
 }
