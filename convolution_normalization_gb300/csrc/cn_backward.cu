@@ -23,7 +23,8 @@
 //      the coefficients of dy = a dout + b + c (y - mu) and the plane's
 //      dgamma / dbeta terms;
 //   4. k_bwd_dA: dA in place of A, and per-plane-slice sums for db;
-//   5. dx: the forward plan of the adjoint conv on dA;
+//   5. dx: the forward plan of the adjoint conv on dA, or k_bwd_dx_g8 for a
+//      ConvTranspose2d with 8 channels a group;
 //   6. k_bwd_weight: dw as a GEMM over all positions (split over the
 //      positions), or k_bwd_weight_win for groups of 8 channels (the k x k
 //      window slid along rows); fixed-order sum of the splits in
@@ -468,6 +469,97 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
     }
 }
 
+// Step 5 for the ConvTranspose2d block with 8 input and 8 output channels a
+// group (the l2_p19 block; k <= 3, W a multiple of 4): dx is the valid
+// correlation of dA with the filter,
+//   dx[n][g 8 + ci][i][j] = sum_{co, ky, kx} dA[n][g 8 + co][i + ky][j + kx] w[g 8 + ci][co][ky][kx].
+// A block takes one (group, sample) and a band of kWinRB output rows; it
+// stages the band's dA rows (cp.async, zero past the edges) and the group's
+// filter as [co][ky][kx][ci].  Thread (r, quad) computes the 8 channels of
+// output row r at 4 consecutive columns: per dA channel, 16-byte loads of
+// its k x (k + 3) window and of the taps' 8 filter values (the same for the
+// whole block: broadcast) feed 8 x k^2 x 4 multiply-adds.  Each output is
+// one sum in a fixed order; the stores are 16 bytes a thread, coalesced.
+constexpr int kDxQuads = 64;  // column quads a band row takes per pass
+template <int K>
+__global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_dx_g8(const float *dA, const float *w, int N, int C_in,
+                                                              int C_out, int H, int W, float *dx) {
+    constexpr int KK = K * K;
+    extern __shared__ __align__(16) float dsm[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int VH = H + K - 1, VW = W + K - 1, VR = kWinRB + K - 1;
+    const int vp = (VW + 3) / 4 * 4 + 8;  // the window's 16-byte loads reach 4 columns past W + k - 2
+    float *vs = dsm;                        // [8][VR][vp]
+    float *ws = dsm + 8 * VR * vp;          // [co][ky][kx][ci]
+    const int nband = (H + kWinRB - 1) / kWinRB;
+    int bx = blockIdx.x;
+    const int band = bx % nband;
+    bx /= nband;
+    const int n = bx % N, g = bx / N;
+    const int i0 = band * kWinRB;
+    const float *Vb = dA + ((size_t)n * C_out + (size_t)g * 8) * VH * VW;
+    for (int row = warp; row < 8 * VR; row += kBwdThreads / 32) {
+        const int cc = row / VR, rr = row - cc * VR;
+        float *dst = vs + (size_t)row * vp;
+        const bool ok = i0 + rr < VH;
+        const float *src = Vb + ((size_t)cc * VH + (ok ? i0 + rr : 0)) * VW;
+        for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+        for (int j = VW + lane; j < vp; j += 32) dst[j] = 0.0f;
+    }
+    cp_async_commit();
+    // the group's filter w[g 8 + ci][co][ky][kx] as [co][tap][ci]
+    for (int e = tid; e < 8 * 8 * KK; e += kBwdThreads) {
+        const int ci = e / (8 * KK), rem = e - ci * (8 * KK), co = rem / KK, tap = rem - co * KK;
+        ws[(co * KK + tap) * 8 + ci] = __ldg(w + ((size_t)(g * 8 + ci) * 8 + co) * KK + tap);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const int r = tid / kDxQuads, i = i0 + r;
+    if (i < H) {
+        for (int qd = tid % kDxQuads; 4 * qd < W; qd += kDxQuads) {
+            const int j = 4 * qd;
+            float acc[8][4];
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) acc[ci][t] = 0.0f;
+#pragma unroll 1
+            for (int co = 0; co < 8; ++co) {
+                const float *vr = vs + ((size_t)co * VR + r) * vp + j;
+#pragma unroll
+                for (int ky = 0; ky < K; ++ky) {
+                    const float4 a = *reinterpret_cast<const float4 *>(vr + ky * vp);
+                    const float4 b = *reinterpret_cast<const float4 *>(vr + ky * vp + 4);
+                    const float win[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                    for (int kx = 0; kx < K; ++kx) {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(ws + (co * KK + ky * K + kx) * 8);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(ws + (co * KK + ky * K + kx) * 8 + 4);
+                        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+                        for (int ci = 0; ci < 8; ++ci)
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) acc[ci][t] = fmaf(wv[ci], win[t + kx], acc[ci][t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int ci = 0; ci < 8; ++ci) {
+                float *o = dx + (((size_t)n * C_in + g * 8 + ci) * H + i) * W + j;
+                *reinterpret_cast<float4 *>(o) = make_float4(acc[ci][0], acc[ci][1], acc[ci][2], acc[ci][3]);
+            }
+        }
+    }
+}
+size_t dx_g8_smem_bytes(int K, int W) {
+    const int vp = (W + K - 1 + 3) / 4 * 4 + 8;
+    return 4 * ((size_t)8 * (kWinRB + K - 1) * vp + (size_t)64 * K * K);
+}
+typedef void (*DxKernel)(const float *, const float *, int, int, int, int, int, float *);
+DxKernel dx_g8_kernel(int K) {
+    return K == 1 ? k_bwd_dx_g8<1> : (K == 2 ? k_bwd_dx_g8<2> : (K == 3 ? k_bwd_dx_g8<3> : nullptr));
+}
+
 // Dynamic shared memory of k_bwd_weight_win: the staged rows, or the
 // threads' sums at the end, whichever is larger.
 size_t win_smem_bytes(int CUG, int K, int PW) {
@@ -532,6 +624,8 @@ struct conv_norm_bwd_plan_s {
     int wtile = 1;  // dw: 0 = 8 x 128 tiles (groups of at most 8 channels), 1 = 64 x 64, 2 = 128 x 128, 3 = sliding window
     int wrun = 1, wbpr = 1;  // sliding window: runs of bands per (group, sample), bands a run
     size_t wsmem = 0;
+    int dxg8 = 0;            // dx by k_bwd_dx_g8 (else the adjoint conv's forward plan)
+    size_t dxsmem = 0;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *A = nullptr;      // [N][C_out][S]: A, then dA
@@ -620,6 +714,17 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
             p->wtile = 0;
         }
     }
+    // dx of a ConvTranspose2d with 8 channels a group on both sides
+    if (T && d->C_in / G == 8 && d->C_out / G == 8 && d->k <= 3 && d->W % 4 == 0 && !(nowin && atoi(nowin))) {
+        p->dxsmem = dx_g8_smem_bytes(d->k, d->W);
+        const long long blocks = (long long)G * d->N * ((d->H + kWinRB - 1) / kWinRB);
+        if (p->dxsmem <= 100 * 1024 && blocks <= 0x7fffffffLL &&
+            cudaFuncSetAttribute(dx_g8_kernel(d->k), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)p->dxsmem) == cudaSuccess)
+            p->dxg8 = 1;
+        else
+            cudaGetLastError();
+    }
     if (p->wtile != 3) {
         const int BM = p->wtile == 0 ? 8 : (p->wtile == 1 ? 64 : 128), BN = p->wtile == 1 ? 64 : 128;
         const int tiles = ((CUg + BM - 1) / BM) * ((NN + BN - 1) / BN) * G;
@@ -702,7 +807,15 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
                                                                            p->slices, p->dbpart);
         if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
     }
-    if (st == CN_OK) st = conv_norm_forward(p->conv_adj, p->A, w, nullptr, nullptr, nullptr, dx, stream);
+    if (st == CN_OK) {
+        if (p->dxg8) {
+            const unsigned blocks = (unsigned)((long long)d.groups * d.N * ((d.H + kWinRB - 1) / kWinRB));
+            dx_g8_kernel(d.k)<<<blocks, kBwdThreads, p->dxsmem, s>>>(p->A, w, d.N, d.C_in, d.C_out, d.H, d.W, dx);
+            if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
+        } else {
+            st = conv_norm_forward(p->conv_adj, p->A, w, nullptr, nullptr, nullptr, dx, stream);
+        }
+    }
     if (st == CN_OK) {
         const bool T = d.conv == CN_CONVT2D;
         const float *U = T ? x : p->A, *V = T ? p->A : x;

@@ -105,6 +105,11 @@ BWD_CASES = [
                       norm="instance", affine=0, post_scale=0.5, seed=1205),
     wl.with_overrides(W["convt2d_g8_gelu_gn8_n32"], N=1, C_in=8, C_out=8, H=7, W=7, groups=1,
                       norm="none", affine=0, act="none", seed=1206),
+    # 8 channels a group on both sides with k = 2 and k = 1: the sliding-window dw and dx kernels
+    wl.with_overrides(W["convt2d_g8_gelu_gn8_n32"], N=2, C_in=32, C_out=32, H=13, W=16, groups=4, k=2,
+                      num_groups=4, seed=1208),
+    wl.with_overrides(W["convt2d_g8_gelu_gn8_n32"], N=1, C_in=16, C_out=16, H=9, W=36, groups=2, k=1,
+                      act="hardswish", seed=1209),
 ]
 
 
