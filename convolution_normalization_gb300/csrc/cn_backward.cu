@@ -23,7 +23,9 @@
 //      the coefficients of dy = a dout + b + c (y - mu) and the plane's
 //      dgamma / dbeta terms;
 //   4. k_bwd_dA: dA in place of A, and per-plane-slice sums for db;
-//   5. dx: the forward plan of the adjoint conv on dA, or k_bwd_dx_g8 for a
+//   5. dx: the forward plan of the adjoint conv on dA; for Conv2d the
+//      tensor-core Conv2d plan of the zero-padded dA with the turned filter
+//      (k_bwd_pad, k_bwd_wadj, then k_bwd_crop); k_bwd_dx_g8 for a
 //      ConvTranspose2d with 8 channels a group;
 //   6. k_bwd_weight: dw as a GEMM over all positions (split over the
 //      positions), or k_bwd_weight_win for groups of 8 channels (the k x k
@@ -560,6 +562,54 @@ DxKernel dx_g8_kernel(int K) {
     return K == 1 ? k_bwd_dx_g8<1> : (K == 2 ? k_bwd_dx_g8<2> : (K == 3 ? k_bwd_dx_g8<3> : nullptr));
 }
 
+// Step 5 for Conv2d on the tensor cores: dx is the full correlation of dA
+// with the filter turned by 180 degrees and its channel axes swapped,
+//   dx[n][ci][i][j] = sum_{co, p, q} dAp[n][co][i + p][j + q] w[co][ci][k - 1 - p][k - 1 - q],
+// dAp being dA with k - 1 zero rows and columns before and after, i.e. a
+// valid Conv2d of dAp with w'[ci][co][p][q] = w[co][ci][k - 1 - p][k - 1 - q].
+// The library's tensor-core Conv2d plan runs it; its output channels are
+// padded to a multiple of 128 (zero filters) and its input rows to a
+// multiple of 4 columns (zeros), and k_bwd_crop copies the valid part to dx.
+// One warp per padded row (rows of all planes in order), lanes along it.
+__global__ void __launch_bounds__(kBwdThreads) k_bwd_pad(const float *dA, int Ho, int Wo, int k, int Hp, int Wp,
+                                                         long long rows, float *dAp) {
+    const long long row = (long long)blockIdx.x * (kBwdThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const long long pl = row / Hp;
+    const int i = (int)(row - pl * Hp) - (k - 1);
+    float *dst = dAp + row * Wp;
+    if (i < 0 || i >= Ho) {
+        for (int c = lane; c < Wp; c += 32) dst[c] = 0.0f;
+        return;
+    }
+    const float *src = dA + (pl * Ho + i) * Wo;
+    for (int c = lane; c < Wp; c += 32) {
+        const int j = c - (k - 1);
+        dst[c] = (j >= 0 && j < Wo) ? __ldg(src + j) : 0.0f;
+    }
+}
+__global__ void k_bwd_wadj(const float *w, int Co, int Ci, int Cip, int k, float *wa) {
+    const int e = blockIdx.x * blockDim.x + threadIdx.x, kk = k * k;
+    if (e >= Cip * Co * kk) return;
+    const int ci = e / (Co * kk), rem = e - ci * Co * kk, co = rem / kk, t = rem - co * kk;
+    wa[e] = ci < Ci ? __ldg(w + ((size_t)co * Ci + ci) * kk + (kk - 1 - t)) : 0.0f;
+}
+// One warp per dx row, lanes along it.
+__global__ void __launch_bounds__(kBwdThreads) k_bwd_crop(const float *src, int Cs, int Hs, int Ws, int C, int H,
+                                                          int W, long long rows, float *dx) {
+    const long long row = (long long)blockIdx.x * (kBwdThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    const long long pl = row / H;  // n * C + c
+    const int i = (int)(row - pl * H);
+    const long long n = pl / C;
+    const int c = (int)(pl - n * C);
+    const float *s = src + (((size_t)n * Cs + c) * Hs + i) * Ws;
+    float *d = dx + row * W;
+    for (int j = lane; j < W; j += 32) d[j] = __ldg(s + j);
+}
+
 // Dynamic shared memory of k_bwd_weight_win: the staged rows, or the
 // threads' sums at the end, whichever is larger.
 size_t win_smem_bytes(int CUG, int K, int PW) {
@@ -626,6 +676,9 @@ struct conv_norm_bwd_plan_s {
     size_t wsmem = 0;
     int dxg8 = 0;            // dx by k_bwd_dx_g8 (else the adjoint conv's forward plan)
     size_t dxsmem = 0;
+    conv_norm_plan adj_tc = nullptr;  // Conv2d: dx as a tensor-core Conv2d of the padded dA
+    int Cip = 0, Hp = 0, Wp = 0, Hs = 0, Ws = 0;
+    float *dAp = nullptr, *wadj = nullptr, *adjout = nullptr;
     void *ws = nullptr;
     size_t ws_bytes = 0;
     float *A = nullptr;      // [N][C_out][S]: A, then dA
@@ -684,6 +737,30 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     j.W = p->Wo;
     j.has_bias = 0;
     if ((st = conv_norm_plan_create(&j, &p->conv_adj)) != CN_OK) return fail(st);
+    // Conv2d: the adjoint as a valid Conv2d of the zero-padded dA, on the
+    // tensor-core kernel where the padded shape takes it
+    const char *notc = getenv("CN_NO_TC");
+    if (!T && d->groups == 1 && !(notc && atoi(notc))) {
+        conv_norm_desc a = f;
+        a.C_in = d->C_out;
+        a.C_out = (d->C_in + 127) / 128 * 128;
+        a.H = p->Ho + 2 * (d->k - 1);
+        a.W = (p->Wo + 2 * (d->k - 1) + 3) / 4 * 4;
+        a.has_bias = 0;
+        conv_norm_plan q = nullptr;
+        conv_norm_info qi;
+        if (conv_norm_plan_create(&a, &q) == CN_OK && conv_norm_plan_info(q, &qi) == CN_OK && qi.kernel_names &&
+            strstr(qi.kernel_names, "k_conv2d_tc")) {
+            p->adj_tc = q;
+            p->Cip = a.C_out;
+            p->Hp = a.H;
+            p->Wp = a.W;
+            p->Hs = a.H - d->k + 1;
+            p->Ws = a.W - d->k + 1;
+        } else {
+            conv_norm_plan_destroy(q);
+        }
+    }
     // db slices: about 16 K values per block
     p->slices = (int)std::max(1LL, std::min(64LL, p->S / 16384));
     // dw: enough position splits for ~4 blocks per SM
@@ -708,8 +785,7 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
         p->wsplits = d->N * p->wrun;
         p->wsmem = win_smem_bytes(CUg, d->k, PWw);
         if (gn * p->wrun > 0x7fffffffLL || p->wsmem > 200 * 1024 ||
-            cudaFuncSetAttribute(win_kernel(CUg, d->k), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)p->wsmem) != cudaSuccess) {
+            raise_dyn_smem(reinterpret_cast<const void *>(win_kernel(CUg, d->k)), (int)p->wsmem) != cudaSuccess) {
             cudaGetLastError();
             p->wtile = 0;
         }
@@ -719,8 +795,7 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
         p->dxsmem = dx_g8_smem_bytes(d->k, d->W);
         const long long blocks = (long long)G * d->N * ((d->H + kWinRB - 1) / kWinRB);
         if (p->dxsmem <= 100 * 1024 && blocks <= 0x7fffffffLL &&
-            cudaFuncSetAttribute(dx_g8_kernel(d->k), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)p->dxsmem) == cudaSuccess)
+            raise_dyn_smem(reinterpret_cast<const void *>(dx_g8_kernel(d->k)), (int)p->dxsmem) == cudaSuccess)
             p->dxg8 = 1;
         else
             cudaGetLastError();
@@ -738,7 +813,10 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     const size_t bA = al256((size_t)p->planes * p->S * 4), bps = al256((size_t)p->planes * 32),
                  bcoef = al256((size_t)p->planes * 16), bg = al256((size_t)p->planes * 8),
                  bdb = al256((size_t)p->planes * p->slices * 4), bw = al256((size_t)p->wsplits * p->wtotal * 4);
-    p->ws_bytes = bA + bps + bcoef + bg + bdb + bw;
+    const size_t bdap = p->adj_tc ? al256((size_t)d->N * d->C_out * p->Hp * p->Wp * 4) : 0,
+                 bwa = p->adj_tc ? al256((size_t)p->Cip * d->C_out * d->k * d->k * 4) : 0,
+                 bout = p->adj_tc ? al256((size_t)d->N * p->Cip * p->Hs * p->Ws * 4) : 0;
+    p->ws_bytes = bA + bps + bcoef + bg + bdb + bw + bdap + bwa + bout;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         return fail(CN_ERR_ALLOC);
@@ -750,6 +828,11 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
     p->gpart = reinterpret_cast<float2 *>(b + bA + bps + bcoef);
     p->dbpart = reinterpret_cast<float *>(b + bA + bps + bcoef + bg);
     p->wpart = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb);
+    if (p->adj_tc) {
+        p->dAp = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb + bw);
+        p->wadj = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb + bw + bdap);
+        p->adjout = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb + bw + bdap + bwa);
+    }
     *out = p;
     return CN_OK;
 }
@@ -761,6 +844,7 @@ void conv_norm_bwd_plan_destroy(conv_norm_bwd_plan p) {
     if (p->device >= 0 && cur != p->device) cudaSetDevice(p->device);
     conv_norm_plan_destroy(p->conv_fwd);
     conv_norm_plan_destroy(p->conv_adj);
+    conv_norm_plan_destroy(p->adj_tc);
     cudaFree(p->ws);
     if (cur >= 0 && p->device >= 0 && cur != p->device) cudaSetDevice(cur);
     cudaGetLastError();
@@ -769,7 +853,8 @@ void conv_norm_bwd_plan_destroy(conv_norm_bwd_plan p) {
 
 size_t conv_norm_bwd_workspace_bytes(conv_norm_bwd_plan p) {
     if (!p) return 0;
-    return p->ws_bytes + conv_norm_workspace_bytes(p->conv_fwd) + conv_norm_workspace_bytes(p->conv_adj);
+    return p->ws_bytes + conv_norm_workspace_bytes(p->conv_fwd) + conv_norm_workspace_bytes(p->conv_adj) +
+           (p->adj_tc ? conv_norm_workspace_bytes(p->adj_tc) : 0);
 }
 
 int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, const float *b,
@@ -812,6 +897,21 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
             const unsigned blocks = (unsigned)((long long)d.groups * d.N * ((d.H + kWinRB - 1) / kWinRB));
             dx_g8_kernel(d.k)<<<blocks, kBwdThreads, p->dxsmem, s>>>(p->A, w, d.N, d.C_in, d.C_out, d.H, d.W, dx);
             if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
+        } else if (p->adj_tc) {
+            const long long prow = (long long)d.N * d.C_out * p->Hp, rpb = kBwdThreads / 32;
+            k_bwd_pad<<<(unsigned)((prow + rpb - 1) / rpb), kBwdThreads, 0, s>>>(p->A, p->Ho, p->Wo, d.k, p->Hp, p->Wp,
+                                                                              prow, p->dAp);
+            const int nw = p->Cip * d.C_out * d.k * d.k;
+            k_bwd_wadj<<<(nw + 255) / 256, 256, 0, s>>>(w, d.C_out, d.C_in, p->Cip, d.k, p->wadj);
+            st = cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
+            if (st == CN_OK)
+                st = conv_norm_forward(p->adj_tc, p->dAp, p->wadj, nullptr, nullptr, nullptr, p->adjout, stream);
+            if (st == CN_OK) {
+                const long long xrow = (long long)d.N * d.C_in * d.H, rpb = kBwdThreads / 32;
+                k_bwd_crop<<<(unsigned)((xrow + rpb - 1) / rpb), kBwdThreads, 0, s>>>(
+                    p->adjout, p->Cip, p->Hs, p->Ws, d.C_in, d.H, d.W, xrow, dx);
+                if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
+            }
         } else {
             st = conv_norm_forward(p->conv_adj, p->A, w, nullptr, nullptr, nullptr, dx, stream);
         }
@@ -848,7 +948,8 @@ int conv_norm_bwd_check_device(conv_norm_bwd_plan p, void *stream) {
     if (!p) return CN_ERR_INVALID_ARG;
     const int a = conv_norm_plan_check_device(p->conv_fwd, stream);
     const int c = conv_norm_plan_check_device(p->conv_adj, stream);
-    return a != CN_OK ? a : c;
+    const int t = p->adj_tc ? conv_norm_plan_check_device(p->adj_tc, stream) : CN_OK;
+    return a != CN_OK ? a : (c != CN_OK ? c : t);
 }
 
 }  // extern "C"

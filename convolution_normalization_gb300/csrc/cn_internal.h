@@ -24,6 +24,10 @@ inline void record_launch(const LaunchEvents *e, int i, cudaStream_t s) {
 
 // Tensor-map encoding (cn_tma_host.cu).
 bool tma_available();
+// Raises (never lowers) a kernel's dynamic shared-memory limit on the
+// current device: plans of one kernel with different sizes live side by
+// side, and each launch needs the limit at or above its own size.
+cudaError_t raise_dyn_smem(const void *kern, int bytes);
 int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], const uint32_t box[4]);
 int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[5],

@@ -1,5 +1,6 @@
 // Host side of TMA: encodes tiled tensor maps through the driver entry point
-// (fetched once through the runtime, so the library does not link libcuda).
+// (fetched once through the runtime, so the library does not link libcuda);
+// and the kernels' dynamic shared-memory limits.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -31,6 +32,14 @@ void fetch_encode() {
 bool tma_available() {
     std::call_once(g_once, fetch_encode);
     return g_encode != nullptr;
+}
+
+cudaError_t raise_dyn_smem(const void *kern, int bytes) {
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 // fp32 tensor of rank 4 (dims innermost first, strides in bytes for dims

@@ -885,7 +885,7 @@ void full2d_bind_workspace(Full2dArgs &a, char *base, int *err_flag) {
 }
 
 int full2d_prepare(Full2dConfig &cfg, Full2dArgs &a) {
-    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+    if (raise_dyn_smem(reinterpret_cast<const void *>(cfg.kern), cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
     // persistent grid: every CTA slot of the device, capped by the tiles

@@ -507,7 +507,7 @@ size_t mean3d_workspace(const Mean3dArgs &a) {
 
 int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
     if (a.small)  // the grid is one CTA per (sample, normalization group)
-        return cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) ==
+        return raise_dyn_smem(reinterpret_cast<const void *>(cfg.kern), cfg.smem) ==
                        cudaSuccess
                    ? CN_OK
                    : CN_ERR_CUDA;
@@ -516,7 +516,7 @@ int mean3d_prepare(Mean3dConfig &cfg, const Mean3dArgs &a) {
         cfg.grid = cfg.tc3.grid;
         return st;
     }
-    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+    if (raise_dyn_smem(reinterpret_cast<const void *>(cfg.kern), cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
     // persistent grid: every CTA slot of the device, capped by the work items

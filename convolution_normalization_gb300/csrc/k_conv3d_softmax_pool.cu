@@ -286,7 +286,7 @@ int pool3d_prepare(Pool3dConfig &cfg, const Pool3dArgs &a) {
         cfg.grid = cfg.tc3.grid;
         return st;
     }
-    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+    if (raise_dyn_smem(reinterpret_cast<const void *>(cfg.kern), cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
     return CN_OK;

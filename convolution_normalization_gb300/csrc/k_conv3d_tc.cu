@@ -1064,7 +1064,7 @@ int tc3_plan(const conv_norm_desc &d, Tc3Args &a, Tc3Config &cfg) {
 }
 
 int tc3_prepare(Tc3Config &cfg, const Tc3Args &a) {
-    if (cudaFuncSetAttribute(cfg.kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem) !=
+    if (raise_dyn_smem(reinterpret_cast<const void *>(cfg.kern), cfg.smem) !=
         cudaSuccess)
         return CN_ERR_CUDA;
     // persistent grid: one CTA per SM, capped by the work items

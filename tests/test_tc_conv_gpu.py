@@ -83,3 +83,25 @@ def test_tc_and_cuda_core_paths_agree_with_oracle(monkeypatch):
     monkeypatch.setenv("CN_NO_TC", "1")
     assert not uses_tc(s)
     assert_parity(run_gpu(s, inp), ref, "CUDA cores")
+
+
+@pytest.mark.parametrize("order", ["larger_first", "smaller_first"])
+def test_plans_of_one_kernel_with_different_shared_memory_coexist(order):
+    # Two live plans of k_conv2d_tc whose launches need different dynamic
+    # shared memory: creating the second must not lower the kernel's limit
+    # below what the first plan's launches need.
+    a = wl.with_overrides(BASE, N=1, C_in=64, C_out=128, H=24, W=128, seed=740)   # 2 rows a tile
+    b = wl.with_overrides(BASE, N=1, C_in=128, C_out=128, H=12, W=132, seed=741)  # 1 row a tile
+    smem = {}
+    for s in (a, b):
+        with B.Plan(s) as p:
+            info = p.info()
+            assert "k_conv2d_tc" in info["kernel_names"]
+            smem[s["name"]] = info["smem_bytes_per_cta"]
+    assert smem[a["name"]] != smem[b["name"]]
+    big, small = (a, b) if smem[a["name"]] > smem[b["name"]] else (b, a)
+    first, second = (big, small) if order == "larger_first" else (small, big)
+    with B.Plan(first) as p1, B.Plan(second) as p2:
+        for s, p in ((first, p1), (second, p2), (first, p1)):
+            inp = wl.make_inputs(s)
+            assert_parity(run_gpu(s, inp, plan=p), oracle.forward(s, inp), s["name"])
