@@ -571,8 +571,10 @@ DxKernel dx_g8_kernel(int K) {
 // padded to a multiple of 128 (zero filters) and its input rows to a
 // multiple of 4 columns (zeros), and k_bwd_crop copies the valid part to dx.
 // One warp per padded row (rows of all planes in order), lanes along it.
+// Rows of dA inside the padding also go to dAq, rows of pitch Pq with
+// zeros past Wo (the tensor-core dw's operand), when dAq is given.
 __global__ void __launch_bounds__(kBwdThreads) k_bwd_pad(const float *dA, int Ho, int Wo, int k, int Hp, int Wp,
-                                                         long long rows, float *dAp) {
+                                                         long long rows, float *dAp, float *dAq, int Pq) {
     const long long row = (long long)blockIdx.x * (kBwdThreads / 32) + (threadIdx.x >> 5);
     if (row >= rows) return;
     const int lane = threadIdx.x & 31;
@@ -587,6 +589,10 @@ __global__ void __launch_bounds__(kBwdThreads) k_bwd_pad(const float *dA, int Ho
     for (int c = lane; c < Wp; c += 32) {
         const int j = c - (k - 1);
         dst[c] = (j >= 0 && j < Wo) ? __ldg(src + j) : 0.0f;
+    }
+    if (dAq) {
+        float *q = dAq + (pl * Ho + i) * Pq;
+        for (int j = lane; j < Pq; j += 32) q[j] = j < Wo ? __ldg(src + j) : 0.0f;
     }
 }
 __global__ void k_bwd_wadj(const float *w, int Co, int Ci, int Cip, int k, float *wa) {
@@ -677,6 +683,10 @@ struct conv_norm_bwd_plan_s {
     int dxg8 = 0;            // dx by k_bwd_dx_g8 (else the adjoint conv's forward plan)
     size_t dxsmem = 0;
     conv_norm_plan adj_tc = nullptr;  // Conv2d: dx as a tensor-core Conv2d of the padded dA
+    BwdWtState *wt = nullptr;         // Conv2d: dw on the tensor cores (with adj_tc)
+    int wt_nrun = 0, wt_pitch = 0, wsplits_gemm = 1;
+    float *dAq = nullptr;             // dA rows of pitch wt_pitch
+    int *werr = nullptr;              // device error flag of the tensor-core dw
     int Cip = 0, Hp = 0, Wp = 0, Hs = 0, Ws = 0;
     float *dAp = nullptr, *wadj = nullptr, *adjout = nullptr;
     void *ws = nullptr;
@@ -810,13 +820,25 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
         p->wgrid = tiles;
         if (p->wsplits > 65535) return fail(CN_ERR_UNSUPPORTED);
     }
+    p->wsplits_gemm = p->wsplits;
+    // dense Conv2d: dw on the tensor cores, fed by the padded-row copy of dA
+    // that the tensor-core adjoint's pad pass writes beside its own
+    if (p->adj_tc && p->wtile != 3 &&
+        bwd_wt_plan(d->N, d->C_out, d->C_in, d->H, d->W, d->k, sms, nullptr, &p->wt, &p->wt_nrun, &p->wt_pitch) !=
+            CN_OK) {
+        p->wt = nullptr;
+    }
     const size_t bA = al256((size_t)p->planes * p->S * 4), bps = al256((size_t)p->planes * 32),
                  bcoef = al256((size_t)p->planes * 16), bg = al256((size_t)p->planes * 8),
-                 bdb = al256((size_t)p->planes * p->slices * 4), bw = al256((size_t)p->wsplits * p->wtotal * 4);
+                 bdb = al256((size_t)p->planes * p->slices * 4);
+    size_t bw = al256((size_t)p->wsplits * p->wtotal * 4);
+    const size_t bwt = p->wt ? al256((size_t)std::max(p->wt_nrun, p->wsplits_gemm) * p->wtotal * 4) : 0,
+                 bdaq = p->wt ? al256((size_t)d->N * d->C_out * p->Ho * p->wt_pitch * 4) + 256 : 0;
+    if (p->wt) bw = bwt;
     const size_t bdap = p->adj_tc ? al256((size_t)d->N * d->C_out * p->Hp * p->Wp * 4) : 0,
                  bwa = p->adj_tc ? al256((size_t)p->Cip * d->C_out * d->k * d->k * 4) : 0,
                  bout = p->adj_tc ? al256((size_t)d->N * p->Cip * p->Hs * p->Ws * 4) : 0;
-    p->ws_bytes = bA + bps + bcoef + bg + bdb + bw + bdap + bwa + bout;
+    p->ws_bytes = bA + bps + bcoef + bg + bdb + bw + bdap + bwa + bout + bdaq;
     if (cudaMalloc(&p->ws, p->ws_bytes) != cudaSuccess) {
         cudaGetLastError();
         return fail(CN_ERR_ALLOC);
@@ -833,6 +855,16 @@ int conv_norm_bwd_plan_create(const conv_norm_desc *d, conv_norm_bwd_plan *out) 
         p->wadj = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb + bw + bdap);
         p->adjout = reinterpret_cast<float *>(b + bA + bps + bcoef + bg + bdb + bw + bdap + bwa);
     }
+    if (p->wt) {
+        char *q = b + bA + bps + bcoef + bg + bdb + bw + bdap + bwa + bout;
+        p->werr = reinterpret_cast<int *>(q);
+        p->dAq = reinterpret_cast<float *>(q + 256);
+        if (cudaMemset(p->werr, 0, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CN_ERR_CUDA);
+        }
+        bwd_wt_set_err(p->wt, p->werr);
+    }
     *out = p;
     return CN_OK;
 }
@@ -845,6 +877,7 @@ void conv_norm_bwd_plan_destroy(conv_norm_bwd_plan p) {
     conv_norm_plan_destroy(p->conv_fwd);
     conv_norm_plan_destroy(p->conv_adj);
     conv_norm_plan_destroy(p->adj_tc);
+    bwd_wt_destroy(p->wt);
     cudaFree(p->ws);
     if (cur >= 0 && p->device >= 0 && cur != p->device) cudaSetDevice(cur);
     cudaGetLastError();
@@ -899,8 +932,8 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
             if (cudaGetLastError() != cudaSuccess) st = CN_ERR_CUDA;
         } else if (p->adj_tc) {
             const long long prow = (long long)d.N * d.C_out * p->Hp, rpb = kBwdThreads / 32;
-            k_bwd_pad<<<(unsigned)((prow + rpb - 1) / rpb), kBwdThreads, 0, s>>>(p->A, p->Ho, p->Wo, d.k, p->Hp, p->Wp,
-                                                                              prow, p->dAp);
+            k_bwd_pad<<<(unsigned)((prow + rpb - 1) / rpb), kBwdThreads, 0, s>>>(
+                p->A, p->Ho, p->Wo, d.k, p->Hp, p->Wp, prow, p->dAp, p->wt ? p->dAq : nullptr, p->wt_pitch);
             const int nw = p->Cip * d.C_out * d.k * d.k;
             k_bwd_wadj<<<(nw + 255) / 256, 256, 0, s>>>(w, d.C_out, d.C_in, p->Cip, d.k, p->wadj);
             st = cudaGetLastError() == cudaSuccess ? CN_OK : CN_ERR_CUDA;
@@ -921,8 +954,12 @@ int conv_norm_backward(conv_norm_bwd_plan p, const float *x, const float *w, con
         const float *U = T ? x : p->A, *V = T ? p->A : x;
         const int CU = T ? d.C_in : d.C_out, CV = T ? d.C_out : d.C_in;
         const int PH = T ? d.H : p->Ho, PW = T ? d.W : p->Wo;
-        const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits);
-        if (p->wtile == 3)
+        const dim3 grid((unsigned)p->wgrid, (unsigned)p->wsplits_gemm);
+        const bool wt = p->wt && p->adj_tc && reinterpret_cast<uintptr_t>(x) % 16 == 0;
+        p->wsplits = wt ? p->wt_nrun : p->wsplits_gemm;
+        if (wt) {
+            st = bwd_wt_launch(p->wt, p->dAq, x, p->wpart, s);
+        } else if (p->wtile == 3)
             win_kernel(CU / d.groups, d.k)<<<(unsigned)p->wgrid, kBwdThreads, p->wsmem, s>>>(
                 U, V, d.N, CU, CV, PH, PW, p->wrun, p->wbpr, p->wpart);
         else if (p->wtile == 0)
@@ -949,7 +986,19 @@ int conv_norm_bwd_check_device(conv_norm_bwd_plan p, void *stream) {
     const int a = conv_norm_plan_check_device(p->conv_fwd, stream);
     const int c = conv_norm_plan_check_device(p->conv_adj, stream);
     const int t = p->adj_tc ? conv_norm_plan_check_device(p->adj_tc, stream) : CN_OK;
-    return a != CN_OK ? a : (c != CN_OK ? c : t);
+    int w = CN_OK;
+    if (p->werr) {
+        int flag = 0;
+        if (cudaMemcpy(&flag, p->werr, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            w = CN_ERR_CUDA;
+        } else if (flag != 0) {
+            const int zero = 0;
+            cudaMemcpy(p->werr, &zero, sizeof(int), cudaMemcpyHostToDevice);
+            w = flag == 1 ? CN_ERR_TIMEOUT : CN_ERR_DEVICE_CHECK;
+        }
+    }
+    return a != CN_OK ? a : (c != CN_OK ? c : (t != CN_OK ? t : w));
 }
 
 }  // extern "C"

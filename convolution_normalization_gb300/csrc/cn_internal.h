@@ -28,6 +28,14 @@ bool tma_available();
 // current device: plans of one kernel with different sizes live side by
 // side, and each launch needs the limit at or above its own size.
 cudaError_t raise_dyn_smem(const void *kern, int bytes);
+
+// Backward dw of a dense Conv2d on the tensor cores (k_bwd_weight_tc.cu).
+struct BwdWtState;
+int bwd_wt_plan(int N, int C_out, int C_in, int H, int W, int k, int sms, int *err, BwdWtState **out, int *nrun,
+                int *pitch);
+void bwd_wt_destroy(BwdWtState *st);
+void bwd_wt_set_err(BwdWtState *st, int *err);  // the device flag its bounded waits report to
+int bwd_wt_launch(BwdWtState *st, const float *dAq, const float *x, float *part, cudaStream_t s);
 int encode_tmap_f32_4d(CUtensorMap *map, const float *base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], const uint32_t box[4]);
 int encode_tmap_f32_5d(CUtensorMap *map, const float *base, const uint64_t dims[5],

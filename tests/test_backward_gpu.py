@@ -105,6 +105,13 @@ BWD_CASES = [
                       norm="instance", affine=0, post_scale=0.5, seed=1205),
     wl.with_overrides(W["convt2d_g8_gelu_gn8_n32"], N=1, C_in=8, C_out=8, H=7, W=7, groups=1,
                       norm="none", affine=0, act="none", seed=1206),
+    # dense Conv2d with 128 output channels and 16 k input channels: dw and dx on the tensor cores
+    wl.with_overrides(W["conv2d_in_half_n32"], N=2, C_in=16, C_out=128, H=10, W=12, act="gelu_erf",
+                      seed=1210),
+    wl.with_overrides(W["conv2d_in_half_n32"], N=3, C_in=32, C_out=256, H=7, W=40, k=2, norm="group",
+                      num_groups=8, affine=1, seed=1211),
+    wl.with_overrides(W["conv2d_in_half_n32"], N=1, C_in=16, C_out=128, H=5, W=36, k=1, has_bias=0,
+                      seed=1212),
     # 8 channels a group on both sides with k = 2 and k = 1: the sliding-window dw and dx kernels
     wl.with_overrides(W["convt2d_g8_gelu_gn8_n32"], N=2, C_in=32, C_out=32, H=13, W=16, groups=4, k=2,
                       num_groups=4, seed=1208),
