@@ -324,7 +324,11 @@ typedef struct conv_norm_bwd_plan_s *conv_norm_bwd_plan;
  * also be one: (C_in / groups) % 4 == 0).  Allocates, on the CURRENT device,
  * a workspace of N C_out H_out W_out floats (the conv output, then its
  * gradient) plus small per-plane and per-split buffers, and two forward plans
- * (the conv alone and its adjoint).
+ * (the conv alone and its adjoint); for a dense Conv2d that fits the
+ * tensor-core path also a third (the adjoint as a Conv2d of the gradient
+ * padded by k - 1 zeros, with its output channels padded to a multiple of
+ * 128) and that plan's input and output, about three more copies of the
+ * gradient's size.
  * Errors: CN_ERR_INVALID_ARG, CN_ERR_UNSUPPORTED, CN_ERR_CUDA, CN_ERR_ALLOC. */
 int conv_norm_bwd_plan_create(const conv_norm_desc *desc, conv_norm_bwd_plan *out_plan);
 
@@ -350,14 +354,15 @@ int conv_norm_backward(conv_norm_bwd_plan plan, const float *x, const float *w, 
                        float *dw, float *db, float *dgamma, float *dbeta, void *cuda_stream);
 
 /* Cites: as conv_norm_bwd_plan_create.
- * Bytes of device memory the backward plan holds (its workspace and its two
+ * Bytes of device memory the backward plan holds (its workspace and its
  * forward plans'); 0 for NULL. */
 size_t conv_norm_bwd_workspace_bytes(conv_norm_bwd_plan plan);
 
 /* Cites: as conv_norm_plan_check_device.
  * Synchronizes cuda_stream and reads and clears the error flags of the
- * backward plan's forward plans (CN_OK, CN_ERR_TIMEOUT, CN_ERR_DEVICE_CHECK,
- * CN_ERR_CUDA); CN_ERR_INVALID_ARG for NULL. */
+ * backward plan's forward plans and of its own tensor-core kernels (CN_OK,
+ * CN_ERR_TIMEOUT, CN_ERR_DEVICE_CHECK, CN_ERR_CUDA); CN_ERR_INVALID_ARG for
+ * NULL. */
 int conv_norm_bwd_check_device(conv_norm_bwd_plan plan, void *cuda_stream);
 
 /* Cites: as conv_norm_plan_destroy.
