@@ -45,8 +45,8 @@
 // matrices, 16 bytes a row.  Tap offsets move the start address only.
 //
 // Warp roles (one persistent CTA per SM, items claimed from a counter: an
-// item is some bands of one group of ZG output planes of one sample; a
-// half the group's bands for the mean, one band for the pool):
+// item is some bands of one group of ZG output planes of one sample: half
+// the group's bands for the mean, one band for the pool):
 //   warp 0      producer: one TMA tensor copy per stage (W x (RB + k - 1)
 //               rows x (ZG + k - 1) planes x C_in, zero fill outside x) into
 //               a ring of up to four landing buffers (as many as fit); for
