@@ -48,6 +48,13 @@ namespace {
 
 constexpr int kBwdThreads = 256;
 
+// Copies 8 bytes global -> shared; when !pred the destination is zero-filled
+// and the source is not read.
+CN_DEV void cp_async8(void *smem, const void *gmem, bool pred) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
+                 "r"(pred ? 8 : 0));
+}
+
 // act'(a): HardSwish 0 below -3, a/3 + 1/2 on [-3, 3], 1 above; GELU (erf
 // form) Phi(a) + a phi(a), erf by Abramowitz & Stegun 7.1.26 as in the
 // forward (|error| <= 1.5e-7).
@@ -373,6 +380,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
     const float *Vb = V + ((size_t)n * CV + (size_t)g * CVG) * VH * VW;
     const int nseg = (PW + kWinSeg - 1) / kWinSeg;
     const bool u4 = (PW & 3) == 0 && (reinterpret_cast<uintptr_t>(U) & 15) == 0;
+    // V rows in 8-byte copies where every row and its shared-memory place start on 8 bytes
+    const bool v8 = (VW & 1) == 0 && (vpad & 1) == 0 && (reinterpret_cast<uintptr_t>(V) & 7) == 0;
     float acc[CUG][KK];
 #pragma unroll
     for (int m = 0; m < CUG; ++m)
@@ -406,7 +415,11 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_weight_win(const float *
             float *dst = vs + (size_t)cc * vcs + (size_t)rr * vp + vpad;
             const bool ok = i0 + rr < VH;
             const float *src = Vb + ((size_t)cc * VH + (ok ? i0 + rr : 0)) * VW;
-            for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+            if (v8) {
+                for (int j = 2 * lane; j < VW; j += 64) cp_async8(dst + j, src + j, ok);
+            } else {
+                for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+            }
         }
         cp_async_commit();
         cp_async_wait_all();
@@ -500,12 +513,18 @@ __global__ void __launch_bounds__(kBwdThreads, 2) k_bwd_dx_g8(const float *dA, c
     const int n = bx % N, g = bx / N;
     const int i0 = band * kWinRB;
     const float *Vb = dA + ((size_t)n * C_out + (size_t)g * 8) * VH * VW;
+    // rows in 8-byte copies where every row starts on 8 bytes
+    const bool v8 = (VW & 1) == 0 && (reinterpret_cast<uintptr_t>(dA) & 7) == 0;
     for (int row = warp; row < 8 * VR; row += kBwdThreads / 32) {
         const int cc = row / VR, rr = row - cc * VR;
         float *dst = vs + (size_t)row * vp;
         const bool ok = i0 + rr < VH;
         const float *src = Vb + ((size_t)cc * VH + (ok ? i0 + rr : 0)) * VW;
-        for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+        if (v8) {
+            for (int j = 2 * lane; j < VW; j += 64) cp_async8(dst + j, src + j, ok);
+        } else {
+            for (int j = lane; j < VW; j += 32) cp_async4(dst + j, src + j, ok);
+        }
         for (int j = VW + lane; j < vp; j += 32) dst[j] = 0.0f;
     }
     cp_async_commit();
