@@ -142,8 +142,9 @@ def test_backward_large_dc_offset():
     assert_grads(run_backward(spec, inp, dout), reference(spec, inp, dout), "x + 30")
 
 
-def test_backward_repeat_is_bitwise_deterministic():
-    spec = BWD_CASES[1]
+@pytest.mark.parametrize("idx", [1, 7], ids=["sliding_window", "tensor_cores"])
+def test_backward_repeat_is_bitwise_deterministic(idx):
+    spec = BWD_CASES[idx]
     inp, dout = case(spec, 3)
     with B.BwdPlan(spec) as p:
         a = run_backward(spec, inp, dout, plan=p)
@@ -151,6 +152,15 @@ def test_backward_repeat_is_bitwise_deterministic():
     for k in a:
         if a[k] is not None:
             assert np.array_equal(a[k], b[k]), k
+
+
+def test_backward_conv2d_tensor_cores_large_dc_offset():
+    # the Conv2d block's dx and dw on the tensor cores with inputs far from
+    # zero mean: the split-TF32 products keep fp32 accuracy on x + 30
+    spec = wl.with_overrides(W["conv2d_in_half_n32"], N=2, C_in=16, C_out=128, H=12, W=16, seed=1213)
+    inp, dout = case(spec, 4)
+    inp = dict(inp, x=(inp["x"] + np.float32(30.0)).astype(np.float32))
+    assert_grads(run_backward(spec, inp, dout), reference(spec, inp, dout), "conv2d x + 30")
 
 
 def test_backward_argument_checks():
