@@ -291,8 +291,8 @@ int conv_norm_plan_set_launch_events(conv_norm_plan plan, void *const *events, i
  *    It depends on the kernel the problem runs on: small batches (up to about
  *    16 M multiply-adds) 16 bytes per (sample, channel, row split) plus 4
  *    bytes per (sample, normalization group); the tensor-core kernel 16 bytes
- *    per (sample, item, channel) plus 4 bytes per sample (2 MB for N=512,
- *    16x32x32, k=4: 16 items a sample); the CUDA-core kernel 24 bytes per
+ *    per (sample, item, channel) plus 4 bytes per sample (1 MB for N=512,
+ *    16x32x32, k=4: 8 items a sample); the CUDA-core kernel 24 bytes per
  *    (sample, row chunk, channel) plus 4 bytes per sample;
  *  - other problem kinds return CN_ERR_UNSUPPORTED; malformed descriptors or
  *    null/misaligned pointers CN_ERR_INVALID_ARG; a failed launch CN_ERR_CUDA;
