@@ -60,7 +60,7 @@ def test_noalloc_matches_plan_forward_twice(spec):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    # 4096 samples of the 16x32x32 k=4 problem need about 19 MB of scratch
+    # 4096 samples of the 16x32x32 k=4 problem need about 8.4 MB of scratch (4 MiB is the limit)
     spec = wl.with_overrides(W["conv3d_hswish_gn4_mean_n512"], N=4096)
     desc = B.make_desc(spec)
     dummy = torch.zeros(16, device="cuda")
