@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kWtThreads, 1) k_bwd_weight_tc(const __grid_co
                 const int c = e & (kWtKT / 4 - 1), co = e >> 3;
                 const float4 v = *reinterpret_cast<const float4 *>(LA + co * kWtKT + 4 * c);
                 const int off = c * P::ACH + (co >> 3) * 128 + (co & 7) * 16;
+                if (!CN_CHECK(off + 16 <= P::AHALF, a.err)) continue;
                 *reinterpret_cast<float4 *>(S + P::AHALF + off) = v;
                 *reinterpret_cast<float4 *>(S + off) =
                     make_float4(tf32_rest(v.x), tf32_rest(v.y), tf32_rest(v.z), tf32_rest(v.w));
@@ -202,6 +203,7 @@ __global__ void __launch_bounds__(kWtThreads, 1) k_bwd_weight_tc(const __grid_co
                 const float *src = LB + (ci * K + p) * P::BOXW + 4 * c + q;
                 const float4 v = make_float4(src[0], src[1], src[2], src[3]);
                 const int off = 2 * P::AHALF + c * P::BCH + (nn >> 3) * 128 + (nn & 7) * 16;
+                if (!CN_CHECK(off + 16 <= 2 * P::AHALF + P::BHALF, a.err)) continue;
                 *reinterpret_cast<float4 *>(S + off) = v;
                 *reinterpret_cast<float4 *>(S + P::BHALF + off) =
                     make_float4(tf32_rest(v.x), tf32_rest(v.y), tf32_rest(v.z), tf32_rest(v.w));
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kWtThreads, 1) k_bwd_weight_tc(const __grid_co
             uint32_t v[16];
             tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)c0, v);
             tmem_wait_ld();
-            if (co < a.Co)
+            if (co < a.Co && CN_CHECK(nt * P::NT + c0 + 16 <= NN && run < a.nrun, a.err))
 #pragma unroll
                 for (int u = 0; u < 16; ++u) dst[c0 + u] = __uint_as_float(v[u]);
         }

@@ -203,12 +203,14 @@ def test_forward_host_matches():
 @pytest.mark.parametrize("name,N,chunks", [("conv3d_hswish_gn4_mean_n512", 203, None),
                                            ("conv3d_hswish_gn4_mean_n512", 203, 3),
                                            ("conv3d_hswish_gn4_mean_n512", 203, 8),
+                                           ("conv3d_hswish_gn4_mean_n512", 203, 16),
                                            ("convt2d_g8_gelu_gn8_n32", 5, None)])
 def test_forward_host_chunked_matches_device_forward(name, N, chunks, monkeypatch):
     # more than 16 MB of input: the host entry point pipelines chunks of whole
     # samples, alternating between two compute streams (203 samples: by
     # default 6 chunks, five of 34 and one of 33; in 3 chunks: 68, 68, 67;
-    # in 8: seven of 26 and one of 21; 5 large samples: one per chunk)
+    # in 8: seven of 26 and one of 21; in 16, the most: fifteen of 13 and one
+    # of 8; 5 large samples: one per chunk)
     if chunks is not None:
         monkeypatch.setenv("CN_HOST_CHUNKS", str(chunks))
     s = wl.with_overrides(W[name], N=N)
