@@ -630,6 +630,9 @@ const Inst kInst[] = {
     CN_FULL_INST(2, 16, 8, 4, 0, -1), CN_FULL_INST(4, 16, 8, 4, 0, -1), CN_FULL_INST(3, 13, 4, 1, 1, -1),
     CN_FULL_INST(3, 16, 4, 2, 1, -1), CN_FULL_INST(1, 16, 8, 4, 1, -1), CN_FULL_INST(2, 16, 8, 1, 1, -1),
     CN_FULL_INST(4, 16, 8, 1, 1, -1),
+    // four output channels a conv group (C_out / groups % 8 == 4) at the other extents
+    CN_FULL_INST(1, 16, 4, 4, 0, -1), CN_FULL_INST(2, 16, 4, 4, 0, -1), CN_FULL_INST(4, 16, 4, 4, 0, -1),
+    CN_FULL_INST(1, 16, 4, 4, 1, -1), CN_FULL_INST(2, 16, 4, 1, 1, -1), CN_FULL_INST(4, 16, 4, 1, 1, -1),
 };
 #undef CN_FULL_INST
 #undef CN_FULL_INST_OFF

@@ -114,7 +114,8 @@ typedef struct {
  * Supported: spatial mean after Conv3d (groups 1, k <= 4, C_out % 4 == 0);
  * the double max pool after Conv3d + channel softmax (C_out = 16, k <= 4, no
  * norm, post_scale > 0); the full output after Conv2d, ConvTranspose2d ((C_out/groups) % 4
- * == 0, k <= 4) or Conv3d (groups 1, k <= 4), any activation but softmax. */
+ * == 0, k <= 4) or Conv3d (groups 1, C_out % 4 == 0, k <= 4), any activation
+ * but softmax. */
 int conv_norm_desc_validate(const conv_norm_desc *desc);
 
 /* Writes the output shape implied by desc into dims[0..*ndim-1] (ndim <= 5):

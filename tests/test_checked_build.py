@@ -22,7 +22,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PARITY_FILES = ["tests/test_parity_gpu.py", "tests/test_tc_conv_gpu.py", "tests/test_tc_mean_gpu.py",
                 "tests/test_tc_pool_gpu.py", "tests/test_tc_convt_gpu.py",
                 "tests/test_conv3d_full_gpu.py", "tests/test_numerics_edges_gpu.py",
-                "tests/test_backward_gpu.py"]
+                "tests/test_backward_gpu.py", "tests/test_fuzz_gpu.py"]
 
 
 def test_checked_library_builds_and_exports_the_abi():
