@@ -14,7 +14,8 @@ On the CPU: every drawn descriptor is valid and supported (a host-only
 query of the library), and the draws cover every conv kind, reduction,
 activation and normalization.  On the GPU: each case matches the oracle
 within |gpu - ref| <= 1e-4 + 1e-4 |ref|, and the kernels' error flags stay
-clear.
+clear.  A second set of random 2-D blocks goes through the backward, against
+the oracle's backward at the backward suite's tolerance.
 """
 import numpy as np
 import pytest
@@ -114,3 +115,55 @@ def test_fuzz_case_matches_oracle(s):
     gpu = run_gpu(s, inp)
     ref = oracle.forward(s, inp)
     assert_parity(gpu, ref, s["name"])
+
+
+# ---- the backward: seeded random 2-D blocks ----------------------------------
+
+NBWD = 40
+
+
+def draw_bwd(rng, i):
+    """One random block the backward takes: Conv2d or grouped ConvTranspose2d
+    (input and output channels a group multiples of 4), any activation but
+    softmax, any norm.  Every other block is in the shape class of the
+    tensor-core gradient kernels (dense Conv2d to 128 output channels from a
+    multiple of 16 input channels; 8 channels a group on both sides of a
+    transposed conv)."""
+    kind = ["conv2d", "convt2d"][i % 2]
+    tc = (i // 2) % 2 == 1
+    k = int(rng.integers(1, 5))
+    groups = int(rng.choice([1, 2, 4, 8]))
+    cin_g, cout_g = int(rng.choice([4, 8, 12, 16])), int(rng.choice([4, 8, 12]))
+    if tc and kind == "conv2d":
+        k, groups, cin_g, cout_g = int(rng.integers(1, 4)), 1, int(16 * rng.integers(1, 3)), 128
+    if tc and kind == "convt2d":
+        k, cin_g, cout_g = int(rng.integers(1, 4)), 8, 8
+    H, W = (int(v) for v in rng.integers(k, k + 24, 2))
+    norm = str(rng.choice(["group", "instance", "none"]))
+    C_out = groups * cout_g
+    return wl.spec(kind, int(rng.integers(1, 4)), groups * cin_g, C_out, 1, H, W, k, groups=groups,
+                   has_bias=int(rng.integers(0, 2)), act=str(rng.choice(["none", "hardswish", "gelu_erf"])),
+                   norm=norm, num_groups=int(rng.choice(_divisors(C_out))),
+                   affine=int(rng.integers(0, 2)) if norm != "none" else 0,
+                   eps=float(rng.choice([1e-5, 1e-3])), post_scale=float(rng.choice([1.0, 0.5, 2.0])),
+                   seed=SEED + 1000 + i, name=f"fuzz_bwd{i}_{kind}")
+
+
+BWD = [draw_bwd(np.random.default_rng(SEED + 1000 + i), i) for i in range(NBWD)]
+
+
+def test_backward_draws_are_supported_forwards_with_supported_adjoints():
+    for s in BWD:
+        assert B.conv_norm_desc_validate(B.make_desc(s)) == B.CN_OK, s["name"]
+        assert (s["C_in"] // s["groups"]) % 4 == 0, s["name"]
+    assert {s["k"] for s in BWD} == {1, 2, 3, 4}
+    assert {s["act"] for s in BWD} == {"none", "hardswish", "gelu_erf"}
+    assert {s["norm"] for s in BWD} == set(wl.NORMS)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("s", BWD, ids=[s["name"] for s in BWD])
+def test_fuzz_backward_matches_oracle(s):
+    from test_backward_gpu import assert_grads, case, reference, run_backward
+    inp, dout = case(s, 7)
+    assert_grads(run_backward(s, inp, dout), reference(s, inp, dout), s["name"])
