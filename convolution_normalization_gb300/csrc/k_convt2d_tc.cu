@@ -97,6 +97,8 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 static_assert(kZG % kEpiRows == 0 && kCog % kEpiCo == 0 && kEpiCo % 2 == 0, "epilogue split");
 static_assert(kEpiCo * kK == 6 || kEpiCo * kK == 12, "TMEM loads of a warp's row columns");
 static_assert(kN % 16 == 0 && kN <= kAccCols, "MMA N");
+static_assert((kZG - 1) * kCog * kK + (kCog - kEpiCo) * kK + 8 <= kAccCols,
+              "an epilogue row's 8-column load stays inside the accumulator");
 static_assert(kBlk % 128 == 0, "a block is whole 8-row core-matrix groups");
 static_assert(kUnitLand % 128 == 0, "landing units stay 128-byte aligned");
 static_assert(kSmemBytes <= 227 * 1024 - 1024, "shared memory");
@@ -368,8 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
                 const int col = c0 + lane;
                 const bool col_ok = lane < kSegV && col < a.Wo;
                 const uint32_t tq = tmem + (uint32_t)(b * kAccCols) + ((uint32_t)(q * 32) << 16);
-                // every column this warp needs, then one wait
-                uint32_t v[kEpiRows][NV];
+                // every column this warp needs, then one wait (a row's six
+                // columns by one 8-column load: the two past them are unused
+                // and stay inside the accumulator's allocation)
+                uint32_t v[kEpiRows][NV == 6 ? 8 : NV];
 #pragma unroll
                 for (int zi = 0; zi < kEpiRows; ++zi) {
                     const uint32_t ta = tq + (uint32_t)((kEpiRows * rp + zi) * kCog * kK + kEpiCo * h * kK);
@@ -377,8 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_convt2d_tc(const __grid_constan
                         tmem_ld8(ta, v[zi]);
                         tmem_ld4(ta + 8, v[zi] + 8);
                     } else {
-                        tmem_ld4(ta, v[zi]);
-                        tmem_ld2(ta + 4, v[zi] + 4);
+                        tmem_ld8(ta, v[zi]);
                     }
                 }
                 tmem_wait_ld();
