@@ -191,7 +191,7 @@ int conv_norm_forward(conv_norm_plan plan, const float *x, const float *w,
  * buffers owned by the plan, runs the forward on cuda_stream, copies the
  * result back into the host buffer out and synchronizes before returning.
  * Batches of more than about 16 MB of input are cut into chunks of whole
- * samples, about 6 MB of input each and at most 8 (every step is per
+ * samples, about 6 MB of input each and at most 16 (every step is per
  * sample): chunk i+1 uploads on a
  * plan-owned stream while chunk i computes, even chunks on cuda_stream and
  * odd ones on a plan-owned compute stream (so one chunk's kernels can start
