@@ -514,6 +514,44 @@ __global__ void __launch_bounds__(256, full_min_ctas(COT, RW))
 // are split into `parts` contiguous ranges, one warp each: warp w takes
 // range w % parts of channels w / parts, w / parts + warps / parts, ...;
 // the warps' results still merge in warp order.
+// channel_moments with each lane's partials (at most 8) all loaded before
+// the first is used, so the loads overlap instead of following one another;
+// the same shift, order of additions and result.  Longer ranges take
+// channel_moments.
+constexpr int kStatsBatch = 8;
+CN_DEV Moments<float> channel_moments_batched(const float4 *p, int n, int lane) {
+    if (n > 32 * kStatsBatch) return channel_moments(p, n, lane);
+    float4 q[kStatsBatch];
+#pragma unroll
+    for (int j = 0; j < kStatsBatch; ++j)
+        q[j] = lane + 32 * j < n ? p[lane + 32 * j] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // common shift: the first non-empty partial's (lowest index)
+    float K0 = 0.0f;
+    bool found = false;
+#pragma unroll
+    for (int j = 0; j < kStatsBatch; ++j) {
+        const unsigned has = __ballot_sync(0xffffffffu, q[j].x > 0.0f);
+        if (!found && has) {
+            K0 = __shfl_sync(0xffffffffu, q[j].y, __ffs(has) - 1);
+            found = true;
+        }
+    }
+    if (!found) return Moments<float>{0.0f, 0.0f, 0.0f};
+    float3 v = make_float3(0.0f, 0.0f, 0.0f);  // (count, S1', S2') about K0
+#pragma unroll
+    for (int j = 0; j < kStatsBatch; ++j) {
+        if (lane + 32 * j >= n) break;
+        const float d = q[j].y - K0;
+        v.x += q[j].x;
+        v.y += fmaf(q[j].x, d, q[j].z);
+        v.z += fmaf(d, fmaf(q[j].x, d, 2.0f * q[j].z), q[j].w);
+    }
+    v = warp_sum3(v);
+    if (!(v.x > 0.0f)) return Moments<float>{0.0f, 0.0f, 0.0f};
+    const float mu_s = v.y / v.x;  // mean - K0
+    return Moments<float>{v.x, K0 + mu_s, fmaxf(v.z - v.y * mu_s, 0.0f)};
+}
+
 constexpr int kStatsWarps = 16;  // most warps of a statistics block
 constexpr int kStatsGroupsPerBlock = 8;  // one-channel groups: one warp each
 __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_constant__ Full2dArgs a, int parts) {
@@ -532,9 +570,9 @@ __global__ void __launch_bounds__(32 * kStatsWarps) k_group_stats(const __grid_c
         const int lo = (int)((long long)per_c * part / parts);
         const int hi = (int)((long long)per_c * (part + 1) / parts);
         for (int cl = slot; cl < cpg; cl += nw / parts)
-            m = merge(m, channel_moments(p0 + (size_t)cl * per_c + lo, hi - lo, lane));
+            m = merge(m, channel_moments_batched(p0 + (size_t)cl * per_c + lo, hi - lo, lane));
     } else {
-        m = channel_moments(p0, per_c, lane);
+        m = channel_moments_batched(p0, per_c, lane);
     }
     if (wide) {
         if (lane == 0) {
