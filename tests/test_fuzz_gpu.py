@@ -24,7 +24,7 @@ import oracle
 from convolution_normalization_gb300 import binding as B
 from convolution_normalization_gb300 import workloads as wl
 
-NCASES = 200
+NCASES = 320
 SEED = 20261203
 
 
@@ -119,7 +119,7 @@ def test_fuzz_case_matches_oracle(s):
 
 # ---- the backward: seeded random 2-D blocks ----------------------------------
 
-NBWD = 40
+NBWD = 80
 
 
 def draw_bwd(rng, i):
